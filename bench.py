@@ -1,0 +1,474 @@
+"""Benchmark of the W4A16 speculative-verify hot path on one GB300 (or N replicas).
+
+One step = one verify pass of the hot path on Llama-3-70B shapes:
+  * the four per-layer verify linears (fused QKV 8192->10240, O 8192->8192,
+    gate+up 8192->57344, down 28672->8192), int4 g128, at M = 1, 4 and 64
+    tokens (12 w4a16_linear calls; each (M, shape) pair streams its own copy of
+    the weights, 1.32 GB per step, so nothing is served from the 126 MB L2);
+  * the stochastic accept step (batch 16, K = 4 drafts, vocab 128256);
+  * the greedy tree accept step (batch 16, 64-node tree, vocab 128256).
+`value` is microseconds per step (device time, CUDA events, inputs resident).
+The JSON line also carries the per-call sweep (us, GB/s, fraction of the HBM
+roofline), the full 80-layer + lm_head verify-forward time at M = 1/4/64 and
+its M=64/M=1 ratio, the end-to-end time with host buffers, and the CPU-oracle
+baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-stack]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "W4A16 verify-linear µs & % HBM roofline at M=1/4/64, Llama-3-70B shapes"
+SHAPES = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate_up", 8192, 57344), ("down", 28672, 8192)]
+LM_HEAD = ("lm_head", 8192, 128256)
+STEP_MS = (1, 4, 64)
+ACC_B, ACC_K, VOCAB = 16, 4, synth.LLAMA3_VOCAB
+TREE_B, TREE_N = 16, 64
+N_LAYERS = 80
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+def linear_bytes(M, N, K):
+    """Algorithmic bytes of one call: packed weights + fp16 scales + x + out, each once."""
+    return N * K // 2 + N * K // 64 + M * K * 2 + M * N * 2
+
+
+def accept_bytes_seq(B, K, V):
+    return (B * (K + 1) * V + B * K * V) * 4 + B * K * 4 + B * (K + 1) * 4 + 2 * B * 4
+
+
+def accept_bytes_tree(B, n, V):
+    return B * n * V * 4 + 2 * B * n * 4 + 2 * B * 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs"))
+        bf = float(d.get("bf16_tflops"))
+        bfs = float(d.get("bf16_tflops_sustained", bf))
+        return {"hbm_gbs": hbm, "bf16_tflops": bf, "bf16_tflops_sustained": bfs, "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_weight(sv, torch, N, K, gen, device):
+    w = torch.randn((N, K), generator=gen, device=device, dtype=torch.float32).mul_(0.02)
+    qw, sc = sv.quantize(w)
+    del w
+    pw = sv.prepack(qw, sc)
+    del qw, sc
+    return pw
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decode_verify_w4a16_gb300 as sv
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    sv.lib()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234 + rank)
+
+    # ---- weights: layers 0..2 serve the step's M = 1 / 4 / 64 calls; the stack adds the rest
+    n_layers = N_LAYERS if args.stack else len(STEP_MS)
+    layers = []
+    for li in range(n_layers):
+        layers.append({name: make_weight(sv, torch, N, K, gen, device) for name, K, N in SHAPES})
+    lm_head = make_weight(sv, torch, LM_HEAD[2], LM_HEAD[1], gen, device) if args.stack else None
+    torch.cuda.synchronize()
+
+    # ---- step inputs
+    xs = {}
+    for M in STEP_MS:
+        for name, K, N in SHAPES:
+            xs[(M, name)] = torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16)
+    outs = {(M, name): torch.empty((M, N), dtype=torch.bfloat16, device=device) for M in STEP_MS
+            for name, K, N in SHAPES}
+    wss = {}
+    for M in STEP_MS:
+        need = max(sv.linear_workspace_bytes(M, N, K) for _, K, N in SHAPES + [LM_HEAD])
+        wss[M] = torch.zeros(need, dtype=torch.uint8, device=device)
+    p_np, q_np, d_np, u_np = synth.accept_seq_case(ACC_B, ACC_K, VOCAB, seed=7 + rank)
+    tp_np, td_np, tpar_np = synth.greedy_tree_case(TREE_B, TREE_N, VOCAB, seed=8 + rank)
+    acc_in = [torch.from_numpy(a).to(device) for a in (p_np, q_np, d_np, u_np)]
+    tree_in = [torch.from_numpy(a).to(device) for a in (tp_np, td_np, tpar_np)]
+    acc_ws = torch.zeros(max(sv.accept_workspace_bytes(ACC_B, ACC_K, VOCAB),
+                             sv.accept_workspace_bytes(TREE_B, TREE_N, VOCAB)), dtype=torch.uint8, device=device)
+    acc_ws2 = torch.zeros_like(acc_ws)
+    acc_out = [torch.empty(ACC_B, dtype=torch.int32, device=device) for _ in range(2)]
+    tree_out = [torch.empty(TREE_B, dtype=torch.int32, device=device) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+    calls = [(M, name, K, N, li) for li, M in enumerate(STEP_MS) for name, K, N in SHAPES]
+    n_launch_per_step = len(calls) + 2 + 1
+
+    def step(evs=None):
+        for j, (M, name, K, N, li) in enumerate(calls):
+            if evs is not None:
+                evs[j][0].record(stream)
+            sv.linear(xs[(M, name)], layers[li][name], out=outs[(M, name)], ws=wss[M])
+            if evs is not None:
+                evs[j][1].record(stream)
+        if evs is not None:
+            evs[len(calls)][0].record(stream)
+        sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3], accepted_len=acc_out[0],
+                       next_token=acc_out[1], ws=acc_ws)
+        if evs is not None:
+            evs[len(calls)][1].record(stream)
+            evs[len(calls) + 1][0].record(stream)
+        sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
+                       next_token=tree_out[1], ws=acc_ws2)
+        if evs is not None:
+            evs[len(calls) + 1][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert sv.check_device_status() == 0
+
+    # ---- timed region
+    nseg = len(calls) + 2
+    all_evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nseg)]
+               for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for s in range(args.steps):
+        step(all_evs[s])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t0.elapsed_time(t1)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    assert sv.check_device_status() == 0
+    seg_us = np.array([[all_evs[s][j][0].elapsed_time(all_evs[s][j][1]) * 1e3 for j in range(nseg)]
+                       for s in range(args.steps)])
+    seg_mean = seg_us.mean(axis=0)
+    pk = peaks()
+
+    sweep = []
+    lin_bytes = lin_us = 0.0
+    for j, (M, name, K, N, li) in enumerate(calls):
+        b = linear_bytes(M, N, K)
+        us = float(seg_mean[j])
+        gbs = b / (us * 1e-6) / 1e9
+        tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        sweep.append({"shape": name, "M": M, "K": K, "N": N, "us": round(us, 2), "GB_s": round(gbs, 1),
+                      "TFLOP_s": round(tflops, 2), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
+        lin_bytes += b
+        lin_us += us
+    acc_us, tree_us = float(seg_mean[len(calls)]), float(seg_mean[len(calls) + 1])
+    ab, tb = accept_bytes_seq(ACC_B, ACC_K, VOCAB), accept_bytes_tree(TREE_B, TREE_N, VOCAB)
+    accept = {"seq_us": round(acc_us, 2), "seq_GB_s": round(ab / (acc_us * 1e-6) / 1e9, 1),
+              "seq_frac_hbm": round(ab / (acc_us * 1e-6) / 1e9 / pk["hbm_gbs"], 3),
+              "tree_us": round(tree_us, 2), "tree_GB_s": round(tb / (tree_us * 1e-6) / 1e9, 1),
+              "tree_frac_hbm": round(tb / (tree_us * 1e-6) / 1e9 / pk["hbm_gbs"], 3)}
+    per_m = {}
+    for M in STEP_MS:
+        sel = [s for s in sweep if s["M"] == M]
+        us = sum(s["us"] for s in sel)
+        b = sum(linear_bytes(M, s["N"], s["K"]) for s in sel)
+        per_m[str(M)] = {"layer_us": round(us, 2), "GB_s": round(b / (us * 1e-6) / 1e9, 1),
+                         "frac_hbm": round(b / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 3)}
+    lin_gbs = lin_bytes / (lin_us * 1e-6) / 1e9
+
+    # ---- full 80-layer + lm_head verify forward at M = 1 / 4 / 64 (outside the timed step)
+    stack = None
+    if args.stack:
+        stack = {}
+        sx = {M: {K: torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16) for K in (8192, 28672)}
+              for M in STEP_MS}
+        souts = {M: {name: torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                     for name, K, N in SHAPES + [LM_HEAD]} for M in STEP_MS}
+
+        def forward(M):
+            for li in range(N_LAYERS):
+                for name, K, N in SHAPES:
+                    sv.linear(sx[M][K], layers[li][name], out=souts[M][name], ws=wss[M])
+            sv.linear(sx[M][8192], lm_head, out=souts[M]["lm_head"], ws=wss[M])
+
+        stack_bytes = {M: N_LAYERS * sum(linear_bytes(M, N, K) for _, K, N in SHAPES)
+                       + linear_bytes(M, LM_HEAD[2], LM_HEAD[1]) for M in STEP_MS}
+        for M in STEP_MS:
+            forward(M)
+            forward(M)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 3
+            e0.record(stream)
+            for _ in range(reps):
+                forward(M)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / reps
+            gbs = stack_bytes[M] / (us * 1e-6) / 1e9
+            stack[str(M)] = {"us": round(us, 1), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
+                             "tokens_per_s": round(M / (us * 1e-6), 1)}
+        stack["ratio_m64_m1"] = round(stack["64"]["us"] / stack["1"]["us"], 3)
+        stack["ratio_m4_m1"] = round(stack["4"]["us"] / stack["1"]["us"], 3)
+        stack["weights_GB"] = round(stack_bytes[1] / 1e9, 2)
+        assert sv.check_device_status() == 0
+
+    # ---- end to end: host buffers, H2D of the step's inputs and D2H of its results inside the timing
+    e2e = run_e2e(sv, torch, device, stream, calls, layers, wss, (p_np, q_np, d_np, u_np), (tp_np, td_np, tpar_np),
+                  acc_ws, acc_ws2, args)
+
+    ms_per_step = total_ms / args.steps
+    line = {
+        "metric": METRIC,
+        "value": round(ms_per_step * 1e3, 2),
+        "unit": "us/step",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; weights ~N(0,0.02) quantized int4 g128 on device, x ~N(0,1); "
+                "logits ~N(0,3), draft = target + N(0,1); planted-argmax random trees)",
+        "config": {
+            "workload": "Llama-3-70B verify linears (QKV/O/gate-up/down) at M=1,4,64 + spec_accept seq "
+                        "(B=16,K=4,V=128256) + greedy tree (B=16,64 nodes,V=128256)",
+            "weights_int4": "g128, fp16 scales, 8 nibbles/uint32",
+            "l2": "inputs larger than L2: 1.32 GB of distinct weights streamed per step",
+            "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
+        },
+        "sweep": sweep,
+        "per_m_layer": per_m,
+        "accept": accept,
+        "stack_verify_forward": stack,
+        "roofline": {"bound": "hbm", "kernel": "w4a16_skinny_kernel (all 12 step launches)",
+                     "achieved": round(lin_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(lin_gbs / pk["hbm_gbs"], 3), "traffic": None,
+                     "peak_source": pk["source"] + " (burst copy bandwidth)"},
+        "clocks": clk,
+        "gpu_launches": n_launch_per_step * args.steps,
+        "e2e": e2e,
+    }
+    if rank == 0 and args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(sample_cols=args.cpu_cols)
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(sv, torch, device, stream, calls, layers, wss, acc_np, tree_np, acc_ws, acc_ws2, args):
+    """The same step through the public API with pinned host inputs and outputs."""
+    h_x = {(M, name): torch.randn((M, K)).to(torch.bfloat16).pin_memory() for (M, name, K, N, li) in calls}
+    d_x = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h_x.items()}
+    h_out = {(M, name): torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for (M, name, K, N, li) in calls}
+    d_out = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h_out.items()}
+    h_acc = [torch.from_numpy(a).pin_memory() for a in acc_np]
+    d_acc = [torch.empty(a.shape, dtype=a.dtype, device=device) for a in h_acc]
+    h_tree = [torch.from_numpy(a).pin_memory() for a in tree_np]
+    d_tree = [torch.empty(a.shape, dtype=a.dtype, device=device) for a in h_tree]
+    h_res = [torch.empty(ACC_B, dtype=torch.int32).pin_memory() for _ in range(4)]
+    d_res = [torch.empty(ACC_B, dtype=torch.int32, device=device) for _ in range(4)]
+    h2d = sum(t.numel() * t.element_size() for t in list(h_x.values()) + h_acc + h_tree)
+    d2h = sum(t.numel() * t.element_size() for t in list(h_out.values()) + h_res)
+
+    def step():
+        for k in h_x:
+            d_x[k].copy_(h_x[k], non_blocking=True)
+        for d, h in zip(d_acc + d_tree, h_acc + h_tree):
+            d.copy_(h, non_blocking=True)
+        for (M, name, K, N, li) in calls:
+            sv.linear(d_x[(M, name)], layers[li][name], out=d_out[(M, name)], ws=wss[M])
+        sv.spec_accept(d_acc[0], d_acc[2], q_logits=d_acc[1], uniforms=d_acc[3], accepted_len=d_res[0],
+                       next_token=d_res[1], ws=acc_ws)
+        sv.spec_accept(d_tree[0], d_tree[1], tree_parents=d_tree[2], accepted_len=d_res[2], next_token=d_res[3],
+                       ws=acc_ws2)
+        for k in h_out:
+            h_out[k].copy_(d_out[k], non_blocking=True)
+        for h, d in zip(h_res, d_res):
+            h.copy_(d, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    steps = max(1, args.steps)
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    us = (time.perf_counter() - t) / steps * 1e6
+    return {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------- CPU oracle baseline
+
+def cpu_baseline_sample(sample_cols=64, seed=0):
+    """The oracle (plain C, fp64, OpenMP over output columns) on a bounded
+    sample of one step: `sample_cols` output columns of each of the 12 linear
+    calls (extrapolated to all N columns) plus the full accept and tree steps."""
+    import oracle
+
+    oracle.build()
+    t_lin = 0.0
+    g = synth.rng(seed)
+    for M in STEP_MS:
+        for name, K, N in SHAPES:
+            # only the sampled rows of W are generated and quantised (the rest do not enter the sample)
+            w = synth.weights(sample_cols, K, seed=seed + K + N)
+            qw, sc = oracle.quantize(w)
+            x = synth.activations(M, K, seed=seed + M)
+            cols = np.arange(sample_cols, dtype=np.int64)
+            t = time.perf_counter()
+            oracle.linear_cols(x, qw, sc, cols)
+            t_lin += (time.perf_counter() - t) * (N / sample_cols)
+    p, q, d, u = synth.accept_seq_case(ACC_B, ACC_K, VOCAB, seed=seed + 1)
+    t = time.perf_counter()
+    oracle.spec_accept_seq(p, q, d, u)
+    t_acc = time.perf_counter() - t
+    tp, td, tpar = synth.greedy_tree_case(TREE_B, TREE_N, VOCAB, seed=seed + 2)
+    t = time.perf_counter()
+    oracle.greedy_tree(tp, td, tpar)
+    t_tree = time.perf_counter() - t
+    total_us = (t_lin + t_acc + t_tree) * 1e6
+    return {"value": round(total_us, 1), "unit": "us/step", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{sample_cols} output columns of each of the 12 linear calls (time scaled by N/"
+                      f"{sample_cols}) + full accept (B=16,K=4) + full greedy tree (B=16,64 nodes)",
+            "linear_us": round(t_lin * 1e6, 1), "accept_us": round(t_acc * 1e6, 1), "tree_us": round(t_tree * 1e6, 1)}
+
+
+def run_reference(args):
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_baseline_sample(sample_cols=args.cpu_cols)
+    vals = []
+    t = time.perf_counter()
+    for s in range(args.steps):
+        vals.append(cpu_baseline_sample(sample_cols=args.cpu_cols, seed=s)["value"])
+    wall = time.perf_counter() - t
+    v = float(np.mean(vals))
+    last = cpu_baseline_sample(sample_cols=args.cpu_cols)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": "Llama-3-70B verify linears (QKV/O/gate-up/down) at M=1,4,64 + spec_accept seq "
+                                   "(B=16,K=4,V=128256) + greedy tree (B=16,64 nodes,V=128256)",
+                       "parallelism": "CPU oracle, host cores"},
+            "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-stack", dest="stack", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-cols", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,173 @@
+/*
+ * w4a16sv — W4A16 speculative-verify library for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI: plain pointers and sizes. Every `void* stream` is a cudaStream_t
+ * (NULL = the legacy default stream). Every buffer is caller-allocated; the
+ * library never allocates or frees device memory. Every call that takes a
+ * stream only enqueues work and returns after host-side argument checks; a
+ * failure inside a kernel (a wait that ran out, an out-of-range id found on
+ * the device) is recorded in a device error word and reported by
+ * w4a16_check_device_status(). Errors are return codes: nothing here traps,
+ * asserts or throws.
+ *
+ * What it computes follows the pages of "Speculative Decoding Meets
+ * Quantization" (Zhang et al. 2025: verifying drafts on a 4-bit weight-only
+ * quantised target, whose forward is bound by weight memory traffic) and the
+ * tutorial "Speculative Decoding이란?" (section 3, Steps 2-4; sections 5-6:
+ * the acceptance test, sequential acceptance, corrected distribution,
+ * greedy equivalence). The 4-bit format is int4 symmetric, group size 128
+ * along K, fp16 scales, 8 nibbles per uint32.
+ */
+#ifndef W4A16SV_H_
+#define W4A16SV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int w4a16_status;
+#define W4A16_OK 0
+#define W4A16_ERR_INVALID_ARG 1     /* null pointer, bad size, misaligned buffer */
+#define W4A16_ERR_UNSUPPORTED 2     /* valid request this build does not handle */
+#define W4A16_ERR_CUDA 3            /* a CUDA runtime call failed */
+#define W4A16_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait ran out (device error word) */
+#define W4A16_ERR_DEVICE_INPUT 5    /* a kernel found an out-of-range id or a bad parent (device error word) */
+#define W4A16_ERR_WORKSPACE 6       /* workspace pointer missing or smaller than required */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* w4a16_status_string(w4a16_status status);
+
+/* ABI version of this header (incremented on any signature change). */
+int w4a16_abi_version(void);
+
+/* ------------------------------------------------------------------------
+ * 4-bit weight format
+ *
+ * Canonical layout (task specification; the pages fix no format):
+ *   qweight[N][K/8] uint32: code of W[n][k] in bits 4*(k%8) .. 4*(k%8)+3 of
+ *   qweight[n][k/8], two's complement in [-8, 7];
+ *   scales[N][K/128] fp16 (IEEE half bits): W[n][k] = code * scales[n][k/128].
+ * N and K must be multiples of 128.
+ * ---------------------------------------------------------------------- */
+
+/* Bytes of the prepacked weight / scale buffers for an N x K matrix
+ * (equal to the canonical sizes: N*K/2 and N*K/64). 0 if N or K is invalid. */
+size_t w4a16_packed_weight_bytes(int64_t N, int64_t K);
+size_t w4a16_packed_scale_bytes(int64_t N, int64_t K);
+
+/*
+ * Group quantiser (device). w[N][K] fp32 (device) -> canonical qweight and
+ * scales (device, caller-allocated). Per row n and group g:
+ *   s = fp16_rne(max_j |w| / 7)  (fp32 quotient, then round to half),
+ *   code = clamp(rne(w / s), -8, 7), or 0 when s == 0.
+ * This is the spec's "scale = max|w|/7" symmetric int4 format; the rounding
+ * rules are this library's reading. Bit-exact with the CPU oracle.
+ */
+w4a16_status w4a16_quantize(const float* w, int64_t N, int64_t K, uint32_t* qweight, uint16_t* scales,
+                            void* stream);
+
+/*
+ * Prepack (device, one time per weight): canonical (qweight, scales) ->
+ * the GPU streaming layout consumed by w4a16_linear. Both outputs are
+ * caller-allocated device buffers of w4a16_packed_weight_bytes /
+ * w4a16_packed_scale_bytes bytes, 16-byte aligned. The packed layout is
+ * opaque: 128 x 128 tiles in (row-tile, group) order with the nibbles placed
+ * where the tensor-core fragments want them, codes stored offset by +8.
+ */
+w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
+                           void* qweight_packed, void* scales_packed, void* stream);
+
+/* ------------------------------------------------------------------------
+ * W4A16 verify linear: out[M][N] = bf16( x[M][K] . W^T ), W = code * scale.
+ *
+ * The verify forward of a speculative step runs every target linear at the
+ * number of draft tokens being checked (the tutorial's section 3 Step 2: all
+ * K positions in one forward; "Speculative Decoding Meets Quantization":
+ * M = 1 decode, small M for a sequence draft, M up to 64 for a tree draft).
+ * The dequantisation is fused into the contraction: codes are exact in bf16,
+ * each 128-wide group is accumulated in fp32 and scaled once in fp32.
+ *
+ *   x            device, bf16 [M][K] row-major, 16-byte aligned
+ *   M            1 .. 64
+ *   K, N         multiples of 128, K >= 1024
+ *   qweight_packed, scales_packed   from w4a16_prepack (device)
+ *   out          device, bf16 [M][N] row-major
+ *   workspace    device scratch of at least w4a16_linear_workspace_bytes(M,N,K)
+ *                bytes, 256-byte aligned, ZERO-FILLED before its first use;
+ *                every call leaves it zeroed again for the next call. After a
+ *                W4A16_ERR_DEVICE_TIMEOUT, zero it again before reuse. Calls
+ *                that share a workspace must not overlap in time.
+ * Returns W4A16_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED before launching.
+ */
+size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K);
+w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_packed,
+                          const void* scales_packed, int64_t N, void* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Speculative accept step (the tutorial page, section 3 Steps 3-4 and
+ * section 6; greedy mode: section 5, "greedy decoding result identical").
+ *
+ * Modes (chosen by which pointers are NULL):
+ *   stochastic sequence  q_logits != NULL, tree_parents == NULL
+ *       p_logits [B][n+1][V] fp32: row i = target logits for draft position
+ *                i+1 (row n: the extra position after all drafts)
+ *       q_logits [B][n][V] fp32: draft logits for draft position i+1
+ *       draft_ids [B][n] int32, uniforms [B][n+1] fp32 in [0, 1)
+ *       For i = 1..n: alpha_i = min(1, P_i(d_i) / Q_i(d_i)) (P, Q = softmax
+ *       at temperature 1; Q(d) == 0 gives alpha = 1); d_i is accepted iff
+ *       u_i < alpha_i; stop at the first rejection r. next_token is drawn
+ *       with u_{n+1} from normalize(max(0, P_r - Q_r)) (P_r itself if that
+ *       sums to 0), or from P_{n+1} when all n are accepted. A draw is the
+ *       smallest x whose ascending running sum exceeds u * total.
+ *       accepted_len in [0, n].
+ *   greedy sequence      q_logits == NULL, tree_parents == NULL
+ *       p_logits [B][n+1][V], draft_ids [B][n]; uniforms may be NULL.
+ *       accepted while d_i == argmax(p row i-1); next = argmax of the row
+ *       after the last accepted token. argmax ties go to the smallest id.
+ *   greedy tree          q_logits == NULL, tree_parents != NULL
+ *       p_logits [B][n][V] (row j: after the path root..j), draft_ids [B][n]
+ *       (slot 0 = root, ignored), tree_parents [B][n] int32 with
+ *       parent[0] = -1 and 0 <= parent[j] < j. Node j is accepted iff its
+ *       parent is and draft[j] == argmax(parent's row); accepted_len is the
+ *       depth of the deepest accepted node (smallest index on ties) and
+ *       next_token the argmax of its row.
+ *   q_logits != NULL with tree_parents != NULL -> W4A16_ERR_UNSUPPORTED.
+ * Logits must be finite. Outputs accepted_len[B], next_token[B] int32
+ * (device). An id outside [0, V) or a bad parent sets W4A16_ERR_DEVICE_INPUT
+ * in the device error word (the row then reports accepted_len = 0).
+ * All pointers are device pointers; p/q rows must be 16-byte aligned when
+ * V % 4 == 0. workspace: device scratch of spec_accept_workspace_bytes(B,n,V)
+ * bytes, 256-byte aligned, zero-filled before first use (left zeroed).
+ * Limits: 1 <= B <= 65535, 1 <= n <= 1024, 2 <= V < 2^31.
+ * ---------------------------------------------------------------------- */
+size_t spec_accept_workspace_bytes(int B, int n, int V);
+w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                         const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                         int32_t* accepted_len, int32_t* next_token, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Device status: synchronises `stream`, reads and clears the device error
+ * word of the current device. W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT,
+ * W4A16_ERR_DEVICE_INPUT or W4A16_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+w4a16_status w4a16_check_device_status(void* stream);
+
+/* ------------------------------------------------------------------------
+ * Host-side planning helpers (no GPU needed; exported so tests can check
+ * the stream-K work split).
+ * The linear splits U = (N/128)*(K/128) tile units over C CTAs: CTA c owns
+ * units [floor(c*U/C), floor((c+1)*U/C)).
+ * ---------------------------------------------------------------------- */
+int64_t w4a16_streamk_unit_begin(int64_t U, int64_t C, int64_t c);
+int64_t w4a16_streamk_owner(int64_t U, int64_t C, int64_t u);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16SV_H_ */

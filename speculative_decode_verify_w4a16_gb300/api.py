@@ -1,0 +1,171 @@
+"""Python binding of libw4a16sv: argument marshalling from torch tensors to the
+C ABI (include/w4a16sv.h). PyTorch supplies device memory and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from ._lib import W4A16Error, check, lib
+
+GROUP = 128
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# --------------------------------------------------------------- workspace
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device: Optional[torch.device] = None, key: str = "default") -> torch.Tensor:
+    """A zero-filled scratch buffer of at least nbytes on `device`, cached per
+    (device, key). The kernels leave it zeroed after every call."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    k = (dev.index if dev.index is not None else torch.cuda.current_device(), key)
+    buf = _ws_cache.get(k)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        _ws_cache[k] = buf
+    return buf
+
+
+# ------------------------------------------------------------------ format
+
+def packed_weight_bytes(N: int, K: int) -> int:
+    return int(lib().w4a16_packed_weight_bytes(N, K))
+
+
+def packed_scale_bytes(N: int, K: int) -> int:
+    return int(lib().w4a16_packed_scale_bytes(N, K))
+
+
+def quantize(w: torch.Tensor, stream=None):
+    """w fp32 [N, K] (CUDA) -> canonical (qweight int32 [N, K/8] holding the
+    uint32 words, scales fp16 [N, K/128])."""
+    _need(w, "w", torch.float32)
+    N, K = w.shape
+    qw = torch.empty((N, K // 8), dtype=torch.int32, device=w.device)
+    sc = torch.empty((N, K // GROUP), dtype=torch.float16, device=w.device)
+    check(lib().w4a16_quantize(_ptr(w), N, K, _ptr(qw), _ptr(sc), _stream(stream)), "w4a16_quantize")
+    return qw, sc
+
+
+@dataclass
+class PackedWeight:
+    """A prepacked W4A16 weight (N x K) ready for linear()."""
+    N: int
+    K: int
+    qweight: torch.Tensor  # uint8 [N*K/2], streaming layout
+    scales: torch.Tensor   # uint8 [N*K/64], streaming layout
+
+    @property
+    def nbytes(self) -> int:
+        return self.qweight.numel() + self.scales.numel()
+
+
+def prepack(qweight: torch.Tensor, scales: torch.Tensor, stream=None) -> PackedWeight:
+    """Canonical (qweight int32/uint32 [N, K/8], scales fp16 [N, K/128]) -> PackedWeight."""
+    if qweight.dtype not in (torch.int32, torch.uint32):
+        raise ValueError("qweight must hold 32-bit words")
+    _need(qweight, "qweight", qweight.dtype)
+    _need(scales, "scales", torch.float16)
+    N, K8 = qweight.shape
+    K = K8 * 8
+    if tuple(scales.shape) != (N, K // GROUP):
+        raise ValueError("scales shape mismatch")
+    qp = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=qweight.device)
+    sp = torch.empty(packed_scale_bytes(N, K), dtype=torch.uint8, device=qweight.device)
+    if qp.numel() == 0:
+        raise W4A16Error(1, "w4a16_prepack: N and K must be positive multiples of 128")
+    check(lib().w4a16_prepack(_ptr(qweight), _ptr(scales), N, K, _ptr(qp), _ptr(sp), _stream(stream)),
+          "w4a16_prepack")
+    return PackedWeight(N, K, qp, sp)
+
+
+# ------------------------------------------------------------------ linear
+
+def linear_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().w4a16_linear_workspace_bytes(M, N, K))
+
+
+def linear(x: torch.Tensor, w: PackedWeight, out: Optional[torch.Tensor] = None,
+           ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[M, N] = bf16(x[M, K] . W^T) with W the dequantised int4 weight."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if K != w.K:
+        raise ValueError(f"x has K={K}, weight has K={w.K}")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (M, w.N))
+    need = linear_workspace_bytes(M, w.N, K)
+    if ws is None:
+        ws = workspace(need, x.device, "linear")
+    check(lib().w4a16_linear(_ptr(x), M, K, _ptr(w.qweight), _ptr(w.scales), w.N, _ptr(out), _ptr(ws),
+                             ws.numel(), _stream(stream)), "w4a16_linear")
+    return out
+
+
+# ------------------------------------------------------------------ accept
+
+def accept_workspace_bytes(B: int, n: int, V: int) -> int:
+    return int(lib().spec_accept_workspace_bytes(B, n, V))
+
+
+def spec_accept(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: Optional[torch.Tensor] = None,
+                tree_parents: Optional[torch.Tensor] = None, uniforms: Optional[torch.Tensor] = None,
+                accepted_len: Optional[torch.Tensor] = None, next_token: Optional[torch.Tensor] = None,
+                ws: Optional[torch.Tensor] = None, stream=None):
+    """Speculative accept step; see the header for the three modes.
+    Returns (accepted_len int32 [B], next_token int32 [B])."""
+    _need(p_logits, "p_logits", torch.float32)
+    _need(draft_ids, "draft_ids", torch.int32)
+    B, rows, V = p_logits.shape
+    if tree_parents is not None:
+        n = rows
+        _need(tree_parents, "tree_parents", torch.int32, (B, n))
+        _need(draft_ids, "draft_ids", torch.int32, (B, n))
+    else:
+        n = rows - 1
+        _need(draft_ids, "draft_ids", torch.int32, (B, n))
+    if q_logits is not None:
+        _need(q_logits, "q_logits", torch.float32, (B, n, V))
+    if uniforms is not None:
+        _need(uniforms, "uniforms", torch.float32, (B, n + 1))
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=p_logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=p_logits.device)
+    need = accept_workspace_bytes(B, n, V)
+    if ws is None:
+        ws = workspace(need, p_logits.device, "accept")
+    check(lib().spec_accept(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), _ptr(tree_parents), _ptr(uniforms),
+                            B, n, V, _ptr(accepted_len), _ptr(next_token), _ptr(ws), ws.numel(),
+                            _stream(stream)), "spec_accept")
+    return accepted_len, next_token
+
+
+def check_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(lib().w4a16_check_device_status(_stream(stream)))

@@ -1,0 +1,178 @@
+// C-ABI layer of libw4a16sv: argument checks, dispatch, device state.
+// Declarations and the contract of every entry point are in w4a16sv.h.
+#include <mutex>
+
+#include "../../include/w4a16sv.h"
+#include "common.cuh"
+#include "format.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+
+// Device error word (one per device that loads the library).
+__device__ unsigned g_error_word;
+
+namespace {
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev[dev].device != dev) {
+    DeviceInfo d;
+    d.device = dev;
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) return e;
+    d.err = static_cast<unsigned*>(p);
+    g_dev[dev] = d;
+  }
+  *out = g_dev[dev];
+  return cudaSuccess;
+}
+
+}  // namespace w4a16
+
+using namespace w4a16;
+
+static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static inline bool valid_nk(int64_t N, int64_t K) {
+  return N > 0 && K > 0 && N % kUnitRows == 0 && K % kGroup == 0 && N <= (int64_t(1) << 31) &&
+         K <= (int64_t(1) << 24);
+}
+
+extern "C" {
+
+const char* w4a16_status_string(w4a16_status s) {
+  switch (s) {
+    case W4A16_OK: return "W4A16_OK";
+    case W4A16_ERR_INVALID_ARG: return "W4A16_ERR_INVALID_ARG";
+    case W4A16_ERR_UNSUPPORTED: return "W4A16_ERR_UNSUPPORTED";
+    case W4A16_ERR_CUDA: return "W4A16_ERR_CUDA";
+    case W4A16_ERR_DEVICE_TIMEOUT: return "W4A16_ERR_DEVICE_TIMEOUT";
+    case W4A16_ERR_DEVICE_INPUT: return "W4A16_ERR_DEVICE_INPUT";
+    case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+    default: return "W4A16_ERR_UNKNOWN";
+  }
+}
+
+int w4a16_abi_version(void) { return 1; }
+
+size_t w4a16_packed_weight_bytes(int64_t N, int64_t K) { return valid_nk(N, K) ? (size_t)(N * K / 2) : 0; }
+
+size_t w4a16_packed_scale_bytes(int64_t N, int64_t K) { return valid_nk(N, K) ? (size_t)(N * K / 64) : 0; }
+
+int64_t w4a16_streamk_unit_begin(int64_t U, int64_t C, int64_t c) {
+  if (U <= 0 || C <= 0 || C > U || c < 0 || c > C) return -1;
+  return streamk_begin(U, C, c);
+}
+
+int64_t w4a16_streamk_owner(int64_t U, int64_t C, int64_t u) {
+  if (U <= 0 || C <= 0 || C > U || u < 0 || u >= U) return -1;
+  return streamk_owner(U, C, u);
+}
+
+w4a16_status w4a16_quantize(const float* w, int64_t N, int64_t K, uint32_t* qweight, uint16_t* scales,
+                            void* stream) {
+  if (!w || !qweight || !scales || !valid_nk(N, K)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(qweight, 4) || !aligned(scales, 2)) return W4A16_ERR_INVALID_ARG;
+  return launch_quantize(w, N, K, qweight, scales, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
+                           void* qweight_packed, void* scales_packed, void* stream) {
+  if (!qweight || !scales || !qweight_packed || !scales_packed || !valid_nk(N, K)) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(qweight_packed, 16) || !aligned(scales_packed, 16) || !aligned(qweight, 4) || !aligned(scales, 2))
+    return W4A16_ERR_INVALID_ARG;
+  return launch_prepack(qweight, scales, N, K, static_cast<uint32_t*>(qweight_packed),
+                        static_cast<uint16_t*>(scales_packed), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+static bool linear_shape_ok(int M, int64_t N, int64_t K) { return M >= 1 && M <= 64 && valid_nk(N, K) && K >= 1024; }
+
+size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K) {
+  if (!linear_shape_ok(M, N, K)) return 0;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return 0;
+  SkinnyPlan plan;
+  if (skinny_plan(M, N, K, dev, &plan) != cudaSuccess) return 0;
+  return skinny_workspace_bytes(plan);
+}
+
+w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_packed, const void* scales_packed,
+                          int64_t N, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !qweight_packed || !scales_packed || !out) return W4A16_ERR_INVALID_ARG;
+  if (M < 1 || !valid_nk(N, K)) return W4A16_ERR_INVALID_ARG;
+  if (M > 64 || K < 1024) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(qweight_packed, 16) || !aligned(scales_packed, 16) || !aligned(out, 4))
+    return W4A16_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return W4A16_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  SkinnyPlan plan;
+  if (skinny_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (workspace_bytes < skinny_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
+  return launch_skinny(x, M, K, qweight_packed, scales_packed, N, out, workspace, plan, dev,
+                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+size_t spec_accept_workspace_bytes(int B, int n, int V) {
+  if (B < 1 || B > 65535 || n < 1 || n > 1024 || V < 2) return 0;
+  return accept_plan(B, n, V).total;
+}
+
+w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                         const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                         int32_t* accepted_len, int32_t* next_token, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  if (!p_logits || !draft_ids || !accepted_len || !next_token) return W4A16_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || n < 1 || n > 1024 || V < 2) return W4A16_ERR_INVALID_ARG;
+  if (q_logits && tree_parents) return W4A16_ERR_UNSUPPORTED;
+  if (q_logits && !uniforms) return W4A16_ERR_INVALID_ARG;
+  if (V % 4 == 0 && (!aligned(p_logits, 16) || (q_logits && !aligned(q_logits, 16)))) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(p_logits, 4) || !aligned(draft_ids, 4) || !aligned(accepted_len, 4) || !aligned(next_token, 4))
+    return W4A16_ERR_INVALID_ARG;
+  const AcceptPlan plan = accept_plan(B, n, V);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < plan.total) return W4A16_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  cudaError_t e;
+  if (q_logits)
+    e = launch_accept_seq(p_logits, q_logits, draft_ids, uniforms, B, n, V, accepted_len, next_token, workspace, plan,
+                          dev.err, static_cast<cudaStream_t>(stream));
+  else
+    e = launch_accept_greedy(p_logits, draft_ids, tree_parents, B, n, V, accepted_len, next_token, workspace, plan,
+                             dev.err, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+w4a16_status w4a16_check_device_status(void* stream) {
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return W4A16_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, dev.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (word) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(dev.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return W4A16_ERR_CUDA;
+  }
+  if (word & kErrTimeout) return W4A16_ERR_DEVICE_TIMEOUT;
+  if (word & kErrInput) return W4A16_ERR_DEVICE_INPUT;
+  return W4A16_OK;
+}
+
+}  // extern "C"

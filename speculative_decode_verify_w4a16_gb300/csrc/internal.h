@@ -1,0 +1,58 @@
+// Internal host-side interface between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+struct DeviceInfo {
+  int device = -1;
+  int num_sms = 0;
+  unsigned* err = nullptr;  // device address of the error word
+};
+
+// Per-device state (error word address, SM count); initialised on first use
+// with that device current.
+cudaError_t device_info(DeviceInfo* out);
+
+// ---- format
+cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint32_t* qweight, uint16_t* scales,
+                            cudaStream_t stream);
+cudaError_t launch_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
+                           uint32_t* qw_packed, uint16_t* sc_packed, cudaStream_t stream);
+
+// ---- linear (tensor-core fragments via mma.sync; stream-K over units)
+struct SkinnyPlan {
+  int mt8 = 0;          // ceil(M / 8)
+  int64_t units = 0;    // (N/128) * (K/128)
+  int64_t ctas = 0;     // grid size
+  size_t counter_bytes = 0;
+  size_t partial_bytes = 0;
+  size_t smem_bytes = 0;
+};
+cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, SkinnyPlan* plan);
+size_t skinny_workspace_bytes(const SkinnyPlan& plan);
+cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed,
+                          int64_t N, void* out, void* workspace, const SkinnyPlan& plan, const DeviceInfo& dev,
+                          cudaStream_t stream);
+
+// ---- accept
+struct AcceptPlan {
+  int rows = 0;       // logit rows read by the statistics pass
+  int ch = 0;         // chunks per row (statistics / argmax pass)
+  int chunk = 0;      // elements per chunk (multiple of 4)
+  int ch2 = 0;        // chunks per batch row (residual pass)
+  int chunk2 = 0;
+  size_t stats_off = 0, csum_off = 0, cnt_off = 0, total = 0;
+};
+AcceptPlan accept_plan(int B, int n, int V);
+cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
+                              int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
+                              cudaStream_t stream);
+cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
+                                 int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
+                                 cudaStream_t stream);
+
+}  // namespace w4a16

@@ -1,0 +1,393 @@
+// W4A16 verify linear, tensor-core fragment path (mma.sync m16n8k16 bf16).
+//
+// out[M][N] = bf16(x[M][K] . W^T) with W = code * scale (int4, group 128).
+// Work split: the (row-tile, group) units of the packed weight stream are
+// divided evenly over the grid (stream-K); each CTA streams its contiguous
+// unit range through a ring of shared-memory stages filled by 1-D bulk
+// copies (TMA engine), so every weight byte is read from HBM exactly once.
+//
+// Per CTA: 4 consumer warps (one 32-row slice of the 128-row unit each) and
+// one producer warp. A consumer dequantises 16 packed words per unit into
+// exact bf16 codes (offset-binary nibble OR'ed into the mantissa of 128.0,
+// then 136 subtracted: a bit trick in the spirit of Kim et al. 2022, "Who
+// Says Elephants Can't Run", arXiv:2211.10017), multiplies them with the
+// token fragments on the tensor cores (swap-AB: weight rows are the MMA's M
+// dimension, tokens its N = 8), accumulates the group in fp32 and applies
+// the fp16 group scale once in fp32.
+//
+// A tile whose K range is split between CTAs is finished by whichever
+// contributor arrives last (per tile and warp slice, counted with an atomic),
+// which sums all contributions in CTA order: the result does not depend on
+// timing. Counters reset themselves for the next call.
+#include "common.cuh"
+#include "format.cuh"
+#include "internal.h"
+
+namespace w4a16 {
+
+constexpr int kSkConsumerWarps = 4;
+constexpr int kSkThreads = 32 * (kSkConsumerWarps + 1);
+constexpr int kSkStages = 4;
+constexpr int kXRowStride = 288;  // bytes per token row in a stage (256 used; padding avoids bank conflicts)
+
+template <int MT8>
+struct SkinnyLayout {
+  static constexpr int kW = kUnitBytes;
+  static constexpr int kS = kUnitScaleBytes;
+  static constexpr int kX = MT8 * 8 * kXRowStride;
+  static constexpr int kStage = kW + kS + kX;
+  static constexpr int kBarOff = kSkStages * kStage;
+  static constexpr int kTotal = kBarOff + 2 * kSkStages * 8;
+  static_assert(kStage % 16 == 0, "stage alignment");
+};
+
+struct SkinnyParams {
+  const __nv_bfloat16* x;
+  const uint8_t* qw;
+  const uint8_t* sc;
+  __nv_bfloat16* out;
+  float4* partials;
+  int* counters;
+  unsigned* err;
+  int64_t K, N, U, G, C;
+  int M;
+};
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 8 offset-binary nibbles -> four bf16x2 registers of exact signed codes.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t magic = 0x43004300u;                          // bf16x2 (128, 128)
+  const __nv_bfloat162 bias = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));  // 136
+  uint32_t t[4];
+  t[0] = (w & 0x000F000Fu) | magic;
+  t[1] = ((w >> 4) & 0x000F000Fu) | magic;
+  t[2] = ((w >> 8) & 0x000F000Fu) | magic;
+  t[3] = ((w >> 12) & 0x000F000Fu) | magic;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t[i]), bias);
+    a[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+template <int MT8>
+__device__ __forceinline__ void store_tile(const SkinnyParams& p, int64_t t, int warp, int lane,
+                                           const float (&acc)[2][MT8][4]) {
+  const int gid = lane >> 2, cq = lane & 3;
+#pragma unroll
+  for (int rt = 0; rt < 2; ++rt) {
+    const int64_t n_lo = t * kUnitRows + warp * 32 + rt * 16 + gid;
+#pragma unroll
+    for (int nt = 0; nt < MT8; ++nt) {
+      const int m0 = nt * 8 + 2 * cq;
+      if (m0 < p.M) {
+        p.out[(int64_t)m0 * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][0]);
+        p.out[(int64_t)m0 * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][2]);
+      }
+      if (m0 + 1 < p.M) {
+        p.out[(int64_t)(m0 + 1) * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][1]);
+        p.out[(int64_t)(m0 + 1) * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][3]);
+      }
+    }
+  }
+}
+
+template <int MT8>
+__device__ __forceinline__ float4* partial_slot(const SkinnyParams& p, int64_t cta, int seg, int warp) {
+  return p.partials + ((cta * 2 + seg) * kSkConsumerWarps + warp) * (int64_t)(2 * MT8 * 32);
+}
+
+template <int MT8>
+__device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t, int warp, int lane,
+                                  const float (&acc)[2][MT8][4]) {
+  const int64_t tile_first = streamk_begin(p.U, p.C, cta) / p.G;
+  float4* slot = partial_slot<MT8>(p, cta, t == tile_first ? 0 : 1, warp);
+#pragma unroll
+  for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+    for (int nt = 0; nt < MT8; ++nt)
+      __stcg(&slot[(rt * MT8 + nt) * 32 + lane],
+             make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]));
+  __threadfence();
+  __syncwarp();
+  int old = 0;
+  if (lane == 0) old = atomicAdd(&p.counters[t * kSkConsumerWarps + warp], 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  const int64_t cf = streamk_owner(p.U, p.C, t * p.G);
+  const int64_t cl = streamk_owner(p.U, p.C, t * p.G + p.G - 1);
+  if (old != (int)(cl - cf)) return;  // not the last contributor
+  __threadfence();
+  float sum[2][MT8][4];
+#pragma unroll
+  for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+    for (int nt = 0; nt < MT8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sum[rt][nt][e] = 0.0f;
+  for (int64_t cc = cf; cc <= cl; ++cc) {
+    const int64_t tf = streamk_begin(p.U, p.C, cc) / p.G;
+    const float4* sl = partial_slot<MT8>(p, cc, t == tf ? 0 : 1, warp);
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int nt = 0; nt < MT8; ++nt) {
+        const float4 v = __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]);
+        sum[rt][nt][0] += v.x;
+        sum[rt][nt][1] += v.y;
+        sum[rt][nt][2] += v.z;
+        sum[rt][nt][3] += v.w;
+      }
+  }
+  store_tile<MT8>(p, t, warp, lane, sum);
+  if (lane == 0) p.counters[t * kSkConsumerWarps + warp] = 0;
+}
+
+template <int MT8>
+__global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyParams p) {
+  using L = SkinnyLayout<MT8>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + kSkStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t cta = blockIdx.x;
+  const int64_t u0 = streamk_begin(p.U, p.C, cta);
+  const int n_units = (int)(streamk_begin(p.U, p.C, cta + 1) - u0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSkStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kSkConsumerWarps);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kSkConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane != 0) return;
+    const uint64_t pol = policy_evict_first();
+    const uint32_t tx = (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256);
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < n_units; ++i) {
+      const int s = i % kSkStages;
+      const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
+      if (i >= kSkStages && !mbar_wait(&empty[s], ph ^ 1u, p.err)) {
+        ok = false;
+        break;
+      }
+      const int64_t u = u0 + i;
+      const int64_t g = u % p.G;
+      uint8_t* st = smem + s * L::kStage;
+      mbar_arrive_expect_tx(&full[s], tx);
+      bulk_g2s_hint(st, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
+      bulk_g2s(st + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
+      for (int m = 0; m < p.M; ++m)
+        bulk_g2s(st + kUnitBytes + kUnitScaleBytes + m * kXRowStride, p.x + (int64_t)m * p.K + g * kGroup, 256,
+                 &full[s]);
+      issued = i + 1;
+    }
+    if (!ok) {  // let copies already in flight land before the CTA exits
+      for (int i = (issued > kSkStages ? issued - kSkStages : 0); i < issued; ++i)
+        mbar_wait(&full[i % kSkStages], (uint32_t)(i / kSkStages) & 1u, p.err);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int gid = lane >> 2, cq = lane & 3;
+  float acc[2][MT8][4];
+#pragma unroll
+  for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+    for (int nt = 0; nt < MT8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
+  int64_t seg_g0 = u0 % p.G;
+
+  for (int i = 0; i < n_units; ++i) {
+    const int s = i % kSkStages;
+    if (!mbar_wait(&full[s], (uint32_t)(i / kSkStages) & 1u, p.err)) return;
+    const int64_t u = u0 + i;
+    const int64_t t = u / p.G;
+    const int64_t g = u - t * p.G;
+    const uint32_t st = smem_u32(smem + s * L::kStage);
+    uint4 wq[2][2];
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(st + ((warp * 2 + rt) * 2 + h) * 512 + lane * 16);
+    const uint2 sc2 = lds64(st + kUnitBytes + (warp * 8 + gid) * 8);
+
+    float part[2][MT8][4];
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int nt = 0; nt < MT8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) part[rt][nt][e] = 0.0f;
+
+    const uint32_t xbase = st + kUnitBytes + kUnitScaleBytes + cq * 8;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t b[MT8][2];
+#pragma unroll
+      for (int nt = 0; nt < MT8; ++nt) {
+        const int tok = nt * 8 + gid;
+        if (tok < p.M) {
+          const uint2 v = lds64(xbase + tok * kXRowStride + kk * 32);
+          b[nt][0] = v.x;
+          b[nt][1] = v.y;
+        } else {
+          b[nt][0] = 0u;
+          b[nt][1] = 0u;
+        }
+      }
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        const uint4 q4 = wq[rt][kk >> 2];
+        const uint32_t word = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
+        uint32_t a[4];
+        dequant8(word, a);
+#pragma unroll
+        for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt][0], b[nt][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    const __half2 s_rt0 = *reinterpret_cast<const __half2*>(&sc2.x);
+    const __half2 s_rt1 = *reinterpret_cast<const __half2*>(&sc2.y);
+    const float sc[2][2] = {{__low2float(s_rt0), __high2float(s_rt0)}, {__low2float(s_rt1), __high2float(s_rt1)}};
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int nt = 0; nt < MT8; ++nt) {
+        acc[rt][nt][0] = fmaf(sc[rt][0], part[rt][nt][0], acc[rt][nt][0]);
+        acc[rt][nt][1] = fmaf(sc[rt][0], part[rt][nt][1], acc[rt][nt][1]);
+        acc[rt][nt][2] = fmaf(sc[rt][1], part[rt][nt][2], acc[rt][nt][2]);
+        acc[rt][nt][3] = fmaf(sc[rt][1], part[rt][nt][3], acc[rt][nt][3]);
+      }
+
+    if (g == p.G - 1 || i == n_units - 1) {  // end of this CTA's segment of tile t
+      if (seg_g0 == 0 && g == p.G - 1)
+        store_tile<MT8>(p, t, warp, lane, acc);
+      else
+        finish_split_tile<MT8>(p, cta, t, warp, lane, acc);
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int nt = 0; nt < MT8; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
+      seg_g0 = 0;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+template <int MT8>
+static cudaError_t skinny_occupancy(int* blocks_per_sm) {
+  using L = SkinnyLayout<MT8>;
+  cudaError_t e =
+      cudaFuncSetAttribute(w4a16_skinny_kernel<MT8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, w4a16_skinny_kernel<MT8>, kSkThreads,
+                                                      L::kTotal);
+}
+
+static int skinny_smem(int mt8) {
+  switch (mt8) {
+    case 1: return SkinnyLayout<1>::kTotal;
+    case 2: return SkinnyLayout<2>::kTotal;
+    case 3: return SkinnyLayout<3>::kTotal;
+    case 4: return SkinnyLayout<4>::kTotal;
+    case 5: return SkinnyLayout<5>::kTotal;
+    case 6: return SkinnyLayout<6>::kTotal;
+    case 7: return SkinnyLayout<7>::kTotal;
+    default: return SkinnyLayout<8>::kTotal;
+  }
+}
+
+static cudaError_t skinny_occupancy_dispatch(int mt8, int* nb) {
+  switch (mt8) {
+    case 1: return skinny_occupancy<1>(nb);
+    case 2: return skinny_occupancy<2>(nb);
+    case 3: return skinny_occupancy<3>(nb);
+    case 4: return skinny_occupancy<4>(nb);
+    case 5: return skinny_occupancy<5>(nb);
+    case 6: return skinny_occupancy<6>(nb);
+    case 7: return skinny_occupancy<7>(nb);
+    default: return skinny_occupancy<8>(nb);
+  }
+}
+
+cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, SkinnyPlan* plan) {
+  static int cached_nb[64][9];  // [device][mt8] blocks per SM (0 = unknown)
+  plan->mt8 = (M + 7) / 8;
+  plan->units = (N / kUnitRows) * (K / kGroup);
+  int nb = 0;
+  if (dev.device >= 0 && dev.device < 64) nb = cached_nb[dev.device][plan->mt8];
+  if (nb == 0) {
+    cudaError_t e = skinny_occupancy_dispatch(plan->mt8, &nb);
+    if (e != cudaSuccess) return e;
+    if (nb < 1) nb = 1;
+    if (nb > 4) nb = 4;
+    if (dev.device >= 0 && dev.device < 64) cached_nb[dev.device][plan->mt8] = nb;
+  }
+  int64_t ctas = (int64_t)dev.num_sms * nb;
+  if (ctas > plan->units) ctas = plan->units;
+  plan->ctas = ctas;
+  plan->counter_bytes = (size_t)(((N / kUnitRows) * kSkConsumerWarps * sizeof(int) + 255) / 256 * 256);
+  plan->partial_bytes = (size_t)ctas * 2 * kSkConsumerWarps * 2 * plan->mt8 * 32 * sizeof(float4);
+  plan->smem_bytes = (size_t)skinny_smem(plan->mt8);
+  return cudaSuccess;
+}
+
+size_t skinny_workspace_bytes(const SkinnyPlan& plan) { return plan.counter_bytes + plan.partial_bytes; }
+
+template <int MT8>
+static cudaError_t launch_skinny_t(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t stream) {
+  using L = SkinnyLayout<MT8>;
+  w4a16_skinny_kernel<MT8><<<(unsigned)plan.ctas, kSkThreads, L::kTotal, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                          void* out, void* workspace, const SkinnyPlan& plan, const DeviceInfo& dev,
+                          cudaStream_t stream) {
+  SkinnyParams p;
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.qw = static_cast<const uint8_t*>(qw_packed);
+  p.sc = static_cast<const uint8_t*>(sc_packed);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.counters = static_cast<int*>(workspace);
+  p.partials = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + plan.counter_bytes);
+  p.err = dev.err;
+  p.K = K;
+  p.N = N;
+  p.U = plan.units;
+  p.G = K / kGroup;
+  p.C = plan.ctas;
+  p.M = M;
+  switch (plan.mt8) {
+    case 1: return launch_skinny_t<1>(p, plan, stream);
+    case 2: return launch_skinny_t<2>(p, plan, stream);
+    case 3: return launch_skinny_t<3>(p, plan, stream);
+    case 4: return launch_skinny_t<4>(p, plan, stream);
+    case 5: return launch_skinny_t<5>(p, plan, stream);
+    case 6: return launch_skinny_t<6>(p, plan, stream);
+    case 7: return launch_skinny_t<7>(p, plan, stream);
+    case 8: return launch_skinny_t<8>(p, plan, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace w4a16

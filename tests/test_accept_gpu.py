@@ -1,0 +1,145 @@
+"""GPU parity of the speculative accept step against the CPU oracle.
+
+Accept lengths and emitted tokens must be bit-exact. Rows whose fp64 oracle
+margin is below 1e-6 (|u_i - alpha_i| for an evaluated draft, or the distance
+of u * S from a CDF boundary divided by S) are near-ties: they are counted,
+reported and left out of the exact comparison.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decode_verify_w4a16_gb300 as sv
+import synth
+from helpers import dev
+
+pytestmark = pytest.mark.gpu
+NEAR_TIE = 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_decode_verify_w4a16_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev())
+
+
+def _gpu_seq(p, q, d, u):
+    acc, nxt = sv.spec_accept(_t(p), _t(d), q_logits=_t(q), uniforms=_t(u))
+    torch.cuda.synchronize()
+    assert sv.check_device_status() == 0
+    return acc.cpu().numpy(), nxt.cpu().numpy()
+
+
+def _compare_seq(p, q, d, u, what):
+    acc_r, nxt_r, _, margin = oracle.spec_accept_seq(p, q, d, u)
+    acc, nxt = _gpu_seq(p, q, d, u)
+    tie = margin < NEAR_TIE
+    bad = ((acc != acc_r) | (nxt != nxt_r)) & ~tie
+    print(f"{what}: {int(tie.sum())} near-ties of {len(tie)}; mean accepted {acc_r.mean():.2f}")
+    assert not bad.any(), f"{what}: rows {np.nonzero(bad)[0][:10]} differ"
+    return acc_r, tie
+
+
+@pytest.mark.parametrize("K", [4, 8])
+def test_config_seq_full_vocab(K):
+    # batch 16, vocab 128256, target ~ N(0, 3), draft = target + N(0, 1), d ~ q
+    p, q, d, u = synth.accept_seq_case(16, K, synth.LLAMA3_VOCAB, seed=50 + K)
+    _compare_seq(p, q, d, u, f"K={K}")
+
+
+@pytest.mark.parametrize("B,K,V,seed", [(512, 4, 1000, 1), (300, 1, 2, 2), (200, 3, 5, 3), (64, 8, 50000, 4),
+                                        (128, 6, 4099, 5), (33, 2, 130000, 6)])
+def test_seq_random_cases(B, K, V, seed):
+    p, q, d, u = synth.accept_seq_case(B, K, V, seed=60 + seed, p_std=2.0)
+    acc_r, tie = _compare_seq(p, q, d, u, f"B={B} K={K} V={V}")
+    assert tie.mean() < 0.05
+
+
+def test_seq_all_accepted_when_p_equals_q():
+    B, K, V = 64, 5, 3000
+    p, q, d, u = synth.accept_seq_case(B, K, V, seed=70)
+    q = np.ascontiguousarray(p[:, :K])
+    acc, _ = _gpu_seq(p, q, d, u)
+    assert np.all(acc == K)
+    _compare_seq(p, q, d, u, "p == q")
+
+
+def test_seq_many_rejections():
+    # draft far from target: most first drafts rejected, residual draws exercised
+    B, K, V = 256, 4, 2048
+    p, q, d, u = synth.accept_seq_case(B, K, V, seed=71, noise_std=4.0)
+    acc_r, _ = _compare_seq(p, q, d, u, "noisy draft")
+    assert (acc_r == 0).mean() > 0.3
+
+
+def test_seq_bad_draft_id_reports_device_input_error():
+    B, K, V = 2, 3, 256
+    p, q, d, u = synth.accept_seq_case(B, K, V, seed=72)
+    d[1, 0] = V + 5
+    sv.spec_accept(_t(p), _t(d), q_logits=_t(q), uniforms=_t(u))
+    assert sv.check_device_status() == 5
+    assert sv.check_device_status() == 0  # cleared by the read
+
+
+# ------------------------------------------------------------------ greedy
+
+def test_greedy_tree_config():
+    # batch 16, 64-node random tree of depth <= 6, vocab 128256
+    p, d, par = synth.greedy_tree_case(16, 64, synth.LLAMA3_VOCAB, seed=80)
+    acc_r, nxt_r = oracle.greedy_tree(p, d, par)
+    acc, nxt = sv.spec_accept(_t(p), _t(d), tree_parents=_t(par))
+    torch.cuda.synchronize()
+    assert sv.check_device_status() == 0
+    assert np.array_equal(acc.cpu().numpy(), acc_r) and np.array_equal(nxt.cpu().numpy(), nxt_r)
+    assert acc_r.max() >= 2
+
+
+@pytest.mark.parametrize("K,V", [(4, 128256), (8, 128256), (1, 7), (16, 3001)])
+def test_greedy_chain(K, V):
+    p, d = synth.greedy_chain_case(16, K, V, seed=81 + K)
+    acc_r, nxt_r = oracle.greedy_chain(p, d)
+    acc, nxt = sv.spec_accept(_t(p), _t(d))
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), acc_r) and np.array_equal(nxt.cpu().numpy(), nxt_r)
+
+
+def test_greedy_ties_across_chunks_take_smallest_index():
+    B, K, V = 4, 2, 128256
+    p = np.zeros((B, K + 1, V), dtype=np.float32)
+    # equal maxima far apart (different chunks of the reduction)
+    p[:, :, [70000, 5, 128255, 64000]] = 3.0
+    p[1, 0, 5] = 2.0
+    d = np.array([[5, 5], [64000, 5], [5, 7], [6, 5]], dtype=np.int32)
+    acc_r, nxt_r = oracle.greedy_chain(p, d)
+    acc, nxt = sv.spec_accept(_t(p), _t(d))
+    torch.cuda.synchronize()
+    assert acc_r.tolist() == [2, 2, 1, 0]
+    assert np.array_equal(acc.cpu().numpy(), acc_r) and np.array_equal(nxt.cpu().numpy(), nxt_r)
+
+
+def test_greedy_tree_small_random_trees():
+    g = synth.rng(82)
+    for trial in range(20):
+        n = int(g.integers(1, 40))
+        B, V = 8, int(g.integers(2, 300))
+        par = np.stack([synth.random_tree_parents(n, int(g.integers(1, 7)), g) for _ in range(B)])
+        p = g.integers(-2, 3, size=(B, n, V)).astype(np.float32)
+        d = g.integers(0, V, size=(B, n)).astype(np.int32)
+        acc_r, nxt_r = oracle.greedy_tree(p, d, par)
+        acc, nxt = sv.spec_accept(_t(p), _t(d), tree_parents=_t(par))
+        torch.cuda.synchronize()
+        assert np.array_equal(acc.cpu().numpy(), acc_r) and np.array_equal(nxt.cpu().numpy(), nxt_r), trial
+
+
+def test_greedy_tree_bad_parent_reports_device_input_error():
+    p, d, par = synth.greedy_tree_case(2, 8, 100, seed=83)
+    par[1, 5] = 6  # parent after child
+    acc, _ = sv.spec_accept(_t(p), _t(d), tree_parents=_t(par))
+    assert sv.check_device_status() == 5
+    assert acc.cpu().numpy()[1] == 0

@@ -1,0 +1,113 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports
+every symbol the header declares, and rejects bad arguments before touching
+the device; the stream-K work split covers every unit exactly once."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+from speculative_decode_verify_w4a16_gb300 import _lib
+from speculative_decode_verify_w4a16_gb300 import build as sv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    sv_build.build()
+    return _lib.lib()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "w4a16sv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_0-9]+)\s*\(", text)) - {"if", "sizeof"})
+
+
+def test_header_symbols_exported(L):
+    names = _header_functions()
+    assert "w4a16_linear" in names and "spec_accept" in names
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in _lib.SIGNATURES, f"binding lacks {n}"
+
+
+def test_no_torch_types_in_header():
+    text = open(os.path.join(ROOT, "include", "w4a16sv.h")).read()
+    for bad in ("torch", "at::", "Tensor", "c10"):
+        assert bad not in text
+
+
+def test_status_strings(L):
+    for code, name in [(0, "W4A16_OK"), (1, "W4A16_ERR_INVALID_ARG"), (2, "W4A16_ERR_UNSUPPORTED"),
+                       (4, "W4A16_ERR_DEVICE_TIMEOUT"), (6, "W4A16_ERR_WORKSPACE")]:
+        assert _lib.status_string(code) == name
+    assert _lib.status_string(99) == "W4A16_ERR_UNKNOWN"
+    assert L.w4a16_abi_version() == 1
+
+
+def test_size_functions(L):
+    assert L.w4a16_packed_weight_bytes(8192, 8192) == 8192 * 8192 // 2
+    assert L.w4a16_packed_scale_bytes(8192, 8192) == 8192 * 8192 // 64
+    assert L.w4a16_packed_weight_bytes(100, 8192) == 0  # N not a multiple of 128
+    assert L.w4a16_packed_weight_bytes(128, 100) == 0
+    assert L.spec_accept_workspace_bytes(16, 4, 128256) > 0
+    assert L.spec_accept_workspace_bytes(0, 4, 128256) == 0
+    assert L.spec_accept_workspace_bytes(16, 2000, 128256) == 0
+    assert L.spec_accept_workspace_bytes(16, 4, 1) == 0
+
+
+def test_linear_rejects_bad_arguments_before_any_launch(L):
+    p = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails validation
+    ws = ctypes.c_void_p(0x20000)
+    args = lambda x, M, K, N, ws_, nbytes: L.w4a16_linear(x, M, K, p, p, N, p, ws_, nbytes, None)
+    assert args(None, 4, 2048, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG
+    assert args(p, 0, 2048, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG
+    assert args(p, 4, 2000, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG
+    assert args(p, 4, 2048, 2000, ws, 1 << 20) == _lib.ERR_INVALID_ARG
+    assert args(p, 65, 2048, 2048, ws, 1 << 20) == _lib.ERR_UNSUPPORTED
+    assert args(p, 4, 512, 2048, ws, 1 << 20) == _lib.ERR_UNSUPPORTED
+    assert args(ctypes.c_void_p(0x10008), 4, 2048, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG  # misaligned x
+    assert args(p, 4, 2048, 2048, None, 1 << 20) == _lib.ERR_WORKSPACE
+    assert args(p, 4, 2048, 2048, ctypes.c_void_p(0x20010), 1 << 20) == _lib.ERR_WORKSPACE
+
+
+def test_accept_rejects_bad_arguments_before_any_launch(L):
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    f = L.spec_accept
+    assert f(None, None, p, None, None, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
+    assert f(p, p, p, p, p, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_UNSUPPORTED  # stochastic tree
+    assert f(p, p, p, None, None, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # no uniforms
+    assert f(p, None, p, None, None, 0, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
+    assert f(p, None, p, None, None, 1, 0, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
+    assert f(p, None, p, None, None, 1, 4, 1, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(0x10004), None, p, None, None, 1, 4, 100, p, p, ws, 1 << 20,
+             None) == _lib.ERR_INVALID_ARG  # V % 4 == 0 wants 16-byte rows
+    assert f(p, None, p, None, None, 1, 4, 100, p, p, None, 1 << 20, None) == _lib.ERR_WORKSPACE
+    assert f(p, None, p, None, None, 1, 4, 100, p, p, ws, 16, None) == _lib.ERR_WORKSPACE
+
+
+def test_format_calls_reject_bad_arguments(L):
+    p = ctypes.c_void_p(0x10000)
+    assert L.w4a16_quantize(None, 128, 128, p, p, None) == _lib.ERR_INVALID_ARG
+    assert L.w4a16_quantize(p, 100, 128, p, p, None) == _lib.ERR_INVALID_ARG
+    assert L.w4a16_prepack(p, p, 128, 128, ctypes.c_void_p(0x10004), p, None) == _lib.ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("U,C", [(1, 1), (7, 3), (256, 256), (1024, 456), (4096, 152), (64128, 456),
+                                 (14336, 304), (33, 32)])
+def test_streamk_split_covers_each_unit_once(L, U, C):
+    begins = [L.w4a16_streamk_unit_begin(U, C, c) for c in range(C + 1)]
+    assert begins[0] == 0 and begins[-1] == U
+    assert all(begins[c + 1] > begins[c] for c in range(C))  # every CTA gets at least one unit
+    sizes = [begins[c + 1] - begins[c] for c in range(C)]
+    assert max(sizes) - min(sizes) <= 1
+    step = max(1, U // 2000)
+    for u in range(0, U, step):
+        c = L.w4a16_streamk_owner(U, C, u)
+        assert begins[c] <= u < begins[c + 1]
+    assert L.w4a16_streamk_owner(U, C, U) == -1
+    assert L.w4a16_streamk_unit_begin(U, U + 1, 0) == -1
