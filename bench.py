@@ -122,6 +122,37 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ ours
 
+def _event(torch):
+    """Timing event that is recorded as a node when captured in a CUDA graph."""
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # older torch without external events
+        return torch.cuda.Event(enable_timing=True)
+
+
+def run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_out, acc_ws, tree_in, tree_out,
+             acc_ws2):
+    """One kind of launch only, eagerly, for profiling (no JSON contract line)."""
+    if args.only == "linear":
+        li = STEP_MS.index(args.m) if args.m in STEP_MS else 0
+        K, N = dict((n, (k, nn)) for n, k, nn in SHAPES)[args.shape]
+        x = torch.randn((args.m, K), device=stream.device).to(torch.bfloat16)
+        out = torch.empty((args.m, N), dtype=torch.bfloat16, device=stream.device)
+        ws = torch.zeros(sv.linear_workspace_bytes(args.m, N, K), dtype=torch.uint8, device=stream.device)
+        fn = lambda: sv.linear(x, layers[li][args.shape], out=out, ws=ws)
+    elif args.only == "accept":
+        fn = lambda: sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3],
+                                    accepted_len=acc_out[0], next_token=acc_out[1], ws=acc_ws)
+    else:
+        fn = lambda: sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
+                                    next_token=tree_out[1], ws=acc_ws2)
+    for _ in range(args.warmup + args.steps):
+        fn()
+        torch.cuda.synchronize()
+    assert sv.check_device_status() == 0
+    print(json.dumps({"only": args.only, "shape": args.shape, "M": args.m, "launches": args.warmup + args.steps}))
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -188,31 +219,43 @@ def run_ours(args):
     def step(evs=None):
         for j, (M, name, K, N, li) in enumerate(calls):
             if evs is not None:
-                evs[j][0].record(stream)
+                evs[j][0].record()
             sv.linear(xs[(M, name)], layers[li][name], out=outs[(M, name)], ws=wss[M])
             if evs is not None:
-                evs[j][1].record(stream)
+                evs[j][1].record()
         if evs is not None:
-            evs[len(calls)][0].record(stream)
+            evs[len(calls)][0].record()
         sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3], accepted_len=acc_out[0],
                        next_token=acc_out[1], ws=acc_ws)
         if evs is not None:
-            evs[len(calls)][1].record(stream)
-            evs[len(calls) + 1][0].record(stream)
+            evs[len(calls)][1].record()
+            evs[len(calls) + 1][0].record()
         sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
                        next_token=tree_out[1], ws=acc_ws2)
         if evs is not None:
-            evs[len(calls) + 1][1].record(stream)
+            evs[len(calls) + 1][1].record()
 
+    if args.only:
+        return run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_out, acc_ws, tree_in,
+                        tree_out, acc_ws2)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert sv.check_device_status() == 0
 
-    # ---- timed region
+    # The step is captured once as a CUDA graph so that the device timeline is
+    # not paced by Python launch overhead; per-call durations come from event
+    # record nodes inside the graph.
     nseg = len(calls) + 2
-    all_evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nseg)]
-               for _ in range(args.steps)]
+    evs = [(_event(torch), _event(torch)) for _ in range(nseg)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(evs)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -221,7 +264,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0.record(stream)
     for s in range(args.steps):
-        step(all_evs[s])
+        graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -233,9 +276,13 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
     assert sv.check_device_status() == 0
-    seg_us = np.array([[all_evs[s][j][0].elapsed_time(all_evs[s][j][1]) * 1e3 for j in range(nseg)]
-                       for s in range(args.steps)])
-    seg_mean = seg_us.mean(axis=0)
+    # per-call device durations: the same graph, one replay at a time
+    seg = []
+    for s in range(args.steps):
+        graph.replay()
+        torch.cuda.synchronize()
+        seg.append([evs[j][0].elapsed_time(evs[j][1]) * 1e3 for j in range(nseg)])
+    seg_mean = np.array(seg).mean(axis=0)
     pk = peaks()
 
     sweep = []
@@ -283,15 +330,21 @@ def run_ours(args):
                        + linear_bytes(M, LM_HEAD[2], LM_HEAD[1]) for M in STEP_MS}
         for M in STEP_MS:
             forward(M)
-            forward(M)
+            torch.cuda.synchronize()
+            gm = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gm):
+                forward(M)
+            gm.replay()
+            gm.replay()
             torch.cuda.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 3
+            reps = 5
             e0.record(stream)
             for _ in range(reps):
-                forward(M)
+                gm.replay()
             e1.record(stream)
             torch.cuda.synchronize()
+            del gm
             us = e0.elapsed_time(e1) * 1e3 / reps
             gbs = stack_bytes[M] / (us * 1e-6) / 1e9
             stack[str(M)] = {"us": round(us, 1), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
@@ -461,6 +514,10 @@ def main():
     ap.add_argument("--no-stack", dest="stack", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-cols", type=int, default=64)
+    ap.add_argument("--only", choices=["linear", "accept", "tree"], default=None,
+                    help="profiling mode: run one kind of launch eagerly, print no contract line")
+    ap.add_argument("--shape", default="gate_up", choices=[n for n, _, _ in SHAPES])
+    ap.add_argument("--m", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -92,12 +92,14 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
  *
  *   x            device, bf16 [M][K] row-major, 16-byte aligned
  *   M            1 .. 64
- *   K, N         multiples of 128, K >= 1024
+ *   K, N         multiples of 128, K >= 1024, N <= 2^21
  *   qweight_packed, scales_packed   from w4a16_prepack (device)
  *   out          device, bf16 [M][N] row-major
  *   workspace    device scratch of at least w4a16_linear_workspace_bytes(M,N,K)
- *                bytes, 256-byte aligned, ZERO-FILLED before its first use;
- *                every call leaves it zeroed again for the next call. After a
+ *                bytes, 256-byte aligned. Its first 256 KiB hold completion
+ *                counters: ZERO-FILL the workspace before its first use; every
+ *                call leaves the counters zero again, so one workspace serves
+ *                any later linear or accept call. After
  *                W4A16_ERR_DEVICE_TIMEOUT, zero it again before reuse. Calls
  *                that share a workspace must not overlap in time.
  * Returns W4A16_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED before launching.
@@ -141,7 +143,8 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
  * in the device error word (the row then reports accepted_len = 0).
  * All pointers are device pointers; p/q rows must be 16-byte aligned when
  * V % 4 == 0. workspace: device scratch of spec_accept_workspace_bytes(B,n,V)
- * bytes, 256-byte aligned, zero-filled before first use (left zeroed).
+ * bytes, 256-byte aligned, with the same zeroed 256 KiB counter region at its
+ * start as the linear's workspace (either can serve both).
  * Limits: 1 <= B <= 65535, 1 <= n <= 1024, 2 <= V < 2^31.
  * ---------------------------------------------------------------------- */
 size_t spec_accept_workspace_bytes(int B, int n, int V);

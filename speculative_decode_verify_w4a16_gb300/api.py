@@ -119,9 +119,8 @@ def linear(x: torch.Tensor, w: PackedWeight, out: Optional[torch.Tensor] = None,
     if out is None:
         out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
     _need(out, "out", torch.bfloat16, (M, w.N))
-    need = linear_workspace_bytes(M, w.N, K)
     if ws is None:
-        ws = workspace(need, x.device, "linear")
+        ws = workspace(linear_workspace_bytes(M, w.N, K), x.device, "linear")
     check(lib().w4a16_linear(_ptr(x), M, K, _ptr(w.qweight), _ptr(w.scales), w.N, _ptr(out), _ptr(ws),
                              ws.numel(), _stream(stream)), "w4a16_linear")
     return out
@@ -157,9 +156,8 @@ def spec_accept(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: Optio
         accepted_len = torch.empty(B, dtype=torch.int32, device=p_logits.device)
     if next_token is None:
         next_token = torch.empty(B, dtype=torch.int32, device=p_logits.device)
-    need = accept_workspace_bytes(B, n, V)
     if ws is None:
-        ws = workspace(need, p_logits.device, "accept")
+        ws = workspace(accept_workspace_bytes(B, n, V), p_logits.device, "accept")
     check(lib().spec_accept(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), _ptr(tree_parents), _ptr(uniforms),
                             B, n, V, _ptr(accepted_len), _ptr(next_token), _ptr(ws), ws.numel(),
                             _stream(stream)), "spec_accept")

@@ -268,21 +268,27 @@ __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
   // ---- the last block of batch row b draws the next token
   __shared__ double sh_t, sh_before;
   __shared__ int sh_chunk, sh_usep;
+  __shared__ ChunkSum sh_cs[64];  // gridDim.x <= 64
+  for (int c = threadIdx.x; c < (int)gridDim.x; c += kAccThreads) {
+    const ChunkSum* cs = csum + (int64_t)b * gridDim.x + c;
+    sh_cs[c].r = __ldcg(&cs->r);
+    sh_cs[c].p = __ldcg(&cs->p);
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    const ChunkSum* cs = csum + (int64_t)b * gridDim.x;
     double S = 0.0;
-    for (int c = 0; c < (int)gridDim.x; ++c) S += __ldcg(&cs[c].r);
+    for (int c = 0; c < (int)gridDim.x; ++c) S += sh_cs[c].r;
     int usep = 0;
     if (f.qrow && S == 0.0) {  // corrected distribution is all zero: draw from P_r
       usep = 1;
       S = 0.0;
-      for (int c = 0; c < (int)gridDim.x; ++c) S += __ldcg(&cs[c].p);
+      for (int c = 0; c < (int)gridDim.x; ++c) S += sh_cs[c].p;
     }
     const double t = (double)u[(int64_t)b * (n + 1) + n] * S;
     double cum = 0.0;
     int cstar = -1;
     for (int c = 0; c < (int)gridDim.x; ++c) {
-      const double v = usep ? __ldcg(&cs[c].p) : __ldcg(&cs[c].r);
+      const double v = usep ? sh_cs[c].p : sh_cs[c].r;
       if (cum + v > t) {
         cstar = c;
         break;
@@ -508,11 +514,9 @@ AcceptPlan accept_plan(int B, int n, int V) {
   const size_t stats_bytes = align256((size_t)rows * ch * (sizeof(RowStat) > sizeof(ArgPart) ? sizeof(RowStat)
                                                                                               : sizeof(ArgPart)));
   const size_t csum_bytes = align256((size_t)B * ch2 * sizeof(ChunkSum));
-  const size_t cnt_bytes = align256((size_t)B * sizeof(int));
-  pl.stats_off = 0;
-  pl.csum_off = stats_bytes;
-  pl.cnt_off = stats_bytes + csum_bytes;
-  pl.total = stats_bytes + csum_bytes + cnt_bytes;
+  pl.stats_off = kCounterRegionBytes;
+  pl.csum_off = pl.stats_off + stats_bytes;
+  pl.total = pl.csum_off + csum_bytes;
   return pl;
 }
 
@@ -522,7 +526,7 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   uint8_t* w = static_cast<uint8_t*>(ws);
   RowStat* stats = reinterpret_cast<RowStat*>(w + pl.stats_off);
   ChunkSum* csum = reinterpret_cast<ChunkSum*>(w + pl.csum_off);
-  int* cnt = reinterpret_cast<int*>(w + pl.cnt_off);
+  int* cnt = reinterpret_cast<int*>(w);
   const dim3 g1(pl.ch, B * (2 * n + 1));
   if (V % 4 == 0)
     accept_stats_kernel<true><<<g1, kAccThreads, 0, stream>>>(p, q, n, V, pl.chunk, stats);
@@ -541,7 +545,7 @@ cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t
                                  cudaStream_t stream) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   ArgPart* parts = reinterpret_cast<ArgPart*>(w + pl.stats_off);
-  int* cnt = reinterpret_cast<int*>(w + pl.cnt_off);
+  int* cnt = reinterpret_cast<int*>(w);
   const int rows_per_b = parents ? n : n + 1;
   const dim3 g(pl.ch, B * rows_per_b);
   if (V % 4 == 0)

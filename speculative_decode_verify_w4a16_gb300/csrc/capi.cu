@@ -45,7 +45,7 @@ using namespace w4a16;
 static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 static inline bool valid_nk(int64_t N, int64_t K) {
-  return N > 0 && K > 0 && N % kUnitRows == 0 && K % kGroup == 0 && N <= (int64_t(1) << 31) &&
+  return N > 0 && K > 0 && N % kUnitRows == 0 && K % kGroup == 0 && N <= (int64_t(1) << 21) &&
          K <= (int64_t(1) << 24);
 }
 

@@ -7,6 +7,12 @@
 
 namespace w4a16 {
 
+// Every workspace starts with this many bytes of zero-initialised completion
+// counters (int32), shared by the linear and the accept step so that one
+// workspace can serve any sequence of calls; each call leaves them zero.
+constexpr size_t kCounterRegionBytes = 256 * 1024;
+constexpr int64_t kMaxCounters = (int64_t)(kCounterRegionBytes / sizeof(int));
+
 struct DeviceInfo {
   int device = -1;
   int num_sms = 0;
@@ -45,7 +51,7 @@ struct AcceptPlan {
   int chunk = 0;      // elements per chunk (multiple of 4)
   int ch2 = 0;        // chunks per batch row (residual pass)
   int chunk2 = 0;
-  size_t stats_off = 0, csum_off = 0, cnt_off = 0, total = 0;
+  size_t stats_off = 0, csum_off = 0, total = 0;  // counters at offset 0
 };
 AcceptPlan accept_plan(int B, int n, int V);
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,

@@ -41,6 +41,13 @@ struct SkinnyLayout {
   static_assert(kStage % 16 == 0, "stage alignment");
 };
 
+// Shift amounts enter as runtime multipliers (w * 2^(32-s) >> 32 == w >> s) so
+// the three right shifts run on the integer multiply path instead of the
+// logic pipe, which the four mask-and-OR operations already keep busy.
+struct DequantConsts {
+  uint32_t m4, m8, m12;
+};
+
 struct SkinnyParams {
   const __nv_bfloat16* x;
   const uint8_t* qw;
@@ -51,6 +58,7 @@ struct SkinnyParams {
   unsigned* err;
   int64_t K, N, U, G, C;
   int M;
+  DequantConsts dq;
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -60,20 +68,33 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 8 offset-binary nibbles -> four bf16x2 registers of exact signed codes.
-__device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t magic = 0x43004300u;                          // bf16x2 (128, 128)
-  const __nv_bfloat162 bias = __halves2bfloat162(__ushort_as_bfloat16(0x4308), __ushort_as_bfloat16(0x4308));  // 136
-  uint32_t t[4];
-  t[0] = (w & 0x000F000Fu) | magic;
-  t[1] = ((w >> 4) & 0x000F000Fu) | magic;
-  t[2] = ((w >> 8) & 0x000F000Fu) | magic;
-  t[3] = ((w >> 12) & 0x000F000Fu) | magic;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 v = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&t[i]), bias);
-    a[i] = *reinterpret_cast<uint32_t*>(&v);
-  }
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
+}
+
+__device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 8 offset-binary nibbles -> four bf16x2 registers of exact signed codes:
+// (nibble | 0x4300) is the bf16 value 128 + c, and (128 + c) * 1 - 136 = c - 8.
+__device__ __forceinline__ void dequant8(uint32_t w, const DequantConsts& k, uint32_t (&a)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;
+  const uint32_t one = 0x3F803F80u, neg136 = 0xC308C308u;
+  a[0] = fma_bf16x2(lop3_and_or(w, mask, magic), one, neg136);
+  a[1] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m4), mask, magic), one, neg136);
+  a[2] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m8), mask, magic), one, neg136);
+  a[3] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m12), mask, magic), one, neg136);
 }
 
 template <int MT8>
@@ -130,19 +151,36 @@ __device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t,
     for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sum[rt][nt][e] = 0.0f;
-  for (int64_t cc = cf; cc <= cl; ++cc) {
-    const int64_t tf = streamk_begin(p.U, p.C, cc) / p.G;
-    const float4* sl = partial_slot<MT8>(p, cc, t == tf ? 0 : 1, warp);
+  // contributors are read RB at a time (loads in flight together), summed in CTA order
+  constexpr int RB = MT8 <= 2 ? 4 : (MT8 <= 4 ? 2 : 1);
+  for (int64_t c0 = cf; c0 <= cl; c0 += RB) {
+    float4 v[RB][2][MT8];
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
+    for (int j = 0; j < RB; ++j) {
+      const int64_t cc = c0 + j;
+      if (cc <= cl) {
+        const int64_t tf = streamk_begin(p.U, p.C, cc) / p.G;
+        const float4* sl = partial_slot<MT8>(p, cc, t == tf ? 0 : 1, warp);
 #pragma unroll
-      for (int nt = 0; nt < MT8; ++nt) {
-        const float4 v = __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]);
-        sum[rt][nt][0] += v.x;
-        sum[rt][nt][1] += v.y;
-        sum[rt][nt][2] += v.z;
-        sum[rt][nt][3] += v.w;
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int nt = 0; nt < MT8; ++nt) v[j][rt][nt] = __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]);
       }
+    }
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      if (c0 + j <= cl) {
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int nt = 0; nt < MT8; ++nt) {
+            sum[rt][nt][0] += v[j][rt][nt].x;
+            sum[rt][nt][1] += v[j][rt][nt].y;
+            sum[rt][nt][2] += v[j][rt][nt].z;
+            sum[rt][nt][3] += v[j][rt][nt].w;
+          }
+      }
+    }
   }
   store_tile<MT8>(p, t, warp, lane, sum);
   if (lane == 0) p.counters[t * kSkConsumerWarps + warp] = 0;
@@ -166,6 +204,16 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
     }
     fence_mbarrier_init();
   }
+  // token rows M .. 8*MT8-1 of every stage are never copied: zero them once
+  {
+    constexpr int kChunks = kXRowStride / 16;
+    const int zrows = MT8 * 8 - p.M;
+    for (int idx = threadIdx.x; idx < kSkStages * zrows * kChunks; idx += blockDim.x) {
+      const int s = idx / (zrows * kChunks), r = (idx / kChunks) % zrows, c16 = idx % kChunks;
+      *reinterpret_cast<uint4*>(smem + s * L::kStage + kUnitBytes + kUnitScaleBytes + (p.M + r) * kXRowStride +
+                                c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   __syncthreads();
 
   if (warp == kSkConsumerWarps) {
@@ -175,7 +223,8 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
     const uint32_t tx = (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256);
     int issued = 0;
     bool ok = true;
-    for (int i = 0; i < n_units; ++i) {
+    int64_t g = u0 % p.G;
+    for (int i = 0; i < n_units; ++i, g = (g + 1 == p.G) ? 0 : g + 1) {
       const int s = i % kSkStages;
       const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
       if (i >= kSkStages && !mbar_wait(&empty[s], ph ^ 1u, p.err)) {
@@ -183,7 +232,6 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
         break;
       }
       const int64_t u = u0 + i;
-      const int64_t g = u % p.G;
       uint8_t* st = smem + s * L::kStage;
       mbar_arrive_expect_tx(&full[s], tx);
       bulk_g2s_hint(st, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
@@ -209,20 +257,20 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
     for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
-  int64_t seg_g0 = u0 % p.G;
+  int64_t t = u0 / p.G;
+  int64_t g = u0 - t * p.G;
+  int64_t seg_g0 = g;
 
   for (int i = 0; i < n_units; ++i) {
     const int s = i % kSkStages;
     if (!mbar_wait(&full[s], (uint32_t)(i / kSkStages) & 1u, p.err)) return;
-    const int64_t u = u0 + i;
-    const int64_t t = u / p.G;
-    const int64_t g = u - t * p.G;
     const uint32_t st = smem_u32(smem + s * L::kStage);
+    const uint32_t wb = st + warp * 2048 + lane * 16;
     uint4 wq[2][2];
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(st + ((warp * 2 + rt) * 2 + h) * 512 + lane * 16);
+      for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(wb + (rt * 2 + h) * 512);
     const uint2 sc2 = lds64(st + kUnitBytes + (warp * 8 + gid) * 8);
 
     float part[2][MT8][4];
@@ -233,30 +281,20 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
 #pragma unroll
         for (int e = 0; e < 4; ++e) part[rt][nt][e] = 0.0f;
 
-    const uint32_t xbase = st + kUnitBytes + kUnitScaleBytes + cq * 8;
+    const uint32_t xb = st + kUnitBytes + kUnitScaleBytes + gid * kXRowStride + cq * 8;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
-      uint32_t b[MT8][2];
+      uint2 b[MT8];
 #pragma unroll
-      for (int nt = 0; nt < MT8; ++nt) {
-        const int tok = nt * 8 + gid;
-        if (tok < p.M) {
-          const uint2 v = lds64(xbase + tok * kXRowStride + kk * 32);
-          b[nt][0] = v.x;
-          b[nt][1] = v.y;
-        } else {
-          b[nt][0] = 0u;
-          b[nt][1] = 0u;
-        }
-      }
+      for (int nt = 0; nt < MT8; ++nt) b[nt] = lds64(xb + nt * 8 * kXRowStride + kk * 32);
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt) {
         const uint4 q4 = wq[rt][kk >> 2];
         const uint32_t word = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
         uint32_t a[4];
-        dequant8(word, a);
+        dequant8(word, p.dq, a);
 #pragma unroll
-        for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt][0], b[nt][1]);
+        for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt].x, b[nt].y);
       }
     }
     __syncwarp();
@@ -287,6 +325,10 @@ __global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyPa
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
       seg_g0 = 0;
+    }
+    if (++g == p.G) {
+      g = 0;
+      ++t;
     }
   }
 }
@@ -345,7 +387,7 @@ cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, Skin
   int64_t ctas = (int64_t)dev.num_sms * nb;
   if (ctas > plan->units) ctas = plan->units;
   plan->ctas = ctas;
-  plan->counter_bytes = (size_t)(((N / kUnitRows) * kSkConsumerWarps * sizeof(int) + 255) / 256 * 256);
+  plan->counter_bytes = kCounterRegionBytes;  // (N/128)*4 counters at its start
   plan->partial_bytes = (size_t)ctas * 2 * kSkConsumerWarps * 2 * plan->mt8 * 32 * sizeof(float4);
   plan->smem_bytes = (size_t)skinny_smem(plan->mt8);
   return cudaSuccess;
@@ -377,6 +419,9 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
   p.G = K / kGroup;
   p.C = plan.ctas;
   p.M = M;
+  p.dq.m4 = 1u << 28;
+  p.dq.m8 = 1u << 24;
+  p.dq.m12 = 1u << 20;
   switch (plan.mt8) {
     case 1: return launch_skinny_t<1>(p, plan, stream);
     case 2: return launch_skinny_t<2>(p, plan, stream);
