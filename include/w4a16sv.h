@@ -154,6 +154,29 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free W4A16 linear. The pages have no counterpart to this call:
+ * it exists for callers that cannot allocate device memory where they call
+ * the linear — a plugin slot that passes only inputs and outputs, a runtime
+ * that owns every device allocation, a hot path that must never reach
+ * cudaMalloc. It computes exactly what w4a16_linear computes (same argument
+ * rules, same kernels) but takes no workspace: its scratch is one static
+ * device array of w4a16_linear_noalloc_scratch_bytes() bytes (12 MiB) that
+ * every GPU this library is used on holds until the process exits. It calls
+ * no cudaMalloc, cudaFree or allocating library routine.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Each call clears the completion counters it needs (a cudaMemsetAsync on
+ *    `stream`) before its kernel.
+ *  - All calls share the array: calls that overlap on the GPU (other streams,
+ *    other host threads) race and give wrong results. Serialise them.
+ *  - A shape whose scratch would exceed the array returns W4A16_ERR_WORKSPACE.
+ * ---------------------------------------------------------------------- */
+size_t w4a16_linear_noalloc_scratch_bytes(void);
+w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, const void* qweight_packed,
+                                  const void* scales_packed, int64_t N, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Device status: synchronises `stream`, reads and clears the device error
  * word of the current device. W4A16_OK, W4A16_ERR_DEVICE_TIMEOUT,
  * W4A16_ERR_DEVICE_INPUT or W4A16_ERR_CUDA.

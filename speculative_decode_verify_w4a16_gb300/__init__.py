@@ -6,12 +6,14 @@ torch-tensor binding:
   spec_accept                                  -- the speculative accept step
   check_device_status                          -- device error word
 """
-from .api import (PackedWeight, accept_workspace_bytes, check_device_status, linear, linear_workspace_bytes,
+from .api import (PackedWeight, accept_workspace_bytes, check_device_status, linear, linear_noalloc,
+                  linear_workspace_bytes,
                   packed_scale_bytes, packed_weight_bytes, prepack, quantize, spec_accept, workspace)
 from ._lib import LIB_PATH, W4A16Error, lib, status_string
 
 __all__ = [
-    "PackedWeight", "accept_workspace_bytes", "check_device_status", "linear", "linear_workspace_bytes",
+    "PackedWeight", "accept_workspace_bytes", "check_device_status", "linear", "linear_noalloc",
+    "linear_workspace_bytes",
     "packed_scale_bytes", "packed_weight_bytes", "prepack", "quantize", "spec_accept", "workspace",
     "LIB_PATH", "W4A16Error", "lib", "status_string",
 ]

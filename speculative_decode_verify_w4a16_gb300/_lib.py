@@ -41,6 +41,8 @@ SIGNATURES = {
     "w4a16_check_device_status": (_i32, [_vp]),
     "w4a16_streamk_unit_begin": (_i64, [_i64, _i64, _i64]),
     "w4a16_streamk_owner": (_i64, [_i64, _i64, _i64]),
+    "w4a16_linear_noalloc_scratch_bytes": (_sz, []),
+    "w4a16_linear_noalloc": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp]),
 }
 
 

@@ -126,6 +126,21 @@ def linear(x: torch.Tensor, w: PackedWeight, out: Optional[torch.Tensor] = None,
     return out
 
 
+def linear_noalloc(x: torch.Tensor, w: PackedWeight, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """linear() without a workspace: the library uses its static device scratch
+    (see w4a16_linear_noalloc in the header for the rules on sharing it)."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if K != w.K:
+        raise ValueError(f"x has K={K}, weight has K={w.K}")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, (M, w.N))
+    check(lib().w4a16_linear_noalloc(_ptr(x), M, K, _ptr(w.qweight), _ptr(w.scales), w.N, _ptr(out),
+                                     _stream(stream)), "w4a16_linear_noalloc")
+    return out
+
+
 # ------------------------------------------------------------------ accept
 
 def accept_workspace_bytes(B: int, n: int, V: int) -> int:
