@@ -92,7 +92,7 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
  *
  *   x            device, bf16 [M][K] row-major, 16-byte aligned
  *   M            1 .. 64
- *   K, N         multiples of 128, K >= 1024, N <= 2^21
+ *   K, N         multiples of 128, K >= 1024, N <= 2^20
  *   qweight_packed, scales_packed   from w4a16_prepack (device)
  *   out          device, bf16 [M][N] row-major
  *   workspace    device scratch of at least w4a16_linear_workspace_bytes(M,N,K)
@@ -160,7 +160,7 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
  * that owns every device allocation, a hot path that must never reach
  * cudaMalloc. It computes exactly what w4a16_linear computes (same argument
  * rules, same kernels) but takes no workspace: its scratch is one static
- * device array of w4a16_linear_noalloc_scratch_bytes() bytes (12 MiB) that
+ * device array of w4a16_linear_noalloc_scratch_bytes() bytes (24 MiB) that
  * every GPU this library is used on holds until the process exits. It calls
  * no cudaMalloc, cudaFree or allocating library routine.
  *  - The first call on a device looks up the array's device address

@@ -38,6 +38,26 @@ cudaError_t device_info(DeviceInfo* out) {
   return cudaSuccess;
 }
 
+cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan) {
+  plan->use_tc = M >= kTcMinM;
+  cudaError_t e;
+  if (plan->use_tc) {
+    e = tc_plan(M, N, K, dev, &plan->tc);
+    plan->workspace_bytes = tc_workspace_bytes(plan->tc);
+  } else {
+    e = skinny_plan(M, N, K, dev, &plan->sk);
+    plan->workspace_bytes = skinny_workspace_bytes(plan->sk);
+  }
+  return e;
+}
+
+cudaError_t launch_linear(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                          void* out, void* workspace, const LinearPlan& plan, const DeviceInfo& dev,
+                          cudaStream_t stream) {
+  if (plan.use_tc) return launch_tc(x, M, K, qw_packed, sc_packed, N, out, workspace, plan.tc, dev, stream);
+  return launch_skinny(x, M, K, qw_packed, sc_packed, N, out, workspace, plan.sk, dev, stream);
+}
+
 }  // namespace w4a16
 
 using namespace w4a16;
@@ -45,7 +65,7 @@ using namespace w4a16;
 static inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 static inline bool valid_nk(int64_t N, int64_t K) {
-  return N > 0 && K > 0 && N % kUnitRows == 0 && K % kGroup == 0 && N <= (int64_t(1) << 21) &&
+  return N > 0 && K > 0 && N % kUnitRows == 0 && K % kGroup == 0 && N <= (int64_t(1) << 20) &&
          K <= (int64_t(1) << 24);
 }
 
@@ -106,9 +126,9 @@ size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K) {
   if (!linear_shape_ok(M, N, K)) return 0;
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return 0;
-  SkinnyPlan plan;
-  if (skinny_plan(M, N, K, dev, &plan) != cudaSuccess) return 0;
-  return skinny_workspace_bytes(plan);
+  LinearPlan plan;
+  if (linear_plan(M, N, K, dev, &plan) != cudaSuccess) return 0;
+  return plan.workspace_bytes;
 }
 
 w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_packed, const void* scales_packed,
@@ -121,10 +141,10 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
   if (!workspace || !aligned(workspace, 256)) return W4A16_ERR_WORKSPACE;
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
-  SkinnyPlan plan;
-  if (skinny_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
-  if (workspace_bytes < skinny_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
-  return launch_skinny(x, M, K, qweight_packed, scales_packed, N, out, workspace, plan, dev,
+  LinearPlan plan;
+  if (linear_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (workspace_bytes < plan.workspace_bytes) return W4A16_ERR_WORKSPACE;
+  return launch_linear(x, M, K, qweight_packed, scales_packed, N, out, workspace, plan, dev,
                        static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? W4A16_OK
              : W4A16_ERR_CUDA;

@@ -44,6 +44,33 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
                           int64_t N, void* out, void* workspace, const SkinnyPlan& plan, const DeviceInfo& dev,
                           cudaStream_t stream);
 
+// ---- linear on tcgen05 / TMEM (M >= kTcMinM)
+constexpr int kTcMinM = 16;
+struct TcPlan {
+  int nt = 0;           // MMA N: M rounded up to a multiple of 16
+  int64_t units = 0;
+  int64_t ctas = 0;
+  size_t counter_bytes = 0;
+  size_t partial_bytes = 0;
+  size_t smem_bytes = 0;
+};
+cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan);
+size_t tc_workspace_bytes(const TcPlan& plan);
+cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                      void* out, void* workspace, const TcPlan& plan, const DeviceInfo& dev, cudaStream_t stream);
+
+// ---- linear dispatch (by M)
+struct LinearPlan {
+  bool use_tc = false;
+  SkinnyPlan sk;
+  TcPlan tc;
+  size_t workspace_bytes = 0;
+};
+cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan);
+cudaError_t launch_linear(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                          void* out, void* workspace, const LinearPlan& plan, const DeviceInfo& dev,
+                          cudaStream_t stream);
+
 // ---- accept
 struct AcceptPlan {
   int rows = 0;       // logit rows read by the statistics pass

@@ -14,7 +14,7 @@
 
 namespace w4a16 {
 
-constexpr size_t kNoAllocScratchBytes = 12u << 20;  // 12 MiB
+constexpr size_t kNoAllocScratchBytes = 24u << 20;  // 24 MiB
 
 // Shared by every call on a device; keeps the last call's contents.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -47,7 +47,7 @@ extern "C" size_t w4a16_linear_noalloc_scratch_bytes(void) { return kNoAllocScra
 extern "C" w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, const void* qweight_packed,
                                              const void* scales_packed, int64_t N, void* out, void* stream) {
   if (!x || !qweight_packed || !scales_packed || !out) return W4A16_ERR_INVALID_ARG;
-  if (M < 1 || N <= 0 || K <= 0 || N % kUnitRows != 0 || K % kGroup != 0 || N > (int64_t(1) << 21) ||
+  if (M < 1 || N <= 0 || K <= 0 || N % kUnitRows != 0 || K % kGroup != 0 || N > (int64_t(1) << 20) ||
       K > (int64_t(1) << 24))
     return W4A16_ERR_INVALID_ARG;
   if (M > 64 || K < 1024) return W4A16_ERR_UNSUPPORTED;
@@ -57,17 +57,17 @@ extern "C" w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, co
     return W4A16_ERR_INVALID_ARG;
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
-  SkinnyPlan plan;
-  if (skinny_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
-  if (skinny_workspace_bytes(plan) > kNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
+  LinearPlan plan;
+  if (linear_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (plan.workspace_bytes > kNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (noalloc_scratch(dev.device, &scratch) != cudaSuccess) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The completion counters must start at zero; a previous call (or one that
   // timed out) may have left them otherwise, so clear this call's slice.
-  const size_t counter_bytes = (size_t)(N / kUnitRows) * 4 * sizeof(int);
+  const size_t counter_bytes = (size_t)(N / kUnitRows) * 8 * sizeof(int);
   if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return W4A16_ERR_CUDA;
-  return launch_skinny(x, M, K, qweight_packed, scales_packed, N, out, scratch, plan, dev, s) == cudaSuccess
+  return launch_linear(x, M, K, qweight_packed, scales_packed, N, out, scratch, plan, dev, s) == cudaSuccess
              ? W4A16_OK
              : W4A16_ERR_CUDA;
 }
