@@ -145,7 +145,7 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
  * V % 4 == 0. workspace: device scratch of spec_accept_workspace_bytes(B,n,V)
  * bytes, 256-byte aligned, with the same zeroed 256 KiB counter region at its
  * start as the linear's workspace (either can serve both).
- * Limits: 1 <= B <= 65535, 1 <= n <= 1024, 2 <= V < 2^31.
+ * Limits: 1 <= B <= 32768, 1 <= n <= 1024, B * (2n + 1) <= 65535, 2 <= V <= 2^20.
  * ---------------------------------------------------------------------- */
 size_t spec_accept_workspace_bytes(int B, int n, int V);
 w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int32_t* draft_ids,

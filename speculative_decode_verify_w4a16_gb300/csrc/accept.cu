@@ -2,16 +2,18 @@
 // section 6; greedy equivalence in section 5).
 //
 // Stochastic sequence mode, two launches:
-//  1. accept_stats_kernel: every p / q logit row is cut into chunks; a block
-//     reduces one chunk to (max, sum of exp(l - max)) — one HBM pass over
-//     all logits, fp32 exponentials, per-thread fp32 sums folded into fp64.
-//  2. accept_resid_kernel, grid (chunk, batch row): each block merges the
-//     row statistics of its batch row, evaluates alpha_i = min(1, P/Q) for
-//     the drafts (fp64), finds the first rejection r, then sums the corrected
-//     distribution max(0, P_r - Q_r) (or P_{n+1} after full acceptance) over
-//     its vocabulary chunk. The last block of the batch row (atomic count)
-//     walks the chunk sums, re-scans the one chunk that holds u * S, and
-//     writes accepted_len and next_token.
+//  1. accept_stats_kernel, grid (chunk, row): every p / q logit row is cut
+//     into chunks of at most 16384 logits; a block holds its chunk in
+//     registers (one HBM pass), takes the exact chunk maximum and the sum of
+//     exp(l - max) (pairwise fp32 per thread, fp64 across threads). The last
+//     block of a batch row (atomic count) merges its rows' statistics in fp64,
+//     evaluates alpha_i = min(1, P(d_i) / Q(d_i)) for every draft, finds the
+//     first rejection r and records r with the normalisers of row r.
+//  2. accept_resid_kernel, grid (chunk, batch row): each block sums the
+//     distribution to draw from — max(0, P_r - Q_r), or P_{n+1} after full
+//     acceptance — over its vocabulary chunk. The last block of the batch row
+//     walks the chunk sums, re-scans the chunk that holds u * S with an fp64
+//     block scan, and writes accepted_len and next_token.
 // Greedy modes, one launch: accept_argmax_kernel reduces chunks to
 // (max, smallest index); the last block of a batch row merges them and walks
 // the chain or tree.
@@ -28,17 +30,70 @@ namespace w4a16 {
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
-constexpr int kMaxNodes = 1025;  // rows of one batch element in greedy mode (n <= 1024)
+constexpr int kPerThread = 64;                       // logits a thread holds in the chunk passes
+constexpr int kMaxChunk = kAccThreads * kPerThread;  // 16384
+constexpr int kMaxNodes = 1025;                      // rows of one batch element in greedy mode (n <= 1024)
+constexpr int kCounterBank2 = 32768;                 // second bank of completion counters (B <= 32768)
+constexpr int kRescan = 32;                          // values per thread when the draw re-scans one chunk
+constexpr int kMaxChunk2 = kAccThreads * kRescan;    // 8192
+constexpr int kMaxCh2 = 256;                         // residual chunks per batch row
+constexpr int kStatCache = 512;                      // chunk statistics of one batch row held in smem
+
+// Double-float value hi + lo (two fp32 words). GB300 executes only a couple
+// of fp64 operations per clock per SM, so sums that need more than fp32 are
+// carried in this form with error-free transformations on the fp32 pipe:
+// TwoSum (Knuth, TAOCP vol. 2, 4.2.2) and FastTwoSum (Dekker 1971), and the
+// fma-based exact product.
+struct DF {
+  float hi, lo;
+};
+
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return DF{s, e};
+}
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return DF{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  const DF s = two_sum(a.hi, b);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  const float e = __fmaf_rn(a.hi, b, -p);
+  return fast_two_sum(p, __fmaf_rn(a.lo, b, e));
+}
+__device__ __forceinline__ float df_val(DF a) { return __fadd_rn(a.hi, a.lo); }
+// sign of a - b
+__device__ __forceinline__ bool df_gt(DF a, DF b) {
+  const DF d = df_add(a, DF{-b.hi, -b.lo});
+  return d.hi > 0.0f || (d.hi == 0.0f && d.lo > 0.0f);
+}
 
 struct RowStat {
   float m;
   float pad;
-  double s;
+  DF s;
+};
+
+struct Decision {  // first rejection r and the normalisers of the rows the final draw uses
+  int r;
+  float mp, mq;
+  float izp, izq;  // 1 / Z
+  int pad[3];
 };
 
 struct ChunkSum {
-  double r;  // sum of the distribution being sampled
-  double p;  // sum of P_r (fallback when the corrected distribution is all zero)
+  DF r;  // sum of the distribution being sampled
+  DF p;  // sum of P_r (fallback when the corrected distribution is all zero)
 };
 
 struct ArgPart {
@@ -46,53 +101,58 @@ struct ArgPart {
   int idx;
 };
 
-__device__ __forceinline__ void merge_stat(float& m, double& s, float m2, double s2) {
-  if (s2 == 0.0 && m2 == -FLT_MAX) return;
-  if (m2 > m) {
-    s = s * (double)expf(m - m2) + s2;
-    m = m2;
-  } else {
-    s += s2 * (double)expf(m2 - m);
-  }
-}
-
-// Block-wide merge of (max, sum-of-exp) pairs; result valid in thread 0.
-__device__ void block_merge_stat(float& m, double& s) {
-  __shared__ float sm_m[kAccWarps];
-  __shared__ double sm_s[kAccWarps];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// ---------------------------------------------------------- block helpers
+// Block-wide max / sums, result returned to every thread.
+__device__ float block_max(float v) {
+  __shared__ float sm[kAccWarps];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const double s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    merge_stat(m, s, m2, s2);
-  }
-  if (lane == 0) {
-    sm_m[w] = m;
-    sm_s[w] = s;
-  }
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int i = 1; i < kAccWarps; ++i) merge_stat(m, s, sm_m[i], sm_s[i]);
-  }
-  __syncthreads();
-}
-
-__device__ __forceinline__ double block_sum_double(double v) {
-  __shared__ double sm[kAccWarps];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float r = sm[0];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if (lane == 0) sm[w] = v;
+  for (int i = 1; i < kAccWarps; ++i) r = fmaxf(r, sm[i]);
   __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kAccWarps; ++i) t += sm[i];
-  __syncthreads();
-  return t;  // valid in thread 0
+  return r;
 }
 
-// Row pointer for statistics row rr: batch b's n+1 target rows, then its n draft rows.
+__device__ __forceinline__ DF shfl_xor_df(DF v, int o) {
+  return DF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+
+// Block-wide double-float sum, returned to every thread.
+__device__ DF block_sum(DF v) {
+  __shared__ DF sm[kAccWarps];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = v;
+  __syncthreads();
+  DF r = sm[0];
+#pragma unroll
+  for (int i = 1; i < kAccWarps; ++i) r = df_add(r, sm[i]);
+  __syncthreads();
+  return r;
+}
+
+// Exclusive prefix sum over the block (thread order), double-float.
+__device__ DF block_exclusive_scan(DF v) {
+  __shared__ DF wsum[kAccWarps];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  DF incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+    if (lane >= o) incl = df_add(incl, y);
+  }
+  if (lane == 31) wsum[w] = incl;
+  __syncthreads();
+  DF before{0.0f, 0.0f};
+  for (int i = 0; i < w; ++i) before = df_add(before, wsum[i]);
+  __syncthreads();
+  return df_add(before, df_add(incl, DF{-v.hi, -v.lo}));
+}
+
+// Statistics row rr of a batch row's 2n+1 rows: target rows 0..n, then draft rows.
 __device__ __forceinline__ const float* stat_row_ptr(const float* p, const float* q, int n, int64_t V, int rr) {
   const int per = 2 * n + 1;
   const int b = rr / per, i = rr % per;
@@ -100,245 +160,285 @@ __device__ __forceinline__ const float* stat_row_ptr(const float* p, const float
   return q + ((int64_t)b * n + (i - n - 1)) * V;
 }
 
-// ------------------------------------------------------- pass 1: row stats
-template <bool VEC>
-__global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(const float* __restrict__ p,
-                                                                   const float* __restrict__ q, int n, int V,
-                                                                   int chunk, RowStat* __restrict__ stats) {
-  const int rr = blockIdx.y;
-  const float* row = stat_row_ptr(p, q, n, V, rr);
-  const int x0 = blockIdx.x * chunk;
-  const int x1 = min(V, x0 + chunk);
+// Merge a row's chunk statistics: M = max m_c, Z = sum_c s_c exp(m_c - M).
+__device__ void merge_row(const RowStat* st, int ch, float& M, DF& Z) {
   float m = -FLT_MAX;
-  double s = 0.0;
+  for (int c = 0; c < ch; ++c) m = fmaxf(m, st[c].m);
+  DF z{0.0f, 0.0f};
+  for (int c = 0; c < ch; ++c) z = df_add(z, df_mul_f(st[c].s, expf(__fsub_rn(st[c].m, m))));
+  M = m;
+  Z = z;
+}
+
+// Load this thread's share of [x0, x1) into registers (missing slots: -FLT_MAX).
+template <bool VEC>
+__device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, float (&v)[kPerThread]) {
   if (VEC) {
-    constexpr int U = 4;
-    for (int base = x0 + threadIdx.x * 4; base < x1; base += kAccThreads * 4 * U) {
-      float4 v[U];
-      float bm = -FLT_MAX;
 #pragma unroll
-      for (int k = 0; k < U; ++k) {
-        const int xi = base + k * kAccThreads * 4;
-        if (xi < x1) {
-          v[k] = ldg_stream_f4(reinterpret_cast<const float4*>(row + xi));
-          bm = fmaxf(bm, fmaxf(fmaxf(v[k].x, v[k].y), fmaxf(v[k].z, v[k].w)));
-        } else {
-          v[k] = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
-        }
-      }
-      if (bm > m) {
-        if (s != 0.0) s *= (double)expf(m - bm);
-        m = bm;
-      }
-      float fs = 0.0f;
-#pragma unroll
-      for (int k = 0; k < U; ++k)
-        if (base + k * kAccThreads * 4 < x1)
-          fs += (expf(v[k].x - m) + expf(v[k].y - m)) + (expf(v[k].z - m) + expf(v[k].w - m));
-      s += (double)fs;
+    for (int j = 0; j < kPerThread / 4; ++j) {
+      const int xi = x0 + (j * kAccThreads + (int)threadIdx.x) * 4;
+      float4 t = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      if (xi < x1) t = ldg_stream_f4(reinterpret_cast<const float4*>(row + xi));
+      v[4 * j] = t.x;
+      v[4 * j + 1] = t.y;
+      v[4 * j + 2] = t.z;
+      v[4 * j + 3] = t.w;
     }
   } else {
-    for (int xi = x0 + threadIdx.x; xi < x1; xi += kAccThreads) {
-      const float v = ldg_stream_f(row + xi);
-      if (v > m) {
-        if (s != 0.0) s *= (double)expf(m - v);
-        m = v;
-      }
-      s += (double)expf(v - m);
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int xi = x0 + j * kAccThreads + (int)threadIdx.x;
+      v[j] = xi < x1 ? ldg_stream_f(row + xi) : -FLT_MAX;
     }
-  }
-  block_merge_stat(m, s);
-  if (threadIdx.x == 0) {
-    RowStat r;
-    r.m = m;
-    r.pad = 0.0f;
-    r.s = s;
-    stats[(int64_t)rr * gridDim.x + blockIdx.x] = r;
   }
 }
 
-// --------------------------------------- pass 2: decide, residual, sample
-struct SeqShared {
-  float mp[kMaxNodes];
-  double zp[kMaxNodes];
-  float mq[kMaxNodes];
-  double zq[kMaxNodes];
-  int reject[kMaxNodes];
-  int r;
-};
+// ------------------------------------------------------- pass 1: row stats
+template <bool VEC>
+__global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(
+    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
+    const float* __restrict__ u, int n, int V, int chunk, RowStat* __restrict__ stats, Decision* __restrict__ dec,
+    int* __restrict__ counters, unsigned* err) {
+  const int rr = blockIdx.y;
+  const int per = 2 * n + 1;
+  const int b = rr / per;
+  const float* row = stat_row_ptr(p, q, n, V, rr);
+  const int x0 = blockIdx.x * chunk;
+  const int x1 = min(V, x0 + chunk);
+  float v[kPerThread];
+  load_chunk<VEC>(row, x0, x1, v);
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) m = fmaxf(m, v[j]);
+  m = block_max(m);
+  // pairwise sum of exp(v - m); padding (-FLT_MAX) contributes 0
+  // exp via ex2.approx (__expf): relative error grows with |v - m|, so it is
+  // smallest on the terms that carry the sum; about 1e-7 of the total.
+  float t[kPerThread / 4];
+#pragma unroll
+  for (int j = 0; j < kPerThread / 4; ++j)
+    t[j] = (__expf(v[4 * j] - m) + __expf(v[4 * j + 1] - m)) + (__expf(v[4 * j + 2] - m) + __expf(v[4 * j + 3] - m));
+#pragma unroll
+  for (int w = kPerThread / 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] += t[j + w];
+  const DF s = block_sum(DF{t[0], 0.0f});
 
+  __shared__ int last;
+  if (threadIdx.x == 0) {
+    stats[(int64_t)rr * gridDim.x + blockIdx.x] = RowStat{m, 0.0f, s};
+    __threadfence();
+    last = atomicAdd(&counters[b], 1) == per * (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+
+  // ---- last block of batch row b: acceptance test per draft, first rejection
+  const int ch = gridDim.x;
+  // this batch row's chunk statistics, copied to shared memory in parallel
+  // (at most kStatCache entries; larger cases read them from L2)
+  __shared__ RowStat cache[kStatCache];
+  __shared__ int first_reject;
+  const RowStat* gst = stats + (int64_t)b * per * ch;
+  const bool cached = per * ch <= kStatCache;
+  if (cached)
+    for (int e = threadIdx.x; e < per * ch; e += kAccThreads) {
+      cache[e].m = __ldcg(&gst[e].m);
+      cache[e].s = DF{__ldcg(&gst[e].s.hi), __ldcg(&gst[e].s.lo)};
+    }
+  if (threadIdx.x == 0) first_reject = n;
+  __syncthreads();
+  const RowStat* st = cached ? cache : gst;
+  for (int i = threadIdx.x; i < n; i += kAccThreads) {
+    float mp, mq;
+    DF zp, zq;
+    merge_row(st + i * ch, ch, mp, zp);
+    merge_row(st + (n + 1 + i) * ch, ch, mq, zq);
+    const int di = d[(int64_t)b * n + i];
+    bool reject;
+    if (di < 0 || di >= V) {
+      report_error(err, kErrInput);
+      reject = true;
+    } else {
+      // alpha = min(1, P / Q) = min(1, (e_p * Z_q) / (e_q * Z_p)), fp32 (a few ulp)
+      const float ep = expf(__fsub_rn(p[((int64_t)b * (n + 1) + i) * V + di], mp));
+      const float eq = expf(__fsub_rn(q[((int64_t)b * n + i) * V + di], mq));
+      const float num = __fmul_rn(ep, df_val(zq)), den = __fmul_rn(eq, df_val(zp));
+      const float alpha = den > 0.0f ? fminf(1.0f, __fdiv_rn(num, den)) : 1.0f;
+      reject = !(u[(int64_t)b * (n + 1) + i] < alpha);
+    }
+    if (reject) atomicMin(&first_reject, i);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Decision D;
+    D.r = first_reject;
+    D.pad[0] = D.pad[1] = D.pad[2] = 0;
+    DF z;
+    merge_row(st + D.r * ch, ch, D.mp, z);
+    D.izp = __frcp_rn(df_val(z));
+    if (D.r < n) {
+      merge_row(st + (n + 1 + D.r) * ch, ch, D.mq, z);
+      D.izq = __frcp_rn(df_val(z));
+    } else {
+      D.mq = 0.0f;
+      D.izq = 0.0f;
+    }
+    dec[b] = D;
+    counters[b] = 0;
+  }
+}
+
+// --------------------------------------------- pass 2: residual and draw
 // Value of the distribution being sampled at x (bit-identical wherever computed).
 struct ResidFn {
   const float* prow;  // P_r row logits (or P_{n+1} after full acceptance)
   const float* qrow;  // Q_r row logits, NULL after full acceptance
   float mp, ip, mq, iq;
-  __device__ __forceinline__ float pval(int x) const { return __fmul_rn(expf(__fsub_rn(prow[x], mp)), ip); }
-  __device__ __forceinline__ float rval(int x) const {
-    const float pv = pval(x);
+  __device__ __forceinline__ float pv_of(float lp) const { return __fmul_rn(__expf(__fsub_rn(lp, mp)), ip); }
+  __device__ __forceinline__ float rv_of(float lp, float lq) const {
+    const float pv = pv_of(lp);
     if (!qrow) return pv;
-    const float qv = __fmul_rn(expf(__fsub_rn(qrow[x], mq)), iq);
+    const float qv = __fmul_rn(__expf(__fsub_rn(lq, mq)), iq);
     return fmaxf(__fsub_rn(pv, qv), 0.0f);
   }
+  __device__ __forceinline__ float pval(int x) const { return pv_of(prow[x]); }
+  __device__ __forceinline__ float rval(int x) const { return rv_of(prow[x], qrow ? qrow[x] : 0.0f); }
 };
 
 __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
-    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
-    const float* __restrict__ u, int n, int V, int ch, int chunk2, const RowStat* __restrict__ stats,
-    ChunkSum* __restrict__ csum, int* __restrict__ counters, int32_t* __restrict__ acc_out,
-    int32_t* __restrict__ next_out, unsigned* err) {
-  __shared__ SeqShared sh;
+    const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
+    int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out) {
   const int b = blockIdx.y;
-  const int per = 2 * n + 1;
-  // merge the chunk statistics of this batch row's 2n+1 rows
-  for (int i = threadIdx.x; i < per; i += kAccThreads) {
-    const RowStat* st = stats + ((int64_t)b * per + i) * ch;
-    float m = -FLT_MAX;
-    double s = 0.0;
-    for (int c = 0; c < ch; ++c) merge_stat(m, s, st[c].m, st[c].s);
-    if (i <= n) {
-      sh.mp[i] = m;
-      sh.zp[i] = s;
-    } else {
-      sh.mq[i - n - 1] = m;
-      sh.zq[i - n - 1] = s;
-    }
-  }
-  __syncthreads();
-  // acceptance test for each draft position (in parallel), first rejection after
-  for (int i = threadIdx.x; i < n; i += kAccThreads) {
-    const int di = d[(int64_t)b * n + i];
-    int rej;
-    if (di < 0 || di >= V) {
-      report_error(err, kErrInput);
-      rej = 1;
-    } else {
-      const double ep = (double)expf(__fsub_rn(p[((int64_t)b * (n + 1) + i) * V + di], sh.mp[i]));
-      const double eq = (double)expf(__fsub_rn(q[((int64_t)b * n + i) * V + di], sh.mq[i]));
-      const double P = ep / sh.zp[i], Q = eq / sh.zq[i];
-      const double alpha = Q > 0.0 ? fmin(1.0, P / Q) : 1.0;
-      rej = ((double)u[(int64_t)b * (n + 1) + i] < alpha) ? 0 : 1;
-    }
-    sh.reject[i] = rej;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int r = n;
-    for (int i = 0; i < n; ++i)
-      if (sh.reject[i]) {
-        r = i;
-        break;
-      }
-    sh.r = r;
-  }
-  __syncthreads();
-  const int r = sh.r;
+  const int r = __ldcg(&dec[b].r);
   ResidFn f;
   f.prow = p + ((int64_t)b * (n + 1) + r) * V;
-  f.mp = sh.mp[r];
-  f.ip = (float)(1.0 / sh.zp[r]);
+  f.mp = __ldcg(&dec[b].mp);
+  f.ip = __ldcg(&dec[b].izp);
   if (r < n) {
     f.qrow = q + ((int64_t)b * n + r) * V;
-    f.mq = sh.mq[r];
-    f.iq = (float)(1.0 / sh.zq[r]);
+    f.mq = __ldcg(&dec[b].mq);
+    f.iq = __ldcg(&dec[b].izq);
   } else {
     f.qrow = nullptr;
     f.mq = 0.0f;
     f.iq = 0.0f;
   }
-  // this block's chunk sums
   const int x0 = blockIdx.x * chunk2, x1 = min(V, x0 + chunk2);
-  double sr = 0.0, sp = 0.0;
-  for (int x = x0 + threadIdx.x; x < x1; x += kAccThreads) {
-    sr += (double)f.rval(x);
-    if (f.qrow) sp += (double)f.pval(x);
+  // all of this thread's logits are loaded before any is used (one latency)
+  float lp[kRescan], lq[kRescan];
+#pragma unroll
+  for (int j = 0; j < kRescan; ++j) {
+    const int x = x0 + j * kAccThreads + (int)threadIdx.x;
+    lp[j] = x < x1 ? f.prow[x] : 0.0f;
+    lq[j] = (x < x1 && f.qrow) ? f.qrow[x] : 0.0f;
   }
-  sr = block_sum_double(sr);
-  sp = block_sum_double(sp);
+  float sr = 0.0f, sp = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kRescan; ++j) {
+    if (x0 + j * kAccThreads + (int)threadIdx.x < x1) {
+      sr += f.rv_of(lp[j], lq[j]);
+      if (f.qrow) sp += f.pv_of(lp[j]);
+    }
+  }
+  const DF SR = block_sum(DF{sr, 0.0f});
+  const DF SP = block_sum(DF{sp, 0.0f});
   __shared__ int last;
   if (threadIdx.x == 0) {
-    csum[(int64_t)b * gridDim.x + blockIdx.x] = ChunkSum{sr, sp};
+    csum[(int64_t)b * gridDim.x + blockIdx.x] = ChunkSum{SR, SP};
     __threadfence();
-    const int old = atomicAdd(&counters[b], 1);
-    last = (old == (int)gridDim.x - 1);
+    last = atomicAdd(&counters[b], 1) == (int)gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
 
   // ---- the last block of batch row b draws the next token
-  __shared__ double sh_t, sh_before;
-  __shared__ int sh_chunk, sh_usep;
-  __shared__ ChunkSum sh_cs[64];  // gridDim.x <= 64
+  __shared__ DF sh_t, sh_before;
+  __shared__ int sh_chunk, sh_usep, sh_found;
+  __shared__ ChunkSum sh_cs[kMaxCh2];  // gridDim.x <= kMaxCh2
   for (int c = threadIdx.x; c < (int)gridDim.x; c += kAccThreads) {
     const ChunkSum* cs = csum + (int64_t)b * gridDim.x + c;
-    sh_cs[c].r = __ldcg(&cs->r);
-    sh_cs[c].p = __ldcg(&cs->p);
+    sh_cs[c].r = DF{__ldcg(&cs->r.hi), __ldcg(&cs->r.lo)};
+    sh_cs[c].p = DF{__ldcg(&cs->p.hi), __ldcg(&cs->p.lo)};
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double S = 0.0;
-    for (int c = 0; c < (int)gridDim.x; ++c) S += sh_cs[c].r;
+    DF S{0.0f, 0.0f};
+    for (int c = 0; c < (int)gridDim.x; ++c) S = df_add(S, sh_cs[c].r);
     int usep = 0;
-    if (f.qrow && S == 0.0) {  // corrected distribution is all zero: draw from P_r
+    if (f.qrow && S.hi == 0.0f) {  // corrected distribution is all zero: draw from P_r
       usep = 1;
-      S = 0.0;
-      for (int c = 0; c < (int)gridDim.x; ++c) S += sh_cs[c].p;
+      S = DF{0.0f, 0.0f};
+      for (int c = 0; c < (int)gridDim.x; ++c) S = df_add(S, sh_cs[c].p);
     }
-    const double t = (double)u[(int64_t)b * (n + 1) + n] * S;
-    double cum = 0.0;
+    const DF t = df_mul_f(S, u[(int64_t)b * (n + 1) + n]);
+    DF cum{0.0f, 0.0f};
     int cstar = -1;
     for (int c = 0; c < (int)gridDim.x; ++c) {
-      const double v = usep ? sh_cs[c].p : sh_cs[c].r;
-      if (cum + v > t) {
+      const DF nxt = df_add(cum, usep ? sh_cs[c].p : sh_cs[c].r);
+      if (df_gt(nxt, t)) {
         cstar = c;
         break;
       }
-      cum += v;
+      cum = nxt;
     }
     sh_t = t;
     sh_before = cum;
     sh_chunk = cstar;
     sh_usep = usep;
+    sh_found = INT_MAX;
     counters[b] = 0;
   }
   __syncthreads();
   const int usep = sh_usep;
   auto val = [&](int x) { return usep ? f.pval(x) : f.rval(x); };
-  int found = INT_MAX;
   if (sh_chunk >= 0) {
-    // contiguous sub-range per thread, exclusive scan of thread sums (fp64)
+    // coalesced loads of the chunk (stride kAccThreads) into shared memory,
+    // then a contiguous sub-range per thread (at most kRescan values) for the
+    // double-float running sums from a block scan
+    __shared__ float sv[kMaxChunk2 + kMaxChunk2 / 32];  // one pad word per 32: conflict-free row reads
     const int c0 = sh_chunk * chunk2, c1 = min(V, c0 + chunk2);
-    const int len = c1 - c0;
-    const int per_t = (len + kAccThreads - 1) / kAccThreads;
-    const int a0 = c0 + threadIdx.x * per_t, a1 = min(c1, a0 + per_t);
-    double mine = 0.0;
-    for (int x = a0; x < a1; ++x) mine += (double)val(x);
-    __shared__ double scan[kAccThreads];
-    scan[threadIdx.x] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double run = sh_before;
-      for (int i = 0; i < kAccThreads; ++i) {
-        const double v = scan[i];
-        scan[i] = run;
-        run += v;
+    {
+      float lp[kRescan], lq[kRescan];
+#pragma unroll
+      for (int j = 0; j < kRescan; ++j) {
+        const int x = min(c0 + j * kAccThreads + (int)threadIdx.x, V - 1);
+        lp[j] = f.prow[x];
+        lq[j] = f.qrow ? f.qrow[x] : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < kRescan; ++j) {
+        const int o = j * kAccThreads + (int)threadIdx.x;
+        if (c0 + o < c1) sv[o + (o >> 5)] = usep ? f.pv_of(lp[j]) : f.rv_of(lp[j], lq[j]);
       }
     }
     __syncthreads();
-    double run = scan[threadIdx.x];
-    for (int x = a0; x < a1; ++x) {
-      run += (double)val(x);
-      if (run > sh_t) {
-        found = x;
-        break;
+    const int per_t = (c1 - c0 + kAccThreads - 1) / kAccThreads;
+    const int a0 = min(c1, c0 + (int)threadIdx.x * per_t), a1 = min(c1, a0 + per_t);
+    float vals[kRescan];
+#pragma unroll
+    for (int j = 0; j < kRescan; ++j) {
+      const int k = a0 + j - c0;
+      vals[j] = (a0 + j < a1) ? sv[k + (k >> 5)] : 0.0f;
+    }
+    DF mine{0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < kRescan; ++j) mine = df_add_f(mine, vals[j]);
+    DF run = df_add(sh_before, block_exclusive_scan(mine));
+    const DF t = sh_t;
+    int hit = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < kRescan; ++j) {
+      if (a0 + j < a1 && hit == INT_MAX) {
+        run = df_add_f(run, vals[j]);
+        if (df_gt(run, t)) hit = a0 + j;
       }
     }
+    if (hit != INT_MAX) atomicMin(&sh_found, hit);
   }
-  // smallest crossing index in the block
-  __shared__ int sh_found;
-  if (threadIdx.x == 0) sh_found = INT_MAX;
-  __syncthreads();
-  if (found != INT_MAX) atomicMin(&sh_found, found);
   __syncthreads();
   if (sh_found == INT_MAX) {
     // rounding left no crossing: first positive index after the chosen chunk,
@@ -393,20 +493,16 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
   const int b = rr / rows_per_b;
   const float* row = p + (int64_t)rr * V;
   const int x0 = blockIdx.x * chunk, x1 = min(V, x0 + chunk);
+  float v[kPerThread];
+  load_chunk<VEC>(row, x0, x1, v);
+  // this thread's indices increase with j (and within a float4), so a strict
+  // comparison keeps the smallest index among equal values
   ArgPart best{-FLT_MAX, -1};
-  if (VEC) {
-    for (int base = x0 + threadIdx.x * 4; base < x1; base += kAccThreads * 4) {
-      const float4 v = ldg_stream_f4(reinterpret_cast<const float4*>(row + base));
-      if (v.x > best.v || best.idx < 0) best = ArgPart{v.x, base};
-      if (v.y > best.v) best = ArgPart{v.y, base + 1};
-      if (v.z > best.v) best = ArgPart{v.z, base + 2};
-      if (v.w > best.v) best = ArgPart{v.w, base + 3};
-    }
-  } else {
-    for (int x = x0 + threadIdx.x; x < x1; x += kAccThreads) {
-      const float v = ldg_stream_f(row + x);
-      if (v > best.v || best.idx < 0) best = ArgPart{v, x};
-    }
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int xi = VEC ? x0 + ((j / 4) * kAccThreads + (int)threadIdx.x) * 4 + (j % 4)
+                       : x0 + j * kAccThreads + (int)threadIdx.x;
+    if (xi < x1 && (v[j] > best.v || best.idx < 0)) best = ArgPart{v[j], xi};
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -423,8 +519,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     for (int i = 1; i < kAccWarps; ++i) best = arg_better(best, wbest[i]);
     parts[(int64_t)rr * gridDim.x + blockIdx.x] = best;
     __threadfence();
-    const int old = atomicAdd(&counters[b], 1);
-    last = (old == rows_per_b * (int)gridDim.x - 1);
+    last = atomicAdd(&counters[b], 1) == rows_per_b * (int)gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
@@ -435,10 +530,10 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     const ArgPart* pp = parts + ((int64_t)b * rows_per_b + j) * gridDim.x;
     ArgPart a{-FLT_MAX, -1};
     for (int c = 0; c < (int)gridDim.x; ++c) {
-      ArgPart v;
-      v.v = __ldcg(&pp[c].v);
-      v.idx = __ldcg(&pp[c].idx);
-      a = arg_better(a, v);
+      ArgPart w;
+      w.v = __ldcg(&pp[c].v);
+      w.idx = __ldcg(&pp[c].idx);
+      a = arg_better(a, w);
     }
     gs.amax[j] = a.idx < 0 ? 0 : a.idx;
   }
@@ -493,29 +588,37 @@ AcceptPlan accept_plan(int B, int n, int V) {
   AcceptPlan pl;
   const int rows = B * (2 * n + 1);  // upper bound over modes (greedy reads B*(n+1) or B*n rows)
   pl.rows = rows;
-  int ch = (1024 + rows - 1) / rows;
-  const int max_ch_v = V / 2048 > 1 ? V / 2048 : 1;
-  ch = ch < 1 ? 1 : ch;
-  ch = ch > 64 ? 64 : ch;
-  ch = ch > max_ch_v ? max_ch_v : ch;
+  // statistics / argmax chunks: at most kMaxChunk logits, about 1024 blocks in all, at most 64 per row
+  int ch = (V + kMaxChunk - 1) / kMaxChunk;
+  const int want = (1024 + rows - 1) / rows;
+  const int cap_v = (V + 2047) / 2048;  // chunks of at least ~2048 logits
+  int more = want < cap_v ? want : cap_v;
+  if (more > 64) more = 64;
+  if (ch < more) ch = more;
   int chunk = (V + ch - 1) / ch;
   chunk = (chunk + 3) / 4 * 4;
+  if (chunk > kMaxChunk) chunk = kMaxChunk;
   ch = (V + chunk - 1) / chunk;
   pl.ch = ch;
   pl.chunk = chunk;
-  int ch2 = (1024 + B - 1) / B;
-  ch2 = ch2 > 64 ? 64 : ch2;
-  ch2 = ch2 > max_ch_v ? max_ch_v : ch2;
-  ch2 = ch2 < 1 ? 1 : ch2;
+  // residual chunks per batch row: about 256 blocks in all (one wave: the
+  // pass is short and latency-bound), at most 64, at least enough that one
+  // chunk fits the draw's register re-scan
+  int ch2 = (256 + B - 1) / B;
+  if (ch2 > 64) ch2 = 64;
+  if (ch2 > cap_v) ch2 = cap_v;
+  if (ch2 < 1) ch2 = 1;
+  if (ch2 < (V + kMaxChunk2 - 1) / kMaxChunk2) ch2 = (V + kMaxChunk2 - 1) / kMaxChunk2;
   int chunk2 = (V + ch2 - 1) / ch2;
   ch2 = (V + chunk2 - 1) / chunk2;
   pl.ch2 = ch2;
   pl.chunk2 = chunk2;
-  const size_t stats_bytes = align256((size_t)rows * ch * (sizeof(RowStat) > sizeof(ArgPart) ? sizeof(RowStat)
-                                                                                              : sizeof(ArgPart)));
+  const size_t stats_bytes = align256((size_t)rows * ch * sizeof(RowStat));  // >= ArgPart storage
+  const size_t dec_bytes = align256((size_t)B * sizeof(Decision));
   const size_t csum_bytes = align256((size_t)B * ch2 * sizeof(ChunkSum));
   pl.stats_off = kCounterRegionBytes;
-  pl.csum_off = pl.stats_off + stats_bytes;
+  pl.dec_off = pl.stats_off + stats_bytes;
+  pl.csum_off = pl.dec_off + dec_bytes;
   pl.total = pl.csum_off + csum_bytes;
   return pl;
 }
@@ -525,18 +628,19 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
                               cudaStream_t stream) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   RowStat* stats = reinterpret_cast<RowStat*>(w + pl.stats_off);
+  Decision* dec = reinterpret_cast<Decision*>(w + pl.dec_off);
   ChunkSum* csum = reinterpret_cast<ChunkSum*>(w + pl.csum_off);
-  int* cnt = reinterpret_cast<int*>(w);
+  int* cnt1 = reinterpret_cast<int*>(w);
+  int* cnt2 = cnt1 + kCounterBank2;
   const dim3 g1(pl.ch, B * (2 * n + 1));
   if (V % 4 == 0)
-    accept_stats_kernel<true><<<g1, kAccThreads, 0, stream>>>(p, q, n, V, pl.chunk, stats);
+    accept_stats_kernel<true><<<g1, kAccThreads, 0, stream>>>(p, q, d, u, n, V, pl.chunk, stats, dec, cnt1, err);
   else
-    accept_stats_kernel<false><<<g1, kAccThreads, 0, stream>>>(p, q, n, V, pl.chunk, stats);
+    accept_stats_kernel<false><<<g1, kAccThreads, 0, stream>>>(p, q, d, u, n, V, pl.chunk, stats, dec, cnt1, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 g2(pl.ch2, B);
-  accept_resid_kernel<<<g2, kAccThreads, 0, stream>>>(p, q, d, u, n, V, pl.ch, pl.chunk2, stats, csum, cnt, acc,
-                                                       next, err);
+  accept_resid_kernel<<<g2, kAccThreads, 0, stream>>>(p, q, u, n, V, pl.chunk2, dec, csum, cnt2, acc, next);
   return cudaGetLastError();
 }
 

@@ -150,8 +150,14 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
              : W4A16_ERR_CUDA;
 }
 
+static bool accept_shape_ok(int B, int n, int V) {
+  // grid rows: B * (2n + 1) statistics rows must fit one grid dimension
+  return B >= 1 && B <= 32768 && n >= 1 && n <= 1024 && V >= 2 && V <= (1 << 20) &&
+         (int64_t)B * (2 * n + 1) <= 65535;
+}
+
 size_t spec_accept_workspace_bytes(int B, int n, int V) {
-  if (B < 1 || B > 65535 || n < 1 || n > 1024 || V < 2) return 0;
+  if (!accept_shape_ok(B, n, V)) return 0;
   return accept_plan(B, n, V).total;
 }
 
@@ -160,7 +166,7 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
                          int32_t* accepted_len, int32_t* next_token, void* workspace, size_t workspace_bytes,
                          void* stream) {
   if (!p_logits || !draft_ids || !accepted_len || !next_token) return W4A16_ERR_INVALID_ARG;
-  if (B < 1 || B > 65535 || n < 1 || n > 1024 || V < 2) return W4A16_ERR_INVALID_ARG;
+  if (!accept_shape_ok(B, n, V)) return W4A16_ERR_INVALID_ARG;
   if (q_logits && tree_parents) return W4A16_ERR_UNSUPPORTED;
   if (q_logits && !uniforms) return W4A16_ERR_INVALID_ARG;
   if (V % 4 == 0 && (!aligned(p_logits, 16) || (q_logits && !aligned(q_logits, 16)))) return W4A16_ERR_INVALID_ARG;

@@ -48,26 +48,39 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test for completion of the phase with the given parity; if it is not
+// complete the thread may sleep in hardware for up to `hint_ns` before the
+// test returns false (so waiting warps do not spin through issue slots).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns = 0) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (hint_ns == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+  }
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Gives up after
-// kWaitLimitNs, records kErrTimeout and returns false.
+// Wait for the phase with the given parity to complete, sleeping in hardware
+// between tests. Gives up after kWaitLimitNs, records kErrTimeout and returns
+// false.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = globaltimer_ns();
+  if (mbar_try_wait(bar, parity, 1000000u)) return true;
+  const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, 1000000u)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       report_error(err, kErrTimeout);
       return false;

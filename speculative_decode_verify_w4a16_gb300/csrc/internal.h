@@ -78,7 +78,7 @@ struct AcceptPlan {
   int chunk = 0;      // elements per chunk (multiple of 4)
   int ch2 = 0;        // chunks per batch row (residual pass)
   int chunk2 = 0;
-  size_t stats_off = 0, csum_off = 0, total = 0;  // counters at offset 0
+  size_t stats_off = 0, dec_off = 0, csum_off = 0, total = 0;  // counters at offset 0
 };
 AcceptPlan accept_plan(int B, int n, int V);
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,

@@ -152,7 +152,7 @@ __device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t,
 #pragma unroll
       for (int e = 0; e < 4; ++e) sum[rt][nt][e] = 0.0f;
   // contributors are read RB at a time (loads in flight together), summed in CTA order
-  constexpr int RB = MT8 <= 2 ? 4 : (MT8 <= 4 ? 2 : 1);
+  constexpr int RB = MT8 <= 2 ? 2 : 1;
   for (int64_t c0 = cf; c0 <= cl; c0 += RB) {
     float4 v[RB][2][MT8];
 #pragma unroll
@@ -186,8 +186,15 @@ __device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t,
   if (lane == 0) p.counters[t * kSkConsumerWarps + warp] = 0;
 }
 
+// Blocks per SM the register budget is shaped for (more resident warps hide
+// the dequant -> MMA dependency latency).
 template <int MT8>
-__global__ void __launch_bounds__(kSkThreads) w4a16_skinny_kernel(const SkinnyParams p) {
+constexpr int skinny_min_blocks() {
+  return MT8 == 1 ? 4 : (MT8 == 2 ? 3 : 1);
+}
+
+template <int MT8>
+__global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_skinny_kernel(const SkinnyParams p) {
   using L = SkinnyLayout<MT8>;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -341,6 +348,9 @@ static cudaError_t skinny_occupancy(int* blocks_per_sm) {
   cudaError_t e =
       cudaFuncSetAttribute(w4a16_skinny_kernel<MT8>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(w4a16_skinny_kernel<MT8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, w4a16_skinny_kernel<MT8>, kSkThreads,
                                                       L::kTotal);
 }
@@ -381,7 +391,7 @@ cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, Skin
     cudaError_t e = skinny_occupancy_dispatch(plan->mt8, &nb);
     if (e != cudaSuccess) return e;
     if (nb < 1) nb = 1;
-    if (nb > 4) nb = 4;
+    if (nb > 5) nb = 5;
     if (dev.device >= 0 && dev.device < 64) cached_nb[dev.device][plan->mt8] = nb;
   }
   int64_t ctas = (int64_t)dev.num_sms * nb;

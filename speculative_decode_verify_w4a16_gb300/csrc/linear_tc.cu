@@ -382,12 +382,35 @@ static int tc_smem_dispatch(int nt) {
   }
 }
 
+// CTAs per SM, from the shared-memory, register and TMEM budgets (the
+// occupancy query under-reports for this kernel, so the limits are applied
+// directly).
 template <int NT>
-static cudaError_t tc_prepare(int* nb) {
+static cudaError_t tc_prepare(int device, int* nb) {
   cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TcLayout<NT>::kTotal);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(nb, w4a16_tc_kernel<NT>, kTcThreads, TcLayout<NT>::kTotal);
+  e = cudaFuncSetAttribute(w4a16_tc_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, w4a16_tc_kernel<NT>);
+  if (e != cudaSuccess) return e;
+  int smem_sm = 0, smem_reserved = 0, regs_sm = 0;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device)) != cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, device)) != cudaSuccess)
+    return e;
+  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device)) != cudaSuccess)
+    return e;
+  const int by_smem = smem_sm / (TcLayout<NT>::kTotal + (int)fa.sharedSizeBytes + smem_reserved);
+  const int regs_cta = ((fa.numRegs * 32 + 255) / 256 * 256) * (kTcThreads / 32);
+  const int by_regs = regs_sm / (regs_cta > 0 ? regs_cta : 1);
+  const int by_tmem = 512 / (int)kTcTmemCols;
+  int n = by_smem < by_regs ? by_smem : by_regs;
+  n = n < by_tmem ? n : by_tmem;
+  *nb = n;
+  return cudaSuccess;
 }
 
 cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan) {
@@ -399,10 +422,10 @@ cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* 
   if (nb == 0) {
     cudaError_t e;
     switch (plan->nt) {
-      case 16: e = tc_prepare<16>(&nb); break;
-      case 32: e = tc_prepare<32>(&nb); break;
-      case 48: e = tc_prepare<48>(&nb); break;
-      default: e = tc_prepare<64>(&nb); break;
+      case 16: e = tc_prepare<16>(dev.device, &nb); break;
+      case 32: e = tc_prepare<32>(dev.device, &nb); break;
+      case 48: e = tc_prepare<48>(dev.device, &nb); break;
+      default: e = tc_prepare<64>(dev.device, &nb); break;
     }
     if (e != cudaSuccess) return e;
     if (nb < 1) nb = 1;
