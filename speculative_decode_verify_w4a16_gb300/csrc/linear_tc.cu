@@ -31,11 +31,17 @@ constexpr int kTcConsumerWarps = 8;
 constexpr int kTcProducerWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcThreads = 32 * 10;
-constexpr int kTcStages = 4;
 constexpr uint32_t kTcTmemCols = 256;  // A: 2 x 64 columns at 0 / 64; D: 2 x NT columns from 128
 
 template <int NT>
 struct TcLayout {
+  // ring depth: as many stages as two CTAs per SM can hold
+  static constexpr int kStages = NT <= 16 ? 8 : (NT <= 32 ? 6 : (NT <= 48 ? 5 : 4));
+  // TMEM: 2 A buffers of 64 columns, kDBuf accumulators of NT columns; the
+  // epilogue of a unit runs kDBuf - 1 units after its dequantisation so the
+  // MMAs have that long to complete before anyone waits for them
+  static constexpr int kDBuf = NT <= 32 ? 3 : 2;
+  static constexpr int kLag = kDBuf - 1;
   static constexpr int kX = NT * 128;                 // one 64-wide K half of the token tile
   static constexpr int kXOff0 = 0;
   static constexpr int kXOff1 = kX;
@@ -43,9 +49,9 @@ struct TcLayout {
   static constexpr int kSOff = kWOff + kUnitBytes;
   static constexpr int kStageRaw = kSOff + kUnitScaleBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kBarOff = kTcStages * kStage;
-  // full[S], empty[S], a_full[2], mma_done[2], d_free[2], tmem base
-  static constexpr int kTotal = kBarOff + (2 * kTcStages + 6) * 8 + 16 + 1024;  // +1024: alignment slack
+  static constexpr int kBarOff = kStages * kStage;
+  // full[S], empty[S], a_full[2], mma_done[kDBuf], d_free[kDBuf], tmem base
+  static constexpr int kTotal = kBarOff + (2 * kStages + 2 + 2 * kDBuf) * 8 + 16 + 1024;  // +1024: alignment slack
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
 };
 
@@ -165,11 +171,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + kTcStages;
-  uint64_t* a_full = empty + kTcStages;
+  uint64_t* empty = full + L::kStages;
+  uint64_t* a_full = empty + L::kStages;
   uint64_t* mma_done = a_full + 2;
-  uint64_t* d_free = mma_done + 2;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(d_free + 2);
+  uint64_t* d_free = mma_done + L::kDBuf;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(d_free + L::kDBuf);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t cta = blockIdx.x;
@@ -177,12 +183,12 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   const int n_units = (int)(streamk_begin(p.U, p.C, cta + 1) - u0);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kTcConsumerWarps);
+      mbar_init(&empty[s], 1);  // released by the commit of the unit's MMAs
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&a_full[b], kTcConsumerWarps);
+    for (int b = 0; b < 2; ++b) mbar_init(&a_full[b], kTcConsumerWarps);
+    for (int b = 0; b < L::kDBuf; ++b) {
       mbar_init(&mma_done[b], 1);
       mbar_init(&d_free[b], kTcConsumerWarps);
     }
@@ -197,7 +203,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
   const uint32_t a_col[2] = {0u, 64u};
-  const uint32_t d_col[2] = {128u, 128u + (uint32_t)NT};
+  auto d_col = [](int buf) { return 128u + (uint32_t)(buf * NT); };
   int mma_issued = 0;  // units whose MMAs were committed (MMA warp only)
 
   if (warp == kTcProducerWarp) {
@@ -209,8 +215,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
       bool ok = true;
       int64_t g = u0 % p.G;
       for (int i = 0; i < n_units; ++i, g = (g + 1 == p.G) ? 0 : g + 1) {
-        const int s = i % kTcStages;
-        if (i >= kTcStages && !mbar_wait(&empty[s], ((uint32_t)(i / kTcStages) & 1u) ^ 1u, p.err)) {
+        const int s = i % L::kStages;
+        if (i >= L::kStages && !mbar_wait(&empty[s], ((uint32_t)(i / L::kStages) & 1u) ^ 1u, p.err)) {
           ok = false;
           break;
         }
@@ -224,26 +230,27 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
         issued = i + 1;
       }
       if (!ok)
-        for (int i = (issued > kTcStages ? issued - kTcStages : 0); i < issued; ++i)
-          mbar_wait(&full[i % kTcStages], (uint32_t)(i / kTcStages) & 1u, p.err);
+        for (int i = (issued > L::kStages ? issued - L::kStages : 0); i < issued; ++i)
+          mbar_wait(&full[i % L::kStages], (uint32_t)(i / L::kStages) & 1u, p.err);
     }
   } else if (warp == kTcMmaWarp) {
     // ------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(NT);
       for (int i = 0; i < n_units; ++i) {
-        const int s = i % kTcStages, b = i & 1;
-        if (!mbar_wait(&full[s], (uint32_t)(i / kTcStages) & 1u, p.err)) break;
+        const int s = i % L::kStages, b = i & 1, db = i % L::kDBuf;
+        if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
         if (!mbar_wait(&a_full[b], (uint32_t)(i >> 1) & 1u, p.err)) break;
-        if (i >= 2 && !mbar_wait(&d_free[b], ((uint32_t)(i >> 1) & 1u) ^ 1u, p.err)) break;
+        if (i >= L::kDBuf && !mbar_wait(&d_free[db], ((uint32_t)(i / L::kDBuf) & 1u) ^ 1u, p.err)) break;
         tc_fence_after();
         const uint32_t xs = smem_u32(smem + s * L::kStage);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = umma_desc_sw128_kmajor(xs + (kk < 4 ? L::kXOff0 : L::kXOff1) + 32 * (kk & 3));
-          umma_bf16_ts(tmem + d_col[b], tmem + a_col[b] + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
+          umma_bf16_ts(tmem + d_col(db), tmem + a_col[b] + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&mma_done[b]);
+        umma_commit(&mma_done[db]);
+        umma_commit(&empty[s]);  // codes were read before a_full, the token tile by these MMAs
         mma_issued = i + 1;
       }
     }
@@ -255,21 +262,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
     float acc[NT / 2];
 #pragma unroll
     for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
-    float sc_prev = 0.0f;
+    float sc_q[L::kLag + 1];  // scales of units i, i-1, .., i-kLag
+#pragma unroll
+    for (int k = 0; k <= L::kLag; ++k) sc_q[k] = 0.0f;
     int64_t te = u0 / p.G, ge = u0 - te * p.G;  // (tile, group) of the unit in the epilogue
     int64_t seg_g0 = ge;
-    bool ok = true;
-    for (int i = 0; i <= n_units && ok; ++i) {
-      float sc_cur = 0.0f;
+    for (int i = 0; i < n_units + L::kLag; ++i) {
+#pragma unroll
+      for (int k = L::kLag; k > 0; --k) sc_q[k] = sc_q[k - 1];
+      sc_q[0] = 0.0f;
       if (i < n_units) {
-        const int s = i % kTcStages, b = i & 1;
-        if (!mbar_wait(&full[s], (uint32_t)(i / kTcStages) & 1u, p.err)) {
-          ok = false;
-          break;
+        const int s = i % L::kStages, b = i & 1;
+        if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
+        if (i >= 2) {  // A[b] is free once the MMAs of unit i-2 have completed
+          const int e2 = i - 2;
+          if (!mbar_wait(&mma_done[e2 % L::kDBuf], (uint32_t)(e2 / L::kDBuf) & 1u, p.err)) break;
+          tc_fence_after();
         }
         const uint32_t st = smem_u32(smem + s * L::kStage);
         const uint32_t wb = st + L::kWOff + ((q * 2 + h) * 2) * 512 + lane * 16;
-        sc_cur = __half2float(__ushort_as_half(
+        sc_q[0] = __half2float(__ushort_as_half(
             *reinterpret_cast<const unsigned short*>(smem + s * L::kStage + L::kSOff + 2 * sc_half)));
         const uint32_t ta = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col[b];
 #pragma unroll
@@ -287,22 +299,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[b]);
       }
-      if (i >= 1) {
-        // epilogue of unit e = i - 1
-        const int e = i - 1, be = e & 1, se = e % kTcStages;
-        if (!mbar_wait(&mma_done[be], (uint32_t)(e >> 1) & 1u, p.err)) {
-          ok = false;
-          break;
-        }
+      if (i >= L::kLag) {
+        // epilogue of unit e = i - kLag
+        const int e = i - L::kLag, db = e % L::kDBuf;
+        if (!mbar_wait(&mma_done[db], (uint32_t)(e / L::kDBuf) & 1u, p.err)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16) + d_col[be] + h * (NT / 2);
+        const float sc_e = sc_q[L::kLag];
+        const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16) + d_col(db) + h * (NT / 2);
         if constexpr (NT / 2 >= 16) {
 #pragma unroll
           for (int c0 = 0; c0 + 16 <= NT / 2; c0 += 16) {
             uint32_t v[16];
             tmem_ld16_sync(dt + c0, v);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(sc_prev, __uint_as_float(v[c]), acc[c0 + c]);
+            for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(sc_e, __uint_as_float(v[c]), acc[c0 + c]);
           }
         }
         if constexpr ((NT / 2) % 16 != 0) {
@@ -310,14 +320,11 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
           uint32_t v[8];
           tmem_ld8_sync(dt + c0, v);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(sc_prev, __uint_as_float(v[c]), acc[c0 + c]);
+          for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(sc_e, __uint_as_float(v[c]), acc[c0 + c]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&d_free[be]);
-          mbar_arrive(&empty[se]);
-        }
+        if (lane == 0) mbar_arrive(&d_free[db]);
         if (ge == p.G - 1 || e == n_units - 1) {
           if (seg_g0 == 0 && ge == p.G - 1)
             tc_store<NT>(p, te, q, h, lane, acc);
@@ -332,7 +339,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
           ++te;
         }
       }
-      sc_prev = sc_cur;
     }
   }
 
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   if (warp == kTcMmaWarp) {
     if (lane == 0 && mma_issued > 0) {  // normally already observed by the consumers
       const int e = mma_issued - 1;
-      mbar_wait(&mma_done[e & 1], (uint32_t)(e >> 1) & 1u, p.err);
+      mbar_wait(&mma_done[e % L::kDBuf], (uint32_t)(e / L::kDBuf) & 1u, p.err);
     }
     __syncwarp();
     tc_fence_after();
