@@ -244,15 +244,21 @@ def run_ours(args):
     assert sv.check_device_status() == 0
 
     # The step is captured once as a CUDA graph so that the device timeline is
-    # not paced by Python launch overhead; per-call durations come from event
-    # record nodes inside the graph.
+    # not paced by Python launch overhead. The timed graph holds the kernels
+    # only (consecutive launches overlap through programmatic dependent
+    # launch); per-call durations come from a second capture of the same step
+    # with event record nodes between the calls.
     nseg = len(calls) + 2
     evs = [(_event(torch), _event(torch)) for _ in range(nseg)]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
+        step()
+    graph_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_ev):
         step(evs)
     for _ in range(args.warmup):
         graph.replay()
+        graph_ev.replay()
     torch.cuda.synchronize()
 
     # ---- timed region
@@ -276,10 +282,10 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
     assert sv.check_device_status() == 0
-    # per-call device durations: the same graph, one replay at a time
+    # per-call device durations: the step with event nodes, one replay at a time
     seg = []
     for s in range(args.steps):
-        graph.replay()
+        graph_ev.replay()
         torch.cuda.synchronize()
         seg.append([evs[j][0].elapsed_time(evs[j][1]) * 1e3 for j in range(nseg)])
     seg_mean = np.array(seg).mean(axis=0)

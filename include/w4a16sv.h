@@ -96,12 +96,16 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
  *   qweight_packed, scales_packed   from w4a16_prepack (device)
  *   out          device, bf16 [M][N] row-major
  *   workspace    device scratch of at least w4a16_linear_workspace_bytes(M,N,K)
- *                bytes, 256-byte aligned. Its first 256 KiB hold completion
- *                counters: ZERO-FILL the workspace before its first use; every
- *                call leaves the counters zero again, so one workspace serves
- *                any later linear or accept call. After
- *                W4A16_ERR_DEVICE_TIMEOUT, zero it again before reuse. Calls
- *                that share a workspace must not overlap in time.
+ *                bytes, 256-byte aligned. Its first 262,400 bytes (256 KiB +
+ *                256) hold counters (work-item claims, split-tile completions):
+ *                ZERO-FILL the workspace before its first use; every call
+ *                leaves the counters zero again, so one workspace serves any
+ *                later linear or accept call. After W4A16_ERR_DEVICE_TIMEOUT,
+ *                zero it again before reuse. Calls that share a workspace must
+ *                not overlap in time (calls on one stream never do).
+ * Kernels are launched with programmatic dependent launch: one may start
+ * while the previous kernel on the stream finishes, but it reads x and the
+ * workspace and writes out only after that kernel has completed.
  * Returns W4A16_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED before launching.
  */
 size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K);
@@ -143,8 +147,8 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
  * in the device error word (the row then reports accepted_len = 0).
  * All pointers are device pointers; p/q rows must be 16-byte aligned when
  * V % 4 == 0. workspace: device scratch of spec_accept_workspace_bytes(B,n,V)
- * bytes, 256-byte aligned, with the same zeroed 256 KiB counter region at its
- * start as the linear's workspace (either can serve both).
+ * bytes, 256-byte aligned, with the same zeroed counter region (256 KiB + 256
+ * bytes) at its start as the linear's workspace (either can serve both).
  * Limits: 1 <= B <= 32768, 1 <= n <= 1024, B * (2n + 1) <= 65535, 2 <= V <= 2^20.
  * ---------------------------------------------------------------------- */
 size_t spec_accept_workspace_bytes(int B, int n, int V);
@@ -185,12 +189,23 @@ w4a16_status w4a16_check_device_status(void* stream);
 
 /* ------------------------------------------------------------------------
  * Host-side planning helpers (no GPU needed; exported so tests can check
- * the stream-K work split).
- * The linear splits U = (N/128)*(K/128) tile units over C CTAs: CTA c owns
- * units [floor(c*U/C), floor((c+1)*U/C)).
+ * the work split of the linear).
+ * The linear cuts U = (N/128)*(K/128) (row-tile, group) units into R rounds
+ * of C items (C = its grid size): round r covers units [rb[r], rb[r+1]) and
+ * item i = r*C + j owns units [rb[r] + floor(j*len/C), rb[r] +
+ * floor((j+1)*len/C)), len = rb[r+1] - rb[r]. Each round takes half of the
+ * units left until items would hold fewer than min_units units, or
+ * max_rounds (1..8) is reached; the last round takes the rest. CTAs claim
+ * items in index order; split tiles are summed in item order.
+ *   w4a16_item_rounds  writes rb[0..R] (room for 9) and returns R, or 0 on
+ *                      bad arguments (U < C, C < 1, min_units < 1).
+ *   w4a16_item_begin   first unit of item i (i in [0, R*C]; R*C gives U),
+ *                      -1 on bad arguments.
+ *   w4a16_item_owner   item holding unit u (0 <= u < U), -1 on bad arguments.
  * ---------------------------------------------------------------------- */
-int64_t w4a16_streamk_unit_begin(int64_t U, int64_t C, int64_t c);
-int64_t w4a16_streamk_owner(int64_t U, int64_t C, int64_t u);
+int w4a16_item_rounds(int64_t U, int C, int min_units, int max_rounds, int64_t* rb);
+int64_t w4a16_item_begin(int64_t U, int C, int min_units, int max_rounds, int i);
+int64_t w4a16_item_owner(int64_t U, int C, int min_units, int max_rounds, int64_t u);
 
 #ifdef __cplusplus
 }

@@ -39,8 +39,9 @@ SIGNATURES = {
     "spec_accept_workspace_bytes": (_sz, [_i32, _i32, _i32]),
     "spec_accept": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "w4a16_check_device_status": (_i32, [_vp]),
-    "w4a16_streamk_unit_begin": (_i64, [_i64, _i64, _i64]),
-    "w4a16_streamk_owner": (_i64, [_i64, _i64, _i64]),
+    "w4a16_item_rounds": (ctypes.c_int, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "w4a16_item_begin": (_i64, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "w4a16_item_owner": (_i64, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64]),
     "w4a16_linear_noalloc_scratch_bytes": (_sz, []),
     "w4a16_linear_noalloc": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp]),
 }

@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
     const float* __restrict__ u, int n, int V, int chunk, RowStat* __restrict__ stats, Decision* __restrict__ dec,
     int* __restrict__ counters, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int rr = blockIdx.y;
   const int per = 2 * n + 1;
   const int b = rr / per;
@@ -311,6 +313,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
     int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
     int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int b = blockIdx.y;
   const int r = __ldcg(&dec[b].r);
   ResidFn f;
@@ -489,6 +493,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     const float* __restrict__ p, const int32_t* __restrict__ d, const int32_t* __restrict__ parents, int n,
     int rows_per_b, int V, int chunk, ArgPart* __restrict__ parts, int* __restrict__ counters,
     int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int rr = blockIdx.y;  // row index over all batch rows
   const int b = rr / rows_per_b;
   const float* row = p + (int64_t)rr * V;
@@ -633,15 +639,17 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   int* cnt1 = reinterpret_cast<int*>(w);
   int* cnt2 = cnt1 + kCounterBank2;
   const dim3 g1(pl.ch, B * (2 * n + 1));
+  cudaError_t e;
   if (V % 4 == 0)
-    accept_stats_kernel<true><<<g1, kAccThreads, 0, stream>>>(p, q, d, u, n, V, pl.chunk, stats, dec, cnt1, err);
+    e = launch_pdl(accept_stats_kernel<true>, g1, dim3(kAccThreads), 0, stream, p, q, d, u, n, V, pl.chunk, stats, dec,
+                   cnt1, err);
   else
-    accept_stats_kernel<false><<<g1, kAccThreads, 0, stream>>>(p, q, d, u, n, V, pl.chunk, stats, dec, cnt1, err);
-  cudaError_t e = cudaGetLastError();
+    e = launch_pdl(accept_stats_kernel<false>, g1, dim3(kAccThreads), 0, stream, p, q, d, u, n, V, pl.chunk, stats,
+                   dec, cnt1, err);
   if (e != cudaSuccess) return e;
   const dim3 g2(pl.ch2, B);
-  accept_resid_kernel<<<g2, kAccThreads, 0, stream>>>(p, q, u, n, V, pl.chunk2, dec, csum, cnt2, acc, next);
-  return cudaGetLastError();
+  return launch_pdl(accept_resid_kernel, g2, dim3(kAccThreads), 0, stream, p, q, u, n, V, pl.chunk2,
+                    (const Decision*)dec, csum, cnt2, acc, next);
 }
 
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
@@ -653,12 +661,10 @@ cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t
   const int rows_per_b = parents ? n : n + 1;
   const dim3 g(pl.ch, B * rows_per_b);
   if (V % 4 == 0)
-    accept_argmax_kernel<true><<<g, kAccThreads, 0, stream>>>(p, d, parents, n, rows_per_b, V, pl.chunk, parts, cnt,
-                                                               acc, next, err);
-  else
-    accept_argmax_kernel<false><<<g, kAccThreads, 0, stream>>>(p, d, parents, n, rows_per_b, V, pl.chunk, parts,
-                                                                cnt, acc, next, err);
-  return cudaGetLastError();
+    return launch_pdl(accept_argmax_kernel<true>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
+                      pl.chunk, parts, cnt, acc, next, err);
+  return launch_pdl(accept_argmax_kernel<false>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
+                    pl.chunk, parts, cnt, acc, next, err);
 }
 
 }  // namespace w4a16

@@ -38,14 +38,15 @@ cudaError_t device_info(DeviceInfo* out) {
   return cudaSuccess;
 }
 
-cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan) {
+cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan,
+                        size_t max_partial_bytes) {
   plan->use_tc = M >= kTcMinM;
   cudaError_t e;
   if (plan->use_tc) {
-    e = tc_plan(M, N, K, dev, &plan->tc);
+    e = tc_plan(M, N, K, dev, max_partial_bytes, &plan->tc);
     plan->workspace_bytes = tc_workspace_bytes(plan->tc);
   } else {
-    e = skinny_plan(M, N, K, dev, &plan->sk);
+    e = skinny_plan(M, N, K, dev, max_partial_bytes, &plan->sk);
     plan->workspace_bytes = skinny_workspace_bytes(plan->sk);
   }
   return e;
@@ -90,14 +91,27 @@ size_t w4a16_packed_weight_bytes(int64_t N, int64_t K) { return valid_nk(N, K) ?
 
 size_t w4a16_packed_scale_bytes(int64_t N, int64_t K) { return valid_nk(N, K) ? (size_t)(N * K / 64) : 0; }
 
-int64_t w4a16_streamk_unit_begin(int64_t U, int64_t C, int64_t c) {
-  if (U <= 0 || C <= 0 || C > U || c < 0 || c > C) return -1;
-  return streamk_begin(U, C, c);
+static bool item_args_ok(int64_t U, int C, int min_units) {
+  return C >= 1 && U >= C && min_units >= 1 && U <= (int64_t(1) << 40);
 }
 
-int64_t w4a16_streamk_owner(int64_t U, int64_t C, int64_t u) {
-  if (U <= 0 || C <= 0 || C > U || u < 0 || u >= U) return -1;
-  return streamk_owner(U, C, u);
+int w4a16_item_rounds(int64_t U, int C, int min_units, int max_rounds, int64_t* rb) {
+  if (!item_args_ok(U, C, min_units) || !rb) return 0;
+  const ItemSched s = make_item_sched(U, C, min_units, max_rounds);
+  for (int r = 0; r <= s.R; ++r) rb[r] = s.rb[r];
+  return s.R;
+}
+
+int64_t w4a16_item_begin(int64_t U, int C, int min_units, int max_rounds, int i) {
+  if (!item_args_ok(U, C, min_units)) return -1;
+  const ItemSched s = make_item_sched(U, C, min_units, max_rounds);
+  if (i < 0 || (int64_t)i > (int64_t)s.R * C) return -1;
+  return item_begin(s, i);
+}
+
+int64_t w4a16_item_owner(int64_t U, int C, int min_units, int max_rounds, int64_t u) {
+  if (!item_args_ok(U, C, min_units) || u < 0 || u >= U) return -1;
+  return item_owner(make_item_sched(U, C, min_units, max_rounds), u);
 }
 
 w4a16_status w4a16_quantize(const float* w, int64_t N, int64_t K, uint32_t* qweight, uint16_t* scales,

@@ -121,6 +121,36 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Warm L2 with [src, src + bytes) (16-byte aligned, bytes a multiple of 16).
+// L2 is the device's point of coherence, so a prefetch may be issued before
+// the kernel has waited for the grid it depends on: a later read still sees
+// any write that grid makes.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------- programmatic dependent launch
+// Kernels are launched with programmatic stream serialisation: they may start
+// while the previous kernel on the stream is still running. Everything that
+// reads or writes global memory shared with other kernels (inputs, outputs,
+// workspace) comes after grid_dependency_wait(), which returns once the
+// preceding grid has completed and its writes are visible. Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- atomics
+// Device-scope fetch-add with acquire-release semantics: publishes this
+// thread's earlier writes (and those ordered before them, e.g. by __syncwarp)
+// and makes writes published by earlier adders visible to later reads.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ------------------------------------------------------------ shared loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

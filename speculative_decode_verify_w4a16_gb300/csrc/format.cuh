@@ -40,13 +40,4 @@ constexpr int kUnitWords = 2048;       // uint32 per unit
 constexpr int kUnitBytes = 8192;
 constexpr int kUnitScaleBytes = 256;
 
-// Stream-K split of U units over C workers: worker c owns [begin(c), begin(c+1)).
-__host__ __device__ __forceinline__ int64_t streamk_begin(int64_t U, int64_t C, int64_t c) {
-  return (c * U) / C;
-}
-// Worker owning unit u (C <= U).
-__host__ __device__ __forceinline__ int64_t streamk_owner(int64_t U, int64_t C, int64_t u) {
-  return ((u + 1) * C - 1) / U;
-}
-
 }  // namespace w4a16

@@ -5,13 +5,38 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "sched.cuh"
+
 namespace w4a16 {
 
-// Every workspace starts with this many bytes of zero-initialised completion
-// counters (int32), shared by the linear and the accept step so that one
+// Every workspace starts with this many bytes of zero-initialised counters
+// (int32: the linear's item-claim counters, then its per (tile, warp)
+// split-tile counters; the accept step's per-row counters), shared so that one
 // workspace can serve any sequence of calls; each call leaves them zero.
-constexpr size_t kCounterRegionBytes = 256 * 1024;
+constexpr size_t kCounterRegionBytes = 256 * 1024 + 256;
 constexpr int64_t kMaxCounters = (int64_t)(kCounterRegionBytes / sizeof(int));
+
+// Budget for the split-tile partial sums of one linear call.
+constexpr size_t kDefaultPartialBytes = 128u << 20;
+
+// Launch with programmatic stream serialisation (the kernel may begin while
+// the previous kernel on the stream finishes; it waits on that grid with
+// griddepcontrol.wait before touching shared global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 struct DeviceInfo {
   int device = -1;
@@ -29,16 +54,18 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint32_t* qwei
 cudaError_t launch_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
                            uint32_t* qw_packed, uint16_t* sc_packed, cudaStream_t stream);
 
-// ---- linear (tensor-core fragments via mma.sync; stream-K over units)
+// ---- linear (tensor-core fragments via mma.sync; M < 16; dynamically claimed unit items)
 struct SkinnyPlan {
   int mt8 = 0;          // ceil(M / 8)
   int64_t units = 0;    // (N/128) * (K/128)
   int64_t ctas = 0;     // grid size
+  ItemSched sched = {};
   size_t counter_bytes = 0;
   size_t partial_bytes = 0;
   size_t smem_bytes = 0;
 };
-cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, SkinnyPlan* plan);
+cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes,
+                        SkinnyPlan* plan);
 size_t skinny_workspace_bytes(const SkinnyPlan& plan);
 cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed,
                           int64_t N, void* out, void* workspace, const SkinnyPlan& plan, const DeviceInfo& dev,
@@ -50,11 +77,12 @@ struct TcPlan {
   int nt = 0;           // MMA N: M rounded up to a multiple of 16
   int64_t units = 0;
   int64_t ctas = 0;
+  ItemSched sched = {};
   size_t counter_bytes = 0;
   size_t partial_bytes = 0;
   size_t smem_bytes = 0;
 };
-cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan);
+cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes, TcPlan* plan);
 size_t tc_workspace_bytes(const TcPlan& plan);
 cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
                       void* out, void* workspace, const TcPlan& plan, const DeviceInfo& dev, cudaStream_t stream);
@@ -66,7 +94,8 @@ struct LinearPlan {
   TcPlan tc;
   size_t workspace_bytes = 0;
 };
-cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan);
+cudaError_t linear_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, LinearPlan* plan,
+                        size_t max_partial_bytes = kDefaultPartialBytes);
 cudaError_t launch_linear(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
                           void* out, void* workspace, const LinearPlan& plan, const DeviceInfo& dev,
                           cudaStream_t stream);

@@ -1,10 +1,12 @@
-// W4A16 verify linear, tensor-core fragment path (mma.sync m16n8k16 bf16).
+// W4A16 verify linear, tensor-core fragment path (mma.sync m16n8k16 bf16),
+// for the sequence-draft token counts (M = 1..15).
 //
 // out[M][N] = bf16(x[M][K] . W^T) with W = code * scale (int4, group 128).
-// Work split: the (row-tile, group) units of the packed weight stream are
-// divided evenly over the grid (stream-K); each CTA streams its contiguous
-// unit range through a ring of shared-memory stages filled by 1-D bulk
-// copies (TMA engine), so every weight byte is read from HBM exactly once.
+// Work split: the (row-tile, group) units of the packed weight stream are cut
+// into items of contiguous units (sched.cuh) which the CTAs claim one after
+// another; each CTA streams its items' units through a ring of shared-memory
+// stages filled by 1-D bulk copies (TMA engine), so every weight byte is read
+// from HBM exactly once.
 //
 // Per CTA: 4 consumer warps (one 32-row slice of the 128-row unit each) and
 // one producer warp. A consumer dequantises 16 packed words per unit into
@@ -15,13 +17,14 @@
 // dimension, tokens its N = 8), accumulates the group in fp32 and applies
 // the fp16 group scale once in fp32.
 //
-// A tile whose K range is split between CTAs is finished by whichever
-// contributor arrives last (per tile and warp slice, counted with an atomic),
-// which sums all contributions in CTA order: the result does not depend on
-// timing. Counters reset themselves for the next call.
+// A tile covered by one item is stored directly; a tile whose K range is
+// split between items is finished by its last contributor, which adds the
+// fp32 partials of all contributors in item order: the result does not
+// depend on timing. Counters reset themselves for the next call.
 #include "common.cuh"
 #include "format.cuh"
 #include "internal.h"
+#include "sched.cuh"
 
 namespace w4a16 {
 
@@ -30,13 +33,18 @@ constexpr int kSkThreads = 32 * (kSkConsumerWarps + 1);
 constexpr int kSkStages = 4;
 constexpr int kXRowStride = 288;  // bytes per token row in a stage (256 used; padding avoids bank conflicts)
 
+// Stage metadata written by the producer: the unit's item, tile and group.
+constexpr int kUnitFirst = 1;  // first unit of its item
+constexpr int kUnitLast = 2;   // last unit of its item
+
 template <int MT8>
 struct SkinnyLayout {
   static constexpr int kW = kUnitBytes;
   static constexpr int kS = kUnitScaleBytes;
   static constexpr int kX = MT8 * 8 * kXRowStride;
   static constexpr int kStage = kW + kS + kX;
-  static constexpr int kBarOff = kSkStages * kStage;
+  static constexpr int kMetaOff = kSkStages * kStage;
+  static constexpr int kBarOff = kMetaOff + kSkStages * 16;
   static constexpr int kTotal = kBarOff + 2 * kSkStages * 8;
   static_assert(kStage % 16 == 0, "stage alignment");
 };
@@ -53,11 +61,13 @@ struct SkinnyParams {
   const uint8_t* qw;
   const uint8_t* sc;
   __nv_bfloat16* out;
-  float4* partials;
-  int* counters;
+  float4* partials;  // split-tile partial slots
+  int* counters;     // item-claim and split-tile counters
   unsigned* err;
-  int64_t K, N, U, G, C;
+  int64_t K, N, G;
   int M;
+  int items;  // R * C
+  ItemSched sched;
   DequantConsts dq;
 };
 
@@ -119,31 +129,39 @@ __device__ __forceinline__ void store_tile(const SkinnyParams& p, int64_t t, int
   }
 }
 
+// Split tiles. Each item that covers part of a tile's K range writes its
+// fp32 sums to its own slot (item, segment, warp) and counts itself in with
+// an atomic per (tile, warp); whichever contributor arrives last adds all
+// slots in item order and stores the tile: the result does not depend on
+// timing. Counters reset themselves for the next call.
 template <int MT8>
-__device__ __forceinline__ float4* partial_slot(const SkinnyParams& p, int64_t cta, int seg, int warp) {
-  return p.partials + ((cta * 2 + seg) * kSkConsumerWarps + warp) * (int64_t)(2 * MT8 * 32);
+__device__ __forceinline__ float4* partial_slot(const SkinnyParams& p, int item, int seg, int warp) {
+  return p.partials + (((int64_t)item * 2 + seg) * kSkConsumerWarps + warp) * (int64_t)(2 * MT8 * 32);
 }
 
 template <int MT8>
-__device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t, int warp, int lane,
+__device__ void finish_split_tile(const SkinnyParams& p, int item, int seg, int64_t t, int warp, int lane,
                                   const float (&acc)[2][MT8][4]) {
-  const int64_t tile_first = streamk_begin(p.U, p.C, cta) / p.G;
-  float4* slot = partial_slot<MT8>(p, cta, t == tile_first ? 0 : 1, warp);
+  float4* slot = partial_slot<MT8>(p, item, seg, warp);
 #pragma unroll
   for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
     for (int nt = 0; nt < MT8; ++nt)
       __stcg(&slot[(rt * MT8 + nt) * 32 + lane],
              make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]));
-  __threadfence();
   __syncwarp();
+  int* counter = &p.counters[kTileCounterBase + t * kSkConsumerWarps + warp];
   int old = 0;
-  if (lane == 0) old = atomicAdd(&p.counters[t * kSkConsumerWarps + warp], 1);
+  if (lane == 0) old = atomic_add_acq_rel(counter, 1);
   old = __shfl_sync(0xffffffffu, old, 0);
-  const int64_t cf = streamk_owner(p.U, p.C, t * p.G);
-  const int64_t cl = streamk_owner(p.U, p.C, t * p.G + p.G - 1);
-  if (old != (int)(cl - cf)) return;  // not the last contributor
-  __threadfence();
+  const int64_t t_begin = t * p.G;
+  const int cf = item_owner(p.sched, t_begin);
+  const int cl = item_owner(p.sched, t_begin + p.G - 1);
+  if (old != cl - cf) return;  // not the last contributor
+  __syncwarp();
+  // only the first contributor can have started in an earlier tile (its
+  // partial for this tile is then its segment 1)
+  const int seg_cf = item_begin(p.sched, cf) >= t_begin ? 0 : 1;
   float sum[2][MT8][4];
 #pragma unroll
   for (int rt = 0; rt < 2; ++rt)
@@ -151,65 +169,66 @@ __device__ void finish_split_tile(const SkinnyParams& p, int64_t cta, int64_t t,
     for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) sum[rt][nt][e] = 0.0f;
-  // contributors are read RB at a time (loads in flight together), summed in CTA order
-  constexpr int RB = MT8 <= 2 ? 2 : 1;
-  for (int64_t c0 = cf; c0 <= cl; c0 += RB) {
+  constexpr int RB = MT8 == 1 ? 4 : 2;  // contributors loaded together (one L2 round trip)
+  for (int c0 = cf; c0 <= cl; c0 += RB) {
     float4 v[RB][2][MT8];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
-      const int64_t cc = c0 + j;
-      if (cc <= cl) {
-        const int64_t tf = streamk_begin(p.U, p.C, cc) / p.G;
-        const float4* sl = partial_slot<MT8>(p, cc, t == tf ? 0 : 1, warp);
+      const int cc = c0 + j;
+      const float4* sl = partial_slot<MT8>(p, cc, cc == cf ? seg_cf : 0, warp);
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
+      for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-          for (int nt = 0; nt < MT8; ++nt) v[j][rt][nt] = __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]);
-      }
+        for (int nt = 0; nt < MT8; ++nt)
+          v[j][rt][nt] = cc <= cl ? __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < RB; ++j) {
-      if (c0 + j <= cl) {
+    for (int j = 0; j < RB; ++j)
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
+      for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-          for (int nt = 0; nt < MT8; ++nt) {
-            sum[rt][nt][0] += v[j][rt][nt].x;
-            sum[rt][nt][1] += v[j][rt][nt].y;
-            sum[rt][nt][2] += v[j][rt][nt].z;
-            sum[rt][nt][3] += v[j][rt][nt].w;
-          }
-      }
-    }
+        for (int nt = 0; nt < MT8; ++nt) {
+          sum[rt][nt][0] += v[j][rt][nt].x;
+          sum[rt][nt][1] += v[j][rt][nt].y;
+          sum[rt][nt][2] += v[j][rt][nt].z;
+          sum[rt][nt][3] += v[j][rt][nt].w;
+        }
   }
   store_tile<MT8>(p, t, warp, lane, sum);
-  if (lane == 0) p.counters[t * kSkConsumerWarps + warp] = 0;
+  if (lane == 0) *counter = 0;
 }
 
 // Blocks per SM the register budget is shaped for (more resident warps hide
 // the dequant -> MMA dependency latency).
 template <int MT8>
 constexpr int skinny_min_blocks() {
-  return MT8 == 1 ? 4 : (MT8 == 2 ? 3 : 1);
+  return MT8 == 1 ? 4 : 3;
 }
 
 template <int MT8>
 __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_skinny_kernel(const SkinnyParams p) {
   using L = SkinnyLayout<MT8>;
   extern __shared__ __align__(128) uint8_t smem[];
+  int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + kSkStages;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t cta = blockIdx.x;
-  const int64_t u0 = streamk_begin(p.U, p.C, cta);
-  const int n_units = (int)(streamk_begin(p.U, p.C, cta + 1) - u0);
 
+  grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSkStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kSkConsumerWarps);
     }
     fence_mbarrier_init();
+  } else if (threadIdx.x == 32 * kSkConsumerWarps && (int)blockIdx.x < p.items) {
+    // The packed weights are not written by the kernel this one may overlap:
+    // pull the first units of the item this CTA most likely claims into L2.
+    const int64_t u0 = item_begin(p.sched, blockIdx.x);
+    int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
+    if (n > 2 * kSkStages) n = 2 * kSkStages;
+    prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
+    prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
   }
   // token rows M .. 8*MT8-1 of every stage are never copied: zero them once
   {
@@ -222,35 +241,61 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
     }
   }
   __syncthreads();
+  grid_dependency_wait();
 
   if (warp == kSkConsumerWarps) {
     // ---------------------------------------------------------- producer
     if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
     const uint32_t tx = (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256);
-    int issued = 0;
+    int* work = &p.counters[kWorkCounter];
+    int n_stage = 0;  // stages filled so far
     bool ok = true;
-    int64_t g = u0 % p.G;
-    for (int i = 0; i < n_units; ++i, g = (g + 1 == p.G) ? 0 : g + 1) {
-      const int s = i % kSkStages;
-      const uint32_t ph = (uint32_t)(i / kSkStages) & 1u;
-      if (i >= kSkStages && !mbar_wait(&empty[s], ph ^ 1u, p.err)) {
-        ok = false;
-        break;
+    int item = atomicAdd(work, 1);
+    while (ok && item < p.items) {
+      const int64_t ub = item_begin(p.sched, item);
+      const int64_t ue = item_begin(p.sched, item + 1);
+      int64_t t = ub / p.G;
+      int64_t g = ub - t * p.G;
+      for (int64_t u = ub; u < ue; ++u, ++n_stage) {
+        const int s = n_stage % kSkStages;
+        if (n_stage >= kSkStages &&
+            !mbar_wait(&empty[s], ((uint32_t)(n_stage / kSkStages) & 1u) ^ 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        const int flags = (u == ub ? kUnitFirst : 0) | (u == ue - 1 ? kUnitLast : 0);
+        meta[s] = make_int4(item, (int)t, (int)g, flags);
+        uint8_t* st = smem + s * L::kStage;
+        mbar_arrive_expect_tx(&full[s], tx);
+        bulk_g2s_hint(st, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
+        bulk_g2s(st + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
+        for (int m = 0; m < p.M; ++m)
+          bulk_g2s(st + kUnitBytes + kUnitScaleBytes + m * kXRowStride, p.x + (int64_t)m * p.K + g * kGroup, 256,
+                   &full[s]);
+        if (++g == p.G) {
+          g = 0;
+          ++t;
+        }
       }
-      const int64_t u = u0 + i;
-      uint8_t* st = smem + s * L::kStage;
-      mbar_arrive_expect_tx(&full[s], tx);
-      bulk_g2s_hint(st, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
-      bulk_g2s(st + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
-      for (int m = 0; m < p.M; ++m)
-        bulk_g2s(st + kUnitBytes + kUnitScaleBytes + m * kXRowStride, p.x + (int64_t)m * p.K + g * kGroup, 256,
-                 &full[s]);
-      issued = i + 1;
+      if (ok) item = atomicAdd(work, 1);
     }
-    if (!ok) {  // let copies already in flight land before the CTA exits
-      for (int i = (issued > kSkStages ? issued - kSkStages : 0); i < issued; ++i)
+    if (ok) {  // stop marker for the consumers
+      const int s = n_stage % kSkStages;
+      if (n_stage < kSkStages || mbar_wait(&empty[s], ((uint32_t)(n_stage / kSkStages) & 1u) ^ 1u, p.err)) {
+        meta[s] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&full[s]);
+      }
+    } else {  // let copies already in flight land before the CTA exits
+      for (int i = (n_stage > kSkStages ? n_stage - kSkStages : 0); i < n_stage; ++i)
         mbar_wait(&full[i % kSkStages], (uint32_t)(i / kSkStages) & 1u, p.err);
+    }
+    // The last CTA to get here resets the claim counters for the next call
+    // (every CTA has made its final claim before it counts itself out).
+    __threadfence();
+    if (atomicAdd(&p.counters[kExitCounter], 1) == (int)gridDim.x - 1) {
+      p.counters[kWorkCounter] = 0;
+      p.counters[kExitCounter] = 0;
     }
     return;
   }
@@ -264,14 +309,20 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
     for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
-  int64_t t = u0 / p.G;
-  int64_t g = u0 - t * p.G;
-  int64_t seg_g0 = g;
+  int item = 0, item_t0 = 0, seg_g0 = 0;
 
-  for (int i = 0; i < n_units; ++i) {
+  for (int i = 0;; ++i) {
     const int s = i % kSkStages;
     if (!mbar_wait(&full[s], (uint32_t)(i / kSkStages) & 1u, p.err)) return;
     const uint32_t st = smem_u32(smem + s * L::kStage);
+    const uint4 mu = lds128(smem_u32(&meta[s]));
+    const int4 mt = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
+    if (mt.x < 0) break;
+    if (mt.w & kUnitFirst) {
+      item = mt.x;
+      item_t0 = mt.y;
+      seg_g0 = mt.z;
+    }
     const uint32_t wb = st + warp * 2048 + lane * 16;
     uint4 wq[2][2];
 #pragma unroll
@@ -320,11 +371,11 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
         acc[rt][nt][3] = fmaf(sc[rt][1], part[rt][nt][3], acc[rt][nt][3]);
       }
 
-    if (g == p.G - 1 || i == n_units - 1) {  // end of this CTA's segment of tile t
-      if (seg_g0 == 0 && g == p.G - 1)
-        store_tile<MT8>(p, t, warp, lane, acc);
+    if (mt.z == p.G - 1 || (mt.w & kUnitLast)) {  // end of this item's segment of tile mt.y
+      if (seg_g0 == 0 && mt.z == p.G - 1)
+        store_tile<MT8>(p, mt.y, warp, lane, acc);
       else
-        finish_split_tile<MT8>(p, cta, t, warp, lane, acc);
+        finish_split_tile<MT8>(p, item, mt.y == item_t0 ? 0 : 1, mt.y, warp, lane, acc);
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
@@ -332,10 +383,6 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
       seg_g0 = 0;
-    }
-    if (++g == p.G) {
-      g = 0;
-      ++t;
     }
   }
 }
@@ -355,34 +402,16 @@ static cudaError_t skinny_occupancy(int* blocks_per_sm) {
                                                       L::kTotal);
 }
 
-static int skinny_smem(int mt8) {
-  switch (mt8) {
-    case 1: return SkinnyLayout<1>::kTotal;
-    case 2: return SkinnyLayout<2>::kTotal;
-    case 3: return SkinnyLayout<3>::kTotal;
-    case 4: return SkinnyLayout<4>::kTotal;
-    case 5: return SkinnyLayout<5>::kTotal;
-    case 6: return SkinnyLayout<6>::kTotal;
-    case 7: return SkinnyLayout<7>::kTotal;
-    default: return SkinnyLayout<8>::kTotal;
-  }
-}
+static int skinny_smem(int mt8) { return mt8 == 1 ? SkinnyLayout<1>::kTotal : SkinnyLayout<2>::kTotal; }
 
 static cudaError_t skinny_occupancy_dispatch(int mt8, int* nb) {
-  switch (mt8) {
-    case 1: return skinny_occupancy<1>(nb);
-    case 2: return skinny_occupancy<2>(nb);
-    case 3: return skinny_occupancy<3>(nb);
-    case 4: return skinny_occupancy<4>(nb);
-    case 5: return skinny_occupancy<5>(nb);
-    case 6: return skinny_occupancy<6>(nb);
-    case 7: return skinny_occupancy<7>(nb);
-    default: return skinny_occupancy<8>(nb);
-  }
+  return mt8 == 1 ? skinny_occupancy<1>(nb) : skinny_occupancy<2>(nb);
 }
 
-cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, SkinnyPlan* plan) {
-  static int cached_nb[64][9];  // [device][mt8] blocks per SM (0 = unknown)
+cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes,
+                        SkinnyPlan* plan) {
+  static int cached_nb[64][3];  // [device][mt8] blocks per SM (0 = unknown)
+  if (M < 1 || M >= kTcMinM) return cudaErrorInvalidValue;  // M >= 16 runs on the tcgen05 path
   plan->mt8 = (M + 7) / 8;
   plan->units = (N / kUnitRows) * (K / kGroup);
   int nb = 0;
@@ -397,8 +426,15 @@ cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, Skin
   int64_t ctas = (int64_t)dev.num_sms * nb;
   if (ctas > plan->units) ctas = plan->units;
   plan->ctas = ctas;
-  plan->counter_bytes = kCounterRegionBytes;  // (N/128)*4 counters at its start
-  plan->partial_bytes = (size_t)ctas * 2 * kSkConsumerWarps * 2 * plan->mt8 * 32 * sizeof(float4);
+  // partial slots: 2 segments x 4 warps x (32 rows x 8*MT8 tokens) fp32 per
+  // item. Every split tile costs its contributors a partial store and an
+  // atomic round trip, so this path keeps one round: every CTA one contiguous
+  // run of units, at most two split tiles per CTA.
+  (void)max_partial_bytes;
+  const size_t per_item = (size_t)2 * kSkConsumerWarps * 2 * plan->mt8 * 32 * sizeof(float4);
+  plan->sched = make_item_sched(plan->units, (int)ctas, 1, 1);
+  plan->counter_bytes = kCounterRegionBytes;
+  plan->partial_bytes = (size_t)plan->sched.R * ctas * per_item;
   plan->smem_bytes = (size_t)skinny_smem(plan->mt8);
   return cudaSuccess;
 }
@@ -408,8 +444,8 @@ size_t skinny_workspace_bytes(const SkinnyPlan& plan) { return plan.counter_byte
 template <int MT8>
 static cudaError_t launch_skinny_t(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t stream) {
   using L = SkinnyLayout<MT8>;
-  w4a16_skinny_kernel<MT8><<<(unsigned)plan.ctas, kSkThreads, L::kTotal, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(w4a16_skinny_kernel<MT8>, dim3((unsigned)plan.ctas), dim3(kSkThreads), (size_t)L::kTotal, stream,
+                    p);
 }
 
 cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
@@ -425,22 +461,16 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
   p.err = dev.err;
   p.K = K;
   p.N = N;
-  p.U = plan.units;
   p.G = K / kGroup;
-  p.C = plan.ctas;
   p.M = M;
+  p.items = plan.sched.R * plan.sched.C;
+  p.sched = plan.sched;
   p.dq.m4 = 1u << 28;
   p.dq.m8 = 1u << 24;
   p.dq.m12 = 1u << 20;
   switch (plan.mt8) {
     case 1: return launch_skinny_t<1>(p, plan, stream);
     case 2: return launch_skinny_t<2>(p, plan, stream);
-    case 3: return launch_skinny_t<3>(p, plan, stream);
-    case 4: return launch_skinny_t<4>(p, plan, stream);
-    case 5: return launch_skinny_t<5>(p, plan, stream);
-    case 6: return launch_skinny_t<6>(p, plan, stream);
-    case 7: return launch_skinny_t<7>(p, plan, stream);
-    case 8: return launch_skinny_t<8>(p, plan, stream);
     default: return cudaErrorInvalidValue;
   }
 }

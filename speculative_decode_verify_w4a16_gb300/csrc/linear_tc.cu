@@ -1,21 +1,29 @@
-// W4A16 verify linear on the 5th-generation tensor cores (tcgen05 + TMEM),
-// for the larger verify token counts of a tree draft (M = 16..64).
+// W4A16 verify linear on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// Same stream-K split of the packed (row-tile, group) units as the
-// fragment path. Per unit (128 weight rows x 128 K):
-//   producer warp   1-D bulk copies of the packed codes and scales, 2-D TMA
-//                   of the token tile x[0:NT, 128g : 128g+128] (128-byte
-//                   swizzle; token rows past M read as zero)
-//   8 consumer warps  dequantise their 16 rows x 128 K to exact bf16 codes
-//                   and store them into TMEM (the UMMA A operand), then, one
-//                   unit behind, read the fp32 group product from TMEM and
-//                   fold it into registers with the row's fp16 scale
-//   MMA warp        8 x tcgen05.mma kind::f16 (M=128 weight rows, N=NT
-//                   tokens, K=16) per unit into a TMEM accumulator, commit
-// A and D are double-buffered in TMEM so dequantisation of unit i overlaps
-// the MMAs of unit i and the scale epilogue of unit i-1.
-// A tile split between CTAs is finished by its last contributor, summing the
-// fp32 partials in CTA order (deterministic); counters reset themselves.
+// Same item schedule of the packed (row-tile, group) units as the fragment
+// path (sched.cuh); one CTA per SM owns the SM's whole tensor memory.
+// Warp roles, per unit (128 weight rows x 128 K):
+//   producer warp     claims items; 1-D bulk copies of the packed codes and
+//                     scales, 2-D TMA of the token tile x[0:NT, 128g : 128g+128]
+//                     (128-byte swizzle; token rows past M read as zero)
+//   3 dequant groups  of 4 warps (one per TMEM lane quadrant) take the units
+//                     in turn: dequantise the unit to exact bf16 codes and
+//                     store them into TMEM, the UMMA A operand; hand the
+//                     unit's scales and metadata on to the epilogue
+//   3 MMA warps       one per dequant group (its units only): 8 x
+//                     tcgen05.mma kind::f16 (M = 128 weight rows, N = NT
+//                     tokens, K = 16) per unit into a TMEM accumulator,
+//                     commit. Several issuers keep the tensor pipe fed while
+//                     each waits on its barriers.
+//   8 epilogue warps  (quadrant x token half) read each unit's fp32 product
+//                     from TMEM and fold it into registers with the row's
+//                     fp16 group scale; store at the end of a tile segment
+// TMEM holds a ring of kA dequantised units (64 columns each) and kD
+// accumulators (NT columns each); consecutive units are dequantised by
+// different groups, so the dequantisation of several units, the MMAs of
+// another and the epilogues of earlier ones all overlap.
+// A tile split between items is finished by its last contributor, which
+// adds the fp32 partials of all contributors in item order.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -23,36 +31,47 @@
 #include "common.cuh"
 #include "format.cuh"
 #include "internal.h"
+#include "sched.cuh"
 #include "tcgen05.cuh"
 
 namespace w4a16 {
 
-constexpr int kTcConsumerWarps = 8;
-constexpr int kTcProducerWarp = 8;
-constexpr int kTcMmaWarp = 9;
-constexpr int kTcThreads = 32 * 10;
-constexpr uint32_t kTcTmemCols = 256;  // A: 2 x 64 columns at 0 / 64; D: 2 x NT columns from 128
+constexpr int kTcDqGroups = 3;                  // dequant groups of 4 warps, one MMA warp each
+constexpr int kTcDqWarps = 4 * kTcDqGroups;     // warps 0 .. 11
+constexpr int kTcEpWarps = 8;                   // warps 12 .. 19
+constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 20
+constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 21 .. 23
+constexpr int kTcThreads = 32 * (kTcMmaWarp0 + kTcDqGroups);
+constexpr uint32_t kTcTmemCols = 512;  // the whole tensor memory of the SM
+constexpr int kTcRing = 16;            // scale / metadata hand-off ring (units)
 
 template <int NT>
 struct TcLayout {
-  // ring depth: as many stages as two CTAs per SM can hold
-  static constexpr int kStages = NT <= 16 ? 8 : (NT <= 32 ? 6 : (NT <= 48 ? 5 : 4));
-  // TMEM: 2 A buffers of 64 columns, kDBuf accumulators of NT columns; the
-  // epilogue of a unit runs kDBuf - 1 units after its dequantisation so the
-  // MMAs have that long to complete before anyone waits for them
-  static constexpr int kDBuf = NT <= 32 ? 3 : 2;
-  static constexpr int kLag = kDBuf - 1;
-  static constexpr int kX = NT * 128;                 // one 64-wide K half of the token tile
+  // TMEM ring depths: kA dequantised units (64 columns each) at column 0,
+  // kD accumulators (NT columns each) after them
+  static constexpr int kA = NT <= 16 ? 6 : 4;
+  static constexpr int kD = NT <= 16 ? 8 : (NT <= 32 ? 8 : (NT <= 48 ? 5 : 4));
+  static_assert(kA * 64 + kD * NT <= (int)kTcTmemCols, "TMEM budget");
+  // a unit's hand-off entry is rewritten kTcRing units later; by then the
+  // dequantisation of that later unit has waited for the MMAs kA units back,
+  // which waited for the epilogue kD units before those
+  static_assert(kA + kD <= kTcRing, "hand-off ring depth");
+  static constexpr int kX = NT * 128;  // one 64-wide K half of the token tile
   static constexpr int kXOff0 = 0;
   static constexpr int kXOff1 = kX;
   static constexpr int kWOff = 2 * kX;
   static constexpr int kSOff = kWOff + kUnitBytes;
   static constexpr int kStageRaw = kSOff + kUnitScaleBytes;
   static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kBarOff = kStages * kStage;
-  // full[S], empty[S], a_full[2], mma_done[kDBuf], d_free[kDBuf], tmem base
-  static constexpr int kTotal = kBarOff + (2 * kStages + 2 + 2 * kDBuf) * 8 + 16 + 1024;  // +1024: alignment slack
+  static constexpr int kStages = (192 * 1024) / kStage;
+  static constexpr int kScRingOff = kStages * kStage;                 // kTcRing x 256 B scales
+  static constexpr int kMetaRingOff = kScRingOff + kTcRing * kUnitScaleBytes;  // kTcRing x int4
+  static constexpr int kMetaOff = kMetaRingOff + kTcRing * 16;        // kStages x int4 (per stage)
+  static constexpr int kBarOff = kMetaOff + kStages * 16;
+  // full[S], empty[S], a_full[kA], a_free[kA], mma_done[kD], d_free[kD], tmem base
+  static constexpr int kTotal = kBarOff + (2 * kStages + 2 * kA + 2 * kD) * 8 + 16 + 1024;  // +1024: alignment
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
+  static_assert(kStages >= kTcDqGroups + 1, "ring depth");
 };
 
 struct DequantConstsTc {
@@ -63,13 +82,19 @@ struct TcParams {
   const uint8_t* qw;
   const uint8_t* sc;
   __nv_bfloat16* out;
-  float4* partials;
-  int* counters;
+  float4* partials;  // split-tile partial slots
+  int* counters;     // item-claim and split-tile counters
   unsigned* err;
-  int64_t K, N, U, G, C;
+  int64_t K, N, G;
   int M;
+  int items;  // R * C
+  ItemSched sched;
   DequantConstsTc dq;
 };
+
+// Stage metadata written by the producer: the unit's item, tile and group.
+constexpr int kTcUnitFirst = 1;  // first unit of its item
+constexpr int kTcUnitLast = 2;   // last unit of its item
 
 __device__ __forceinline__ uint32_t tc_lop3(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
@@ -89,6 +114,7 @@ __device__ __forceinline__ uint32_t tc_fma_bf16x2(uint32_t a, uint32_t b, uint32
 
 // One packed word -> the four 16x256b TMEM registers of one 16-wide K step:
 // (row g, k 4c..4c+1), (row g, k 4c+2..4c+3), (row g+8, k 4c..), (row g+8, k 4c+2..).
+// (nibble | 0x4300) is the bf16 value 128 + c, and (128 + c) * 1 - 136 = c - 8.
 __device__ __forceinline__ void tc_dequant(uint32_t w, const DequantConstsTc& k, uint32_t* r) {
   const uint32_t mask = 0x000F000Fu, magic = 0x43004300u, one = 0x3F803F80u, neg136 = 0xC308C308u;
   r[0] = tc_fma_bf16x2(tc_lop3(w, mask, magic), one, neg136);                     // bits 0/16
@@ -97,12 +123,7 @@ __device__ __forceinline__ void tc_dequant(uint32_t w, const DequantConstsTc& k,
   r[3] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m12), mask, magic), one, neg136);    // bits 12/28
 }
 
-// Partial-sum slot of one consumer warp: 32 rows x NT/2 fp32, float4-interleaved by lane.
-template <int NT>
-__device__ __forceinline__ float4* tc_slot(const TcParams& p, int64_t cta, int seg, int warp) {
-  return p.partials + ((cta * 2 + seg) * kTcConsumerWarps + warp) * (int64_t)(NT / 8 * 32);
-}
-
+// Epilogue slice of a warp: rows 32q + lane, tokens h*NT/2 + j.
 template <int NT>
 __device__ __forceinline__ void tc_store(const TcParams& p, int64_t t, int q, int h, int lane,
                                          const float (&acc)[NT / 2]) {
@@ -114,58 +135,89 @@ __device__ __forceinline__ void tc_store(const TcParams& p, int64_t t, int q, in
   }
 }
 
+// Split tiles. Each item that covers part of a tile's K range writes the
+// fp32 sums of each epilogue warp's slice (32 rows x NT/2 tokens) to its own
+// slot (item, segment, warp) and counts itself in with an atomic per (tile,
+// warp); whichever contributor arrives last adds all slots in item order and
+// stores the tile: the result does not depend on timing. Counters reset
+// themselves for the next call.
 template <int NT>
-__device__ void tc_finish_split(const TcParams& p, int64_t cta, int64_t t, int warp, int lane,
-                                const float (&acc)[NT / 2]) {
-  const int q = warp & 3, h = warp >> 2;
-  const int64_t tile_first = streamk_begin(p.U, p.C, cta) / p.G;
-  float4* slot = tc_slot<NT>(p, cta, t == tile_first ? 0 : 1, warp);
-#pragma unroll
-  for (int j = 0; j < NT / 8; ++j)
-    __stcg(&slot[j * 32 + lane], make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
-  __threadfence();
-  __syncwarp();
-  int old = 0;
-  if (lane == 0) old = atomicAdd(&p.counters[t * kTcConsumerWarps + warp], 1);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  const int64_t cf = streamk_owner(p.U, p.C, t * p.G);
-  const int64_t cl = streamk_owner(p.U, p.C, t * p.G + p.G - 1);
-  if (old != (int)(cl - cf)) return;
-  __threadfence();
-  float sum[NT / 2];
-#pragma unroll
-  for (int j = 0; j < NT / 2; ++j) sum[j] = 0.0f;
-  constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);
-  for (int64_t c0 = cf; c0 <= cl; c0 += RB) {
-    float4 v[RB][NT / 8];
-#pragma unroll
-    for (int i = 0; i < RB; ++i) {
-      const int64_t cc = c0 + i;
-      if (cc <= cl) {
-        const int64_t tf = streamk_begin(p.U, p.C, cc) / p.G;
-        const float4* sl = tc_slot<NT>(p, cc, t == tf ? 0 : 1, warp);
-#pragma unroll
-        for (int j = 0; j < NT / 8; ++j) v[i][j] = __ldcg(&sl[j * 32 + lane]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < RB; ++i)
-      if (c0 + i <= cl) {
-#pragma unroll
-        for (int j = 0; j < NT / 8; ++j) {
-          sum[4 * j] += v[i][j].x;
-          sum[4 * j + 1] += v[i][j].y;
-          sum[4 * j + 2] += v[i][j].z;
-          sum[4 * j + 3] += v[i][j].w;
-        }
-      }
-  }
-  tc_store<NT>(p, t, q, h, lane, sum);
-  if (lane == 0) p.counters[t * kTcConsumerWarps + warp] = 0;
+__device__ __forceinline__ float4* tc_slot(const TcParams& p, int item, int seg, int epw) {
+  return p.partials + (((int64_t)item * 2 + seg) * kTcEpWarps + epw) * (int64_t)(NT / 8 * 32);
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+__device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t, int q, int h, int lane,
+                                const float (&acc)[NT / 2]) {
+  const int epw = h * 4 + q;
+  float4* slot = tc_slot<NT>(p, item, seg, epw);
+#pragma unroll
+  for (int j = 0; j < NT / 8; ++j)
+    __stcg(&slot[j * 32 + lane], make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+  __syncwarp();
+  int* counter = &p.counters[kTileCounterBase + t * kTcEpWarps + epw];
+  int old = 0;
+  if (lane == 0) old = atomic_add_acq_rel(counter, 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  const int64_t t_begin = t * p.G;
+  const int cf = item_owner(p.sched, t_begin);
+  const int cl = item_owner(p.sched, t_begin + p.G - 1);
+  if (old != cl - cf) return;  // not the last contributor
+  __syncwarp();
+  // only the first contributor can have started in an earlier tile (its
+  // partial for this tile is then its segment 1)
+  const int seg_cf = item_begin(p.sched, cf) >= t_begin ? 0 : 1;
+  float sum[NT / 2];
+#pragma unroll
+  for (int j = 0; j < NT / 2; ++j) sum[j] = 0.0f;
+  constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);  // contributors loaded together
+  for (int c0 = cf; c0 <= cl; c0 += RB) {
+    float4 v[RB][NT / 8];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const int cc = c0 + r;
+      const float4* sl = tc_slot<NT>(p, cc, cc == cf ? seg_cf : 0, epw);
+#pragma unroll
+      for (int j = 0; j < NT / 8; ++j)
+        v[r][j] = cc <= cl ? __ldcg(&sl[j * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+      for (int j = 0; j < NT / 8; ++j) {
+        sum[4 * j] += v[r][j].x;
+        sum[4 * j + 1] += v[r][j].y;
+        sum[4 * j + 2] += v[r][j].z;
+        sum[4 * j + 3] += v[r][j].w;
+      }
+  }
+  tc_store<NT>(p, t, q, h, lane, sum);
+  if (lane == 0) *counter = 0;
+}
+
+// acc[j] += sc * D[lane][col + j], j < W (TMEM columns of this warp's slice)
+template <int W>
+__device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&acc)[W]) {
+  if constexpr (W >= 16) {
+#pragma unroll
+    for (int c0 = 0; c0 + 16 <= W; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld16_sync(dt + c0, v);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(sc, __uint_as_float(v[c]), acc[c0 + c]);
+    }
+  }
+  if constexpr (W % 16 >= 8) {
+    constexpr int c0 = W / 16 * 16;
+    uint32_t v[8];
+    tmem_ld8_sync(dt + c0, v);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(sc, __uint_as_float(v[c]), acc[c0 + c]);
+  }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                 const TcParams p) {
   using L = TcLayout<NT>;
   extern __shared__ uint8_t smem_raw[];
@@ -173,37 +225,50 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + L::kStages;
   uint64_t* a_full = empty + L::kStages;
-  uint64_t* mma_done = a_full + 2;
-  uint64_t* d_free = mma_done + L::kDBuf;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(d_free + L::kDBuf);
-
+  uint64_t* a_free = a_full + L::kA;
+  uint64_t* mma_done = a_free + L::kA;
+  uint64_t* d_free = mma_done + L::kD;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(d_free + L::kD);
+  int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
+  int4* meta_ring = reinterpret_cast<int4*>(smem + L::kMetaRingOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t cta = blockIdx.x;
-  const int64_t u0 = streamk_begin(p.U, p.C, cta);
-  const int n_units = (int)(streamk_begin(p.U, p.C, cta + 1) - u0);
 
+  grid_launch_dependents();
+  if (warp == kTcProducerWarp && lane == 0 && (int)blockIdx.x < p.items) {
+    // The packed weights are not written by the kernel this one may overlap:
+    // pull the first units of the item this CTA most likely claims into L2.
+    const int64_t u0 = item_begin(p.sched, blockIdx.x);
+    int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
+    if (n > 2 * L::kStages) n = 2 * L::kStages;
+    prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
+    prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);  // released by the commit of the unit's MMAs
     }
-    for (int b = 0; b < 2; ++b) mbar_init(&a_full[b], kTcConsumerWarps);
-    for (int b = 0; b < L::kDBuf; ++b) {
-      mbar_init(&mma_done[b], 1);
-      mbar_init(&d_free[b], kTcConsumerWarps);
+    for (int b = 0; b < L::kA; ++b) {
+      mbar_init(&a_full[b], 4);  // the 4 warps of the dequant group
+      mbar_init(&a_free[b], 1);  // commit of the MMAs that read A[b]
+    }
+    for (int b = 0; b < L::kD; ++b) {
+      mbar_init(&mma_done[b], 2);  // commit of the unit's MMAs + the MMA thread's release of the hand-off
+      mbar_init(&d_free[b], kTcEpWarps);
     }
     fence_mbarrier_init();
   }
-  if (warp == kTcMmaWarp) {
+  if (warp == kTcMmaWarp0) {
     tmem_alloc(tmem_base_s, kTcTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dependency_wait();
   const uint32_t tmem = *tmem_base_s;
-  const uint32_t a_col[2] = {0u, 64u};
-  auto d_col = [](int buf) { return 128u + (uint32_t)(buf * NT); };
+  auto a_col = [](int buf) { return (uint32_t)(buf * 64); };
+  auto d_col = [](int buf) { return (uint32_t)(L::kA * 64 + buf * NT); };
   int mma_issued = 0;  // units whose MMAs were committed (MMA warp only)
 
   if (warp == kTcProducerWarp) {
@@ -211,133 +276,173 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const uint32_t tx = (uint32_t)(2 * L::kX + kUnitBytes + kUnitScaleBytes);
-      int issued = 0;
+      int* work = &p.counters[kWorkCounter];
+      int n_stage = 0;
       bool ok = true;
-      int64_t g = u0 % p.G;
-      for (int i = 0; i < n_units; ++i, g = (g + 1 == p.G) ? 0 : g + 1) {
-        const int s = i % L::kStages;
-        if (i >= L::kStages && !mbar_wait(&empty[s], ((uint32_t)(i / L::kStages) & 1u) ^ 1u, p.err)) {
+      int item = atomicAdd(work, 1);
+      while (ok && item < p.items) {
+        const int64_t ub = item_begin(p.sched, item);
+        const int64_t ue = item_begin(p.sched, item + 1);
+        int64_t t = ub / p.G;
+        int64_t g = ub - t * p.G;
+        for (int64_t u = ub; u < ue; ++u, ++n_stage) {
+          const int s = n_stage % L::kStages;
+          if (n_stage >= L::kStages &&
+              !mbar_wait(&empty[s], ((uint32_t)(n_stage / L::kStages) & 1u) ^ 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          meta[s] = make_int4(item, (int)t, (int)g, (u == ub ? kTcUnitFirst : 0) | (u == ue - 1 ? kTcUnitLast : 0));
+          uint8_t* st = smem + s * L::kStage;
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d(st + L::kXOff0, &xmap, (int32_t)(g * kGroup), 0, &full[s]);
+          tma_load_2d(st + L::kXOff1, &xmap, (int32_t)(g * kGroup + 64), 0, &full[s]);
+          bulk_g2s_hint(st + L::kWOff, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
+          bulk_g2s(st + L::kSOff, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
+          if (++g == p.G) {
+            g = 0;
+            ++t;
+          }
+        }
+        if (ok) item = atomicAdd(work, 1);
+      }
+      // one stop marker per dequant group (each reads every kTcDqGroups-th
+      // stage): -1 at the first index past the last unit, where the MMA warp
+      // and the epilogue stop too; -2 at the other groups' next indices
+      for (int k = 0; ok && k < kTcDqGroups; ++k, ++n_stage) {
+        const int s = n_stage % L::kStages;
+        if (n_stage >= L::kStages &&
+            !mbar_wait(&empty[s], ((uint32_t)(n_stage / L::kStages) & 1u) ^ 1u, p.err)) {
           ok = false;
           break;
         }
-        const int64_t u = u0 + i;
-        uint8_t* st = smem + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], tx);
-        tma_load_2d(st + L::kXOff0, &xmap, (int32_t)(g * kGroup), 0, &full[s]);
-        tma_load_2d(st + L::kXOff1, &xmap, (int32_t)(g * kGroup + 64), 0, &full[s]);
-        bulk_g2s_hint(st + L::kWOff, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
-        bulk_g2s(st + L::kSOff, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
-        issued = i + 1;
+        meta[s] = make_int4(k == 0 ? -1 : -2, 0, 0, 0);
+        mbar_arrive(&full[s]);
       }
-      if (!ok)
-        for (int i = (issued > L::kStages ? issued - L::kStages : 0); i < issued; ++i)
+      if (!ok) {  // let copies already in flight land before the CTA exits
+        for (int i = (n_stage > L::kStages ? n_stage - L::kStages : 0); i < n_stage; ++i)
           mbar_wait(&full[i % L::kStages], (uint32_t)(i / L::kStages) & 1u, p.err);
+      }
+      // the last CTA to get here resets the claim counters for the next call
+      __threadfence();
+      if (atomicAdd(&p.counters[kExitCounter], 1) == (int)gridDim.x - 1) {
+        p.counters[kWorkCounter] = 0;
+        p.counters[kExitCounter] = 0;
+      }
     }
-  } else if (warp == kTcMmaWarp) {
+  } else if (warp >= kTcMmaWarp0) {
     // ------------------------------------------------------------- MMA
+    // MMA warp j issues the units of dequant group j (i = j, j + 3, ...).
+    // The group waited for the unit's stage before it arrived on a_full, so
+    // the token tile is in shared memory once a_full completes.
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(NT);
-      for (int i = 0; i < n_units; ++i) {
-        const int s = i % L::kStages, b = i & 1, db = i % L::kDBuf;
-        if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
-        if (!mbar_wait(&a_full[b], (uint32_t)(i >> 1) & 1u, p.err)) break;
-        if (i >= L::kDBuf && !mbar_wait(&d_free[db], ((uint32_t)(i / L::kDBuf) & 1u) ^ 1u, p.err)) break;
+      for (int i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
+        const int s = i % L::kStages, b = i % L::kA, db = i % L::kD;
+        if (!mbar_wait(&a_full[b], (uint32_t)(i / L::kA) & 1u, p.err)) break;
+        if (i >= L::kD && !mbar_wait(&d_free[db], ((uint32_t)(i / L::kD) & 1u) ^ 1u, p.err)) break;
+        const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
+        if (mk < 0) {  // stop marker
+          if (mk == -1) {  // the epilogue's last index: complete its phase without MMAs
+            mbar_arrive(&mma_done[db]);
+            mbar_arrive(&mma_done[db]);
+          }
+          break;
+        }
         tc_fence_after();
-        const uint32_t xs = smem_u32(smem + s * L::kStage);
+        const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + s * L::kStage) + L::kXOff0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = umma_desc_sw128_kmajor(xs + (kk < 4 ? L::kXOff0 : L::kXOff1) + 32 * (kk & 3));
-          umma_bf16_ts(tmem + d_col(db), tmem + a_col[b] + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
+          // start-address field (bits 0..13, 16-byte units) of the K step's rows
+          const uint64_t bd = bd0 + (uint64_t)(((kk < 4 ? 0 : L::kX) + 32 * (kk & 3)) >> 4);
+          umma_bf16_ts(tmem + d_col(db), tmem + a_col(b) + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
         }
         umma_commit(&mma_done[db]);
+        umma_commit(&a_free[b]);
         umma_commit(&empty[s]);  // codes were read before a_full, the token tile by these MMAs
+        // release (to the epilogue) of the hand-off entry this thread acquired through a_full
+        mbar_arrive(&mma_done[db]);
         mma_issued = i + 1;
       }
     }
-  } else {
-    // ------------------------------------------------------- consumers
-    const int q = warp & 3, h = warp >> 2;  // TMEM lane quadrant, row-tile / column half
-    const int j = lane;                      // row inside the 32-row slice (epilogue)
-    const int sc_half = ((q * 8 + (j & 7)) * 2 + (j >> 4)) * 2 + ((j >> 3) & 1);
-    float acc[NT / 2];
-#pragma unroll
-    for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
-    float sc_q[L::kLag + 1];  // scales of units i, i-1, .., i-kLag
-#pragma unroll
-    for (int k = 0; k <= L::kLag; ++k) sc_q[k] = 0.0f;
-    int64_t te = u0 / p.G, ge = u0 - te * p.G;  // (tile, group) of the unit in the epilogue
-    int64_t seg_g0 = ge;
-    for (int i = 0; i < n_units + L::kLag; ++i) {
-#pragma unroll
-      for (int k = L::kLag; k > 0; --k) sc_q[k] = sc_q[k - 1];
-      sc_q[0] = 0.0f;
-      if (i < n_units) {
-        const int s = i % L::kStages, b = i & 1;
-        if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
-        if (i >= 2) {  // A[b] is free once the MMAs of unit i-2 have completed
-          const int e2 = i - 2;
-          if (!mbar_wait(&mma_done[e2 % L::kDBuf], (uint32_t)(e2 / L::kDBuf) & 1u, p.err)) break;
-          tc_fence_after();
+  } else if (warp < kTcDqWarps) {
+    // ------------------------------------------------------ dequant groups
+    const int grp = warp >> 2, q = warp & 3;
+    for (int i = grp;; i += kTcDqGroups) {
+      const int s = i % L::kStages, b = i % L::kA;
+      if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
+      const uint4 mu = lds128(smem_u32(&meta[s]));
+      // A[b] is free once the MMAs of unit i - kA have completed
+      if (i >= L::kA && !mbar_wait(&a_free[b], (uint32_t)(i / L::kA - 1) & 1u, p.err)) break;
+      const bool stop = (int)mu.x < 0;
+      if (stop) {
+        // forward the marker to this group's MMA warp (and through it to the
+        // epilogue, which stops at the first one)
+        if (q == 0 && lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, 0, 0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[b]);
+        break;
+      }
+      const uint32_t st = smem_u32(smem + s * L::kStage);
+      if (q == 0) {  // hand the unit's scales and metadata on to the epilogue
+        if (lane < kUnitScaleBytes / 16) {
+          const uint4 v = lds128(st + L::kSOff + lane * 16);
+          *reinterpret_cast<uint4*>(smem + L::kScRingOff + (i % kTcRing) * kUnitScaleBytes + lane * 16) = v;
         }
-        const uint32_t st = smem_u32(smem + s * L::kStage);
-        const uint32_t wb = st + L::kWOff + ((q * 2 + h) * 2) * 512 + lane * 16;
-        sc_q[0] = __half2float(__ushort_as_half(
-            *reinterpret_cast<const unsigned short*>(smem + s * L::kStage + L::kSOff + 2 * sc_half)));
-        const uint32_t ta = tmem + ((uint32_t)(32 * q + 16 * h) << 16) + a_col[b];
+        if (lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
+      }
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {  // K half: 4 words -> 4 K steps -> 32 TMEM columns
-          const uint4 w = lds128(wb + hh * 512);
+      for (int rt = 0; rt < 2; ++rt) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // 16 rows x 64 K -> 16 lanes x 32 TMEM columns
+          const uint4 w = lds128(st + L::kWOff + (((q * 2 + rt) * 2 + hh) * 32 + lane) * 16);
           uint32_t r[16];
           tc_dequant(w.x, p.dq, &r[0]);
           tc_dequant(w.y, p.dq, &r[4]);
           tc_dequant(w.z, p.dq, &r[8]);
           tc_dequant(w.w, p.dq, &r[12]);
-          tmem_st_16x256b_x4(ta + 32 * hh, r);
+          tmem_st_16x256b_x4(tmem + ((uint32_t)(32 * q + 16 * rt) << 16) + a_col(b) + 32 * hh, r);
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[b]);
       }
-      if (i >= L::kLag) {
-        // epilogue of unit e = i - kLag
-        const int e = i - L::kLag, db = e % L::kDBuf;
-        if (!mbar_wait(&mma_done[db], (uint32_t)(e / L::kDBuf) & 1u, p.err)) break;
-        tc_fence_after();
-        const float sc_e = sc_q[L::kLag];
-        const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16) + d_col(db) + h * (NT / 2);
-        if constexpr (NT / 2 >= 16) {
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[b]);
+    }
+  } else if (warp < kTcDqWarps + kTcEpWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3, h = (warp - kTcDqWarps) >> 2;  // TMEM lane quadrant; token half
+    const int sc_half = ((q * 8 + (lane & 7)) * 2 + (lane >> 4)) * 2 + ((lane >> 3) & 1);  // row 32q + lane
+    float acc[NT / 2];
 #pragma unroll
-          for (int c0 = 0; c0 + 16 <= NT / 2; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16_sync(dt + c0, v);
+    for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
+    int item = 0, item_t0 = 0, seg_g0 = 0;
+    for (int e = 0;; ++e) {
+      const int db = e % L::kD;
+      if (!mbar_wait(&mma_done[db], (uint32_t)(e / L::kD) & 1u, p.err)) break;
+      const uint4 mu = lds128(smem_u32(&meta_ring[e % kTcRing]));
+      const int4 me = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
+      if (me.x < 0) break;  // stop marker
+      const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
+          smem + L::kScRingOff + (e % kTcRing) * kUnitScaleBytes + 2 * sc_half)));
+      tc_fence_after();
+      tc_epilogue_fma<NT / 2>(tmem + ((uint32_t)(32 * q) << 16) + d_col(db) + h * (NT / 2), sc, acc);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_free[db]);
+      if (me.w & kTcUnitFirst) {
+        item = me.x;
+        item_t0 = me.y;
+        seg_g0 = me.z;
+      }
+      if (me.z == p.G - 1 || (me.w & kTcUnitLast)) {  // end of this item's segment of tile me.y
+        if (seg_g0 == 0 && me.z == p.G - 1)
+          tc_store<NT>(p, me.y, q, h, lane, acc);
+        else
+          tc_finish_split<NT>(p, item, me.y == item_t0 ? 0 : 1, me.y, q, h, lane, acc);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(sc_e, __uint_as_float(v[c]), acc[c0 + c]);
-          }
-        }
-        if constexpr ((NT / 2) % 16 != 0) {
-          constexpr int c0 = (NT / 2) / 16 * 16;
-          uint32_t v[8];
-          tmem_ld8_sync(dt + c0, v);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(sc_e, __uint_as_float(v[c]), acc[c0 + c]);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&d_free[db]);
-        if (ge == p.G - 1 || e == n_units - 1) {
-          if (seg_g0 == 0 && ge == p.G - 1)
-            tc_store<NT>(p, te, q, h, lane, acc);
-          else
-            tc_finish_split<NT>(p, cta, te, warp, lane, acc);
-#pragma unroll
-          for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
-          seg_g0 = 0;
-        }
-        if (++ge == p.G) {
-          ge = 0;
-          ++te;
-        }
+        for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
+        seg_g0 = 0;
       }
     }
   }
@@ -345,12 +450,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) w4a16_tc_kernel(const __grid_co
   // ---------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == kTcMmaWarp) {
-    if (lane == 0 && mma_issued > 0) {  // normally already observed by the consumers
-      const int e = mma_issued - 1;
-      mbar_wait(&mma_done[e % L::kDBuf], (uint32_t)(e / L::kDBuf) & 1u, p.err);
-    }
-    __syncwarp();
+  if (warp >= kTcMmaWarp0 && lane == 0 && mma_issued > 0) {  // normally already observed by the epilogue
+    const int e = mma_issued - 1;
+    mbar_wait(&mma_done[e % L::kD], (uint32_t)(e / L::kD) & 1u, p.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTcTmemCols);
   }
@@ -412,14 +518,14 @@ static cudaError_t tc_prepare(int device, int* nb) {
   const int by_smem = smem_sm / (TcLayout<NT>::kTotal + (int)fa.sharedSizeBytes + smem_reserved);
   const int regs_cta = ((fa.numRegs * 32 + 255) / 256 * 256) * (kTcThreads / 32);
   const int by_regs = regs_sm / (regs_cta > 0 ? regs_cta : 1);
-  const int by_tmem = 512 / (int)kTcTmemCols;
+  const int by_tmem = 512 / (int)kTcTmemCols;  // 1: the kernel takes the whole tensor memory
   int n = by_smem < by_regs ? by_smem : by_regs;
   n = n < by_tmem ? n : by_tmem;
   *nb = n;
   return cudaSuccess;
 }
 
-cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan) {
+cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes, TcPlan* plan) {
   static int cached[64][5];
   plan->nt = tc_nt(M);
   plan->units = (N / kUnitRows) * (K / kGroup);
@@ -435,14 +541,21 @@ cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* 
     }
     if (e != cudaSuccess) return e;
     if (nb < 1) nb = 1;
-    if (nb > 2) nb = 2;  // two CTAs x 256 TMEM columns fill the SM's 512
+    if (nb > 1) nb = 1;  // one CTA owns the SM's 512 TMEM columns
     if (dev.device >= 0 && dev.device < 64) cached[dev.device][slot] = nb;
   }
   int64_t ctas = (int64_t)dev.num_sms * nb;
   if (ctas > plan->units) ctas = plan->units;
   plan->ctas = ctas;
+  // partial slots: 2 segments x 128 rows x NT fp32 per item. A split costs
+  // 4*NT*128 bytes of partials written and read again (at M = 64, four units'
+  // worth of weight bytes), so this path keeps one round: every CTA one
+  // contiguous run of units, at most two split tiles per CTA.
+  (void)max_partial_bytes;
+  const size_t per_item = (size_t)2 * plan->nt * kUnitRows * sizeof(float);
+  plan->sched = make_item_sched(plan->units, (int)ctas, 1, 1);
   plan->counter_bytes = kCounterRegionBytes;
-  plan->partial_bytes = (size_t)ctas * 2 * kTcConsumerWarps * (plan->nt / 2) * 32 * sizeof(float);
+  plan->partial_bytes = (size_t)plan->sched.R * ctas * per_item;
   plan->smem_bytes = (size_t)tc_smem_dispatch(plan->nt);
   return cudaSuccess;
 }
@@ -451,8 +564,8 @@ size_t tc_workspace_bytes(const TcPlan& plan) { return plan.counter_bytes + plan
 
 template <int NT>
 static cudaError_t launch_tc_t(const CUtensorMap& map, const TcParams& p, const TcPlan& plan, cudaStream_t stream) {
-  w4a16_tc_kernel<NT><<<(unsigned)plan.ctas, kTcThreads, TcLayout<NT>::kTotal, stream>>>(map, p);
-  return cudaGetLastError();
+  return launch_pdl(w4a16_tc_kernel<NT>, dim3((unsigned)plan.ctas), dim3(kTcThreads), (size_t)TcLayout<NT>::kTotal,
+                    stream, map, p);
 }
 
 cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
@@ -477,20 +590,22 @@ cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, co
   p.err = dev.err;
   p.K = K;
   p.N = N;
-  p.U = plan.units;
   p.G = K / kGroup;
-  p.C = plan.ctas;
   p.M = M;
+  p.items = plan.sched.R * plan.sched.C;
+  p.sched = plan.sched;
   p.dq.m4 = 1u << 28;
   p.dq.m8 = 1u << 24;
   p.dq.m12 = 1u << 20;
+  cudaError_t e;
   switch (plan.nt) {
-    case 16: return launch_tc_t<16>(map, p, plan, stream);
-    case 32: return launch_tc_t<32>(map, p, plan, stream);
-    case 48: return launch_tc_t<48>(map, p, plan, stream);
-    case 64: return launch_tc_t<64>(map, p, plan, stream);
+    case 16: e = launch_tc_t<16>(map, p, plan, stream); break;
+    case 32: e = launch_tc_t<32>(map, p, plan, stream); break;
+    case 48: e = launch_tc_t<48>(map, p, plan, stream); break;
+    case 64: e = launch_tc_t<64>(map, p, plan, stream); break;
     default: return cudaErrorInvalidValue;
   }
+  return e;
 }
 
 }  // namespace w4a16

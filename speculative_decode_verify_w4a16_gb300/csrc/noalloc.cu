@@ -58,14 +58,15 @@ extern "C" w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, co
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
   LinearPlan plan;
-  if (linear_plan(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (linear_plan(M, N, K, dev, &plan, kNoAllocScratchBytes - kCounterRegionBytes) != cudaSuccess)
+    return W4A16_ERR_CUDA;
   if (plan.workspace_bytes > kNoAllocScratchBytes) return W4A16_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (noalloc_scratch(dev.device, &scratch) != cudaSuccess) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The completion counters must start at zero; a previous call (or one that
   // timed out) may have left them otherwise, so clear this call's slice.
-  const size_t counter_bytes = (size_t)(N / kUnitRows) * 8 * sizeof(int);
+  const size_t counter_bytes = (kTileCounterBase + (size_t)(N / kUnitRows) * 8) * sizeof(int);
   if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return W4A16_ERR_CUDA;
   return launch_linear(x, M, K, qweight_packed, scales_packed, N, out, scratch, plan, dev, s) == cudaSuccess
              ? W4A16_OK

@@ -97,17 +97,31 @@ def test_format_calls_reject_bad_arguments(L):
     assert L.w4a16_prepack(p, p, 128, 128, ctypes.c_void_p(0x10004), p, None) == _lib.ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("U,C", [(1, 1), (7, 3), (256, 256), (1024, 456), (4096, 152), (64128, 456),
-                                 (14336, 304), (33, 32)])
-def test_streamk_split_covers_each_unit_once(L, U, C):
-    begins = [L.w4a16_streamk_unit_begin(U, C, c) for c in range(C + 1)]
+@pytest.mark.parametrize("U,C,min_units,max_rounds", [
+    (1, 1, 2, 8), (7, 3, 2, 8), (256, 256, 2, 8), (1024, 456, 2, 8), (4096, 608, 2, 8), (64128, 456, 2, 8),
+    (28672, 608, 2, 8), (28672, 608, 2, 3), (14336, 152, 4, 8), (33, 32, 2, 8), (5120, 608, 2, 1)])
+def test_item_schedule_covers_each_unit_once(L, U, C, min_units, max_rounds):
+    rb = (ctypes.c_int64 * 9)()
+    R = L.w4a16_item_rounds(U, C, min_units, max_rounds, rb)
+    assert 1 <= R <= max_rounds
+    rb = list(rb)[:R + 1]
+    assert rb[0] == 0 and rb[-1] == U
+    # every round holds at least C units (no empty item); rounds shrink
+    lens = [rb[r + 1] - rb[r] for r in range(R)]
+    assert all(n >= C for n in lens)
+    assert all(lens[r + 1] <= lens[r] for r in range(R - 2))
+    # all but the last round are at least 2*C*min_units long (split only when that leaves >= C*min_units)
+    assert all(n >= C * min_units for n in lens[:-1])
+    begins = [L.w4a16_item_begin(U, C, min_units, max_rounds, i) for i in range(R * C + 1)]
     assert begins[0] == 0 and begins[-1] == U
-    assert all(begins[c + 1] > begins[c] for c in range(C))  # every CTA gets at least one unit
-    sizes = [begins[c + 1] - begins[c] for c in range(C)]
-    assert max(sizes) - min(sizes) <= 1
-    step = max(1, U // 2000)
-    for u in range(0, U, step):
-        c = L.w4a16_streamk_owner(U, C, u)
-        assert begins[c] <= u < begins[c + 1]
-    assert L.w4a16_streamk_owner(U, C, U) == -1
-    assert L.w4a16_streamk_unit_begin(U, U + 1, 0) == -1
+    assert all(begins[i + 1] > begins[i] for i in range(R * C))  # no empty item
+    for r in range(R):  # inside a round, item sizes differ by at most one
+        sizes = [begins[r * C + j + 1] - begins[r * C + j] for j in range(C)]
+        assert max(sizes) - min(sizes) <= 1
+    step = max(1, U // 3000)
+    for u in list(range(0, U, step)) + [U - 1]:
+        i = L.w4a16_item_owner(U, C, min_units, max_rounds, u)
+        assert begins[i] <= u < begins[i + 1]
+    assert L.w4a16_item_owner(U, C, min_units, max_rounds, U) == -1
+    assert L.w4a16_item_begin(U, C, min_units, max_rounds, R * C + 1) == -1
+    assert L.w4a16_item_rounds(C - 1, C, min_units, max_rounds, (ctypes.c_int64 * 9)()) == 0
