@@ -130,6 +130,11 @@ def _event(torch):
         return torch.cuda.Event(enable_timing=True)
 
 
+def _check(sv, where):
+    st = sv.check_device_status()
+    assert st == 0, f"device status {st} ({sv.status_string(st)}) after {where}"
+
+
 def run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_out, acc_ws, tree_in, tree_out,
              acc_ws2):
     """One kind of launch only, eagerly, for profiling (no JSON contract line)."""
@@ -149,7 +154,7 @@ def run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_
     for _ in range(args.warmup + args.steps):
         fn()
         torch.cuda.synchronize()
-    assert sv.check_device_status() == 0
+    _check(sv, "profiling launches")
     print(json.dumps({"only": args.only, "shape": args.shape, "M": args.m, "launches": args.warmup + args.steps}))
 
 
@@ -241,7 +246,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    assert sv.check_device_status() == 0
+    _check(sv, "warm-up steps")
 
     # The step is captured once as a CUDA graph so that the device timeline is
     # not paced by Python launch overhead. The timed graph holds the kernels
@@ -281,7 +286,7 @@ def run_ours(args):
         tt = torch.tensor([total_ms], device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         total_ms = float(tt.item())
-    assert sv.check_device_status() == 0
+    _check(sv, "timed graph replays")
     # per-call device durations: the step with event nodes, one replay at a time
     seg = []
     for s in range(args.steps):
@@ -358,7 +363,7 @@ def run_ours(args):
         stack["ratio_m64_m1"] = round(stack["64"]["us"] / stack["1"]["us"], 3)
         stack["ratio_m4_m1"] = round(stack["4"]["us"] / stack["1"]["us"], 3)
         stack["weights_GB"] = round(stack_bytes[1] / 1e9, 2)
-        assert sv.check_device_status() == 0
+        _check(sv, "the stack forward")
 
     # ---- end to end: host buffers, H2D of the step's inputs and D2H of its results inside the timing
     e2e = run_e2e(sv, torch, device, stream, calls, layers, wss, (p_np, q_np, d_np, u_np), (tp_np, td_np, tpar_np),

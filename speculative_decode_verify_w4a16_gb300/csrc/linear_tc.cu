@@ -4,13 +4,15 @@
 // path (sched.cuh); one CTA per SM owns the SM's whole tensor memory.
 // Warp roles, per unit (128 weight rows x 128 K):
 //   producer warp     claims items; 1-D bulk copies of the packed codes and
-//                     scales, 2-D TMA of the token tile x[0:NT, 128g : 128g+128]
-//                     (128-byte swizzle; token rows past M read as zero)
-//   3 dequant groups  of 4 warps (one per TMEM lane quadrant) take the units
+//                     scales into a deep ring
+//   token-tile warp   2-D TMA of the token tile x[0:NT, 128g : 128g+128]
+//                     (128-byte swizzle; token rows past M read as zero) into
+//                     a shallow ring (L2 hits), following the codes ring
+//   2 dequant groups  of 4 warps (one per TMEM lane quadrant) take the units
 //                     in turn: dequantise the unit to exact bf16 codes and
 //                     store them into TMEM, the UMMA A operand; hand the
 //                     unit's scales and metadata on to the epilogue
-//   3 MMA warps       one per dequant group (its units only): 8 x
+//   2 MMA warps       one per dequant group (its units only): 8 x
 //                     tcgen05.mma kind::f16 (M = 128 weight rows, N = NT
 //                     tokens, K = 16) per unit into a TMEM accumulator,
 //                     commit. Several issuers keep the tensor pipe fed while
@@ -36,12 +38,13 @@
 
 namespace w4a16 {
 
-constexpr int kTcDqGroups = 3;                  // dequant groups of 4 warps, one MMA warp each
-constexpr int kTcDqWarps = 4 * kTcDqGroups;     // warps 0 .. 11
-constexpr int kTcEpWarps = 8;                   // warps 12 .. 19
-constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 20
-constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 21 .. 23
-constexpr int kTcThreads = 32 * (kTcMmaWarp0 + kTcDqGroups);
+constexpr int kTcDqGroups = 2;                  // dequant groups of 4 warps, one MMA warp each
+constexpr int kTcDqWarps = 4 * kTcDqGroups;     // warps 0 .. 7
+constexpr int kTcEpWarps = 8;                   // warps 8 .. 15
+constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 16: claims items, codes + scales
+constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 17, 18
+constexpr int kTcXWarp = kTcMmaWarp0 + kTcDqGroups;       // warp 19: token tiles
+constexpr int kTcThreads = 32 * (kTcXWarp + 1);
 constexpr uint32_t kTcTmemCols = 512;  // the whole tensor memory of the SM
 constexpr int kTcRing = 16;            // scale / metadata hand-off ring (units)
 
@@ -49,29 +52,43 @@ template <int NT>
 struct TcLayout {
   // TMEM ring depths: kA dequantised units (64 columns each) at column 0,
   // kD accumulators (NT columns each) after them
+  //
+  // Every ring below has a multiple of kTcDqGroups slots, so that a slot is
+  // always used by units of one dequant group and one MMA warp, in order:
+  // each waiter is then at most one phase ahead of the slot's barrier, which
+  // a parity wait requires (units are dealt round-robin to the groups).
   static constexpr int kA = NT <= 16 ? 6 : 4;
-  static constexpr int kD = NT <= 16 ? 8 : (NT <= 32 ? 8 : (NT <= 48 ? 5 : 4));
+  static constexpr int kD = NT <= 16 ? 8 : (NT <= 32 ? 8 : 4);
   static_assert(kA * 64 + kD * NT <= (int)kTcTmemCols, "TMEM budget");
+  static_assert(kA % kTcDqGroups == 0 && kD % kTcDqGroups == 0, "ring slots per group");
+  static_assert(kD >= 2, "the epilogue takes units in pairs");
   // a unit's hand-off entry is rewritten kTcRing units later; by then the
   // dequantisation of that later unit has waited for the MMAs kA units back,
   // which waited for the epilogue kD units before those
   static_assert(kA + kD <= kTcRing, "hand-off ring depth");
-  static constexpr int kX = NT * 128;  // one 64-wide K half of the token tile
-  static constexpr int kXOff0 = 0;
-  static constexpr int kXOff1 = kX;
-  static constexpr int kWOff = 2 * kX;
-  static constexpr int kSOff = kWOff + kUnitBytes;
-  static constexpr int kStageRaw = kSOff + kUnitScaleBytes;
-  static constexpr int kStage = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kStages = (192 * 1024) / kStage;
-  static constexpr int kScRingOff = kStages * kStage;                 // kTcRing x 256 B scales
+  // Two shared-memory rings: token tiles (read by the MMAs, a few units
+  // ahead; they come from L2) and packed codes + scales (read by the dequant
+  // groups and released as soon as they are in registers; deep, so that
+  // enough HBM reads are in flight).
+  static constexpr int kX = NT * 128;             // one 64-wide K half of the token tile
+  static constexpr int kXStage = 2 * kX;          // 1024-aligned (swizzled UMMA operand)
+  static constexpr int kXStages = NT <= 16 ? 6 : 4;
+  static constexpr int kWStage = kUnitBytes + kUnitScaleBytes;  // codes, then scales
+  static constexpr int kXOff = 0;
+  static constexpr int kWOff = kXOff + kXStages * kXStage;
+  static constexpr int kWStages = (200 * 1024 - kWOff) / kWStage / kTcDqGroups * kTcDqGroups;
+  static constexpr int kScRingOff = kWOff + kWStages * kWStage;       // kTcRing x 256 B scales
   static constexpr int kMetaRingOff = kScRingOff + kTcRing * kUnitScaleBytes;  // kTcRing x int4
-  static constexpr int kMetaOff = kMetaRingOff + kTcRing * 16;        // kStages x int4 (per stage)
-  static constexpr int kBarOff = kMetaOff + kStages * 16;
-  // full[S], empty[S], a_full[kA], a_free[kA], mma_done[kD], d_free[kD], tmem base
-  static constexpr int kTotal = kBarOff + (2 * kStages + 2 * kA + 2 * kD) * 8 + 16 + 1024;  // +1024: alignment
+  static constexpr int kMetaOff = kMetaRingOff + kTcRing * 16;        // kWStages x int4 (per stage)
+  static constexpr int kBarOff = kMetaOff + kWStages * 16;
+  // wfull[SW], wempty[SW], xfull[SX], xempty[SX], a_full[kA], a_free[kA], mma_done[kD], d_free[kD],
+  // mma_fin[groups], tmem base
+  static constexpr int kTotal =
+      kBarOff + (2 * kWStages + 2 * kXStages + 2 * kA + 2 * kD + kTcDqGroups) * 8 + 16 + 1024;  // +1024: alignment
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
-  static_assert(kStages >= kTcDqGroups + 1, "ring depth");
+  static_assert(kWStage % 16 == 0, "bulk copy alignment");
+  static_assert(kWStages >= 2 * kTcDqGroups, "ring depth");
+  static_assert(kWStages % kTcDqGroups == 0 && kXStages % kTcDqGroups == 0, "ring slots per group");
 };
 
 struct DequantConstsTc {
@@ -216,19 +233,60 @@ __device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&a
   }
 }
 
+// Two units at once: acc[j] += s0 * D0[lane][col + j], then += s1 * D1[...];
+// the loads of both accumulators are in flight together.
+template <int W>
+__device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, float s0, float s1, float (&acc)[W]) {
+  if constexpr (W >= 32) {  // 8 columns of each at a time: the register budget holds no more
+#pragma unroll
+    for (int c0 = 0; c0 + 8 <= W; c0 += 8) {
+      uint32_t v0[8], v1[8];
+      tmem_ld_32x32b_x8(dt0 + c0, v0);
+      tmem_ld_32x32b_x8(dt1 + c0, v1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+    }
+    return;
+  }
+  if constexpr (W >= 16) {
+#pragma unroll
+    for (int c0 = 0; c0 + 16 <= W; c0 += 16) {
+      uint32_t v0[16], v1[16];
+      tmem_ld_32x32b_x16(dt0 + c0, v0);
+      tmem_ld_32x32b_x16(dt1 + c0, v1);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+    }
+  }
+  if constexpr (W % 16 >= 8) {
+    constexpr int c0 = W / 16 * 16;
+    uint32_t v0[8], v1[8];
+    tmem_ld_32x32b_x8(dt0 + c0, v0);
+    tmem_ld_32x32b_x8(dt1 + c0, v1);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                 const TcParams p) {
   using L = TcLayout<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + L::kStages;
-  uint64_t* a_full = empty + L::kStages;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* wempty = wfull + L::kWStages;
+  uint64_t* xfull = wempty + L::kWStages;
+  uint64_t* xempty = xfull + L::kXStages;
+  uint64_t* a_full = xempty + L::kXStages;
   uint64_t* a_free = a_full + L::kA;
   uint64_t* mma_done = a_free + L::kA;
   uint64_t* d_free = mma_done + L::kD;
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(d_free + L::kD);
+  uint64_t* mma_fin = d_free + L::kD;  // per MMA warp: all its MMAs complete (teardown)
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(mma_fin + kTcDqGroups);
   int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   int4* meta_ring = reinterpret_cast<int4*>(smem + L::kMetaRingOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,14 +297,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     // pull the first units of the item this CTA most likely claims into L2.
     const int64_t u0 = item_begin(p.sched, blockIdx.x);
     int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
-    if (n > 2 * L::kStages) n = 2 * L::kStages;
+    if (n > 2 * L::kWStages) n = 2 * L::kWStages;
     prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
     prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);  // released by the commit of the unit's MMAs
+    for (int s = 0; s < L::kWStages; ++s) {
+      mbar_init(&wfull[s], 1);
+      mbar_init(&wempty[s], 5);  // the dequant group's 4 warps (codes used) + the token-tile warp (g read)
+    }
+    for (int s = 0; s < L::kXStages; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);  // commit of the MMAs that read the token tile
     }
     for (int b = 0; b < L::kA; ++b) {
       mbar_init(&a_full[b], 4);  // the 4 warps of the dequant group
@@ -256,6 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       mbar_init(&mma_done[b], 2);  // commit of the unit's MMAs + the MMA thread's release of the hand-off
       mbar_init(&d_free[b], kTcEpWarps);
     }
+    for (int j = 0; j < kTcDqGroups; ++j) mbar_init(&mma_fin[j], 1);
     fence_mbarrier_init();
   }
   if (warp == kTcMmaWarp0) {
@@ -273,11 +336,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
 
   if (warp == kTcProducerWarp) {
     // ---------------------------------------------------------- producer
+    // Codes + scales run up to kWStages units ahead of the dequant groups.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const uint32_t tx = (uint32_t)(2 * L::kX + kUnitBytes + kUnitScaleBytes);
       int* work = &p.counters[kWorkCounter];
-      int n_stage = 0;
+      int n_w = 0;  // units whose codes have been issued
       bool ok = true;
       int item = atomicAdd(work, 1);
       while (ok && item < p.items) {
@@ -285,20 +348,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         const int64_t ue = item_begin(p.sched, item + 1);
         int64_t t = ub / p.G;
         int64_t g = ub - t * p.G;
-        for (int64_t u = ub; u < ue; ++u, ++n_stage) {
-          const int s = n_stage % L::kStages;
-          if (n_stage >= L::kStages &&
-              !mbar_wait(&empty[s], ((uint32_t)(n_stage / L::kStages) & 1u) ^ 1u, p.err)) {
+        for (int64_t u = ub; u < ue; ++u, ++n_w) {
+          const int s = n_w % L::kWStages;
+          if (n_w >= L::kWStages &&
+              !mbar_wait(&wempty[s], ((uint32_t)(n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
             ok = false;
             break;
           }
           meta[s] = make_int4(item, (int)t, (int)g, (u == ub ? kTcUnitFirst : 0) | (u == ue - 1 ? kTcUnitLast : 0));
-          uint8_t* st = smem + s * L::kStage;
-          mbar_arrive_expect_tx(&full[s], tx);
-          tma_load_2d(st + L::kXOff0, &xmap, (int32_t)(g * kGroup), 0, &full[s]);
-          tma_load_2d(st + L::kXOff1, &xmap, (int32_t)(g * kGroup + 64), 0, &full[s]);
-          bulk_g2s_hint(st + L::kWOff, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
-          bulk_g2s(st + L::kSOff, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
+          uint8_t* ws = smem + L::kWOff + s * L::kWStage;
+          mbar_arrive_expect_tx(&wfull[s], (uint32_t)L::kWStage);
+          bulk_g2s_hint(ws, p.qw + u * kUnitBytes, kUnitBytes, &wfull[s], pol);
+          bulk_g2s(ws + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &wfull[s]);
           if (++g == p.G) {
             g = 0;
             ++t;
@@ -309,19 +370,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       // one stop marker per dequant group (each reads every kTcDqGroups-th
       // stage): -1 at the first index past the last unit, where the MMA warp
       // and the epilogue stop too; -2 at the other groups' next indices
-      for (int k = 0; ok && k < kTcDqGroups; ++k, ++n_stage) {
-        const int s = n_stage % L::kStages;
-        if (n_stage >= L::kStages &&
-            !mbar_wait(&empty[s], ((uint32_t)(n_stage / L::kStages) & 1u) ^ 1u, p.err)) {
+      for (int k = 0; ok && k < kTcDqGroups; ++k, ++n_w) {
+        const int s = n_w % L::kWStages;
+        if (n_w >= L::kWStages &&
+            !mbar_wait(&wempty[s], ((uint32_t)(n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
           ok = false;
           break;
         }
         meta[s] = make_int4(k == 0 ? -1 : -2, 0, 0, 0);
-        mbar_arrive(&full[s]);
+        mbar_arrive(&wfull[s]);
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
-        for (int i = (n_stage > L::kStages ? n_stage - L::kStages : 0); i < n_stage; ++i)
-          mbar_wait(&full[i % L::kStages], (uint32_t)(i / L::kStages) & 1u, p.err);
+        for (int i = (n_w > L::kWStages ? n_w - L::kWStages : 0); i < n_w; ++i)
+          mbar_wait(&wfull[i % L::kWStages], (uint32_t)(i / L::kWStages) & 1u, p.err);
       }
       // the last CTA to get here resets the claim counters for the next call
       __threadfence();
@@ -329,6 +390,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         p.counters[kWorkCounter] = 0;
         p.counters[kExitCounter] = 0;
       }
+    }
+  } else if (warp == kTcXWarp) {
+    // ------------------------------------------------------- token tiles
+    // Follows the codes ring: once unit i's codes have landed its group g is
+    // known (stage metadata); the token tile goes to the x ring as soon as the
+    // MMAs free a slot. Counting in on wempty keeps the stage (and its
+    // metadata) from being recycled before it was read here.
+    if (lane == 0) {
+      int n_x = 0;
+      for (;; ++n_x) {
+        const int s = n_x % L::kWStages, sx = n_x % L::kXStages;
+        if (!mbar_wait(&wfull[s], (uint32_t)(n_x / L::kWStages) & 1u, p.err)) break;
+        const int4 m = meta[s];
+        if (m.x < 0) break;  // stop marker
+        mbar_arrive(&wempty[s]);
+        if (n_x >= L::kXStages &&
+            !mbar_wait(&xempty[sx], ((uint32_t)(n_x / L::kXStages) & 1u) ^ 1u, p.err))
+          break;
+        uint8_t* xs = smem + L::kXOff + sx * L::kXStage;
+        mbar_arrive_expect_tx(&xfull[sx], (uint32_t)L::kXStage);
+        tma_load_2d(xs, &xmap, m.z * kGroup, 0, &xfull[sx]);
+        tma_load_2d(xs + L::kX, &xmap, m.z * kGroup + 64, 0, &xfull[sx]);
+      }
+      // let token tiles in flight land before the CTA exits (normally the MMAs
+      // have consumed them all already)
+      for (int i = (n_x > L::kXStages ? n_x - L::kXStages : 0); i < n_x; ++i)
+        mbar_wait(&xfull[i % L::kXStages], (uint32_t)(i / L::kXStages) & 1u, p.err);
     }
   } else if (warp >= kTcMmaWarp0) {
     // ------------------------------------------------------------- MMA
@@ -338,7 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(NT);
       for (int i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
-        const int s = i % L::kStages, b = i % L::kA, db = i % L::kD;
+        const int sx = i % L::kXStages, b = i % L::kA, db = i % L::kD;
         if (!mbar_wait(&a_full[b], (uint32_t)(i / L::kA) & 1u, p.err)) break;
         if (i >= L::kD && !mbar_wait(&d_free[db], ((uint32_t)(i / L::kD) & 1u) ^ 1u, p.err)) break;
         const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
@@ -349,8 +437,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           }
           break;
         }
+        if (!mbar_wait(&xfull[sx], (uint32_t)(i / L::kXStages) & 1u, p.err)) break;
         tc_fence_after();
-        const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + s * L::kStage) + L::kXOff0);
+        const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + L::kXOff + sx * L::kXStage));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // start-address field (bits 0..13, 16-byte units) of the K step's rows
@@ -359,18 +448,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         }
         umma_commit(&mma_done[db]);
         umma_commit(&a_free[b]);
-        umma_commit(&empty[s]);  // codes were read before a_full, the token tile by these MMAs
+        umma_commit(&xempty[sx]);  // the token tile was read by these MMAs
         // release (to the epilogue) of the hand-off entry this thread acquired through a_full
         mbar_arrive(&mma_done[db]);
         mma_issued = i + 1;
       }
+      if (mma_issued > 0) umma_commit(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this thread's MMAs
     }
   } else if (warp < kTcDqWarps) {
     // ------------------------------------------------------ dequant groups
     const int grp = warp >> 2, q = warp & 3;
     for (int i = grp;; i += kTcDqGroups) {
-      const int s = i % L::kStages, b = i % L::kA;
-      if (!mbar_wait(&full[s], (uint32_t)(i / L::kStages) & 1u, p.err)) break;
+      const int s = i % L::kWStages, b = i % L::kA;
+      if (!mbar_wait(&wfull[s], (uint32_t)(i / L::kWStages) & 1u, p.err)) break;
       const uint4 mu = lds128(smem_u32(&meta[s]));
       // A[b] is free once the MMAs of unit i - kA have completed
       if (i >= L::kA && !mbar_wait(&a_free[b], (uint32_t)(i / L::kA - 1) & 1u, p.err)) break;
@@ -383,27 +473,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         if (lane == 0) mbar_arrive(&a_full[b]);
         break;
       }
-      const uint32_t st = smem_u32(smem + s * L::kStage);
+      const uint32_t st = smem_u32(smem + L::kWOff + s * L::kWStage);
       if (q == 0) {  // hand the unit's scales and metadata on to the epilogue
         if (lane < kUnitScaleBytes / 16) {
-          const uint4 v = lds128(st + L::kSOff + lane * 16);
+          const uint4 v = lds128(st + kUnitBytes + lane * 16);
           *reinterpret_cast<uint4*>(smem + L::kScRingOff + (i % kTcRing) * kUnitScaleBytes + lane * 16) = v;
         }
         if (lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
       }
+      uint4 w[2][2];  // this warp's 32 rows: codes in registers, then the stage is released
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) w[rt][hh] = lds128(st + (((q * 2 + rt) * 2 + hh) * 32 + lane) * 16);
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {  // 16 rows x 64 K -> 16 lanes x 32 TMEM columns
-          const uint4 w = lds128(st + L::kWOff + (((q * 2 + rt) * 2 + hh) * 32 + lane) * 16);
           uint32_t r[16];
-          tc_dequant(w.x, p.dq, &r[0]);
-          tc_dequant(w.y, p.dq, &r[4]);
-          tc_dequant(w.z, p.dq, &r[8]);
-          tc_dequant(w.w, p.dq, &r[12]);
+          tc_dequant(w[rt][hh].x, p.dq, &r[0]);
+          tc_dequant(w[rt][hh].y, p.dq, &r[4]);
+          tc_dequant(w[rt][hh].z, p.dq, &r[8]);
+          tc_dequant(w[rt][hh].w, p.dq, &r[12]);
           tmem_st_16x256b_x4(tmem + ((uint32_t)(32 * q + 16 * rt) << 16) + a_col(b) + 32 * hh, r);
         }
       }
+      // every code of the stage has been used, so its loads have completed:
+      // release it to the producer (the scale / metadata copies are done too)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wempty[s]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -417,43 +515,68 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
 #pragma unroll
     for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
     int item = 0, item_t0 = 0, seg_g0 = 0;
-    for (int e = 0;; ++e) {
+    auto scale_of = [&](int u) {
+      return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
+          smem + L::kScRingOff + (u % kTcRing) * kUnitScaleBytes + 2 * sc_half)));
+    };
+    auto meta_of = [&](int u) {
+      const uint4 mu = lds128(smem_u32(&meta_ring[u % kTcRing]));
+      return make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
+    };
+    // Units are taken two at a time (both accumulators read together) unless
+    // the first one ends a tile segment or the second is the stop marker.
+    for (int e = 0;;) {
       const int db = e % L::kD;
       if (!mbar_wait(&mma_done[db], (uint32_t)(e / L::kD) & 1u, p.err)) break;
-      const uint4 mu = lds128(smem_u32(&meta_ring[e % kTcRing]));
-      const int4 me = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
+      const int4 me = meta_of(e);
       if (me.x < 0) break;  // stop marker
-      const float sc = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
-          smem + L::kScRingOff + (e % kTcRing) * kUnitScaleBytes + 2 * sc_half)));
-      tc_fence_after();
-      tc_epilogue_fma<NT / 2>(tmem + ((uint32_t)(32 * q) << 16) + d_col(db) + h * (NT / 2), sc, acc);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&d_free[db]);
       if (me.w & kTcUnitFirst) {
         item = me.x;
         item_t0 = me.y;
         seg_g0 = me.z;
       }
-      if (me.z == p.G - 1 || (me.w & kTcUnitLast)) {  // end of this item's segment of tile me.y
-        if (seg_g0 == 0 && me.z == p.G - 1)
-          tc_store<NT>(p, me.y, q, h, lane, acc);
+      const bool seg_end = me.z == p.G - 1 || (me.w & kTcUnitLast);
+      bool pair = false;
+      int4 me1 = me;
+      const int db1 = (e + 1) % L::kD;
+      if (!seg_end) {
+        if (!mbar_wait(&mma_done[db1], (uint32_t)((e + 1) / L::kD) & 1u, p.err)) break;
+        me1 = meta_of(e + 1);
+        pair = me1.x >= 0;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16) + h * (NT / 2);
+      if (pair) {
+        tc_epilogue_fma2<NT / 2>(dt + d_col(db), dt + d_col(db1), scale_of(e), scale_of(e + 1), acc);
+      } else {
+        tc_epilogue_fma<NT / 2>(dt + d_col(db), scale_of(e), acc);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&d_free[db]);
+        if (pair) mbar_arrive(&d_free[db1]);
+      }
+      const int4 ml = pair ? me1 : me;  // last unit taken
+      if (ml.z == p.G - 1 || (ml.w & kTcUnitLast)) {  // end of this item's segment of tile ml.y
+        if (seg_g0 == 0 && ml.z == p.G - 1)
+          tc_store<NT>(p, ml.y, q, h, lane, acc);
         else
-          tc_finish_split<NT>(p, item, me.y == item_t0 ? 0 : 1, me.y, q, h, lane, acc);
+          tc_finish_split<NT>(p, item, ml.y == item_t0 ? 0 : 1, ml.y, q, h, lane, acc);
 #pragma unroll
         for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
         seg_g0 = 0;
       }
+      if (!pair && !seg_end) break;  // the second unit was the stop marker
+      e += pair ? 2 : 1;
     }
   }
 
   // ---------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp >= kTcMmaWarp0 && lane == 0 && mma_issued > 0) {  // normally already observed by the epilogue
-    const int e = mma_issued - 1;
-    mbar_wait(&mma_done[e % L::kD], (uint32_t)(e / L::kD) & 1u, p.err);
-  }
+  if (warp >= kTcMmaWarp0 && warp < kTcMmaWarp0 + kTcDqGroups && lane == 0 && mma_issued > 0)
+    mbar_wait(&mma_fin[warp - kTcMmaWarp0], 0u, p.err);  // no MMA in flight when TMEM is freed
   tc_fence_before();
   __syncthreads();
   if (warp == kTcMmaWarp0) {
