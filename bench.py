@@ -42,6 +42,16 @@ ACC_B, ACC_K, VOCAB = 16, 4, synth.LLAMA3_VOCAB
 TREE_B, TREE_N = 16, 64
 N_LAYERS = 80
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+# DRAM bytes (read + write) per launch of each kernel, averaged over the step's
+# launches of it, from the ncu capture summarised in profiles/ (the step's
+# launch list with dram__bytes_read.sum / dram__bytes_write.sum); None until a
+# capture of the current kernels exists.
+NCU_DRAM_BYTES_PER_LAUNCH: dict = {
+    "w4a16_skinny_kernel<1> (M<16)": 110586272,
+    "w4a16_tc_kernel<64> (M>=16)": 112848832,
+    "accept_stats_kernel + accept_resid_kernel": 88935168,
+    "accept_argmax_kernel": 525488640,
+}
 
 
 def linear_bytes(M, N, K):
@@ -297,7 +307,6 @@ def run_ours(args):
     pk = peaks()
 
     sweep = []
-    lin_bytes = lin_us = 0.0
     for j, (M, name, K, N, li) in enumerate(calls):
         b = linear_bytes(M, N, K)
         us = float(seg_mean[j])
@@ -305,8 +314,6 @@ def run_ours(args):
         tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
         sweep.append({"shape": name, "M": M, "K": K, "N": N, "us": round(us, 2), "GB_s": round(gbs, 1),
                       "TFLOP_s": round(tflops, 2), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
-        lin_bytes += b
-        lin_us += us
     acc_us, tree_us = float(seg_mean[len(calls)]), float(seg_mean[len(calls) + 1])
     ab, tb = accept_bytes_seq(ACC_B, ACC_K, VOCAB), accept_bytes_tree(TREE_B, TREE_N, VOCAB)
     accept = {"seq_us": round(acc_us, 2), "seq_GB_s": round(ab / (acc_us * 1e-6) / 1e9, 1),
@@ -320,7 +327,28 @@ def run_ours(args):
         b = sum(linear_bytes(M, s["N"], s["K"]) for s in sel)
         per_m[str(M)] = {"layer_us": round(us, 2), "GB_s": round(b / (us * 1e-6) / 1e9, 1),
                          "frac_hbm": round(b / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 3)}
-    lin_gbs = lin_bytes / (lin_us * 1e-6) / 1e9
+    # per kernel (all launches of the step): time, algorithmic bytes, roofline fraction
+    groups = {
+        "w4a16_skinny_kernel<1> (M<16)": [(linear_bytes(M, N, K), float(seg_mean[j]))
+                                          for j, (M, name, K, N, li) in enumerate(calls) if M < 16],
+        "w4a16_tc_kernel<64> (M>=16)": [(linear_bytes(M, N, K), float(seg_mean[j]))
+                                        for j, (M, name, K, N, li) in enumerate(calls) if M >= 16],
+        "accept_stats_kernel + accept_resid_kernel": [(ab, acc_us)],
+        "accept_argmax_kernel": [(tb, tree_us)],
+    }
+    per_kernel = {}
+    for kname, items in groups.items():
+        if not items:
+            continue
+        b = sum(x[0] for x in items)
+        us = sum(x[1] for x in items)
+        gbs = b / (us * 1e-6) / 1e9
+        per_kernel[kname] = {"launches_per_step": len(items), "us": round(us, 2), "bytes": int(b),
+                             "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)}
+    dominant = max(per_kernel, key=lambda k: per_kernel[k]["us"])
+    dom = per_kernel[dominant]
+    dom_launch_bytes = dom["bytes"] / dom["launches_per_step"]
+    traffic = NCU_DRAM_BYTES_PER_LAUNCH.get(dominant)
 
     # ---- full 80-layer + lm_head verify forward at M = 1 / 4 / 64 (outside the timed step)
     stack = None
@@ -395,10 +423,13 @@ def run_ours(args):
         "per_m_layer": per_m,
         "accept": accept,
         "stack_verify_forward": stack,
-        "roofline": {"bound": "hbm", "kernel": "w4a16_skinny_kernel (all 12 step launches)",
-                     "achieved": round(lin_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(lin_gbs / pk["hbm_gbs"], 3), "traffic": None,
-                     "peak_source": pk["source"] + " (burst copy bandwidth)"},
+        "per_kernel": per_kernel,
+        "roofline": {"bound": "hbm", "kernel": dominant,
+                     "achieved": dom["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": dom["frac_hbm"],
+                     "traffic": traffic,
+                     "algorithmic_bytes_per_launch": int(dom_launch_bytes),
+                     "peak_source": pk["source"] + " (copy bandwidth)"},
         "clocks": clk,
         "gpu_launches": n_launch_per_step * args.steps,
         "e2e": e2e,

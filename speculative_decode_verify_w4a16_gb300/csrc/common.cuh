@@ -164,6 +164,20 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// --------------------------------------------------------- packed fp32 math
+// (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1): two IEEE fp32 fused multiply-adds
+// (round to nearest each, the same results as two fmaf) in one instruction.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // ------------------------------------------------------------ shared loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

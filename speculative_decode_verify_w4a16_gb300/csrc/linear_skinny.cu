@@ -365,10 +365,8 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
       for (int nt = 0; nt < MT8; ++nt) {
-        acc[rt][nt][0] = fmaf(sc[rt][0], part[rt][nt][0], acc[rt][nt][0]);
-        acc[rt][nt][1] = fmaf(sc[rt][0], part[rt][nt][1], acc[rt][nt][1]);
-        acc[rt][nt][2] = fmaf(sc[rt][1], part[rt][nt][2], acc[rt][nt][2]);
-        acc[rt][nt][3] = fmaf(sc[rt][1], part[rt][nt][3], acc[rt][nt][3]);
+        ffma2(acc[rt][nt][0], acc[rt][nt][1], sc[rt][0], sc[rt][0], part[rt][nt][0], part[rt][nt][1]);
+        ffma2(acc[rt][nt][2], acc[rt][nt][3], sc[rt][1], sc[rt][1], part[rt][nt][2], part[rt][nt][3]);
       }
 
     if (mt.z == p.G - 1 || (mt.w & kUnitLast)) {  // end of this item's segment of tile mt.y

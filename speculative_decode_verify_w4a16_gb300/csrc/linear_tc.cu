@@ -221,7 +221,8 @@ __device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&a
       uint32_t v[16];
       tmem_ld16_sync(dt + c0, v);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(sc, __uint_as_float(v[c]), acc[c0 + c]);
+      for (int c = 0; c < 16; c += 2)
+        ffma2(acc[c0 + c], acc[c0 + c + 1], sc, sc, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
     }
   }
   if constexpr (W % 16 >= 8) {
@@ -229,7 +230,8 @@ __device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&a
     uint32_t v[8];
     tmem_ld8_sync(dt + c0, v);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(sc, __uint_as_float(v[c]), acc[c0 + c]);
+    for (int c = 0; c < 8; c += 2)
+      ffma2(acc[c0 + c], acc[c0 + c + 1], sc, sc, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
   }
 }
 
@@ -245,7 +247,10 @@ __device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, flo
       tmem_ld_32x32b_x8(dt1 + c0, v1);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+      for (int c = 0; c < 8; c += 2) {  // unit e first, then e + 1 (the order of the sequential loop)
+        ffma2(acc[c0 + c], acc[c0 + c + 1], s0, s0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
+        ffma2(acc[c0 + c], acc[c0 + c + 1], s1, s1, __uint_as_float(v1[c]), __uint_as_float(v1[c + 1]));
+      }
     }
     return;
   }
@@ -257,7 +262,10 @@ __device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, flo
       tmem_ld_32x32b_x16(dt1 + c0, v1);
       tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 16; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+      for (int c = 0; c < 16; c += 2) {
+        ffma2(acc[c0 + c], acc[c0 + c + 1], s0, s0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
+        ffma2(acc[c0 + c], acc[c0 + c + 1], s1, s1, __uint_as_float(v1[c]), __uint_as_float(v1[c + 1]));
+      }
     }
   }
   if constexpr (W % 16 >= 8) {
@@ -267,7 +275,10 @@ __device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, flo
     tmem_ld_32x32b_x8(dt1 + c0, v1);
     tmem_wait_ld();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc[c0 + c] = fmaf(s1, __uint_as_float(v1[c]), fmaf(s0, __uint_as_float(v0[c]), acc[c0 + c]));
+    for (int c = 0; c < 8; c += 2) {
+      ffma2(acc[c0 + c], acc[c0 + c + 1], s0, s0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
+      ffma2(acc[c0 + c], acc[c0 + c + 1], s1, s1, __uint_as_float(v1[c]), __uint_as_float(v1[c + 1]));
+    }
   }
 }
 
