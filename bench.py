@@ -49,7 +49,7 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 NCU_DRAM_BYTES_PER_LAUNCH: dict = {
     "w4a16_skinny_kernel<1> (M<16)": 110586272,
     "w4a16_tc_kernel<64> (M>=16)": 112848832,
-    "accept_stats_kernel + accept_resid_kernel": 88935168,
+    "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": None,
     "accept_argmax_kernel": 525488640,
 }
 
@@ -229,7 +229,7 @@ def run_ours(args):
     tree_out = [torch.empty(TREE_B, dtype=torch.int32, device=device) for _ in range(2)]
     stream = torch.cuda.current_stream()
     calls = [(M, name, K, N, li) for li, M in enumerate(STEP_MS) for name, K, N in SHAPES]
-    n_launch_per_step = len(calls) + 2 + 1
+    n_launch_per_step = len(calls) + 3 + 1  # linears, stochastic accept (3 kernels), greedy tree (1)
 
     def step(evs=None):
         for j, (M, name, K, N, li) in enumerate(calls):
@@ -333,7 +333,7 @@ def run_ours(args):
                                           for j, (M, name, K, N, li) in enumerate(calls) if M < 16],
         "w4a16_tc_kernel<64> (M>=16)": [(linear_bytes(M, N, K), float(seg_mean[j]))
                                         for j, (M, name, K, N, li) in enumerate(calls) if M >= 16],
-        "accept_stats_kernel + accept_resid_kernel": [(ab, acc_us)],
+        "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": [(ab, acc_us)],
         "accept_argmax_kernel": [(tb, tree_us)],
     }
     per_kernel = {}

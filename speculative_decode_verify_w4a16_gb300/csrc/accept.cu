@@ -1,19 +1,22 @@
 // Speculative accept step ("Speculative Decoding이란?", section 3 Steps 3-4,
 // section 6; greedy equivalence in section 5).
 //
-// Stochastic sequence mode, two launches:
-//  1. accept_stats_kernel, grid (chunk, row): every p / q logit row is cut
-//     into chunks of at most 16384 logits; a block holds its chunk in
-//     registers (one HBM pass), takes the exact chunk maximum and the sum of
-//     exp(l - max) (pairwise fp32 per thread, fp64 across threads). The last
-//     block of a batch row (atomic count) merges its rows' statistics in fp64,
-//     evaluates alpha_i = min(1, P(d_i) / Q(d_i)) for every draft, finds the
-//     first rejection r and records r with the normalisers of row r.
-//  2. accept_resid_kernel, grid (chunk, batch row): each block sums the
+// Stochastic sequence mode, three launches:
+//  1. accept_stats_kernel, persistent warps: every p / q logit row is cut
+//     into items of 1024 logits; a warp holds an item in registers (one HBM
+//     pass, the next item's loads in flight meanwhile), takes the exact item
+//     maximum and the sum of exp(l - max) (pairwise fp32 per lane,
+//     double-float across lanes).
+//  2. accept_decide_kernel, one block per batch row: merges each row's item
+//     statistics (one warp per row), evaluates alpha_i = min(1, P(d_i) /
+//     Q(d_i)) for every draft, finds the first rejection r and records r
+//     with the normalisers of row r.
+//  3. accept_resid_kernel, grid (chunk, batch row): each block sums the
 //     distribution to draw from — max(0, P_r - Q_r), or P_{n+1} after full
 //     acceptance — over its vocabulary chunk. The last block of the batch row
-//     walks the chunk sums, re-scans the chunk that holds u * S with an fp64
-//     block scan, and writes accepted_len and next_token.
+//     finds the chunk that holds u * S with a warp scan of the chunk sums,
+//     re-scans that chunk with a double-float block scan, and writes
+//     accepted_len and next_token.
 // Greedy modes, one launch: accept_argmax_kernel reduces chunks to
 // (max, smallest index); the last block of a batch row merges them and walks
 // the chain or tree.
@@ -23,6 +26,8 @@
 // block that re-scans it compute bit-identical values.
 #include <float.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,14 +35,19 @@ namespace w4a16 {
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
-constexpr int kPerThread = 64;                       // logits a thread holds in the chunk passes
-constexpr int kMaxChunk = kAccThreads * kPerThread;  // 16384
+constexpr int kArgPT = 64;                           // logits a thread holds in the argmax pass
+constexpr int kArgChunk = kAccThreads * kArgPT;      // 16384
+constexpr int kStatPT = 32;                          // logits a lane holds per statistics item
+constexpr int kStatItem = 32 * kStatPT;              // 1024 logits: one warp's item
+constexpr int kStatBlocksPerSm = 2;                  // statistics blocks resident per SM (launch bounds)
+constexpr int kDecThreads = 512;                     // decide kernel: 15 merging warps + 1 loading warp
+constexpr int kMaxStatRows = 2 * 1024 + 1;           // statistics rows of one batch row (n <= 1024)
 constexpr int kMaxNodes = 1025;                      // rows of one batch element in greedy mode (n <= 1024)
 constexpr int kCounterBank2 = 32768;                 // second bank of completion counters (B <= 32768)
-constexpr int kRescan = 32;                          // values per thread when the draw re-scans one chunk
-constexpr int kMaxChunk2 = kAccThreads * kRescan;    // 8192
-constexpr int kMaxCh2 = 256;                         // residual chunks per batch row
-constexpr int kStatCache = 512;                      // chunk statistics of one batch row held in smem
+constexpr int kResidPT = 16;                         // logits a thread holds in the residual pass and re-scan
+constexpr int kMaxChunk2 = kAccThreads * kResidPT;   // 4096
+constexpr int kMinChunk2 = 1024;
+constexpr int kMaxCh2 = 256;                         // residual chunks per batch row (V <= 2^20 fits)
 
 // Double-float value hi + lo (two fp32 words). GB300 executes only a couple
 // of fp64 operations per clock per SM, so sums that need more than fp32 are
@@ -160,22 +170,56 @@ __device__ __forceinline__ const float* stat_row_ptr(const float* p, const float
   return q + ((int64_t)b * n + (i - n - 1)) * V;
 }
 
-// Merge a row's chunk statistics: M = max m_c, Z = sum_c s_c exp(m_c - M).
-__device__ void merge_row(const RowStat* st, int ch, float& M, DF& Z) {
+// Merge a row's chunk statistics with one warp: M = max m_c,
+// Z = sum_c s_c exp(m_c - M); every lane returns the same M and Z (df_add is
+// commutative bit for bit, so the butterfly leaves one value in all lanes).
+// The statistics (written by an earlier kernel) are read through L2; the
+// first kMergeRegs per lane are held in registers between the two passes.
+constexpr int kMergeRegs = 8;
+__device__ void warp_merge_row(const RowStat* st, int ch, float& M, DF& Z) {
+  const int lane = threadIdx.x & 31;
+  float4 e[kMergeRegs];
   float m = -FLT_MAX;
-  for (int c = 0; c < ch; ++c) m = fmaxf(m, st[c].m);
+#pragma unroll
+  for (int k = 0; k < kMergeRegs; ++k) {
+    const int c = lane + 32 * k;
+    e[k] = c < ch ? __ldcg(reinterpret_cast<const float4*>(st + c)) : make_float4(-FLT_MAX, 0.0f, 0.0f, 0.0f);
+    m = fmaxf(m, e[k].x);
+  }
+  for (int c = lane + 32 * kMergeRegs; c < ch; c += 32) m = fmaxf(m, __ldcg(&st[c].m));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   DF z{0.0f, 0.0f};
-  for (int c = 0; c < ch; ++c) z = df_add(z, df_mul_f(st[c].s, expf(__fsub_rn(st[c].m, m))));
+#pragma unroll
+  for (int k = 0; k < kMergeRegs; ++k)
+    if (lane + 32 * k < ch) z = df_add(z, df_mul_f(DF{e[k].z, e[k].w}, expf(__fsub_rn(e[k].x, m))));
+  for (int c = lane + 32 * kMergeRegs; c < ch; c += 32) {
+    const float4 f = __ldcg(reinterpret_cast<const float4*>(st + c));
+    z = df_add(z, df_mul_f(DF{f.z, f.w}, expf(__fsub_rn(f.x, m))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z = df_add(z, shfl_xor_df(z, o));
   M = m;
   Z = z;
 }
 
+// Inclusive prefix sum over the warp (lane order), double-float.
+__device__ __forceinline__ DF warp_inclusive_scan(DF v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if (lane >= o) v = df_add(y, v);
+  }
+  return v;
+}
+
 // Load this thread's share of [x0, x1) into registers (missing slots: -FLT_MAX).
-template <bool VEC>
-__device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, float (&v)[kPerThread]) {
+template <bool VEC, int PT>
+__device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, float (&v)[PT]) {
   if (VEC) {
 #pragma unroll
-    for (int j = 0; j < kPerThread / 4; ++j) {
+    for (int j = 0; j < PT / 4; ++j) {
       const int xi = x0 + (j * kAccThreads + (int)threadIdx.x) * 4;
       float4 t = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
       if (xi < x1) t = ldg_stream_f4(reinterpret_cast<const float4*>(row + xi));
@@ -186,7 +230,7 @@ __device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, flo
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
+    for (int j = 0; j < PT; ++j) {
       const int xi = x0 + j * kAccThreads + (int)threadIdx.x;
       v[j] = xi < x1 ? ldg_stream_f(row + xi) : -FLT_MAX;
     }
@@ -194,79 +238,149 @@ __device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, flo
 }
 
 // ------------------------------------------------------- pass 1: row stats
-template <bool VEC>
-__global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(
-    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
-    const float* __restrict__ u, int n, int V, int chunk, RowStat* __restrict__ stats, Decision* __restrict__ dec,
-    int* __restrict__ counters, unsigned* err) {
-  grid_launch_dependents();
-  grid_dependency_wait();
-  const int rr = blockIdx.y;
-  const int per = 2 * n + 1;
-  const int b = rr / per;
-  const float* row = stat_row_ptr(p, q, n, V, rr);
-  const int x0 = blockIdx.x * chunk;
-  const int x1 = min(V, x0 + chunk);
-  float v[kPerThread];
-  load_chunk<VEC>(row, x0, x1, v);
+// Items are (statistics row, chunk of kStatItem logits); one warp takes one
+// item, its lanes holding kStatPT logits each, and the warps are persistent
+// (item it, it + warps, ...).
+
+// Exact maximum m of the item and sum of exp(l - m) (pairwise fp32 per lane,
+// double-float across lanes); lane 0 stores them. Padding (-FLT_MAX) adds 0.
+// exp via ex2.approx (__expf): its relative error grows with |l - m|, so it is
+// smallest on the terms that carry the sum; about 1e-7 of the total.
+__device__ __forceinline__ void item_stats(const float (&v)[kStatPT], RowStat* out) {
   float m = -FLT_MAX;
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) m = fmaxf(m, v[j]);
-  m = block_max(m);
-  // pairwise sum of exp(v - m); padding (-FLT_MAX) contributes 0
-  // exp via ex2.approx (__expf): relative error grows with |v - m|, so it is
-  // smallest on the terms that carry the sum; about 1e-7 of the total.
-  float t[kPerThread / 4];
+  for (int j = 0; j < kStatPT; ++j) m = fmaxf(m, v[j]);
 #pragma unroll
-  for (int j = 0; j < kPerThread / 4; ++j)
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float t[kStatPT / 4];
+#pragma unroll
+  for (int j = 0; j < kStatPT / 4; ++j)
     t[j] = (__expf(v[4 * j] - m) + __expf(v[4 * j + 1] - m)) + (__expf(v[4 * j + 2] - m) + __expf(v[4 * j + 3] - m));
 #pragma unroll
-  for (int w = kPerThread / 8; w >= 1; w >>= 1)
+  for (int w = kStatPT / 8; w >= 1; w >>= 1)
 #pragma unroll
     for (int j = 0; j < w; ++j) t[j] += t[j + w];
-  const DF s = block_sum(DF{t[0], 0.0f});
+  DF s{t[0], 0.0f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = df_add(s, shfl_xor_df(s, o));
+  if ((threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
+}
 
-  __shared__ int last;
-  if (threadIdx.x == 0) {
-    stats[(int64_t)rr * gridDim.x + blockIdx.x] = RowStat{m, 0.0f, s};
-    __threadfence();
-    last = atomicAdd(&counters[b], 1) == per * (int)gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
+__device__ __forceinline__ void item_range(int n, int V, int ch, int it, int& rr, int& x0, int& x1) {
+  rr = it / ch;
+  x0 = (it - rr * ch) * kStatItem;
+  x1 = min(V, x0 + kStatItem);
+}
 
-  // ---- last block of batch row b: acceptance test per draft, first rejection
-  const int ch = gridDim.x;
-  // this batch row's chunk statistics, copied to shared memory in parallel
-  // (at most kStatCache entries; larger cases read them from L2)
-  __shared__ RowStat cache[kStatCache];
-  __shared__ int first_reject;
-  const RowStat* gst = stats + (int64_t)b * per * ch;
-  const bool cached = per * ch <= kStatCache;
-  if (cached)
-    for (int e = threadIdx.x; e < per * ch; e += kAccThreads) {
-      cache[e].m = __ldcg(&gst[e].m);
-      cache[e].s = DF{__ldcg(&gst[e].s.hi), __ldcg(&gst[e].s.lo)};
+// A warp's item goes into registers (float4 loads when V % 4 == 0: rows are
+// then 16-byte aligned and every float4 lies wholly inside or outside the
+// row). Each warp keeps the next item's loads in flight while it reduces the
+// current one, so the HBM stream does not stop while the exponentials run.
+template <bool VEC>
+__device__ __forceinline__ void load_item(const float* p, const float* q, int n, int V, int ch, int it,
+                                          float (&v)[kStatPT]) {
+  int rr, x0, x1;
+  item_range(n, V, ch, it, rr, x0, x1);
+  const float* row = stat_row_ptr(p, q, n, V, rr);
+  const int lane = threadIdx.x & 31;
+  if (VEC) {
+#pragma unroll
+    for (int j = 0; j < kStatPT / 4; ++j) {
+      const int xi = x0 + (j * 32 + lane) * 4;
+      float4 t = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      if (xi < x1) t = ldg_stream_f4(reinterpret_cast<const float4*>(row + xi));
+      v[4 * j] = t.x;
+      v[4 * j + 1] = t.y;
+      v[4 * j + 2] = t.z;
+      v[4 * j + 3] = t.w;
     }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kStatPT; ++j) {
+      const int xi = x0 + j * 32 + lane;
+      v[j] = xi < x1 ? ldg_stream_f(row + xi) : -FLT_MAX;
+    }
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_kernel(const float* __restrict__ p,
+                                                                       const float* __restrict__ q, int n, int V,
+                                                                       int ch, int items,
+                                                                       RowStat* __restrict__ stats) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int nw = gridDim.x * kAccWarps;
+  int it = blockIdx.x * kAccWarps + (threadIdx.x >> 5);
+  float va[kStatPT], vb[kStatPT];
+  if (it < items) load_item<VEC>(p, q, n, V, ch, it, va);
+  while (it < items) {  // two items per trip: the buffers swap roles
+    const int i1 = it + nw;
+    if (i1 < items) load_item<VEC>(p, q, n, V, ch, i1, vb);
+    item_stats(va, stats + it);
+    if (i1 >= items) break;
+    const int i2 = i1 + nw;
+    if (i2 < items) load_item<VEC>(p, q, n, V, ch, i2, va);
+    item_stats(vb, stats + i1);
+    it = i2;
+  }
+}
+
+// One block per batch row: merge each statistics row's chunks (one warp per
+// row), evaluate alpha_i = min(1, P_i(d_i) / Q_i(d_i)) for every draft, find
+// the first rejection r and record r with the normalisers of row r.
+__global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
+    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
+    const float* __restrict__ u, int n, int V, int ch, const RowStat* __restrict__ stats,
+    Decision* __restrict__ dec, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  constexpr int kMergeWarps = kDecThreads / 32 - 1;
+  const int b = blockIdx.x;
+  const int per = 2 * n + 1;
+  const RowStat* st = stats + (int64_t)b * per * ch;
+  __shared__ float sM[kMaxStatRows];
+  __shared__ DF sZ[kMaxStatRows];
+  __shared__ float sLp[kMaxNodes], sLq[kMaxNodes];  // P_i / Q_i logits at d_i (n <= 1024)
+  __shared__ int first_reject;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kMergeWarps) {
+    // the drafts' own logits, fetched while the other warps merge
+    for (int i = lane; i < n; i += 32) {
+      const int di = d[(int64_t)b * n + i];
+      float lp = 0.0f, lq = 0.0f;
+      if (di < 0 || di >= V) {
+        report_error(err, kErrInput);
+        lp = -FLT_MAX;  // marks the draft rejected
+      } else {
+        lp = p[((int64_t)b * (n + 1) + i) * V + di];
+        lq = q[((int64_t)b * n + i) * V + di];
+      }
+      sLp[i] = lp;
+      sLq[i] = lq;
+    }
+  } else {
+    for (int row = warp; row < per; row += kMergeWarps) {
+      float M;
+      DF Z;
+      warp_merge_row(st + (int64_t)row * ch, ch, M, Z);
+      if (lane == 0) {
+        sM[row] = M;
+        sZ[row] = Z;
+      }
+    }
+  }
   if (threadIdx.x == 0) first_reject = n;
   __syncthreads();
-  const RowStat* st = cached ? cache : gst;
-  for (int i = threadIdx.x; i < n; i += kAccThreads) {
-    float mp, mq;
-    DF zp, zq;
-    merge_row(st + i * ch, ch, mp, zp);
-    merge_row(st + (n + 1 + i) * ch, ch, mq, zq);
-    const int di = d[(int64_t)b * n + i];
+  for (int i = threadIdx.x; i < n; i += kDecThreads) {
     bool reject;
-    if (di < 0 || di >= V) {
-      report_error(err, kErrInput);
+    if (sLp[i] == -FLT_MAX) {
       reject = true;
     } else {
       // alpha = min(1, P / Q) = min(1, (e_p * Z_q) / (e_q * Z_p)), fp32 (a few ulp)
-      const float ep = expf(__fsub_rn(p[((int64_t)b * (n + 1) + i) * V + di], mp));
-      const float eq = expf(__fsub_rn(q[((int64_t)b * n + i) * V + di], mq));
-      const float num = __fmul_rn(ep, df_val(zq)), den = __fmul_rn(eq, df_val(zp));
+      const float ep = expf(__fsub_rn(sLp[i], sM[i]));
+      const float eq = expf(__fsub_rn(sLq[i], sM[n + 1 + i]));
+      const float num = __fmul_rn(ep, df_val(sZ[n + 1 + i])), den = __fmul_rn(eq, df_val(sZ[i]));
       const float alpha = den > 0.0f ? fminf(1.0f, __fdiv_rn(num, den)) : 1.0f;
       reject = !(u[(int64_t)b * (n + 1) + i] < alpha);
     }
@@ -277,18 +391,16 @@ __global__ void __launch_bounds__(kAccThreads) accept_stats_kernel(
     Decision D;
     D.r = first_reject;
     D.pad[0] = D.pad[1] = D.pad[2] = 0;
-    DF z;
-    merge_row(st + D.r * ch, ch, D.mp, z);
-    D.izp = __frcp_rn(df_val(z));
+    D.mp = sM[D.r];
+    D.izp = __frcp_rn(df_val(sZ[D.r]));
     if (D.r < n) {
-      merge_row(st + (n + 1 + D.r) * ch, ch, D.mq, z);
-      D.izq = __frcp_rn(df_val(z));
+      D.mq = sM[n + 1 + D.r];
+      D.izq = __frcp_rn(df_val(sZ[n + 1 + D.r]));
     } else {
       D.mq = 0.0f;
       D.izq = 0.0f;
     }
     dec[b] = D;
-    counters[b] = 0;
   }
 }
 
@@ -309,7 +421,8 @@ struct ResidFn {
   __device__ __forceinline__ float rval(int x) const { return rv_of(prow[x], qrow ? qrow[x] : 0.0f); }
 };
 
-__global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
+template <int RS>  // values per thread in a chunk: chunk2 <= RS * kAccThreads
+__global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
     int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
     int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out) {
@@ -332,16 +445,16 @@ __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
   }
   const int x0 = blockIdx.x * chunk2, x1 = min(V, x0 + chunk2);
   // all of this thread's logits are loaded before any is used (one latency)
-  float lp[kRescan], lq[kRescan];
+  float lp[RS], lq[RS];
 #pragma unroll
-  for (int j = 0; j < kRescan; ++j) {
+  for (int j = 0; j < RS; ++j) {
     const int x = x0 + j * kAccThreads + (int)threadIdx.x;
     lp[j] = x < x1 ? f.prow[x] : 0.0f;
     lq[j] = (x < x1 && f.qrow) ? f.qrow[x] : 0.0f;
   }
   float sr = 0.0f, sp = 0.0f;
 #pragma unroll
-  for (int j = 0; j < kRescan; ++j) {
+  for (int j = 0; j < RS; ++j) {
     if (x0 + j * kAccThreads + (int)threadIdx.x < x1) {
       sr += f.rv_of(lp[j], lq[j]);
       if (f.qrow) sp += f.pv_of(lp[j]);
@@ -369,52 +482,74 @@ __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
     sh_cs[c].p = DF{__ldcg(&cs->p.hi), __ldcg(&cs->p.lo)};
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    DF S{0.0f, 0.0f};
-    for (int c = 0; c < (int)gridDim.x; ++c) S = df_add(S, sh_cs[c].r);
+  if (threadIdx.x < 32) {
+    // warp 0 finds the chunk holding u * S: each lane sums a contiguous run
+    // of chunk sums, a warp scan gives the prefix at each run, and the first
+    // lane whose prefix passes u * S walks its run
+    const int lane = threadIdx.x, C = gridDim.x;
+    const int per_l = (C + 31) / 32;
+    const int c0 = min(C, lane * per_l), c1 = min(C, c0 + per_l);
+    DF mine{0.0f, 0.0f};
+    for (int c = c0; c < c1; ++c) mine = df_add(mine, sh_cs[c].r);
+    DF incl = warp_inclusive_scan(mine);
+    DF S{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
     int usep = 0;
     if (f.qrow && S.hi == 0.0f) {  // corrected distribution is all zero: draw from P_r
       usep = 1;
-      S = DF{0.0f, 0.0f};
-      for (int c = 0; c < (int)gridDim.x; ++c) S = df_add(S, sh_cs[c].p);
+      mine = DF{0.0f, 0.0f};
+      for (int c = c0; c < c1; ++c) mine = df_add(mine, sh_cs[c].p);
+      incl = warp_inclusive_scan(mine);
+      S = DF{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
     }
     const DF t = df_mul_f(S, u[(int64_t)b * (n + 1) + n]);
-    DF cum{0.0f, 0.0f};
-    int cstar = -1;
-    for (int c = 0; c < (int)gridDim.x; ++c) {
-      const DF nxt = df_add(cum, usep ? sh_cs[c].p : sh_cs[c].r);
-      if (df_gt(nxt, t)) {
-        cstar = c;
-        break;
+    const unsigned passed = __ballot_sync(0xffffffffu, c1 > c0 && df_gt(incl, t));
+    const DF excl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+    if (passed == 0u) {
+      if (lane == 0) {  // u * S is not below the total: no chunk holds it
+        sh_t = t;
+        sh_before = S;
+        sh_chunk = -1;
       }
-      cum = nxt;
+    } else if (lane == __ffs(passed) - 1) {
+      DF cum = lane == 0 ? DF{0.0f, 0.0f} : excl;
+      int cstar = c1 - 1;  // the run's prefix passes u * S; rounding may place the step at its end
+      for (int c = c0; c < c1; ++c) {
+        const DF nxt = df_add(cum, usep ? sh_cs[c].p : sh_cs[c].r);
+        if (df_gt(nxt, t)) {
+          cstar = c;
+          break;
+        }
+        if (c + 1 < c1) cum = nxt;
+      }
+      sh_t = t;
+      sh_before = cum;
+      sh_chunk = cstar;
     }
-    sh_t = t;
-    sh_before = cum;
-    sh_chunk = cstar;
-    sh_usep = usep;
-    sh_found = INT_MAX;
-    counters[b] = 0;
+    if (lane == 0) {
+      sh_usep = usep;
+      sh_found = INT_MAX;
+      counters[b] = 0;
+    }
   }
   __syncthreads();
   const int usep = sh_usep;
   auto val = [&](int x) { return usep ? f.pval(x) : f.rval(x); };
   if (sh_chunk >= 0) {
     // coalesced loads of the chunk (stride kAccThreads) into shared memory,
-    // then a contiguous sub-range per thread (at most kRescan values) for the
+    // then a contiguous sub-range per thread (at most RS values) for the
     // double-float running sums from a block scan
-    __shared__ float sv[kMaxChunk2 + kMaxChunk2 / 32];  // one pad word per 32: conflict-free row reads
+    __shared__ float sv[RS * kAccThreads + RS * kAccThreads / 32];  // one pad word per 32: conflict-free row reads
     const int c0 = sh_chunk * chunk2, c1 = min(V, c0 + chunk2);
     {
-      float lp[kRescan], lq[kRescan];
+      float lp[RS], lq[RS];
 #pragma unroll
-      for (int j = 0; j < kRescan; ++j) {
+      for (int j = 0; j < RS; ++j) {
         const int x = min(c0 + j * kAccThreads + (int)threadIdx.x, V - 1);
         lp[j] = f.prow[x];
         lq[j] = f.qrow ? f.qrow[x] : 0.0f;
       }
 #pragma unroll
-      for (int j = 0; j < kRescan; ++j) {
+      for (int j = 0; j < RS; ++j) {
         const int o = j * kAccThreads + (int)threadIdx.x;
         if (c0 + o < c1) sv[o + (o >> 5)] = usep ? f.pv_of(lp[j]) : f.rv_of(lp[j], lq[j]);
       }
@@ -422,20 +557,20 @@ __global__ void __launch_bounds__(kAccThreads) accept_resid_kernel(
     __syncthreads();
     const int per_t = (c1 - c0 + kAccThreads - 1) / kAccThreads;
     const int a0 = min(c1, c0 + (int)threadIdx.x * per_t), a1 = min(c1, a0 + per_t);
-    float vals[kRescan];
+    float vals[RS];
 #pragma unroll
-    for (int j = 0; j < kRescan; ++j) {
+    for (int j = 0; j < RS; ++j) {
       const int k = a0 + j - c0;
       vals[j] = (a0 + j < a1) ? sv[k + (k >> 5)] : 0.0f;
     }
     DF mine{0.0f, 0.0f};
 #pragma unroll
-    for (int j = 0; j < kRescan; ++j) mine = df_add_f(mine, vals[j]);
+    for (int j = 0; j < RS; ++j) mine = df_add_f(mine, vals[j]);
     DF run = df_add(sh_before, block_exclusive_scan(mine));
     const DF t = sh_t;
     int hit = INT_MAX;
 #pragma unroll
-    for (int j = 0; j < kRescan; ++j) {
+    for (int j = 0; j < RS; ++j) {
       if (a0 + j < a1 && hit == INT_MAX) {
         run = df_add_f(run, vals[j]);
         if (df_gt(run, t)) hit = a0 + j;
@@ -499,13 +634,13 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
   const int b = rr / rows_per_b;
   const float* row = p + (int64_t)rr * V;
   const int x0 = blockIdx.x * chunk, x1 = min(V, x0 + chunk);
-  float v[kPerThread];
-  load_chunk<VEC>(row, x0, x1, v);
+  float v[kArgPT];
+  load_chunk<VEC, kArgPT>(row, x0, x1, v);
   // this thread's indices increase with j (and within a float4), so a strict
   // comparison keeps the smallest index among equal values
   ArgPart best{-FLT_MAX, -1};
 #pragma unroll
-  for (int j = 0; j < kPerThread; ++j) {
+  for (int j = 0; j < kArgPT; ++j) {
     const int xi = VEC ? x0 + ((j / 4) * kAccThreads + (int)threadIdx.x) * 4 + (j % 4)
                        : x0 + j * kAccThreads + (int)threadIdx.x;
     if (xi < x1 && (v[j] > best.v || best.idx < 0)) best = ArgPart{v[j], xi};
@@ -594,34 +729,39 @@ AcceptPlan accept_plan(int B, int n, int V) {
   AcceptPlan pl;
   const int rows = B * (2 * n + 1);  // upper bound over modes (greedy reads B*(n+1) or B*n rows)
   pl.rows = rows;
-  // statistics / argmax chunks: at most kMaxChunk logits, about 1024 blocks in all, at most 64 per row
-  int ch = (V + kMaxChunk - 1) / kMaxChunk;
+  pl.rows_seq = rows;
+  // statistics items: chunks of kStatItem logits
+  const int ch = (V + kStatItem - 1) / kStatItem;
+  pl.ch = ch;
+  pl.chunk = kStatItem;
+  // argmax chunks (greedy modes): at most kArgChunk logits, about 1024
+  // blocks in all, at most 64 per row, at least ~2048 logits each
+  int cha = (V + kArgChunk - 1) / kArgChunk;
   const int want = (1024 + rows - 1) / rows;
-  const int cap_v = (V + 2047) / 2048;  // chunks of at least ~2048 logits
+  const int cap_v = (V + 2047) / 2048;
   int more = want < cap_v ? want : cap_v;
   if (more > 64) more = 64;
-  if (ch < more) ch = more;
-  int chunk = (V + ch - 1) / ch;
-  chunk = (chunk + 3) / 4 * 4;
-  if (chunk > kMaxChunk) chunk = kMaxChunk;
-  ch = (V + chunk - 1) / chunk;
-  pl.ch = ch;
-  pl.chunk = chunk;
-  // residual chunks per batch row: about 256 blocks in all (one wave: the
-  // pass is short and latency-bound), at most 64, at least enough that one
-  // chunk fits the draw's register re-scan
-  int ch2 = (256 + B - 1) / B;
-  if (ch2 > 64) ch2 = 64;
-  if (ch2 > cap_v) ch2 = cap_v;
-  if (ch2 < 1) ch2 = 1;
-  if (ch2 < (V + kMaxChunk2 - 1) / kMaxChunk2) ch2 = (V + kMaxChunk2 - 1) / kMaxChunk2;
-  int chunk2 = (V + ch2 - 1) / ch2;
-  ch2 = (V + chunk2 - 1) / chunk2;
-  pl.ch2 = ch2;
-  pl.chunk2 = chunk2;
-  const size_t stats_bytes = align256((size_t)rows * ch * sizeof(RowStat));  // >= ArgPart storage
+  if (cha < more) cha = more;
+  int chunka = (V + cha - 1) / cha;
+  chunka = (chunka + 3) / 4 * 4;
+  if (chunka > kArgChunk) chunka = kArgChunk;
+  cha = (V + chunka - 1) / chunka;
+  pl.cha = cha;
+  pl.chunka = chunka;
+  // residual chunks per batch row: the launch picks ch2 in [lo, hi] so the
+  // grid fits the resident blocks (one wave); the workspace holds hi
+  const int lo = (V + kMaxChunk2 - 1) / kMaxChunk2;  // <= kMaxCh2 for V <= 2^20
+  int hi = (V + kMinChunk2 - 1) / kMinChunk2;
+  if (hi > kMaxCh2) hi = kMaxCh2;
+  if (hi < lo) hi = lo;
+  pl.ch2_lo = lo;
+  pl.ch2 = hi;
+  pl.chunk2 = (V + hi - 1) / hi;
+  size_t stats_bytes = align256((size_t)rows * ch * sizeof(RowStat));
+  const size_t parts_bytes = align256((size_t)rows * cha * sizeof(ArgPart));
+  if (parts_bytes > stats_bytes) stats_bytes = parts_bytes;
   const size_t dec_bytes = align256((size_t)B * sizeof(Decision));
-  const size_t csum_bytes = align256((size_t)B * ch2 * sizeof(ChunkSum));
+  const size_t csum_bytes = align256((size_t)B * hi * sizeof(ChunkSum));
   pl.stats_off = kCounterRegionBytes;
   pl.dec_off = pl.stats_off + stats_bytes;
   pl.csum_off = pl.dec_off + dec_bytes;
@@ -630,25 +770,44 @@ AcceptPlan accept_plan(int B, int n, int V) {
 }
 
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
-                              int32_t* acc, int32_t* next, void* ws, const AcceptPlan& pl, unsigned* err,
+                              int32_t* acc, int32_t* next, void* ws, const AcceptPlan& pl, int num_sms, unsigned* err,
                               cudaStream_t stream) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   RowStat* stats = reinterpret_cast<RowStat*>(w + pl.stats_off);
   Decision* dec = reinterpret_cast<Decision*>(w + pl.dec_off);
   ChunkSum* csum = reinterpret_cast<ChunkSum*>(w + pl.csum_off);
-  int* cnt1 = reinterpret_cast<int*>(w);
-  int* cnt2 = cnt1 + kCounterBank2;
-  const dim3 g1(pl.ch, B * (2 * n + 1));
+  int* cnt2 = reinterpret_cast<int*>(w) + kCounterBank2;
   cudaError_t e;
+  // statistics grid: persistent warps, one wave of resident blocks (the
+  // kernel's launch bounds give two per SM)
+  const int items = pl.rows_seq * pl.ch;
+  int g1 = (items + kAccWarps - 1) / kAccWarps;
+  if (g1 > kStatBlocksPerSm * num_sms) g1 = kStatBlocksPerSm * num_sms;
   if (V % 4 == 0)
-    e = launch_pdl(accept_stats_kernel<true>, g1, dim3(kAccThreads), 0, stream, p, q, d, u, n, V, pl.chunk, stats, dec,
-                   cnt1, err);
+    e = launch_pdl(accept_stats_kernel<true>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, stats);
   else
-    e = launch_pdl(accept_stats_kernel<false>, g1, dim3(kAccThreads), 0, stream, p, q, d, u, n, V, pl.chunk, stats,
-                   dec, cnt1, err);
+    e = launch_pdl(accept_stats_kernel<false>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items,
+                   stats);
   if (e != cudaSuccess) return e;
-  const dim3 g2(pl.ch2, B);
-  return launch_pdl(accept_resid_kernel, g2, dim3(kAccThreads), 0, stream, p, q, u, n, V, pl.chunk2,
+  e = launch_pdl(accept_decide_kernel, dim3(B), dim3(kDecThreads), 0, stream, p, q, d, u, n, V, pl.ch,
+                 (const RowStat*)stats, dec, err);
+  if (e != cudaSuccess) return e;
+  // residual grid: as many chunks per batch row as one wave of resident
+  // blocks allows, within [ch2_lo, ch2]
+  static std::atomic<int> resid_per_sm{0};
+  int per_sm = resid_per_sm.load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_resid_kernel<kResidPT>, kAccThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    resid_per_sm.store(per_sm, std::memory_order_relaxed);
+  }
+  int ch2 = (int)(((int64_t)per_sm * num_sms) / B);
+  if (ch2 > pl.ch2) ch2 = pl.ch2;
+  if (ch2 < pl.ch2_lo) ch2 = pl.ch2_lo;
+  const int chunk2 = (V + ch2 - 1) / ch2;
+  ch2 = (V + chunk2 - 1) / chunk2;
+  return launch_pdl(accept_resid_kernel<kResidPT>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V, chunk2,
                     (const Decision*)dec, csum, cnt2, acc, next);
 }
 
@@ -659,12 +818,12 @@ cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t
   ArgPart* parts = reinterpret_cast<ArgPart*>(w + pl.stats_off);
   int* cnt = reinterpret_cast<int*>(w);
   const int rows_per_b = parents ? n : n + 1;
-  const dim3 g(pl.ch, B * rows_per_b);
+  const dim3 g(pl.cha, B * rows_per_b);
   if (V % 4 == 0)
     return launch_pdl(accept_argmax_kernel<true>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                      pl.chunk, parts, cnt, acc, next, err);
+                      pl.chunka, parts, cnt, acc, next, err);
   return launch_pdl(accept_argmax_kernel<false>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                    pl.chunk, parts, cnt, acc, next, err);
+                    pl.chunka, parts, cnt, acc, next, err);
 }
 
 }  // namespace w4a16

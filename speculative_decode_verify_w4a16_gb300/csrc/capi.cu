@@ -193,7 +193,7 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
   cudaError_t e;
   if (q_logits)
     e = launch_accept_seq(p_logits, q_logits, draft_ids, uniforms, B, n, V, accepted_len, next_token, workspace, plan,
-                          dev.err, static_cast<cudaStream_t>(stream));
+                          dev.num_sms, dev.err, static_cast<cudaStream_t>(stream));
   else
     e = launch_accept_greedy(p_logits, draft_ids, tree_parents, B, n, V, accepted_len, next_token, workspace, plan,
                              dev.err, static_cast<cudaStream_t>(stream));

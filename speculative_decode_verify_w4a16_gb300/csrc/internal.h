@@ -102,17 +102,21 @@ cudaError_t launch_linear(const void* x, int M, int64_t K, const void* qw_packed
 
 // ---- accept
 struct AcceptPlan {
-  int rows = 0;       // logit rows read by the statistics pass
-  int ch = 0;         // chunks per row (statistics / argmax pass)
+  int rows = 0;       // logit rows read by the statistics pass (upper bound over modes)
+  int rows_seq = 0;   // statistics rows in stochastic mode: B * (2n + 1)
+  int ch = 0;         // chunks per row (statistics pass)
   int chunk = 0;      // elements per chunk (multiple of 4)
-  int ch2 = 0;        // chunks per batch row (residual pass)
-  int chunk2 = 0;
+  int cha = 0;        // chunks per row (argmax pass)
+  int chunka = 0;     // elements per chunk (multiple of 4)
+  int ch2_lo = 0;     // fewest chunks per batch row in the residual pass
+  int ch2 = 0;        // most chunks per batch row in the residual pass (workspace)
+  int chunk2 = 0;     // elements per chunk at ch2
   size_t stats_off = 0, dec_off = 0, csum_off = 0, total = 0;  // counters at offset 0
 };
 AcceptPlan accept_plan(int B, int n, int V);
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
-                              int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
-                              cudaStream_t stream);
+                              int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, int num_sms,
+                              unsigned* err, cudaStream_t stream);
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
                                  int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
                                  cudaStream_t stream);

@@ -54,7 +54,11 @@ def test_config_seq_full_vocab(K):
 
 
 @pytest.mark.parametrize("B,K,V,seed", [(512, 4, 1000, 1), (300, 1, 2, 2), (200, 3, 5, 3), (64, 8, 50000, 4),
-                                        (128, 6, 4099, 5), (33, 2, 130000, 6)])
+                                        (128, 6, 4099, 5), (33, 2, 130000, 6),
+                                        # many drafts (statistics rows merged in several rounds per block;
+                                        # more drafts than one warp's lanes) and a vocabulary of more than
+                                        # 256 statistics items per row
+                                        (4, 100, 3000, 7), (3, 40, 1001, 8), (2, 2, 300000, 9)])
 def test_seq_random_cases(B, K, V, seed):
     p, q, d, u = synth.accept_seq_case(B, K, V, seed=60 + seed, p_std=2.0)
     acc_r, tie = _compare_seq(p, q, d, u, f"B={B} K={K} V={V}")
