@@ -62,10 +62,11 @@ struct TcLayout {
   static_assert(kA * 64 + kD * NT <= (int)kTcTmemCols, "TMEM budget");
   static_assert(kA % kTcDqGroups == 0 && kD % kTcDqGroups == 0, "ring slots per group");
   static_assert(kD >= 2, "the epilogue takes units in pairs");
-  // a unit's hand-off entry is rewritten kTcRing units later; by then the
-  // dequantisation of that later unit has waited for the MMAs kA units back,
-  // which waited for the epilogue kD units before those
-  static_assert(kA + kD <= kTcRing, "hand-off ring depth");
+  // a unit's hand-off entry is rewritten kTcRing units later, by the group
+  // that then has finished its previous unit (kTcDqGroups back): that one
+  // waited for the MMAs kA units before it, which waited for the epilogue
+  // kD units before those
+  static_assert(kTcDqGroups + kA + kD <= kTcRing, "hand-off ring depth");
   // Two shared-memory rings: token tiles (read by the MMAs, a few units
   // ahead; they come from L2) and packed codes + scales (read by the dequant
   // groups and released as soon as they are in registers; deep, so that
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       int* work = &p.counters[kWorkCounter];
-      int n_w = 0;  // units whose codes have been issued
+      uint32_t n_w = 0;  // units whose codes have been issued
       bool ok = true;
       int item = atomicAdd(work, 1);
       while (ok && item < p.items) {
@@ -360,9 +361,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         int64_t t = ub / p.G;
         int64_t g = ub - t * p.G;
         for (int64_t u = ub; u < ue; ++u, ++n_w) {
-          const int s = n_w % L::kWStages;
-          if (n_w >= L::kWStages &&
-              !mbar_wait(&wempty[s], ((uint32_t)(n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
+          const uint32_t s = n_w % L::kWStages;
+          if (n_w >= (uint32_t)L::kWStages && !mbar_wait(&wempty[s], ((n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
             ok = false;
             break;
           }
@@ -382,9 +382,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       // stage): -1 at the first index past the last unit, where the MMA warp
       // and the epilogue stop too; -2 at the other groups' next indices
       for (int k = 0; ok && k < kTcDqGroups; ++k, ++n_w) {
-        const int s = n_w % L::kWStages;
-        if (n_w >= L::kWStages &&
-            !mbar_wait(&wempty[s], ((uint32_t)(n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
+        const uint32_t s = n_w % L::kWStages;
+        if (n_w >= (uint32_t)L::kWStages && !mbar_wait(&wempty[s], ((n_w / L::kWStages) & 1u) ^ 1u, p.err)) {
           ok = false;
           break;
         }
@@ -392,8 +391,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         mbar_arrive(&wfull[s]);
       }
       if (!ok) {  // let copies already in flight land before the CTA exits
-        for (int i = (n_w > L::kWStages ? n_w - L::kWStages : 0); i < n_w; ++i)
-          mbar_wait(&wfull[i % L::kWStages], (uint32_t)(i / L::kWStages) & 1u, p.err);
+        for (uint32_t i = (n_w > (uint32_t)L::kWStages ? n_w - L::kWStages : 0u); i < n_w; ++i)
+          mbar_wait(&wfull[i % L::kWStages], (i / L::kWStages) & 1u, p.err);
       }
       // the last CTA to get here resets the claim counters for the next call
       __threadfence();
@@ -409,16 +408,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     // MMAs free a slot. Counting in on wempty keeps the stage (and its
     // metadata) from being recycled before it was read here.
     if (lane == 0) {
-      int n_x = 0;
+      uint32_t n_x = 0;
       for (;; ++n_x) {
-        const int s = n_x % L::kWStages, sx = n_x % L::kXStages;
-        if (!mbar_wait(&wfull[s], (uint32_t)(n_x / L::kWStages) & 1u, p.err)) break;
+        const uint32_t s = n_x % L::kWStages, sx = n_x % L::kXStages;
+        const uint32_t pw = (n_x / L::kWStages) & 1u, pe = ((n_x / L::kXStages) & 1u) ^ 1u;
+        // both barriers tested at once (one latency); wait in order only if one is still open
+        const bool tw = mbar_test(&wfull[s], pw);
+        const bool te = mbar_test(&xempty[sx], pe) | (n_x < (uint32_t)L::kXStages);
+        if (!tw && !mbar_wait(&wfull[s], pw, p.err)) break;
         const int4 m = meta[s];
         if (m.x < 0) break;  // stop marker
         mbar_arrive(&wempty[s]);
-        if (n_x >= L::kXStages &&
-            !mbar_wait(&xempty[sx], ((uint32_t)(n_x / L::kXStages) & 1u) ^ 1u, p.err))
-          break;
+        if (!te && !mbar_wait(&xempty[sx], pe, p.err)) break;
         uint8_t* xs = smem + L::kXOff + sx * L::kXStage;
         mbar_arrive_expect_tx(&xfull[sx], (uint32_t)L::kXStage);
         tma_load_2d(xs, &xmap, m.z * kGroup, 0, &xfull[sx]);
@@ -426,8 +427,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       }
       // let token tiles in flight land before the CTA exits (normally the MMAs
       // have consumed them all already)
-      for (int i = (n_x > L::kXStages ? n_x - L::kXStages : 0); i < n_x; ++i)
-        mbar_wait(&xfull[i % L::kXStages], (uint32_t)(i / L::kXStages) & 1u, p.err);
+      for (uint32_t i = (n_x > (uint32_t)L::kXStages ? n_x - L::kXStages : 0u); i < n_x; ++i)
+        mbar_wait(&xfull[i % L::kXStages], (i / L::kXStages) & 1u, p.err);
     }
   } else if (warp >= kTcMmaWarp0) {
     // ------------------------------------------------------------- MMA
@@ -436,10 +437,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     // the token tile is in shared memory once a_full completes.
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(NT);
-      for (int i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
-        const int sx = i % L::kXStages, b = i % L::kA, db = i % L::kD;
-        if (!mbar_wait(&a_full[b], (uint32_t)(i / L::kA) & 1u, p.err)) break;
-        if (i >= L::kD && !mbar_wait(&d_free[db], ((uint32_t)(i / L::kD) & 1u) ^ 1u, p.err)) break;
+      for (uint32_t i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
+        const uint32_t sx = i % L::kXStages, b = i % L::kA, db = i % L::kD;
+        const uint32_t pa = (i / L::kA) & 1u, pd = ((i / L::kD) & 1u) ^ 1u, px = (i / L::kXStages) & 1u;
+        // the three barriers tested at once (one latency); waits in order only
+        // for those still open (the token tile after the stop check)
+        const bool ta = mbar_test(&a_full[b], pa);
+        const bool td = mbar_test(&d_free[db], pd) | (i < (uint32_t)L::kD);
+        const bool tx = mbar_test(&xfull[sx], px);
+        if (!ta && !mbar_wait(&a_full[b], pa, p.err)) break;
+        if (!td && !mbar_wait(&d_free[db], pd, p.err)) break;
         const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
         if (mk < 0) {  // stop marker
           if (mk == -1) {  // the epilogue's last index: complete its phase without MMAs
@@ -448,7 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           }
           break;
         }
-        if (!mbar_wait(&xfull[sx], (uint32_t)(i / L::kXStages) & 1u, p.err)) break;
+        if (!tx && !mbar_wait(&xfull[sx], px, p.err)) break;
         tc_fence_after();
         const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + L::kXOff + sx * L::kXStage));
 #pragma unroll
@@ -462,21 +469,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         umma_commit(&xempty[sx]);  // the token tile was read by these MMAs
         // release (to the epilogue) of the hand-off entry this thread acquired through a_full
         mbar_arrive(&mma_done[db]);
-        mma_issued = i + 1;
+        mma_issued = (int)i + 1;
       }
       if (mma_issued > 0) umma_commit(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this thread's MMAs
     }
   } else if (warp < kTcDqWarps) {
     // ------------------------------------------------------ dequant groups
     const int grp = warp >> 2, q = warp & 3;
-    for (int i = grp;; i += kTcDqGroups) {
-      const int s = i % L::kWStages, b = i % L::kA;
-      if (!mbar_wait(&wfull[s], (uint32_t)(i / L::kWStages) & 1u, p.err)) break;
+    for (uint32_t i = grp;; i += kTcDqGroups) {
+      const uint32_t s = i % L::kWStages, b = i % L::kA;
+      const uint32_t pw = (i / L::kWStages) & 1u, pa = (i / L::kA - 1u) & 1u;
+      // A[b] is free once the MMAs of unit i - kA have completed; both
+      // barriers tested at once, waits only for one still open
+      const bool tw = mbar_test(&wfull[s], pw);
+      const bool ta = mbar_test(&a_free[b], pa) | (i < (uint32_t)L::kA);
+      if (!tw && !mbar_wait(&wfull[s], pw, p.err)) break;
       const uint4 mu = lds128(smem_u32(&meta[s]));
-      // A[b] is free once the MMAs of unit i - kA have completed
-      if (i >= L::kA && !mbar_wait(&a_free[b], (uint32_t)(i / L::kA - 1) & 1u, p.err)) break;
       const bool stop = (int)mu.x < 0;
       if (stop) {
+        if (!ta && !mbar_wait(&a_free[b], pa, p.err)) break;
         // forward the marker to this group's MMA warp (and through it to the
         // epilogue, which stops at the first one)
         if (q == 0 && lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, 0, 0, 0);
@@ -492,27 +503,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         }
         if (lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
       }
-      uint4 w[2][2];  // this warp's 32 rows: codes in registers, then the stage is released
+      uint4 w[2][2];  // this warp's 32 rows
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) w[rt][hh] = lds128(st + (((q * 2 + rt) * 2 + hh) * 32 + lane) * 16);
+      // the whole unit is dequantised into registers before A[b] is needed,
+      // so the arithmetic overlaps the MMAs that still read A[b]
+      uint32_t r[2][2][16];  // 16 rows x 64 K -> 16 lanes x 32 TMEM columns, per (rt, hh)
 #pragma unroll
-      for (int rt = 0; rt < 2; ++rt) {
+      for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {  // 16 rows x 64 K -> 16 lanes x 32 TMEM columns
-          uint32_t r[16];
-          tc_dequant(w[rt][hh].x, p.dq, &r[0]);
-          tc_dequant(w[rt][hh].y, p.dq, &r[4]);
-          tc_dequant(w[rt][hh].z, p.dq, &r[8]);
-          tc_dequant(w[rt][hh].w, p.dq, &r[12]);
-          tmem_st_16x256b_x4(tmem + ((uint32_t)(32 * q + 16 * rt) << 16) + a_col(b) + 32 * hh, r);
+        for (int hh = 0; hh < 2; ++hh) {
+          tc_dequant(w[rt][hh].x, p.dq, &r[rt][hh][0]);
+          tc_dequant(w[rt][hh].y, p.dq, &r[rt][hh][4]);
+          tc_dequant(w[rt][hh].z, p.dq, &r[rt][hh][8]);
+          tc_dequant(w[rt][hh].w, p.dq, &r[rt][hh][12]);
         }
-      }
-      // every code of the stage has been used, so its loads have completed:
-      // release it to the producer (the scale / metadata copies are done too)
+      // every code and scale of the stage has been used, so its loads have
+      // completed: release it to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[s]);
+      if (!ta && !mbar_wait(&a_free[b], pa, p.err)) break;
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          tmem_st_16x256b_x4(tmem + ((uint32_t)(32 * q + 16 * rt) << 16) + a_col(b) + 32 * hh, r[rt][hh]);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -526,19 +543,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
 #pragma unroll
     for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
     int item = 0, item_t0 = 0, seg_g0 = 0;
-    auto scale_of = [&](int u) {
+    auto scale_of = [&](uint32_t u) {
       return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
           smem + L::kScRingOff + (u % kTcRing) * kUnitScaleBytes + 2 * sc_half)));
     };
-    auto meta_of = [&](int u) {
+    auto meta_of = [&](uint32_t u) {
       const uint4 mu = lds128(smem_u32(&meta_ring[u % kTcRing]));
       return make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
     };
     // Units are taken two at a time (both accumulators read together) unless
     // the first one ends a tile segment or the second is the stop marker.
-    for (int e = 0;;) {
-      const int db = e % L::kD;
-      if (!mbar_wait(&mma_done[db], (uint32_t)(e / L::kD) & 1u, p.err)) break;
+    for (uint32_t e = 0;;) {
+      const uint32_t db = e % L::kD, db1 = (e + 1) % L::kD;
+      const uint32_t p0 = (e / L::kD) & 1u, p1 = ((e + 1) / L::kD) & 1u;
+      // both accumulators tested at once; waits only for one still open
+      const bool t0 = mbar_test(&mma_done[db], p0);
+      const bool t1 = mbar_test(&mma_done[db1], p1);
+      if (!t0 && !mbar_wait(&mma_done[db], p0, p.err)) break;
       const int4 me = meta_of(e);
       if (me.x < 0) break;  // stop marker
       if (me.w & kTcUnitFirst) {
@@ -549,9 +570,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       const bool seg_end = me.z == p.G - 1 || (me.w & kTcUnitLast);
       bool pair = false;
       int4 me1 = me;
-      const int db1 = (e + 1) % L::kD;
       if (!seg_end) {
-        if (!mbar_wait(&mma_done[db1], (uint32_t)((e + 1) / L::kD) & 1u, p.err)) break;
+        if (!t1 && !mbar_wait(&mma_done[db1], p1, p.err)) break;
         me1 = meta_of(e + 1);
         pair = me1.x >= 0;
       }
@@ -579,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         seg_g0 = 0;
       }
       if (!pair && !seg_end) break;  // the second unit was the stop marker
-      e += pair ? 2 : 1;
+      e += pair ? 2u : 1u;
     }
   }
 
