@@ -57,8 +57,15 @@ struct TcLayout {
   // always used by units of one dequant group and one MMA warp, in order:
   // each waiter is then at most one phase ahead of the slot's barrier, which
   // a parity wait requires (units are dealt round-robin to the groups).
-  static constexpr int kA = NT <= 16 ? 6 : 4;
-  static constexpr int kD = NT <= 16 ? 8 : (NT <= 32 ? 8 : 4);
+  //
+  // The A buffers, the accumulators and the token tiles have the same depth
+  // kR, so that slot i % kR of all three is released by the same event, the
+  // completion of unit i's MMAs: one commit per unit to done[i % kR] serves
+  // the dequant group (A), the epilogue (D) and the token-tile warp (x).
+  // Each tcgen05.commit costs the tensor pipe about as much as an MMA.
+  static constexpr int kR = NT <= 16 ? 6 : 4;
+  static constexpr int kA = kR;
+  static constexpr int kD = kR;
   static_assert(kA * 64 + kD * NT <= (int)kTcTmemCols, "TMEM budget");
   static_assert(kA % kTcDqGroups == 0 && kD % kTcDqGroups == 0, "ring slots per group");
   static_assert(kD >= 2, "the epilogue takes units in pairs");
@@ -73,7 +80,7 @@ struct TcLayout {
   // enough HBM reads are in flight).
   static constexpr int kX = NT * 128;             // one 64-wide K half of the token tile
   static constexpr int kXStage = 2 * kX;          // 1024-aligned (swizzled UMMA operand)
-  static constexpr int kXStages = NT <= 16 ? 6 : 4;
+  static constexpr int kXStages = kR;
   static constexpr int kWStage = kUnitBytes + kUnitScaleBytes;  // codes, then scales
   static constexpr int kXOff = 0;
   static constexpr int kWOff = kXOff + kXStages * kXStage;
@@ -82,10 +89,8 @@ struct TcLayout {
   static constexpr int kMetaRingOff = kScRingOff + kTcRing * kUnitScaleBytes;  // kTcRing x int4
   static constexpr int kMetaOff = kMetaRingOff + kTcRing * 16;        // kWStages x int4 (per stage)
   static constexpr int kBarOff = kMetaOff + kWStages * 16;
-  // wfull[SW], wempty[SW], xfull[SX], xempty[SX], a_full[kA], a_free[kA], mma_done[kD], d_free[kD],
-  // mma_fin[groups], tmem base
-  static constexpr int kTotal =
-      kBarOff + (2 * kWStages + 2 * kXStages + 2 * kA + 2 * kD + kTcDqGroups) * 8 + 16 + 1024;  // +1024: alignment
+  // wfull[SW], wempty[SW], xfull[kR], a_full[kR], done[kR], d_free[kR], mma_fin[groups], tmem base
+  static constexpr int kTotal = kBarOff + (2 * kWStages + 4 * kR + kTcDqGroups) * 8 + 16 + 1024;  // +1024: alignment
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
   static_assert(kWStage % 16 == 0, "bulk copy alignment");
   static_assert(kWStages >= 2 * kTcDqGroups, "ring depth");
@@ -292,12 +297,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* wempty = wfull + L::kWStages;
   uint64_t* xfull = wempty + L::kWStages;
-  uint64_t* xempty = xfull + L::kXStages;
-  uint64_t* a_full = xempty + L::kXStages;
-  uint64_t* a_free = a_full + L::kA;
-  uint64_t* mma_done = a_free + L::kA;
-  uint64_t* d_free = mma_done + L::kD;
-  uint64_t* mma_fin = d_free + L::kD;  // per MMA warp: all its MMAs complete (teardown)
+  uint64_t* a_full = xfull + L::kR;
+  uint64_t* done = a_full + L::kR;  // unit i's MMAs complete: frees A, x and hands D to the epilogue
+  uint64_t* d_free = done + L::kR;
+  uint64_t* mma_fin = d_free + L::kR;  // per MMA warp: all its MMAs complete (teardown)
+  uint64_t* const xempty = done;
+  uint64_t* const a_free = done;
+  uint64_t* const mma_done = done;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(mma_fin + kTcDqGroups);
   int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   int4* meta_ring = reinterpret_cast<int4*>(smem + L::kMetaRingOff);
@@ -318,16 +324,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       mbar_init(&wfull[s], 1);
       mbar_init(&wempty[s], 5);  // the dequant group's 4 warps (codes used) + the token-tile warp (g read)
     }
-    for (int s = 0; s < L::kXStages; ++s) {
-      mbar_init(&xfull[s], 1);
-      mbar_init(&xempty[s], 1);  // commit of the MMAs that read the token tile
-    }
-    for (int b = 0; b < L::kA; ++b) {
+    for (int b = 0; b < L::kR; ++b) {
+      mbar_init(&xfull[b], 1);
       mbar_init(&a_full[b], 4);  // the 4 warps of the dequant group
-      mbar_init(&a_free[b], 1);  // commit of the MMAs that read A[b]
-    }
-    for (int b = 0; b < L::kD; ++b) {
-      mbar_init(&mma_done[b], 2);  // commit of the unit's MMAs + the MMA thread's release of the hand-off
+      mbar_init(&done[b], 2);    // commit of the unit's MMAs + the MMA thread's release of the hand-off
       mbar_init(&d_free[b], kTcEpWarps);
     }
     for (int j = 0; j < kTcDqGroups; ++j) mbar_init(&mma_fin[j], 1);
@@ -464,11 +464,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           const uint64_t bd = bd0 + (uint64_t)(((kk < 4 ? 0 : L::kX) + 32 * (kk & 3)) >> 4);
           umma_bf16_ts(tmem + d_col(db), tmem + a_col(b) + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&mma_done[db]);
-        umma_commit(&a_free[b]);
-        umma_commit(&xempty[sx]);  // the token tile was read by these MMAs
+        umma_commit(&done[db]);  // frees A[b] and the token tile, hands D[db] to the epilogue (b == db == sx)
         // release (to the epilogue) of the hand-off entry this thread acquired through a_full
-        mbar_arrive(&mma_done[db]);
+        mbar_arrive(&done[db]);
         mma_issued = (int)i + 1;
       }
       if (mma_issued > 0) umma_commit(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this thread's MMAs
