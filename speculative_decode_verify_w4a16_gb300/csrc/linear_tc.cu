@@ -17,9 +17,10 @@
 //                     tokens, K = 16) per unit into a TMEM accumulator,
 //                     commit. Several issuers keep the tensor pipe fed while
 //                     each waits on its barriers.
-//   8 epilogue warps  (quadrant x token half) read each unit's fp32 product
-//                     from TMEM and fold it into registers with the row's
-//                     fp16 group scale; store at the end of a tile segment
+//   4 epilogue warps  (one per TMEM lane quadrant, all NT tokens) read each
+//                     unit's fp32 product from TMEM and fold it into
+//                     registers with the row's fp16 group scale; store at the
+//                     end of a tile segment
 // TMEM holds a ring of kA dequantised units (64 columns each) and kD
 // accumulators (NT columns each); consecutive units are dequantised by
 // different groups, so the dequantisation of several units, the MMAs of
@@ -40,10 +41,10 @@ namespace w4a16 {
 
 constexpr int kTcDqGroups = 2;                  // dequant groups of 4 warps, one MMA warp each
 constexpr int kTcDqWarps = 4 * kTcDqGroups;     // warps 0 .. 7
-constexpr int kTcEpWarps = 8;                   // warps 8 .. 15
-constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 16: claims items, codes + scales
-constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 17, 18
-constexpr int kTcXWarp = kTcMmaWarp0 + kTcDqGroups;       // warp 19: token tiles
+constexpr int kTcEpWarps = 4;                   // warps 8 .. 11, one per TMEM lane quadrant
+constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 12: claims items, codes + scales
+constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 13, 14
+constexpr int kTcXWarp = kTcMmaWarp0 + kTcDqGroups;       // warp 15: token tiles
 constexpr int kTcThreads = 32 * (kTcXWarp + 1);
 constexpr uint32_t kTcTmemCols = 512;  // the whole tensor memory of the SM
 constexpr int kTcRing = 16;            // scale / metadata hand-off ring (units)
@@ -146,36 +147,33 @@ __device__ __forceinline__ void tc_dequant(uint32_t w, const DequantConstsTc& k,
   r[3] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m12), mask, magic), one, neg136);    // bits 12/28
 }
 
-// Epilogue slice of a warp: rows 32q + lane, tokens h*NT/2 + j.
+// Epilogue slice of a warp: rows 32q + lane, tokens 0 .. NT - 1.
 template <int NT>
-__device__ __forceinline__ void tc_store(const TcParams& p, int64_t t, int q, int h, int lane,
-                                         const float (&acc)[NT / 2]) {
+__device__ __forceinline__ void tc_store(const TcParams& p, int64_t t, int q, int lane, const float (&acc)[NT]) {
   const int64_t n = t * kUnitRows + 32 * q + lane;
 #pragma unroll
-  for (int j = 0; j < NT / 2; ++j) {
-    const int m = h * (NT / 2) + j;
-    if (m < p.M) p.out[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[j]);
-  }
+  for (int m = 0; m < NT; ++m)
+    if (m < p.M) p.out[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
 }
 
 // Split tiles. Each item that covers part of a tile's K range writes the
-// fp32 sums of each epilogue warp's slice (32 rows x NT/2 tokens) to its own
+// fp32 sums of each epilogue warp's slice (32 rows x NT tokens) to its own
 // slot (item, segment, warp) and counts itself in with an atomic per (tile,
 // warp); whichever contributor arrives last adds all slots in item order and
 // stores the tile: the result does not depend on timing. Counters reset
 // themselves for the next call.
 template <int NT>
 __device__ __forceinline__ float4* tc_slot(const TcParams& p, int item, int seg, int epw) {
-  return p.partials + (((int64_t)item * 2 + seg) * kTcEpWarps + epw) * (int64_t)(NT / 8 * 32);
+  return p.partials + (((int64_t)item * 2 + seg) * kTcEpWarps + epw) * (int64_t)(NT / 4 * 32);
 }
 
 template <int NT>
-__device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t, int q, int h, int lane,
-                                const float (&acc)[NT / 2]) {
-  const int epw = h * 4 + q;
+__device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t, int q, int lane,
+                                const float (&acc)[NT]) {
+  const int epw = q;
   float4* slot = tc_slot<NT>(p, item, seg, epw);
 #pragma unroll
-  for (int j = 0; j < NT / 8; ++j)
+  for (int j = 0; j < NT / 4; ++j)
     __stcg(&slot[j * 32 + lane], make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
   __syncwarp();
   int* counter = &p.counters[kTileCounterBase + t * kTcEpWarps + epw];
@@ -190,31 +188,35 @@ __device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t,
   // only the first contributor can have started in an earlier tile (its
   // partial for this tile is then its segment 1)
   const int seg_cf = item_begin(p.sched, cf) >= t_begin ? 0 : 1;
-  float sum[NT / 2];
+  float sum[NT];
 #pragma unroll
-  for (int j = 0; j < NT / 2; ++j) sum[j] = 0.0f;
+  for (int j = 0; j < NT; ++j) sum[j] = 0.0f;
   constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);  // contributors loaded together
+  constexpr int JB = NT / 4 < 8 ? NT / 4 : 8;             // float4 of a slot per pass (register budget)
   for (int c0 = cf; c0 <= cl; c0 += RB) {
-    float4 v[RB][NT / 8];
 #pragma unroll
-    for (int r = 0; r < RB; ++r) {
-      const int cc = c0 + r;
-      const float4* sl = tc_slot<NT>(p, cc, cc == cf ? seg_cf : 0, epw);
+    for (int j0 = 0; j0 < NT / 4; j0 += JB) {
+      float4 v[RB][JB];
 #pragma unroll
-      for (int j = 0; j < NT / 8; ++j)
-        v[r][j] = cc <= cl ? __ldcg(&sl[j * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+      for (int r = 0; r < RB; ++r) {
+        const int cc = c0 + r;
+        const float4* sl = tc_slot<NT>(p, cc, cc == cf ? seg_cf : 0, epw);
 #pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-      for (int j = 0; j < NT / 8; ++j) {
-        sum[4 * j] += v[r][j].x;
-        sum[4 * j + 1] += v[r][j].y;
-        sum[4 * j + 2] += v[r][j].z;
-        sum[4 * j + 3] += v[r][j].w;
+        for (int j = 0; j < JB; ++j)
+          v[r][j] = cc <= cl ? __ldcg(&sl[(j0 + j) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int j = 0; j < JB; ++j) {
+          sum[4 * (j0 + j)] += v[r][j].x;
+          sum[4 * (j0 + j) + 1] += v[r][j].y;
+          sum[4 * (j0 + j) + 2] += v[r][j].z;
+          sum[4 * (j0 + j) + 3] += v[r][j].w;
+        }
+    }
   }
-  tc_store<NT>(p, t, q, h, lane, sum);
+  tc_store<NT>(p, t, q, lane, sum);
   if (lane == 0) *counter = 0;
 }
 
@@ -245,21 +247,8 @@ __device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&a
 // the loads of both accumulators are in flight together.
 template <int W>
 __device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, float s0, float s1, float (&acc)[W]) {
-  if constexpr (W >= 32) {  // 8 columns of each at a time: the register budget holds no more
-#pragma unroll
-    for (int c0 = 0; c0 + 8 <= W; c0 += 8) {
-      uint32_t v0[8], v1[8];
-      tmem_ld_32x32b_x8(dt0 + c0, v0);
-      tmem_ld_32x32b_x8(dt1 + c0, v1);
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 8; c += 2) {  // unit e first, then e + 1 (the order of the sequential loop)
-        ffma2(acc[c0 + c], acc[c0 + c + 1], s0, s0, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
-        ffma2(acc[c0 + c], acc[c0 + c + 1], s1, s1, __uint_as_float(v1[c]), __uint_as_float(v1[c + 1]));
-      }
-    }
-    return;
-  }
+  // 16 columns of each accumulator at a time; unit e is added first, then
+  // e + 1 (the order of the one-at-a-time loop)
   if constexpr (W >= 16) {
 #pragma unroll
     for (int c0 = 0; c0 + 16 <= W; c0 += 16) {
@@ -535,11 +524,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     }
   } else if (warp < kTcDqWarps + kTcEpWarps) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3, h = (warp - kTcDqWarps) >> 2;  // TMEM lane quadrant; token half
+    const int q = warp & 3;  // TMEM lane quadrant
     const int sc_half = ((q * 8 + (lane & 7)) * 2 + (lane >> 4)) * 2 + ((lane >> 3) & 1);  // row 32q + lane
-    float acc[NT / 2];
+    float acc[NT];
 #pragma unroll
-    for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
+    for (int c = 0; c < NT; ++c) acc[c] = 0.0f;
     int item = 0, item_t0 = 0, seg_g0 = 0;
     auto scale_of = [&](uint32_t u) {
       return __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(
@@ -574,11 +563,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         pair = me1.x >= 0;
       }
       tc_fence_after();
-      const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16) + h * (NT / 2);
+      const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16);
       if (pair) {
-        tc_epilogue_fma2<NT / 2>(dt + d_col(db), dt + d_col(db1), scale_of(e), scale_of(e + 1), acc);
+        tc_epilogue_fma2<NT>(dt + d_col(db), dt + d_col(db1), scale_of(e), scale_of(e + 1), acc);
       } else {
-        tc_epilogue_fma<NT / 2>(dt + d_col(db), scale_of(e), acc);
+        tc_epilogue_fma<NT>(dt + d_col(db), scale_of(e), acc);
       }
       tc_fence_before();
       __syncwarp();
@@ -589,11 +578,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       const int4 ml = pair ? me1 : me;  // last unit taken
       if (ml.z == p.G - 1 || (ml.w & kTcUnitLast)) {  // end of this item's segment of tile ml.y
         if (seg_g0 == 0 && ml.z == p.G - 1)
-          tc_store<NT>(p, ml.y, q, h, lane, acc);
+          tc_store<NT>(p, ml.y, q, lane, acc);
         else
-          tc_finish_split<NT>(p, item, ml.y == item_t0 ? 0 : 1, ml.y, q, h, lane, acc);
+          tc_finish_split<NT>(p, item, ml.y == item_t0 ? 0 : 1, ml.y, q, lane, acc);
 #pragma unroll
-        for (int c = 0; c < NT / 2; ++c) acc[c] = 0.0f;
+        for (int c = 0; c < NT; ++c) acc[c] = 0.0f;
         seg_g0 = 0;
       }
       if (!pair && !seg_end) break;  // the second unit was the stop marker
