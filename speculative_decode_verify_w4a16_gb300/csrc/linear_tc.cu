@@ -30,6 +30,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <string.h>
 
 #include "common.cuh"
 #include "format.cuh"
@@ -84,7 +85,11 @@ struct TcLayout {
   static constexpr int kXStages = kR;
   static constexpr int kWStage = kUnitBytes + kUnitScaleBytes;  // codes, then scales
   static constexpr int kXOff = 0;
-  static constexpr int kWOff = kXOff + kXStages * kXStage;
+  // output staging: one [NT tokens][32 rows] bf16 slice per epilogue warp,
+  // written to global memory by a 2-D TMA store
+  static constexpr int kOutSlice = NT * 32 * 2;
+  static constexpr int kOutOff = kXOff + kXStages * kXStage;
+  static constexpr int kWOff = kOutOff + kTcEpWarps * kOutSlice;
   static constexpr int kWStages = (200 * 1024 - kWOff) / kWStage / kTcDqGroups * kTcDqGroups;
   static constexpr int kScRingOff = kWOff + kWStages * kWStage;       // kTcRing x 256 B scales
   static constexpr int kMetaRingOff = kScRingOff + kTcRing * kUnitScaleBytes;  // kTcRing x int4
@@ -93,6 +98,7 @@ struct TcLayout {
   // wfull[SW], wempty[SW], xfull[kR], a_full[kR], done[kR], d_free[kR], mma_fin[groups], tmem base
   static constexpr int kTotal = kBarOff + (2 * kWStages + 4 * kR + kTcDqGroups) * 8 + 16 + 1024;  // +1024: alignment
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
+  static_assert(kOutSlice % 128 == 0, "TMA store source alignment");
   static_assert(kWStage % 16 == 0, "bulk copy alignment");
   static_assert(kWStages >= 2 * kTcDqGroups, "ring depth");
   static_assert(kWStages % kTcDqGroups == 0 && kXStages % kTcDqGroups == 0, "ring slots per group");
@@ -104,6 +110,7 @@ struct DequantConstsTc {
 
 struct TcParams {
   const uint8_t* qw;
+  int tma_store;  // output tiles through the 2-D TMA store (out 16-byte aligned)
   const uint8_t* sc;
   __nv_bfloat16* out;
   float4* partials;  // split-tile partial slots
@@ -147,10 +154,28 @@ __device__ __forceinline__ void tc_dequant(uint32_t w, const DequantConstsTc& k,
   r[3] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m12), mask, magic), one, neg136);    // bits 12/28
 }
 
-// Epilogue slice of a warp: rows 32q + lane, tokens 0 .. NT - 1.
+// Epilogue slice of a warp: rows 32q + lane, tokens 0 .. NT - 1. With the
+// TMA store the slice goes through the warp's [NT][32] staging area (token
+// rows past M are not written: the tensor map ends at M); otherwise one
+// 2-byte store per token.
 template <int NT>
-__device__ __forceinline__ void tc_store(const TcParams& p, int64_t t, int q, int lane, const float (&acc)[NT]) {
+__device__ __forceinline__ void tc_store(const TcParams& p, const CUtensorMap* omap, uint8_t* stage, int64_t t, int q,
+                                         int lane, const float (&acc)[NT]) {
   const int64_t n = t * kUnitRows + 32 * q + lane;
+  if (p.tma_store) {
+    if (lane == 0) bulk_wait_group_read0();  // the previous store of this area has read it
+    __syncwarp();
+    __nv_bfloat16* sv = reinterpret_cast<__nv_bfloat16*>(stage);
+#pragma unroll
+    for (int m = 0; m < NT; ++m) sv[m * 32 + lane] = __float2bfloat16_rn(acc[m]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(omap, (int32_t)(t * kUnitRows + 32 * q), 0, stage);
+      bulk_commit_group();
+    }
+    return;
+  }
 #pragma unroll
   for (int m = 0; m < NT; ++m)
     if (m < p.M) p.out[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
@@ -168,8 +193,8 @@ __device__ __forceinline__ float4* tc_slot(const TcParams& p, int item, int seg,
 }
 
 template <int NT>
-__device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t, int q, int lane,
-                                const float (&acc)[NT]) {
+__device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint8_t* stage, int item, int seg,
+                                int64_t t, int q, int lane, const float (&acc)[NT]) {
   const int epw = q;
   float4* slot = tc_slot<NT>(p, item, seg, epw);
 #pragma unroll
@@ -216,7 +241,7 @@ __device__ void tc_finish_split(const TcParams& p, int item, int seg, int64_t t,
         }
     }
   }
-  tc_store<NT>(p, t, q, lane, sum);
+  tc_store<NT>(p, omap, stage, t, q, lane, sum);
   if (lane == 0) *counter = 0;
 }
 
@@ -279,6 +304,7 @@ __device__ __forceinline__ void tc_epilogue_fma2(uint32_t dt0, uint32_t dt1, flo
 
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                const __grid_constant__ CUtensorMap omap,
                                                                 const TcParams p) {
   using L = TcLayout<NT>;
   extern __shared__ uint8_t smem_raw[];
@@ -578,9 +604,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       const int4 ml = pair ? me1 : me;  // last unit taken
       if (ml.z == p.G - 1 || (ml.w & kTcUnitLast)) {  // end of this item's segment of tile ml.y
         if (seg_g0 == 0 && ml.z == p.G - 1)
-          tc_store<NT>(p, ml.y, q, lane, acc);
+          tc_store<NT>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, ml.y, q, lane, acc);
         else
-          tc_finish_split<NT>(p, item, ml.y == item_t0 ? 0 : 1, ml.y, q, lane, acc);
+          tc_finish_split<NT>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, item, ml.y == item_t0 ? 0 : 1, ml.y,
+                              q, lane, acc);
 #pragma unroll
         for (int c = 0; c < NT; ++c) acc[c] = 0.0f;
         seg_g0 = 0;
@@ -591,6 +618,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   }
 
   // ---------------------------------------------------------- teardown
+  if (warp >= kTcDqWarps && warp < kTcDqWarps + kTcEpWarps && lane == 0 && p.tma_store)
+    bulk_wait_group0();  // this warp's output tiles are written
   tc_fence_before();
   __syncthreads();
   if (warp >= kTcMmaWarp0 && warp < kTcMmaWarp0 + kTcDqGroups && lane == 0 && mma_issued > 0)
@@ -704,9 +733,10 @@ cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t m
 size_t tc_workspace_bytes(const TcPlan& plan) { return plan.counter_bytes + plan.partial_bytes; }
 
 template <int NT>
-static cudaError_t launch_tc_t(const CUtensorMap& map, const TcParams& p, const TcPlan& plan, cudaStream_t stream) {
+static cudaError_t launch_tc_t(const CUtensorMap& map, const CUtensorMap& omap, const TcParams& p, const TcPlan& plan,
+                               cudaStream_t stream) {
   return launch_pdl(w4a16_tc_kernel<NT>, dim3((unsigned)plan.ctas), dim3(kTcThreads), (size_t)TcLayout<NT>::kTotal,
-                    stream, map, p);
+                    stream, map, omap, p);
 }
 
 cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
@@ -722,7 +752,22 @@ cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, co
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  // output tiles: [M][N] bf16, boxes of 32 rows (n) x NT tokens (m); the TMA
+  // store wants a 16-byte aligned base, else the kernel stores per element
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  int tma_store = 0;
+  if ((reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    const cuuint64_t odims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t ostrides[1] = {(cuuint64_t)N * 2};
+    const cuuint32_t obox[2] = {32u, (cuuint32_t)plan.nt};
+    if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, odims, ostrides, obox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+        CUDA_SUCCESS)
+      tma_store = 1;
+  }
   TcParams p;
+  p.tma_store = tma_store;
   p.qw = static_cast<const uint8_t*>(qw_packed);
   p.sc = static_cast<const uint8_t*>(sc_packed);
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -740,10 +785,10 @@ cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, co
   p.dq.m12 = 1u << 20;
   cudaError_t e;
   switch (plan.nt) {
-    case 16: e = launch_tc_t<16>(map, p, plan, stream); break;
-    case 32: e = launch_tc_t<32>(map, p, plan, stream); break;
-    case 48: e = launch_tc_t<48>(map, p, plan, stream); break;
-    case 64: e = launch_tc_t<64>(map, p, plan, stream); break;
+    case 16: e = launch_tc_t<16>(map, omap, p, plan, stream); break;
+    case 32: e = launch_tc_t<32>(map, omap, p, plan, stream); break;
+    case 48: e = launch_tc_t<48>(map, omap, p, plan, stream); break;
+    case 64: e = launch_tc_t<64>(map, omap, p, plan, stream); break;
     default: return cudaErrorInvalidValue;
   }
   return e;

@@ -64,6 +64,23 @@ def test_shapes(M, N, K):
     assert_linear_close(_gpu_linear(x, qw, sc), oracle.linear(x, qw, sc), f"{M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M", [4, 40, 64])
+def test_output_not_16_byte_aligned(M):
+    # an output that starts 4 bytes past a 16-byte boundary takes the
+    # per-element store path (tiles are otherwise written by TMA stores);
+    # the rows around it are untouched
+    x, qw, sc = _case(M, 640, 3072, seed=200 + M)
+    w = sv.prepack(*canon_to_dev(qw, sc))
+    buf = torch.full((M * 640 + 16,), 7.0, dtype=torch.bfloat16, device=dev())
+    out = buf[2:2 + M * 640].view(M, 640)
+    assert out.data_ptr() % 16 == 4
+    sv.linear(bf16_to_dev(x), w, out=out)
+    torch.cuda.synchronize()
+    assert sv.check_device_status() == 0
+    assert_linear_close(bf16_bits(out), oracle.linear(x, qw, sc), f"unaligned out M={M}")
+    assert torch.all(buf[:2] == 7.0) and torch.all(buf[2 + M * 640:] == 7.0)
+
+
 def test_one_hot_codes_select_columns_exactly():
     M, N, K = 6, 384, 1024
     g = synth.rng(40)
