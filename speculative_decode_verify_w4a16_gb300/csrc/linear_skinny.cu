@@ -8,8 +8,14 @@
 // stages filled by 1-D bulk copies (TMA engine), so every weight byte is read
 // from HBM exactly once.
 //
-// Per CTA: 4 consumer warps (one 32-row slice of the 128-row unit each) and
-// one producer warp. A consumer dequantises 16 packed words per unit into
+// One CTA per SM: 4 consumer groups of 4 warps (a warp owns one 32-row slice
+// of the 128-row unit) and one producer warp. A ring stage holds up to 4
+// consecutive units of one tile segment and group j takes unit j, so all 16
+// consumer warps of the SM move through the weight stream together (four
+// independent CTAs per SM let the hardware's oldest-first scheduling starve
+// the youngest, which then finishes far behind). The groups' sums of a
+// segment meet in shared memory, group 0 stores the tile. A consumer
+// dequantises 16 packed words per unit into
 // exact bf16 codes (offset-binary nibble OR'ed into the mantissa of 128.0,
 // then 136 subtracted: a bit trick in the spirit of Kim et al. 2022, "Who
 // Says Elephants Can't Run", arXiv:2211.10017), multiplies them with the
@@ -28,25 +34,36 @@
 
 namespace w4a16 {
 
-constexpr int kSkConsumerWarps = 4;
-constexpr int kSkThreads = 32 * (kSkConsumerWarps + 1);
-constexpr int kSkStages = 4;
-constexpr int kXRowStride = 288;  // bytes per token row in a stage (256 used; padding avoids bank conflicts)
+constexpr int kSkConsumerWarps = 4;  // warps of a group: one 32-row slice each
+constexpr int kSkGroups = 4;         // consumer groups: units per stage
+constexpr int kSkConsumers = kSkGroups * kSkConsumerWarps;  // warps 0 .. 15
+constexpr int kSkProducerWarp = kSkConsumers;               // warp 16
+constexpr int kSkThreads = 32 * (kSkConsumers + 1);
+// bytes per token row of a stage's token tile: the 4 units' 128-wide K
+// slices side by side (1024) + padding, so rows fall 32 bytes apart mod 128
+constexpr int kXRowStride = kSkGroups * 256 + 32;
 
-// Stage metadata written by the producer: the unit's item, tile and group.
-constexpr int kUnitFirst = 1;  // first unit of its item
-constexpr int kUnitLast = 2;   // last unit of its item
+// Stage metadata written by the producer: {item, tile, first group, flags | n << 8}
+constexpr int kStItemFirst = 1;  // the stage holds the item's first unit
+constexpr int kStSegFirst = 2;   // the stage starts a tile segment of the item
+constexpr int kStSegLast = 4;    // the stage ends it
 
 template <int MT8>
 struct SkinnyLayout {
-  static constexpr int kW = kUnitBytes;
-  static constexpr int kS = kUnitScaleBytes;
-  static constexpr int kX = MT8 * 8 * kXRowStride;
+  static constexpr int kStages = MT8 == 1 ? 4 : 3;
+  static constexpr int kW = kSkGroups * kUnitBytes;                   // codes of the stage's units
+  static constexpr int kS = kSkGroups * kUnitScaleBytes;              // their scales
+  static constexpr int kX = MT8 * 8 * kXRowStride;                    // token rows
   static constexpr int kStage = kW + kS + kX;
-  static constexpr int kMetaOff = kSkStages * kStage;
-  static constexpr int kBarOff = kMetaOff + kSkStages * 16;
-  static constexpr int kTotal = kBarOff + 2 * kSkStages * 8;
-  static_assert(kStage % 16 == 0, "stage alignment");
+  // group sums of a segment end, double-buffered: [2][group 1..3][slice][2*MT8 float4][32 lanes]
+  static constexpr int kRedSlot = 2 * MT8 * 32 * 16;
+  static constexpr int kRedOff = kStages * kStage;
+  static constexpr int kMetaOff = kRedOff + 2 * (kSkGroups - 1) * kSkConsumerWarps * kRedSlot;
+  static constexpr int kBarOff = kMetaOff + kStages * 16;
+  // full[stages], empty[stages], red_full[2], red_empty[2]
+  static constexpr int kTotal = kBarOff + (2 * kStages + 4) * 8;
+  static_assert(kStage % 128 == 0 && kW % 16 == 0 && (kW + kS) % 16 == 0, "stage alignment");
+  static_assert(kTotal <= 227 * 1024, "shared memory");
 };
 
 // Shift amounts enter as runtime multipliers (w * 2^(32-s) >> 32 == w >> s) so
@@ -198,35 +215,35 @@ __device__ void finish_split_tile(const SkinnyParams& p, int item, int seg, int6
   if (lane == 0) *counter = 0;
 }
 
-// Blocks per SM the register budget is shaped for (more resident warps hide
-// the dequant -> MMA dependency latency).
 template <int MT8>
-constexpr int skinny_min_blocks() {
-  return MT8 == 1 ? 4 : 3;
-}
-
-template <int MT8>
-__global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_skinny_kernel(const SkinnyParams p) {
+__global__ void __launch_bounds__(kSkThreads, 1) w4a16_skinny_kernel(const SkinnyParams p) {
   using L = SkinnyLayout<MT8>;
+  constexpr int S = L::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + kSkStages;
+  uint64_t* empty = full + S;
+  uint64_t* red_full = empty + S;   // [2]: groups 1..3 have written their sums
+  uint64_t* red_empty = red_full + 2;  // [2]: group 0 has read them
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   grid_launch_dependents();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSkStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kSkConsumerWarps);
+    for (int st = 0; st < S; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kSkConsumers);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&red_full[b], (kSkGroups - 1) * kSkConsumerWarps);
+      mbar_init(&red_empty[b], kSkConsumerWarps);
     }
     fence_mbarrier_init();
-  } else if (threadIdx.x == 32 * kSkConsumerWarps && (int)blockIdx.x < p.items) {
+  } else if (threadIdx.x == 32 * kSkProducerWarp && (int)blockIdx.x < p.items) {
     // The packed weights are not written by the kernel this one may overlap:
     // pull the first units of the item this CTA most likely claims into L2.
     const int64_t u0 = item_begin(p.sched, blockIdx.x);
     int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
-    if (n > 2 * kSkStages) n = 2 * kSkStages;
+    if (n > 2 * S * kSkGroups) n = 2 * S * kSkGroups;
     prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
     prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
   }
@@ -234,20 +251,22 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
   {
     constexpr int kChunks = kXRowStride / 16;
     const int zrows = MT8 * 8 - p.M;
-    for (int idx = threadIdx.x; idx < kSkStages * zrows * kChunks; idx += blockDim.x) {
-      const int s = idx / (zrows * kChunks), r = (idx / kChunks) % zrows, c16 = idx % kChunks;
-      *reinterpret_cast<uint4*>(smem + s * L::kStage + kUnitBytes + kUnitScaleBytes + (p.M + r) * kXRowStride +
-                                c16 * 16) = make_uint4(0u, 0u, 0u, 0u);
+    for (int idx = threadIdx.x; idx < S * zrows * kChunks; idx += blockDim.x) {
+      const int st = idx / (zrows * kChunks), r = (idx / kChunks) % zrows, c16 = idx % kChunks;
+      *reinterpret_cast<uint4*>(smem + st * L::kStage + L::kW + L::kS + (p.M + r) * kXRowStride + c16 * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
     }
   }
   __syncthreads();
   grid_dependency_wait();
 
-  if (warp == kSkConsumerWarps) {
+  if (warp == kSkProducerWarp) {
     // ---------------------------------------------------------- producer
+    // A stage takes up to kSkGroups consecutive units of one tile segment of
+    // the item: codes, scales and each token row's K range are contiguous in
+    // global memory, so a stage is 2 + M bulk copies.
     if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
-    const uint32_t tx = (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256);
     int* work = &p.counters[kWorkCounter];
     int n_stage = 0;  // stages filled so far
     bool ok = true;
@@ -255,40 +274,39 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
     while (ok && item < p.items) {
       const int64_t ub = item_begin(p.sched, item);
       const int64_t ue = item_begin(p.sched, item + 1);
-      int64_t t = ub / p.G;
-      int64_t g = ub - t * p.G;
-      for (int64_t u = ub; u < ue; ++u, ++n_stage) {
-        const int s = n_stage % kSkStages;
-        if (n_stage >= kSkStages &&
-            !mbar_wait(&empty[s], ((uint32_t)(n_stage / kSkStages) & 1u) ^ 1u, p.err)) {
+      for (int64_t u = ub; u < ue; ++n_stage) {
+        const int64_t t = u / p.G, g0 = u - t * p.G;
+        int64_t n = ue - u;
+        if (n > kSkGroups) n = kSkGroups;
+        if (n > p.G - g0) n = p.G - g0;
+        const int st = n_stage % S;
+        if (n_stage >= S && !mbar_wait(&empty[st], ((uint32_t)(n_stage / S) & 1u) ^ 1u, p.err)) {
           ok = false;
           break;
         }
-        const int flags = (u == ub ? kUnitFirst : 0) | (u == ue - 1 ? kUnitLast : 0);
-        meta[s] = make_int4(item, (int)t, (int)g, flags);
-        uint8_t* st = smem + s * L::kStage;
-        mbar_arrive_expect_tx(&full[s], tx);
-        bulk_g2s_hint(st, p.qw + u * kUnitBytes, kUnitBytes, &full[s], pol);
-        bulk_g2s(st + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &full[s]);
+        const int flags = (u == ub ? kStItemFirst : 0) | ((u == ub || g0 == 0) ? kStSegFirst : 0) |
+                          ((u + n == ue || g0 + n == p.G) ? kStSegLast : 0) | ((int)n << 8);
+        meta[st] = make_int4(item, (int)t, (int)g0, flags);
+        uint8_t* sb = smem + st * L::kStage;
+        const uint32_t nb = (uint32_t)n;
+        mbar_arrive_expect_tx(&full[st], nb * (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256));
+        bulk_g2s_hint(sb, p.qw + u * kUnitBytes, nb * kUnitBytes, &full[st], pol);
+        bulk_g2s(sb + L::kW, p.sc + u * kUnitScaleBytes, nb * kUnitScaleBytes, &full[st]);
         for (int m = 0; m < p.M; ++m)
-          bulk_g2s(st + kUnitBytes + kUnitScaleBytes + m * kXRowStride, p.x + (int64_t)m * p.K + g * kGroup, 256,
-                   &full[s]);
-        if (++g == p.G) {
-          g = 0;
-          ++t;
-        }
+          bulk_g2s(sb + L::kW + L::kS + m * kXRowStride, p.x + (int64_t)m * p.K + g0 * kGroup, nb * 256u, &full[st]);
+        u += n;
       }
       if (ok) item = atomicAdd(work, 1);
     }
     if (ok) {  // stop marker for the consumers
-      const int s = n_stage % kSkStages;
-      if (n_stage < kSkStages || mbar_wait(&empty[s], ((uint32_t)(n_stage / kSkStages) & 1u) ^ 1u, p.err)) {
-        meta[s] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&full[s]);
+      const int st = n_stage % S;
+      if (n_stage < S || mbar_wait(&empty[st], ((uint32_t)(n_stage / S) & 1u) ^ 1u, p.err)) {
+        meta[st] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&full[st]);
       }
     } else {  // let copies already in flight land before the CTA exits
-      for (int i = (n_stage > kSkStages ? n_stage - kSkStages : 0); i < n_stage; ++i)
-        mbar_wait(&full[i % kSkStages], (uint32_t)(i / kSkStages) & 1u, p.err);
+      for (int i = (n_stage > S ? n_stage - S : 0); i < n_stage; ++i)
+        mbar_wait(&full[i % S], (uint32_t)(i / S) & 1u, p.err);
     }
     // The last CTA to get here resets the claim counters for the next call
     // (every CTA has made its final claim before it counts itself out).
@@ -301,6 +319,7 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
   }
 
   // ------------------------------------------------------------ consumers
+  const int grp = warp >> 2, q = warp & 3;  // group (unit of the stage), 32-row slice
   const int gid = lane >> 2, cq = lane & 3;
   float acc[2][MT8][4];
 #pragma unroll
@@ -309,78 +328,117 @@ __global__ void __launch_bounds__(kSkThreads, skinny_min_blocks<MT8>()) w4a16_sk
     for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
-  int item = 0, item_t0 = 0, seg_g0 = 0;
+  int item = 0, item_t0 = 0, seg_g0 = 0, n_seg = 0;
 
   for (int i = 0;; ++i) {
-    const int s = i % kSkStages;
-    if (!mbar_wait(&full[s], (uint32_t)(i / kSkStages) & 1u, p.err)) return;
-    const uint32_t st = smem_u32(smem + s * L::kStage);
-    const uint4 mu = lds128(smem_u32(&meta[s]));
+    const int st = i % S;
+    if (!mbar_wait(&full[st], (uint32_t)(i / S) & 1u, p.err)) return;
+    const uint32_t sb = smem_u32(smem + st * L::kStage);
+    const uint4 mu = lds128(smem_u32(&meta[st]));
     const int4 mt = make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
     if (mt.x < 0) break;
-    if (mt.w & kUnitFirst) {
+    const int flags = mt.w & 0xff, n = mt.w >> 8;
+    if (flags & kStItemFirst) {
       item = mt.x;
       item_t0 = mt.y;
-      seg_g0 = mt.z;
     }
-    const uint32_t wb = st + warp * 2048 + lane * 16;
-    uint4 wq[2][2];
+    if (flags & kStSegFirst) seg_g0 = mt.z;
+    if (grp < n) {
+      const uint32_t wb = sb + grp * kUnitBytes + q * 2048 + lane * 16;
+      uint4 wq[2][2];
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
+      for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(wb + (rt * 2 + h) * 512);
-    const uint2 sc2 = lds64(st + kUnitBytes + (warp * 8 + gid) * 8);
+        for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(wb + (rt * 2 + h) * 512);
+      const uint2 sc2 = lds64(sb + L::kW + grp * kUnitScaleBytes + (q * 8 + gid) * 8);
 
-    float part[2][MT8][4];
+      float part[2][MT8][4];
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
+      for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-      for (int nt = 0; nt < MT8; ++nt)
+        for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) part[rt][nt][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) part[rt][nt][e] = 0.0f;
 
-    const uint32_t xb = st + kUnitBytes + kUnitScaleBytes + gid * kXRowStride + cq * 8;
+      const uint32_t xb = sb + L::kW + L::kS + gid * kXRowStride + grp * 256 + cq * 8;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint2 b[MT8];
+      for (int kk = 0; kk < 8; ++kk) {
+        uint2 b[MT8];
 #pragma unroll
-      for (int nt = 0; nt < MT8; ++nt) b[nt] = lds64(xb + nt * 8 * kXRowStride + kk * 32);
+        for (int nt = 0; nt < MT8; ++nt) b[nt] = lds64(xb + nt * 8 * kXRowStride + kk * 32);
 #pragma unroll
-      for (int rt = 0; rt < 2; ++rt) {
-        const uint4 q4 = wq[rt][kk >> 2];
-        const uint32_t word = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
-        uint32_t a[4];
-        dequant8(word, p.dq, a);
+        for (int rt = 0; rt < 2; ++rt) {
+          const uint4 q4 = wq[rt][kk >> 2];
+          const uint32_t word = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
+          uint32_t a[4];
+          dequant8(word, p.dq, a);
 #pragma unroll
-        for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt].x, b[nt].y);
+          for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt].x, b[nt].y);
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+
+      const __half2 s_rt0 = *reinterpret_cast<const __half2*>(&sc2.x);
+      const __half2 s_rt1 = *reinterpret_cast<const __half2*>(&sc2.y);
+      const float sc[2][2] = {{__low2float(s_rt0), __high2float(s_rt0)}, {__low2float(s_rt1), __high2float(s_rt1)}};
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int nt = 0; nt < MT8; ++nt) {
+          ffma2(acc[rt][nt][0], acc[rt][nt][1], sc[rt][0], sc[rt][0], part[rt][nt][0], part[rt][nt][1]);
+          ffma2(acc[rt][nt][2], acc[rt][nt][3], sc[rt][1], sc[rt][1], part[rt][nt][2], part[rt][nt][3]);
+        }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // no unit for this group in the stage
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
 
-    const __half2 s_rt0 = *reinterpret_cast<const __half2*>(&sc2.x);
-    const __half2 s_rt1 = *reinterpret_cast<const __half2*>(&sc2.y);
-    const float sc[2][2] = {{__low2float(s_rt0), __high2float(s_rt0)}, {__low2float(s_rt1), __high2float(s_rt1)}};
+    if (flags & kStSegLast) {  // end of this item's segment of tile mt.y: add the groups' sums
+      const int rb = n_seg & 1;
+      const uint32_t par = (uint32_t)(n_seg >> 1) & 1u;
+      if (grp > 0) {
+        if (n_seg >= 2 && !mbar_wait(&red_empty[rb], par ^ 1u, p.err)) return;
+        float4* slot = reinterpret_cast<float4*>(
+            smem + L::kRedOff + ((rb * (kSkGroups - 1) + grp - 1) * kSkConsumerWarps + q) * L::kRedSlot);
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt)
+        for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-      for (int nt = 0; nt < MT8; ++nt) {
-        ffma2(acc[rt][nt][0], acc[rt][nt][1], sc[rt][0], sc[rt][0], part[rt][nt][0], part[rt][nt][1]);
-        ffma2(acc[rt][nt][2], acc[rt][nt][3], sc[rt][1], sc[rt][1], part[rt][nt][2], part[rt][nt][3]);
+          for (int nt = 0; nt < MT8; ++nt)
+            slot[(rt * MT8 + nt) * 32 + lane] = make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_full[rb]);
+      } else {
+        if (!mbar_wait(&red_full[rb], par, p.err)) return;
+#pragma unroll
+        for (int g = 1; g < kSkGroups; ++g) {  // groups in order: the sum does not depend on timing
+          const float4* slot = reinterpret_cast<const float4*>(
+              smem + L::kRedOff + ((rb * (kSkGroups - 1) + g - 1) * kSkConsumerWarps + q) * L::kRedSlot);
+#pragma unroll
+          for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+            for (int nt = 0; nt < MT8; ++nt) {
+              const float4 v = slot[(rt * MT8 + nt) * 32 + lane];
+              acc[rt][nt][0] += v.x;
+              acc[rt][nt][1] += v.y;
+              acc[rt][nt][2] += v.z;
+              acc[rt][nt][3] += v.w;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_empty[rb]);
+        if (seg_g0 == 0 && mt.z + n - 1 == p.G - 1)
+          store_tile<MT8>(p, mt.y, q, lane, acc);
+        else
+          finish_split_tile<MT8>(p, item, mt.y == item_t0 ? 0 : 1, mt.y, q, lane, acc);
       }
-
-    if (mt.z == p.G - 1 || (mt.w & kUnitLast)) {  // end of this item's segment of tile mt.y
-      if (seg_g0 == 0 && mt.z == p.G - 1)
-        store_tile<MT8>(p, mt.y, warp, lane, acc);
-      else
-        finish_split_tile<MT8>(p, item, mt.y == item_t0 ? 0 : 1, mt.y, warp, lane, acc);
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
         for (int nt = 0; nt < MT8; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) acc[rt][nt][e] = 0.0f;
-      seg_g0 = 0;
+      ++n_seg;
     }
   }
 }
@@ -418,13 +476,13 @@ cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size
     cudaError_t e = skinny_occupancy_dispatch(plan->mt8, &nb);
     if (e != cudaSuccess) return e;
     if (nb < 1) nb = 1;
-    if (nb > 5) nb = 5;
+    if (nb > 1) nb = 1;  // one CTA per SM: its 4 consumer groups share the SM's stream
     if (dev.device >= 0 && dev.device < 64) cached_nb[dev.device][plan->mt8] = nb;
   }
   int64_t ctas = (int64_t)dev.num_sms * nb;
   if (ctas > plan->units) ctas = plan->units;
   plan->ctas = ctas;
-  // partial slots: 2 segments x 4 warps x (32 rows x 8*MT8 tokens) fp32 per
+  // partial slots: 2 segments x 4 slices x (32 rows x 8*MT8 tokens) fp32 per
   // item. Every split tile costs its contributors a partial store and an
   // atomic round trip, so this path keeps one round: every CTA one contiguous
   // run of units, at most two split tiles per CTA.
