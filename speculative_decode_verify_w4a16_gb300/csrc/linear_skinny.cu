@@ -66,13 +66,6 @@ struct SkinnyLayout {
   static_assert(kTotal <= 227 * 1024, "shared memory");
 };
 
-// Shift amounts enter as runtime multipliers (w * 2^(32-s) >> 32 == w >> s) so
-// the three right shifts run on the integer multiply path instead of the
-// logic pipe, which the four mask-and-OR operations already keep busy.
-struct DequantConsts {
-  uint32_t m4, m8, m12;
-};
-
 struct SkinnyParams {
   const __nv_bfloat16* x;
   const uint8_t* qw;
@@ -85,7 +78,6 @@ struct SkinnyParams {
   int M;
   int items;  // R * C
   ItemSched sched;
-  DequantConsts dq;
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -101,12 +93,6 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return d;
 }
 
-__device__ __forceinline__ uint32_t mul_hi(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -115,13 +101,13 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
 
 // 8 offset-binary nibbles -> four bf16x2 registers of exact signed codes:
 // (nibble | 0x4300) is the bf16 value 128 + c, and (128 + c) * 1 - 136 = c - 8.
-__device__ __forceinline__ void dequant8(uint32_t w, const DequantConsts& k, uint32_t (&a)[4]) {
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&a)[4]) {
   const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;
   const uint32_t one = 0x3F803F80u, neg136 = 0xC308C308u;
   a[0] = fma_bf16x2(lop3_and_or(w, mask, magic), one, neg136);
-  a[1] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m4), mask, magic), one, neg136);
-  a[2] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m8), mask, magic), one, neg136);
-  a[3] = fma_bf16x2(lop3_and_or(mul_hi(w, k.m12), mask, magic), one, neg136);
+  a[1] = fma_bf16x2(lop3_and_or(w >> 4, mask, magic), one, neg136);
+  a[2] = fma_bf16x2(lop3_and_or(w >> 8, mask, magic), one, neg136);
+  a[3] = fma_bf16x2(lop3_and_or(w >> 12, mask, magic), one, neg136);
 }
 
 template <int MT8>
@@ -371,7 +357,7 @@ __global__ void __launch_bounds__(kSkThreads, 1) w4a16_skinny_kernel(const Skinn
           const uint4 q4 = wq[rt][kk >> 2];
           const uint32_t word = (kk & 3) == 0 ? q4.x : (kk & 3) == 1 ? q4.y : (kk & 3) == 2 ? q4.z : q4.w;
           uint32_t a[4];
-          dequant8(word, p.dq, a);
+          dequant8(word, a);
 #pragma unroll
           for (int nt = 0; nt < MT8; ++nt) mma_16816(part[rt][nt], a, b[nt].x, b[nt].y);
         }
@@ -521,9 +507,6 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
   p.M = M;
   p.items = plan.sched.R * plan.sched.C;
   p.sched = plan.sched;
-  p.dq.m4 = 1u << 28;
-  p.dq.m8 = 1u << 24;
-  p.dq.m12 = 1u << 20;
   switch (plan.mt8) {
     case 1: return launch_skinny_t<1>(p, plan, stream);
     case 2: return launch_skinny_t<2>(p, plan, stream);

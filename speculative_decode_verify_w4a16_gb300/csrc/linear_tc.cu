@@ -104,10 +104,6 @@ struct TcLayout {
   static_assert(kWStages % kTcDqGroups == 0 && kXStages % kTcDqGroups == 0, "ring slots per group");
 };
 
-struct DequantConstsTc {
-  uint32_t m4, m8, m12;  // 2^28, 2^24, 2^20: multiply-high by these shifts right by 4, 8, 12
-};
-
 struct TcParams {
   const uint8_t* qw;
   int tma_store;  // output tiles through the 2-D TMA store (out 16-byte aligned)
@@ -120,7 +116,6 @@ struct TcParams {
   int M;
   int items;  // R * C
   ItemSched sched;
-  DequantConstsTc dq;
 };
 
 // Stage metadata written by the producer: the unit's item, tile and group.
@@ -132,11 +127,6 @@ __device__ __forceinline__ uint32_t tc_lop3(uint32_t a, uint32_t b, uint32_t c) 
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-__device__ __forceinline__ uint32_t tc_mulhi(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
 __device__ __forceinline__ uint32_t tc_fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
@@ -146,12 +136,12 @@ __device__ __forceinline__ uint32_t tc_fma_bf16x2(uint32_t a, uint32_t b, uint32
 // One packed word -> the four 16x256b TMEM registers of one 16-wide K step:
 // (row g, k 4c..4c+1), (row g, k 4c+2..4c+3), (row g+8, k 4c..), (row g+8, k 4c+2..).
 // (nibble | 0x4300) is the bf16 value 128 + c, and (128 + c) * 1 - 136 = c - 8.
-__device__ __forceinline__ void tc_dequant(uint32_t w, const DequantConstsTc& k, uint32_t* r) {
+__device__ __forceinline__ void tc_dequant(uint32_t w, uint32_t* r) {
   const uint32_t mask = 0x000F000Fu, magic = 0x43004300u, one = 0x3F803F80u, neg136 = 0xC308C308u;
   r[0] = tc_fma_bf16x2(tc_lop3(w, mask, magic), one, neg136);                     // bits 0/16
-  r[2] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m4), mask, magic), one, neg136);     // bits 4/20
-  r[1] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m8), mask, magic), one, neg136);     // bits 8/24
-  r[3] = tc_fma_bf16x2(tc_lop3(tc_mulhi(w, k.m12), mask, magic), one, neg136);    // bits 12/28
+  r[2] = tc_fma_bf16x2(tc_lop3(w >> 4, mask, magic), one, neg136);     // bits 4/20
+  r[1] = tc_fma_bf16x2(tc_lop3(w >> 8, mask, magic), one, neg136);     // bits 8/24
+  r[3] = tc_fma_bf16x2(tc_lop3(w >> 12, mask, magic), one, neg136);    // bits 12/28
 }
 
 // Epilogue slice of a warp: rows 32q + lane, tokens 0 .. NT - 1. With the
@@ -528,10 +518,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          tc_dequant(w[rt][hh].x, p.dq, &r[rt][hh][0]);
-          tc_dequant(w[rt][hh].y, p.dq, &r[rt][hh][4]);
-          tc_dequant(w[rt][hh].z, p.dq, &r[rt][hh][8]);
-          tc_dequant(w[rt][hh].w, p.dq, &r[rt][hh][12]);
+          tc_dequant(w[rt][hh].x, &r[rt][hh][0]);
+          tc_dequant(w[rt][hh].y, &r[rt][hh][4]);
+          tc_dequant(w[rt][hh].z, &r[rt][hh][8]);
+          tc_dequant(w[rt][hh].w, &r[rt][hh][12]);
         }
       // every code and scale of the stage has been used, so its loads have
       // completed: release it to the producer
@@ -780,9 +770,6 @@ cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, co
   p.M = M;
   p.items = plan.sched.R * plan.sched.C;
   p.sched = plan.sched;
-  p.dq.m4 = 1u << 28;
-  p.dq.m8 = 1u << 24;
-  p.dq.m12 = 1u << 20;
   cudaError_t e;
   switch (plan.nt) {
     case 16: e = launch_tc_t<16>(map, omap, p, plan, stream); break;
