@@ -8,14 +8,14 @@
 // stages filled by 1-D bulk copies (TMA engine), so every weight byte is read
 // from HBM exactly once.
 //
-// One CTA per SM: 4 consumer groups of 4 warps (a warp owns one 32-row slice
-// of the 128-row unit) and one producer warp. A ring stage holds up to 4
-// consecutive units of one tile segment and group j takes unit j, so all 16
-// consumer warps of the SM move through the weight stream together (four
-// independent CTAs per SM let the hardware's oldest-first scheduling starve
-// the youngest, which then finishes far behind). The groups' sums of a
-// segment meet in shared memory, group 0 stores the tile. A consumer
-// dequantises 16 packed words per unit into
+// One CTA per SM: 4 or 5 consumer groups of 4 warps (a warp owns one 32-row
+// slice of the 128-row unit) and one producer warp. A ring stage holds one
+// unit per group, consecutive units of one tile segment, and group j takes
+// unit j, so all the consumer warps of the SM move through the weight stream
+// together (four independent CTAs per SM let the hardware's oldest-first
+// scheduling starve the youngest, which then finished far behind). The
+// groups' sums of a segment meet in shared memory, group 0 stores the tile.
+// A consumer dequantises 16 packed words per unit into
 // exact bf16 codes (offset-binary nibble OR'ed into the mantissa of 128.0,
 // then 136 subtracted: a bit trick in the spirit of Kim et al. 2022, "Who
 // Says Elephants Can't Run", arXiv:2211.10017), multiplies them with the
@@ -35,13 +35,6 @@
 namespace w4a16 {
 
 constexpr int kSkConsumerWarps = 4;  // warps of a group: one 32-row slice each
-constexpr int kSkGroups = 4;         // consumer groups: units per stage
-constexpr int kSkConsumers = kSkGroups * kSkConsumerWarps;  // warps 0 .. 15
-constexpr int kSkProducerWarp = kSkConsumers;               // warp 16
-constexpr int kSkThreads = 32 * (kSkConsumers + 1);
-// bytes per token row of a stage's token tile: the 4 units' 128-wide K
-// slices side by side (1024) + padding, so rows fall 32 bytes apart mod 128
-constexpr int kXRowStride = kSkGroups * 256 + 32;
 
 // Stage metadata written by the producer: {item, tile, first group, flags | n << 8}
 constexpr int kStItemFirst = 1;  // the stage holds the item's first unit
@@ -50,19 +43,30 @@ constexpr int kStSegLast = 4;    // the stage ends it
 
 template <int MT8>
 struct SkinnyLayout {
-  static constexpr int kStages = MT8 == 1 ? 4 : 3;
-  static constexpr int kW = kSkGroups * kUnitBytes;                   // codes of the stage's units
-  static constexpr int kS = kSkGroups * kUnitScaleBytes;              // their scales
-  static constexpr int kX = MT8 * 8 * kXRowStride;                    // token rows
+  // consumer groups (units per stage) and ring depth: five groups of four
+  // warps when the token tile is one MMA wide (more warps hide more latency),
+  // four when it is two wide (shared memory)
+  static constexpr int kGroups = MT8 == 1 ? 5 : 4;
+  static constexpr int kStages = 3;
+  static constexpr int kConsumers = kGroups * kSkConsumerWarps;  // warps 0 .. kConsumers - 1
+  static constexpr int kProducerWarp = kConsumers;               // the last warp
+  static constexpr int kThreads = 32 * (kConsumers + 1);
+  // bytes per token row of a stage's token tile: the units' 128-wide K
+  // slices side by side + padding, so rows fall 32 bytes apart mod 128
+  static constexpr int kXRowStride = kGroups * 256 + 32;
+  static constexpr int kW = kGroups * kUnitBytes;       // codes of the stage's units
+  static constexpr int kS = kGroups * kUnitScaleBytes;  // their scales
+  static constexpr int kX = MT8 * 8 * kXRowStride;      // token rows
   static constexpr int kStage = kW + kS + kX;
   // group sums of a segment end, double-buffered: [2][group 1..3][slice][2*MT8 float4][32 lanes]
   static constexpr int kRedSlot = 2 * MT8 * 32 * 16;
   static constexpr int kRedOff = kStages * kStage;
-  static constexpr int kMetaOff = kRedOff + 2 * (kSkGroups - 1) * kSkConsumerWarps * kRedSlot;
+  static constexpr int kMetaOff = kRedOff + 2 * (kGroups - 1) * kSkConsumerWarps * kRedSlot;
   static constexpr int kBarOff = kMetaOff + kStages * 16;
   // full[stages], empty[stages], red_full[2], red_empty[2]
   static constexpr int kTotal = kBarOff + (2 * kStages + 4) * 8;
-  static_assert(kStage % 128 == 0 && kW % 16 == 0 && (kW + kS) % 16 == 0, "stage alignment");
+  static_assert(kStage % 128 == 0 && kW % 16 == 0 && (kW + kS) % 16 == 0 && kXRowStride % 128 == 32,
+                "stage alignment");
   static_assert(kTotal <= 227 * 1024, "shared memory");
 };
 
@@ -202,9 +206,13 @@ __device__ void finish_split_tile(const SkinnyParams& p, int item, int seg, int6
 }
 
 template <int MT8>
-__global__ void __launch_bounds__(kSkThreads, 1) w4a16_skinny_kernel(const SkinnyParams p) {
+__global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_kernel(const SkinnyParams p) {
   using L = SkinnyLayout<MT8>;
   constexpr int S = L::kStages;
+  constexpr int kSkGroups = L::kGroups;
+  constexpr int kSkConsumers = L::kConsumers;
+  constexpr int kSkProducerWarp = L::kProducerWarp;
+  constexpr int kXRowStride = L::kXRowStride;
   extern __shared__ __align__(128) uint8_t smem[];
   int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -440,7 +448,7 @@ static cudaError_t skinny_occupancy(int* blocks_per_sm) {
   e = cudaFuncSetAttribute(w4a16_skinny_kernel<MT8>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, w4a16_skinny_kernel<MT8>, kSkThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, w4a16_skinny_kernel<MT8>, L::kThreads,
                                                       L::kTotal);
 }
 
@@ -486,7 +494,7 @@ size_t skinny_workspace_bytes(const SkinnyPlan& plan) { return plan.counter_byte
 template <int MT8>
 static cudaError_t launch_skinny_t(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t stream) {
   using L = SkinnyLayout<MT8>;
-  return launch_pdl(w4a16_skinny_kernel<MT8>, dim3((unsigned)plan.ctas), dim3(kSkThreads), (size_t)L::kTotal, stream,
+  return launch_pdl(w4a16_skinny_kernel<MT8>, dim3((unsigned)plan.ctas), dim3(L::kThreads), (size_t)L::kTotal, stream,
                     p);
 }
 
