@@ -165,7 +165,7 @@ def test_llama70b_shapes_sampled(full_weights, name, K, N):
     qw, sc, w = full_weights(name, K, N)
     g = synth.rng(2000 + N)
     cols = np.unique(np.concatenate([np.arange(0, 128), np.arange(N - 128, N), g.integers(0, N, 256)]))
-    for M in (1, 4, 8, 16, 64):
+    for M in (1, 4, 8, 12, 16, 40, 64):  # both fragment-path layouts and three token-tile widths
         x = synth.activations(M, K, seed=3000 + M)
         out = bf16_bits(sv.linear(bf16_to_dev(x), w))
         ref = oracle.linear_cols(x, qw, sc, cols)
