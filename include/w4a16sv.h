@@ -97,15 +97,19 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
  *   out          device, bf16 [M][N] row-major
  *   workspace    device scratch of at least w4a16_linear_workspace_bytes(M,N,K)
  *                bytes, 256-byte aligned. Its first 262,400 bytes (256 KiB +
- *                256) hold counters (work-item claims, split-tile completions):
+ *                256) hold counters (split-tile completions, accept steps):
  *                ZERO-FILL the workspace before its first use; every call
  *                leaves the counters zero again, so one workspace serves any
  *                later linear or accept call. After W4A16_ERR_DEVICE_TIMEOUT,
  *                zero it again before reuse. Calls that share a workspace must
  *                not overlap in time (calls on one stream never do).
  * Kernels are launched with programmatic dependent launch: one may start
- * while the previous kernel on the stream finishes, but it reads x and the
- * workspace and writes out only after that kernel has completed.
+ * while the previous kernel on the stream finishes (only a kernel that
+ * signals programmatic completion early lets it, as this library's own
+ * kernels do). It streams qweight_packed and scales_packed at once, but reads
+ * x and the workspace and writes out only after that kernel has completed;
+ * so a kernel that writes the packed weights must not signal early (the
+ * library's quantize and prepack kernels do not).
  * Returns W4A16_ERR_INVALID_ARG / _WORKSPACE / _UNSUPPORTED before launching.
  */
 size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K);
@@ -195,8 +199,8 @@ w4a16_status w4a16_check_device_status(void* stream);
  * item i = r*C + j owns units [rb[r] + floor(j*len/C), rb[r] +
  * floor((j+1)*len/C)), len = rb[r+1] - rb[r]. Each round takes half of the
  * units left until items would hold fewer than min_units units, or
- * max_rounds (1..8) is reached; the last round takes the rest. CTAs claim
- * items in index order; split tiles are summed in item order.
+ * max_rounds (1..8) is reached; the last round takes the rest. CTA c takes
+ * items c, c + C, ...; split tiles are summed in item order.
  *   w4a16_item_rounds  writes rb[0..R] (room for 9) and returns R, or 0 on
  *                      bad arguments (U < C, C < 1, min_units < 1).
  *   w4a16_item_begin   first unit of item i (i in [0, R*C]; R*C gives U),

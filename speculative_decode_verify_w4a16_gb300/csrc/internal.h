@@ -10,8 +10,8 @@
 namespace w4a16 {
 
 // Every workspace starts with this many bytes of zero-initialised counters
-// (int32: the linear's item-claim counters, then its per (tile, warp)
-// split-tile counters; the accept step's per-row counters), shared so that one
+// (int32: from index 64 the linear's per (tile, warp) split-tile counters;
+// the accept step's per-row counters), shared so that one
 // workspace can serve any sequence of calls; each call leaves them zero.
 constexpr size_t kCounterRegionBytes = 256 * 1024 + 256;
 constexpr int64_t kMaxCounters = (int64_t)(kCounterRegionBytes / sizeof(int));
@@ -54,7 +54,7 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint32_t* qwei
 cudaError_t launch_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
                            uint32_t* qw_packed, uint16_t* sc_packed, cudaStream_t stream);
 
-// ---- linear (tensor-core fragments via mma.sync; M < 16; dynamically claimed unit items)
+// ---- linear (tensor-core fragments via mma.sync; M < 16; items of contiguous units)
 struct SkinnyPlan {
   int mt8 = 0;          // ceil(M / 8)
   int64_t units = 0;    // (N/128) * (K/128)

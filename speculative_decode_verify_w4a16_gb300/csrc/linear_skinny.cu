@@ -3,8 +3,8 @@
 //
 // out[M][N] = bf16(x[M][K] . W^T) with W = code * scale (int4, group 128).
 // Work split: the (row-tile, group) units of the packed weight stream are cut
-// into items of contiguous units (sched.cuh) which the CTAs claim one after
-// another; each CTA streams its items' units through a ring of shared-memory
+// into items of contiguous units (sched.cuh); CTA c takes items c, c + C, ...
+// (C = grid size) and streams their units through a ring of shared-memory
 // stages filled by 1-D bulk copies (TMA engine), so every weight byte is read
 // from HBM exactly once.
 //
@@ -76,7 +76,7 @@ struct SkinnyParams {
   const uint8_t* sc;
   __nv_bfloat16* out;
   float4* partials;  // split-tile partial slots
-  int* counters;     // item-claim and split-tile counters
+  int* counters;     // split-tile counters
   unsigned* err;
   int64_t K, N, G;
   int M;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
     fence_mbarrier_init();
   } else if (threadIdx.x == 32 * kSkProducerWarp && (int)blockIdx.x < p.items) {
     // The packed weights are not written by the kernel this one may overlap:
-    // pull the first units of the item this CTA most likely claims into L2.
+    // pull the first units of this CTA's first item into L2.
     const int64_t u0 = item_begin(p.sched, blockIdx.x);
     int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
     if (n > 2 * S * kSkGroups) n = 2 * S * kSkGroups;
@@ -252,20 +252,23 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
     }
   }
   __syncthreads();
-  grid_dependency_wait();
 
   if (warp == kSkProducerWarp) {
     // ---------------------------------------------------------- producer
     // A stage takes up to kSkGroups consecutive units of one tile segment of
     // the item: codes, scales and each token row's K range are contiguous in
     // global memory, so a stage is 2 + M bulk copies.
+    // CTA c takes items c, c + C, ... (C = grid size). The stage copies wait
+    // for the preceding grid (x may come from it; issuing the codes earlier
+    // and the token rows after would queue a stage's token rows behind
+    // several stages of codes, and the L2 prefetch above already moves the
+    // first units' codes during that grid's tail).
     if (lane != 0) return;
+    grid_dependency_wait();
     const uint64_t pol = policy_evict_first();
-    int* work = &p.counters[kWorkCounter];
     int n_stage = 0;  // stages filled so far
     bool ok = true;
-    int item = atomicAdd(work, 1);
-    while (ok && item < p.items) {
+    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
       const int64_t ub = item_begin(p.sched, item);
       const int64_t ue = item_begin(p.sched, item + 1);
       for (int64_t u = ub; u < ue; ++n_stage) {
@@ -290,7 +293,6 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
           bulk_g2s(sb + L::kW + L::kS + m * kXRowStride, p.x + (int64_t)m * p.K + g0 * kGroup, nb * 256u, &full[st]);
         u += n;
       }
-      if (ok) item = atomicAdd(work, 1);
     }
     if (ok) {  // stop marker for the consumers
       const int st = n_stage % S;
@@ -302,17 +304,11 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       for (int i = (n_stage > S ? n_stage - S : 0); i < n_stage; ++i)
         mbar_wait(&full[i % S], (uint32_t)(i / S) & 1u, p.err);
     }
-    // The last CTA to get here resets the claim counters for the next call
-    // (every CTA has made its final claim before it counts itself out).
-    __threadfence();
-    if (atomicAdd(&p.counters[kExitCounter], 1) == (int)gridDim.x - 1) {
-      p.counters[kWorkCounter] = 0;
-      p.counters[kExitCounter] = 0;
-    }
     return;
   }
 
   // ------------------------------------------------------------ consumers
+  grid_dependency_wait();  // out, partials and counters may still be in use by the preceding grid
   const int grp = warp >> 2, q = warp & 3;  // group (unit of the stage), 32-row slice
   const int gid = lane >> 2, cq = lane & 3;
   float acc[2][MT8][4];

@@ -3,7 +3,7 @@
 // Same item schedule of the packed (row-tile, group) units as the fragment
 // path (sched.cuh); one CTA per SM owns the SM's whole tensor memory.
 // Warp roles, per unit (128 weight rows x 128 K):
-//   producer warp     claims items; 1-D bulk copies of the packed codes and
+//   producer warp     takes the CTA's items; 1-D bulk copies of the packed codes and
 //                     scales into a deep ring
 //   token-tile warp   2-D TMA of the token tile x[0:NT, 128g : 128g+128]
 //                     (128-byte swizzle; token rows past M read as zero) into
@@ -43,7 +43,7 @@ namespace w4a16 {
 constexpr int kTcDqGroups = 2;                  // dequant groups of 4 warps, one MMA warp each
 constexpr int kTcDqWarps = 4 * kTcDqGroups;     // warps 0 .. 7
 constexpr int kTcEpWarps = 4;                   // warps 8 .. 11, one per TMEM lane quadrant
-constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 12: claims items, codes + scales
+constexpr int kTcProducerWarp = kTcDqWarps + kTcEpWarps;  // warp 12: items, codes + scales
 constexpr int kTcMmaWarp0 = kTcProducerWarp + 1;          // warps 13, 14
 constexpr int kTcXWarp = kTcMmaWarp0 + kTcDqGroups;       // warp 15: token tiles
 constexpr int kTcThreads = 32 * (kTcXWarp + 1);
@@ -110,7 +110,7 @@ struct TcParams {
   const uint8_t* sc;
   __nv_bfloat16* out;
   float4* partials;  // split-tile partial slots
-  int* counters;     // item-claim and split-tile counters
+  int* counters;     // split-tile counters
   unsigned* err;
   int64_t K, N, G;
   int M;
@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   grid_launch_dependents();
   if (warp == kTcProducerWarp && lane == 0 && (int)blockIdx.x < p.items) {
     // The packed weights are not written by the kernel this one may overlap:
-    // pull the first units of the item this CTA most likely claims into L2.
+    // pull the first units of this CTA's first item into L2.
     const int64_t u0 = item_begin(p.sched, blockIdx.x);
     int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
     if (n > 2 * L::kWStages) n = 2 * L::kWStages;
@@ -345,7 +345,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  grid_dependency_wait();
+  // Programmatic dependent launch: the packed weights and scales are never
+  // written by another kernel, so the producer, the dequant groups and the
+  // MMA warps start while the preceding grid is still finishing; only the
+  // token-tile warp (reads x) and the epilogue (writes out, partials and
+  // counters) wait for it.
   const uint32_t tmem = *tmem_base_s;
   auto a_col = [](int buf) { return (uint32_t)(buf * 64); };
   auto d_col = [](int buf) { return (uint32_t)(L::kA * 64 + buf * NT); };
@@ -354,13 +358,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   if (warp == kTcProducerWarp) {
     // ---------------------------------------------------------- producer
     // Codes + scales run up to kWStages units ahead of the dequant groups.
+    // CTA c takes items c, c + C, ... (C = grid size): fixed before the
+    // preceding grid completes, so no claim counter is read here.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      int* work = &p.counters[kWorkCounter];
       uint32_t n_w = 0;  // units whose codes have been issued
       bool ok = true;
-      int item = atomicAdd(work, 1);
-      while (ok && item < p.items) {
+      for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
         const int64_t ub = item_begin(p.sched, item);
         const int64_t ue = item_begin(p.sched, item + 1);
         int64_t t = ub / p.G;
@@ -381,7 +385,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
             ++t;
           }
         }
-        if (ok) item = atomicAdd(work, 1);
       }
       // one stop marker per dequant group (each reads every kTcDqGroups-th
       // stage): -1 at the first index past the last unit, where the MMA warp
@@ -399,12 +402,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         for (uint32_t i = (n_w > (uint32_t)L::kWStages ? n_w - L::kWStages : 0u); i < n_w; ++i)
           mbar_wait(&wfull[i % L::kWStages], (i / L::kWStages) & 1u, p.err);
       }
-      // the last CTA to get here resets the claim counters for the next call
-      __threadfence();
-      if (atomicAdd(&p.counters[kExitCounter], 1) == (int)gridDim.x - 1) {
-        p.counters[kWorkCounter] = 0;
-        p.counters[kExitCounter] = 0;
-      }
     }
   } else if (warp == kTcXWarp) {
     // ------------------------------------------------------- token tiles
@@ -412,6 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     // known (stage metadata); the token tile goes to the x ring as soon as the
     // MMAs free a slot. Counting in on wempty keeps the stage (and its
     // metadata) from being recycled before it was read here.
+    grid_dependency_wait();  // x may be written by the preceding grid
     if (lane == 0) {
       uint32_t n_x = 0;
       for (;; ++n_x) {
@@ -540,6 +538,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     }
   } else if (warp < kTcDqWarps + kTcEpWarps) {
     // ------------------------------------------------------------ epilogue
+    grid_dependency_wait();  // out, partials and counters may still be in use by the preceding grid
     const int q = warp & 3;  // TMEM lane quadrant
     const int sc_half = ((q * 8 + (lane & 7)) * 2 + (lane >> 4)) * 2 + ((lane >> 3) & 1);  // row 32q + lane
     float acc[NT];

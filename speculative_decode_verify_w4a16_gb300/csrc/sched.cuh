@@ -6,11 +6,11 @@
 // runs (few split tiles) and the last ones are short (the grid finishes
 // together even when some SMs stream faster than others).
 //
-// Items are claimed in index order through one atomic counter: a CTA that
-// finishes early takes more of them. Item boundaries depend only on
-// (U, C, rb), never on timing, and so do the partial-sum slots of split tiles
-// (slot = item index) and the order in which a tile's partials are added:
-// results are bitwise reproducible.
+// CTA c takes items c, c + C, ... in order: the assignment is known before
+// the kernel waits for the grid it depends on, so the weight stream can start
+// at once. Item boundaries depend only on (U, C, rb), never on timing, and so
+// do the partial-sum slots of split tiles (slot = item index) and the order in
+// which a tile's partials are added: results are bitwise reproducible.
 #pragma once
 
 #include <stdint.h>
@@ -68,8 +68,6 @@ inline ItemSched make_item_sched(int64_t U, int C, int min_units, int max_rounds
 }
 
 // Counter layout at the start of every workspace (int32 indices).
-constexpr int kWorkCounter = 0;   // next item to claim
-constexpr int kExitCounter = 1;   // CTAs that found no item left
-constexpr int kTileCounterBase = 64;  // per (tile, warp) split-tile counters follow
+constexpr int kTileCounterBase = 64;  // per (tile, warp) split-tile counters (ints 0..63 reserved)
 
 }  // namespace w4a16
