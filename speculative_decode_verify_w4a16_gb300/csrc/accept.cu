@@ -421,7 +421,8 @@ struct ResidFn {
   __device__ __forceinline__ float rval(int x) const { return rv_of(prow[x], qrow ? qrow[x] : 0.0f); }
 };
 
-template <int RS>  // values per thread in a chunk: chunk2 <= RS * kAccThreads
+// VEC: V and chunk2 multiples of 4, so the chunk is whole float4s.
+template <int RS, bool VEC>  // values per thread in a chunk: chunk2 <= RS * kAccThreads
 __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
     int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
@@ -446,16 +447,33 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
   const int x0 = blockIdx.x * chunk2, x1 = min(V, x0 + chunk2);
   // all of this thread's logits are loaded before any is used (one latency)
   float lp[RS], lq[RS];
+  auto index_of = [&](int j) {
+    return VEC ? x0 + ((j / 4) * kAccThreads + (int)threadIdx.x) * 4 + (j % 4) : x0 + j * kAccThreads + (int)threadIdx.x;
+  };
+  if (VEC) {
 #pragma unroll
-  for (int j = 0; j < RS; ++j) {
-    const int x = x0 + j * kAccThreads + (int)threadIdx.x;
-    lp[j] = x < x1 ? f.prow[x] : 0.0f;
-    lq[j] = (x < x1 && f.qrow) ? f.qrow[x] : 0.0f;
+    for (int j = 0; j < RS / 4; ++j) {
+      const int xi = x0 + (j * kAccThreads + (int)threadIdx.x) * 4;
+      float4 tp = make_float4(0.f, 0.f, 0.f, 0.f), tq = tp;
+      if (xi < x1) {
+        tp = ldg_stream_f4(reinterpret_cast<const float4*>(f.prow + xi));
+        if (f.qrow) tq = ldg_stream_f4(reinterpret_cast<const float4*>(f.qrow + xi));
+      }
+      lp[4 * j] = tp.x, lp[4 * j + 1] = tp.y, lp[4 * j + 2] = tp.z, lp[4 * j + 3] = tp.w;
+      lq[4 * j] = tq.x, lq[4 * j + 1] = tq.y, lq[4 * j + 2] = tq.z, lq[4 * j + 3] = tq.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < RS; ++j) {
+      const int x = index_of(j);
+      lp[j] = x < x1 ? f.prow[x] : 0.0f;
+      lq[j] = (x < x1 && f.qrow) ? f.qrow[x] : 0.0f;
+    }
   }
   float sr = 0.0f, sp = 0.0f;
 #pragma unroll
   for (int j = 0; j < RS; ++j) {
-    if (x0 + j * kAccThreads + (int)threadIdx.x < x1) {
+    if (index_of(j) < x1) {
       sr += f.rv_of(lp[j], lq[j]);
       if (f.qrow) sp += f.pv_of(lp[j]);
     }
@@ -797,7 +815,7 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   static std::atomic<int> resid_per_sm{0};
   int per_sm = resid_per_sm.load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_resid_kernel<kResidPT>, kAccThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, accept_resid_kernel<kResidPT, true>, kAccThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     resid_per_sm.store(per_sm, std::memory_order_relaxed);
@@ -805,10 +823,14 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   int ch2 = (int)(((int64_t)per_sm * num_sms) / B);
   if (ch2 > pl.ch2) ch2 = pl.ch2;
   if (ch2 < pl.ch2_lo) ch2 = pl.ch2_lo;
-  const int chunk2 = (V + ch2 - 1) / ch2;
+  int chunk2 = (V + ch2 - 1) / ch2;
+  if (V % 4 == 0) chunk2 = (chunk2 + 3) / 4 * 4;  // whole float4s (still <= kMaxChunk2)
   ch2 = (V + chunk2 - 1) / chunk2;
-  return launch_pdl(accept_resid_kernel<kResidPT>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V, chunk2,
-                    (const Decision*)dec, csum, cnt2, acc, next);
+  if (V % 4 == 0)
+    return launch_pdl(accept_resid_kernel<kResidPT, true>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
+                      chunk2, (const Decision*)dec, csum, cnt2, acc, next);
+  return launch_pdl(accept_resid_kernel<kResidPT, false>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
+                    chunk2, (const Decision*)dec, csum, cnt2, acc, next);
 }
 
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
