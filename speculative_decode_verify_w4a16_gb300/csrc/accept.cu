@@ -637,6 +637,8 @@ __device__ __forceinline__ ArgPart arg_better(ArgPart a, ArgPart b) {
 
 struct GreedyShared {
   int amax[kMaxNodes];
+  int par[kMaxNodes];    // parents of the batch row's nodes (tree mode)
+  int draft[kMaxNodes];  // its draft ids
   short depth[kMaxNodes];
   unsigned char ok[kMaxNodes];
 };
@@ -685,6 +687,12 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
   __threadfence();
 
   __shared__ GreedyShared gs;
+  // the row's draft ids (and parents) into shared memory with all threads:
+  // the walk below then reads no global memory
+  for (int j = threadIdx.x; j < n; j += kAccThreads) {
+    gs.draft[j] = d[(int64_t)b * n + j];
+    if (parents) gs.par[j] = parents[(int64_t)b * n + j];
+  }
   for (int j = threadIdx.x; j < rows_per_b; j += kAccThreads) {
     const ArgPart* pp = parts + ((int64_t)b * rows_per_b + j) * gridDim.x;
     ArgPart a{-FLT_MAX, -1};
@@ -703,7 +711,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     if (!parents) {  // chain: rows 0..n, drafts d_1..d_n
       acc = n;
       for (int i = 0; i < n; ++i) {
-        const int di = d[(int64_t)b * n + i];
+        const int di = gs.draft[i];
         if (di < 0 || di >= V) report_error(err, kErrInput);
         if (di != gs.amax[i]) {
           acc = i;
@@ -712,8 +720,8 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
       }
       best_node = acc;
     } else {  // tree: rows 0..n-1, node 0 is the root
-      const int32_t* par = parents + (int64_t)b * n;
-      const int32_t* dd = d + (int64_t)b * n;
+      const int* par = gs.par;
+      const int* dd = gs.draft;
       gs.depth[0] = 0;
       gs.ok[0] = 1;
       bool bad = par[0] != -1;
