@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 # launch list with dram__bytes_read.sum / dram__bytes_write.sum); None until a
 # capture of the current kernels exists.
 NCU_DRAM_BYTES_PER_LAUNCH: dict = {
-    "w4a16_skinny_kernel<1> (M<16)": 110601312,
-    "w4a16_tc_kernel<64> (M>=16)": 113116544,
-    "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": 89201920,
-    "accept_argmax_kernel": 525547776,
+    "w4a16_skinny_kernel<1> (M<16)": 110635296,
+    "w4a16_tc_kernel<64> (M>=16)": 113128128,
+    "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": 89212672,
+    "accept_argmax_kernel": 525573120,
 }
 
 
