@@ -175,6 +175,18 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest of every rank's value (all ranks get it); the value itself on one rank."""
+    if ws == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def make_weight(sv, torch, N, K, gen, device):
     w = torch.randn((N, K), generator=gen, device=device, dtype=torch.float32).mul_(0.02)
     qw, sc = sv.quantize(w)
@@ -291,11 +303,7 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), ws, device)
     _check(sv, "timed graph replays")
     # per-call device durations: the step with event nodes, one replay at a time
     seg = []
