@@ -3,25 +3,26 @@
 // Same item schedule of the packed (row-tile, group) units as the fragment
 // path (sched.cuh); one CTA per SM owns the SM's whole tensor memory.
 // Warp roles, per unit (128 weight rows x 128 K):
-//   producer warp     takes the CTA's items; 1-D bulk copies of the packed codes and
-//                     scales into a deep ring
+//   producer warp     the CTA's items; 1-D bulk copies of the packed codes
+//                     and scales into a deep ring
 //   token-tile warp   2-D TMA of the token tile x[0:NT, 128g : 128g+128]
 //                     (128-byte swizzle; token rows past M read as zero) into
-//                     a shallow ring (L2 hits), following the codes ring
+//                     a ring of kR stages (L2 hits), following the codes ring
 //   2 dequant groups  of 4 warps (one per TMEM lane quadrant) take the units
 //                     in turn: dequantise the unit to exact bf16 codes and
 //                     store them into TMEM, the UMMA A operand; hand the
 //                     unit's scales and metadata on to the epilogue
 //   2 MMA warps       one per dequant group (its units only): 8 x
 //                     tcgen05.mma kind::f16 (M = 128 weight rows, N = NT
-//                     tokens, K = 16) per unit into a TMEM accumulator,
-//                     commit. Several issuers keep the tensor pipe fed while
+//                     tokens, K = 16) per unit into a TMEM accumulator and
+//                     one commit. Two issuers keep the tensor pipe fed while
 //                     each waits on its barriers.
 //   4 epilogue warps  (one per TMEM lane quadrant, all NT tokens) read each
 //                     unit's fp32 product from TMEM and fold it into
-//                     registers with the row's fp16 group scale; store at the
-//                     end of a tile segment
-// TMEM holds a ring of kA dequantised units (64 columns each) and kD
+//                     registers with the row's fp16 group scale; at the end
+//                     of a tile segment a 2-D TMA store (or the split-tile
+//                     fix-up)
+// TMEM holds a ring of kR dequantised units (64 columns each) and kR
 // accumulators (NT columns each); consecutive units are dequantised by
 // different groups, so the dequantisation of several units, the MMAs of
 // another and the epilogues of earlier ones all overlap.
