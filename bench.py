@@ -453,7 +453,9 @@ def run_ours(args):
 
 def run_e2e(sv, torch, device, stream, calls, layers, wss, acc_np, tree_np, acc_ws, acc_ws2, args):
     """The same step through the public API with pinned host inputs and outputs."""
-    h_x = {(M, name): torch.randn((M, K)).to(torch.bfloat16).pin_memory() for (M, name, K, N, li) in calls}
+    cpu_gen = torch.Generator().manual_seed(4321)
+    h_x = {(M, name): torch.randn((M, K), generator=cpu_gen).to(torch.bfloat16).pin_memory()
+           for (M, name, K, N, li) in calls}
     d_x = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h_x.items()}
     h_out = {(M, name): torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for (M, name, K, N, li) in calls}
     d_out = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h_out.items()}
