@@ -151,7 +151,8 @@ def run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_
     if args.only == "linear":
         li = STEP_MS.index(args.m) if args.m in STEP_MS else 0
         K, N = dict((n, (k, nn)) for n, k, nn in SHAPES)[args.shape]
-        x = torch.randn((args.m, K), device=stream.device).to(torch.bfloat16)
+        g = torch.Generator(device=stream.device).manual_seed(99)
+        x = torch.randn((args.m, K), generator=g, device=stream.device).to(torch.bfloat16)
         out = torch.empty((args.m, N), dtype=torch.bfloat16, device=stream.device)
         ws = torch.zeros(sv.linear_workspace_bytes(args.m, N, K), dtype=torch.uint8, device=stream.device)
         fn = lambda: sv.linear(x, layers[li][args.shape], out=out, ws=ws)
