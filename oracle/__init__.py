@@ -51,6 +51,8 @@ def lib():
             i64, i32 = ctypes.c_int64, ctypes.c_int
             L.oracle_bf16_round.argtypes = [ctypes.c_float]
             L.oracle_bf16_round.restype = ctypes.c_uint16
+            L.oracle_bf16_round_f64.argtypes = [ctypes.c_double]
+            L.oracle_bf16_round_f64.restype = ctypes.c_uint16
             L.oracle_f16_round.argtypes = [ctypes.c_float]
             L.oracle_f16_round.restype = ctypes.c_uint16
             L.oracle_unpack_codes.argtypes = [_P(np.uint32), i64, i64, _P(np.int8)]
@@ -63,7 +65,7 @@ def lib():
                                              _P(np.int64), i64, _P(np.uint16), ctypes.c_void_p]
             L.oracle_spec_accept_seq.argtypes = [_P(np.float32), _P(np.float32), _P(np.int32), _P(np.float32),
                                                  i32, i32, i32, _P(np.int32), _P(np.int32), _P(np.float64),
-                                                 _P(np.float64)]
+                                                 _P(np.float64), _P(np.float64)]
             L.oracle_greedy_tree.argtypes = [_P(np.float32), _P(np.int32), _P(np.int32), i32, i32, i32,
                                              _P(np.int32), _P(np.int32)]
             L.oracle_greedy_chain.argtypes = [_P(np.float32), _P(np.int32), i32, i32, i32, _P(np.int32),
@@ -83,6 +85,11 @@ def num_threads() -> int:
 
 def bf16_round(f: float) -> int:
     return int(lib().oracle_bf16_round(float(f)))
+
+
+def bf16_round_f64(v: float) -> int:
+    """bf16 bits of a double, rounded to nearest even in one step."""
+    return int(lib().oracle_bf16_round_f64(float(v)))
 
 
 def f16_round(f: float) -> int:
@@ -149,7 +156,9 @@ def linear_cols(x_bf16, qweight, scales, cols, want_y: bool = False):
 
 def spec_accept_seq(p, q, d, u):
     """Stochastic acceptance of a sequence draft. Returns
-    (accepted_len[B], next_token[B], alpha[B,K], margin[B])."""
+    (accepted_len[B], next_token[B], alpha[B,K], margin_alpha[B], margin_cdf[B]):
+    margin_alpha = min |u_i - alpha_i| over the evaluated drafts, margin_cdf =
+    distance of u*S from the nearer end of the drawn token's CDF interval, / S."""
     p, q, d, u = _c(p, np.float32), _c(q, np.float32), _c(d, np.int32), _c(u, np.float32)
     B, K1, V = p.shape
     K = K1 - 1
@@ -157,9 +166,10 @@ def spec_accept_seq(p, q, d, u):
     acc = np.empty(B, dtype=np.int32)
     nxt = np.empty(B, dtype=np.int32)
     alpha = np.empty((B, K), dtype=np.float64)
-    margin = np.empty(B, dtype=np.float64)
-    lib().oracle_spec_accept_seq(p, q, d, u, B, K, V, acc, nxt, alpha, margin)
-    return acc, nxt, alpha, margin
+    margin_alpha = np.empty(B, dtype=np.float64)
+    margin_cdf = np.empty(B, dtype=np.float64)
+    lib().oracle_spec_accept_seq(p, q, d, u, B, K, V, acc, nxt, alpha, margin_alpha, margin_cdf)
+    return acc, nxt, alpha, margin_alpha, margin_cdf
 
 
 def greedy_tree(p, draft, parents):

@@ -25,8 +25,8 @@
  *  - nibble k%8 sits at bits 4*(k%8) of qweight[n][k/8], two's complement;
  *  - scale = fp16_rne(fp32(max|w| / 7)); q = clamp(rne(w / scale), -8, 7);
  *    a zero scale gives q = 0;
- *  - the linear accumulates in fp64 in ascending k and rounds once to bf16
- *    (round to nearest even);
+ *  - the linear accumulates in fp64 in ascending k and rounds the fp64 sum
+ *    once, directly, to bf16 (round to nearest even);
  *  - softmax at temperature 1, no truncation, fp64 throughout;
  *  - the target supplies K+1 distributions; when all K drafts are accepted
  *    the extra token is drawn from the (K+1)-th;
@@ -77,7 +77,28 @@ static uint16_t f32_to_f16(float f) {
     return h;
 }
 
+/* double -> bfloat16 bits, round to nearest even in one step (no fp32
+ * intermediate): the bf16 grid spacing at |v| = m * 2^e (m in [0.5, 1)) is
+ * 2^(e - 8), never finer than the subnormal spacing 2^-133; |v| is scaled
+ * onto that grid (exact: a power of two), rounded with rint (the default
+ * rounding mode is to nearest, ties to even), and scaled back. The result has
+ * at most 8 significant bits, so its conversion to float is exact (or inf
+ * past the largest bf16). */
+static uint16_t f64_to_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    int e;
+    (void)frexp(fabs(v), &e);
+    int q = e - 8;
+    if (q < -133) q = -133;
+    double r = ldexp(rint(ldexp(fabs(v), -q)), q);
+    float f = (float)copysign(r, v); /* keeps the sign of -0 and of negatives that round to 0 */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
 uint16_t oracle_bf16_round(float f) { return f32_to_bf16(f); }
+uint16_t oracle_bf16_round_f64(double v) { return f64_to_bf16(v); }
 uint16_t oracle_f16_round(float f) { return f32_to_f16(f); }
 
 /* ------------------------------------------------------------ 4-bit format */
@@ -156,7 +177,7 @@ void oracle_linear(const uint16_t* x, int64_t M, int64_t K, const uint32_t* qwei
     for (int64_t n = 0; n < N; ++n)
         for (int64_t m = 0; m < M; ++m) {
             double v = dot_row(x, K, m, qweight, scales, n);
-            out[m * N + n] = f32_to_bf16((float)v);
+            out[m * N + n] = f64_to_bf16(v);
             if (y) y[m * N + n] = v;
         }
 }
@@ -169,7 +190,7 @@ void oracle_linear_cols(const uint16_t* x, int64_t M, int64_t K, const uint32_t*
     for (int64_t c = 0; c < ncols; ++c)
         for (int64_t m = 0; m < M; ++m) {
             double v = dot_row(x, K, m, qweight, scales, cols[c]);
-            out[m * ncols + c] = f32_to_bf16((float)v);
+            out[m * ncols + c] = f64_to_bf16(v);
             if (y) y[m * ncols + c] = v;
         }
 }
@@ -190,8 +211,9 @@ static void softmax64(const float* logits, int V, double* P) {
 
 /* Inverse-CDF draw: smallest x with sum_{y<=x} R(y) > u * S (ascending x).
  * If rounding leaves no such x, the last x with R(x) > 0.
- * *margin receives the distance from u*S to the nearest CDF boundary around
- * the chosen x, divided by S. */
+ * *margin receives the distance from t = u*S to the nearer end of the chosen
+ * x's interval [sum_{y<x} R(y), sum_{y<=x} R(y)), divided by S: how far u
+ * would have to move for the draw to change. */
 static int sample_cdf(const double* R, int V, double S, double u, double* margin) {
     double t = u * S, c = 0.0;
     int last_pos = -1;
@@ -214,11 +236,14 @@ static int sample_cdf(const double* R, int V, double S, double u, double* margin
  *  p [B][K+1][V] target logits, q [B][K][V] draft logits, d [B][K] draft ids,
  *  u [B][K+1] uniforms (u[.,0..K-1] for the tests, u[.,K] for the final draw).
  * Outputs accepted_len[B] in [0,K], next_token[B], alpha[B][K] (fp64, NAN for
- * positions not evaluated) and margin[B] = the smallest |u_i - alpha_i| over
- * evaluated positions and the final draw's CDF margin (fp64).
+ * positions not evaluated), margin_alpha[B] = the smallest |u_i - alpha_i|
+ * over the evaluated positions (how close an accept decision came to going
+ * the other way) and margin_cdf[B] = the final draw's CDF margin (see
+ * sample_cdf), both fp64.
  */
 void oracle_spec_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int K, int V,
-                            int32_t* accepted_len, int32_t* next_token, double* alpha, double* margin) {
+                            int32_t* accepted_len, int32_t* next_token, double* alpha, double* margin_alpha,
+                            double* margin_cdf) {
 #pragma omp parallel for schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         double* P = (double*)malloc(sizeof(double) * (size_t)V);
@@ -257,9 +282,9 @@ void oracle_spec_accept_seq(const float* p, const float* q, const int32_t* d, co
         }
         double cm;
         next_token[b] = sample_cdf(R, V, S, (double)ub[K], &cm);
-        mg = cm < mg ? cm : mg;
         accepted_len[b] = r;
-        margin[b] = mg;
+        margin_alpha[b] = mg;
+        margin_cdf[b] = cm;
         free(P);
         free(Q);
         free(R);

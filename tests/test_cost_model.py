@@ -41,7 +41,7 @@ def test_expected_tokens_matches_the_accept_rule_on_the_worked_count():
     q = np.broadcast_to(ql, (B, K, V)).copy()
     d = np.zeros((B, K), dtype=np.int32)
     u = synth.rng(31).random((B, K + 1), dtype=np.float32)
-    acc, _, _, _ = oracle.spec_accept_seq(p, q, d, u)
+    acc, _, _, _, _ = oracle.spec_accept_seq(p, q, d, u)
     tokens = acc + 1
     model = cm.expected_tokens(beta, K)
     assert abs(tokens.mean() - model) < 5 * tokens.std() / math.sqrt(B)

@@ -31,6 +31,61 @@ def test_bf16_round_matches_torch():
     assert np.array_equal(got, ref)
 
 
+def _bf16_exact(bits: int):
+    """The value of a bf16 bit pattern as an exact Fraction (None for inf/nan)."""
+    from fractions import Fraction
+    sign = -1 if bits & 0x8000 else 1
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0xFF:
+        return None
+    if e == 0:
+        return sign * Fraction(m, 2 ** 133)
+    return sign * Fraction(128 + m) * Fraction(2) ** (e - 134)
+
+
+def _bf16_rne_brute_force(v: float) -> int:
+    """Round-to-nearest-even of a double onto the bf16 grid by its definition:
+    among the finite bf16 values around v pick the nearest in exact rational
+    arithmetic, on a tie the one with an even last significand bit; past the
+    largest finite bf16 by half a step or more, infinity."""
+    from fractions import Fraction
+    fv = Fraction(v)
+    base = int(np.array([v], dtype=np.float32).view(np.uint32)[0] >> 16)
+    if v == 0:
+        return base  # +0 / -0 keep their sign bit
+    cands = []
+    for b in range(base - 2, base + 3):
+        b &= 0xFFFF
+        val = _bf16_exact(b)
+        if val is not None and ((val > 0) == (v > 0) or val == 0):
+            cands.append((abs(val - fv), b & 1, (b & 0x8000) != (base & 0x8000), b))
+    cands.sort()
+    best = cands[0][-1]
+    big = _bf16_exact(0x7F7F)
+    if abs(fv) >= big + (big - _bf16_exact(0x7F7E)) / 2:
+        return 0xFF80 if v < 0 else 0x7F80
+    return best
+
+
+def test_bf16_round_from_f64_matches_definition():
+    g = synth.rng(5)
+    vals = list(g.standard_normal(3000) * 10.0 ** g.integers(-40, 38, 3000))
+    # just above / below / on a tie between bf16 neighbours, by less than fp32 can see
+    # (an fp32 intermediate would land on the tie and round to even instead)
+    for b in list(range(0x3F80, 0x3F90)) + [0x0001, 0x0080, 0x4780, 0x7F00, 0x8123, 0xC2F1]:
+        lo, hi = _bf16_exact(b), _bf16_exact(b + 1)
+        mid = float((lo + hi) / 2)
+        step = float(hi - lo)
+        vals += [mid, mid + step * 2.0 ** -20, mid - step * 2.0 ** -20, mid + step * 2.0 ** -40]
+    vals += [0.0, -0.0, 1e-45, -1e-45, 2.0 ** -140, 2.0 ** -134, 3.4e38, -3.4e38, 3.39e38]
+    for v in vals:
+        assert oracle.bf16_round_f64(v) == _bf16_rne_brute_force(v), v
+    # the case a float intermediate gets wrong: 1 + 2^-8 + 2^-30 lies above the tie
+    assert oracle.bf16_round_f64(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert oracle.bf16_round(np.float32(1.0 + 2.0 ** -8 + 2.0 ** -30)) == 0x3F80
+
+
 def test_f16_round_matches_numpy():
     g = synth.rng(2)
     vals = np.concatenate([g.uniform(-65000, 65000, 5000), g.uniform(-1e-3, 1e-3, 5000),
@@ -166,7 +221,8 @@ def test_linear_matches_torch_fp64_matmul(M, N, K):
     ref = xt @ w.T
     bound = (xt.abs() @ w.abs().T) * 1e-13
     assert torch.all((torch.from_numpy(y) - ref).abs() <= bound)
-    ref_bf16 = ref.float().to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    # the output is y rounded once, directly, to bf16 (checked by the definition on every element)
+    ref_bf16 = np.array([_bf16_rne_brute_force(v) for v in y.ravel()], dtype=np.uint16).reshape(out.shape)
     assert np.array_equal(out, ref_bf16)
 
 
@@ -190,22 +246,78 @@ def test_accept_p_equals_q_accepts_everything():
     B, K, V = 64, 6, 50
     p, q, d, u = synth.accept_seq_case(B, K, V, seed=20)
     q = np.ascontiguousarray(p[:, :K])
-    acc, nxt, alpha, margin = oracle.spec_accept_seq(p, q, d, u)
+    acc, nxt, alpha, margin_alpha, margin_cdf = oracle.spec_accept_seq(p, q, d, u)
     assert np.all(acc == K)
     assert np.all(alpha == 1.0)
+    assert np.allclose(margin_alpha, 1.0 - u[:, :K].max(axis=1), rtol=0, atol=1e-15)
 
 
 def test_accept_alpha_matches_library_softmax():
     B, K, V = 8, 4, 300
     p, q, d, u = synth.accept_seq_case(B, K, V, seed=21)
-    u[:] = 0.0  # accept all: every alpha is evaluated
-    acc, nxt, alpha, margin = oracle.spec_accept_seq(p, q, d, u)
+    u[:, :K] = 0.0  # accept all: every alpha is evaluated
+    acc, nxt, alpha, margin_alpha, _ = oracle.spec_accept_seq(p, q, d, u)
     P = _softmax64(p[:, :K])
     Q = _softmax64(q)
     b_idx, i_idx = np.meshgrid(np.arange(B), np.arange(K), indexing="ij")
     ref = np.minimum(1.0, P[b_idx, i_idx, d] / Q[b_idx, i_idx, d])
     assert np.allclose(alpha, ref, rtol=1e-12, atol=0)
     assert np.all(acc == K)
+    assert np.allclose(margin_alpha, ref.min(axis=1), rtol=1e-12, atol=0)  # |0 - alpha_i| = alpha_i
+
+
+NEG = -1000.0  # exp(NEG - max) underflows to exactly 0 in fp64: a token with zero probability
+
+
+def _rows(*ps):
+    """Logit rows whose softmax is exactly the given dyadic distributions: each
+    p lists how many tokens share the mass equally (the rest get NEG), e.g. 2
+    gives (1/2, 1/2, 0, 0) on V = 4."""
+    out = np.full((len(ps), 4), NEG, dtype=np.float32)
+    for i, k in enumerate(ps):
+        out[i, :k] = 0.0
+    return out
+
+
+def test_accept_margins_exact_on_dyadic_rows():
+    """alpha_i = 1, 1/2, 1/4 (target mass 1, 1/2, 1/4 on token 0; draft mass 1
+    on token 0). u = (7/8, 3/8, 5/16): accepted, accepted, rejected; the
+    smallest |u_i - alpha_i| is 1/16. The residual max(0, P - Q) at the
+    rejection is (0, 1/4, 1/4, 1/4), S = 3/4; u_4 = 3/8 gives t = u_4 S = 9/32,
+    inside token 2's interval [1/4, 1/2): margin_cdf = (9/32 - 1/4) / S = 1/24."""
+    p = _rows(1, 2, 4, 4)[None]
+    q = _rows(1, 1, 1)[None]
+    d = np.zeros((1, 3), dtype=np.int32)
+    u = np.array([[0.875, 0.375, 0.3125, 0.375]], dtype=np.float32)
+    acc, nxt, alpha, margin_alpha, margin_cdf = oracle.spec_accept_seq(p, q, d, u)
+    assert acc[0] == 2 and nxt[0] == 2
+    assert alpha[0].tolist() == [1.0, 0.5, 0.25]
+    assert margin_alpha[0] == 0.0625
+    assert abs(margin_cdf[0] - 1.0 / 24.0) < 1e-16
+    # the same rows, u_4 moved to the upper part of token 2's interval: the
+    # nearer end is now the upper one, (1/2 - t) / S with t = (5/8)(3/4)
+    u2 = u.copy()
+    u2[0, 3] = 0.625
+    acc2, nxt2, _, _, margin_cdf2 = oracle.spec_accept_seq(p, q, d, u2)
+    assert acc2[0] == 2 and nxt2[0] == 2
+    assert abs(margin_cdf2[0] - (0.5 - 0.625 * 0.75) / 0.75) < 1e-16
+    # the first decision within 2^-12 of alpha: that is the margin
+    u3 = u.copy()
+    u3[0, 0] = 1.0 - 2.0 ** -12
+    assert oracle.spec_accept_seq(p, q, d, u3)[3][0] == 2.0 ** -12
+
+
+def test_accept_margin_cdf_of_the_extra_token():
+    """All drafts accepted (p == q): the extra token comes from the last target
+    row, uniform over 4 tokens; u = 0.5625 puts t 1/16 past token 2's start."""
+    p = _rows(1, 4)[None]
+    q = _rows(1)[None]
+    d = np.zeros((1, 1), dtype=np.int32)
+    u = np.array([[0.5, 0.5625]], dtype=np.float32)
+    acc, nxt, alpha, margin_alpha, margin_cdf = oracle.spec_accept_seq(p, q, d, u)
+    assert acc[0] == 1 and nxt[0] == 2
+    assert margin_alpha[0] == 0.5
+    assert margin_cdf[0] == 0.0625
 
 
 def _first_token(acc, nxt, d):
@@ -226,7 +338,7 @@ def test_emitted_token_distribution_equals_target():
     Qd = _softmax64(ql)
     d = np.stack([g.choice(V, size=B, p=Qd[i]) for i in range(K)], axis=1).astype(np.int32)
     u = g.random((B, K + 1), dtype=np.float32)
-    acc, nxt, alpha, margin = oracle.spec_accept_seq(p, q, d, u)
+    acc, nxt, alpha, _, _ = oracle.spec_accept_seq(p, q, d, u)
     P1 = _softmax64(pl[0])
     counts = np.bincount(_first_token(acc, nxt, d), minlength=V)
     stat, pval = scipy.stats.chisquare(counts, B * P1)
@@ -252,7 +364,7 @@ def test_extra_token_after_full_acceptance_follows_last_target_row():
     q = np.ascontiguousarray(p[:, :K])
     d = g.integers(0, V, size=(B, K)).astype(np.int32)
     u = g.random((B, K + 1), dtype=np.float32)
-    acc, nxt, _, _ = oracle.spec_accept_seq(p, q, d, u)
+    acc, nxt, _, _, _ = oracle.spec_accept_seq(p, q, d, u)
     assert np.all(acc == K)
     stat, pval = scipy.stats.chisquare(np.bincount(nxt, minlength=V), B * _softmax64(pl[K]))
     assert pval > 1e-4
@@ -273,7 +385,7 @@ def test_expected_tokens_per_step_closed_form_and_worked_count():
     q = np.broadcast_to(ql, (B, K, V)).copy()
     d = np.zeros((B, K), dtype=np.int32)
     u = synth.rng(24).random((B, K + 1), dtype=np.float32)
-    acc, nxt, _, _ = oracle.spec_accept_seq(p, q, d, u)
+    acc, nxt, _, _, _ = oracle.spec_accept_seq(p, q, d, u)
     mean_tokens = np.mean(acc + 1)
     expect = (1 - beta ** (K + 1)) / (1 - beta)
     sd = np.std(acc + 1) / math.sqrt(B)
