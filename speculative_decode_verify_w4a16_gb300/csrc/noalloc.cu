@@ -27,6 +27,7 @@ void* g_na_ptr[64];  // device address of g_noalloc_scratch, per device
 // Once per device, with that device current: look up the array's device
 // address (host code must never use the symbol itself as a pointer).
 static cudaError_t noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;  // g_na_ptr has one slot per device id < 64
   std::lock_guard<std::mutex> lk(g_na_mu);
   if (!g_na_ptr[dev]) {
     void* p = nullptr;
@@ -64,9 +65,10 @@ extern "C" w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, co
   void* scratch = nullptr;
   if (noalloc_scratch(dev.device, &scratch) != cudaSuccess) return W4A16_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The completion counters must start at zero; a previous call (or one that
-  // timed out) may have left them otherwise, so clear this call's slice.
-  const size_t counter_bytes = (kTileCounterBase + (size_t)(N / kUnitRows) * 8) * sizeof(int);
+  // The kernels leave their completion counters at zero, but a call that
+  // timed out may not have: clear the ones this call uses (one per (row tile,
+  // epilogue warp) after the reserved ints).
+  const size_t counter_bytes = (kTileCounterBase + (size_t)(N / kUnitRows) * 4) * sizeof(int);
   if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return W4A16_ERR_CUDA;
   return launch_linear(x, M, K, qweight_packed, scales_packed, N, out, scratch, plan, dev, s) == cudaSuccess
              ? W4A16_OK

@@ -81,27 +81,83 @@ def test_output_not_16_byte_aligned(M):
     assert torch.all(buf[:2] == 7.0) and torch.all(buf[2 + M * 640:] == 7.0)
 
 
-def test_one_hot_codes_select_columns_exactly():
-    M, N, K = 6, 384, 1024
-    g = synth.rng(40)
+@pytest.mark.parametrize("M", [6, 13, 40])
+def test_one_hot_codes_select_columns_exactly(M):
+    # W[n, cols[n]] = 1 (scale 1) selects column cols[n] of x. With integer x
+    # (times a power of two per row) every partial sum of both paths is exact,
+    # so the selection must be bit-exact: this pins the index mapping of the
+    # packed layout, the token tiles and the output tiles.
+    N, K = 384, 1024
+    g = synth.rng(40 + M)
     cols = g.integers(0, K, size=N)
     codes = np.zeros((N, K), dtype=np.int8)
     codes[np.arange(N), cols] = 1
     sc = np.full((N, K // 128), np.float16(1.0)).view(np.uint16)
-    x = synth.activations(M, K, seed=41)
+    xi = g.integers(-64, 65, size=(M, K)).astype(np.float32) * (2.0 ** g.integers(-20, 20, size=(M, 1)))
+    x = synth.bf16_bits_from_f32(xi.astype(np.float32))
     got = _gpu_linear(x, oracle.pack_codes(codes), sc)
     assert np.array_equal(got, x[:, cols])
+    if M >= 16:
+        # the tcgen05 path multiplies exact codes: N(0, 1) tokens stay within the bar too
+        xn = synth.activations(M, K, seed=41)
+        assert_linear_close(_gpu_linear(xn, oracle.pack_codes(codes), sc), xn[:, cols], "one-hot, N(0,1) tokens")
 
 
-def test_extreme_codes_and_scales():
-    M, N, K = 4, 256, 2048
-    codes = np.full((N, K), -8, dtype=np.int8)
-    codes[1::2] = 7
-    sc = np.full((N, K // 128), np.float16(2.0 ** -10)).view(np.uint16)
-    sc[::3] = np.float16(0.0).view(np.uint16)
-    x = synth.activations(M, K, seed=42)
-    qw = oracle.pack_codes(codes)
-    assert_linear_close(_gpu_linear(x, qw, sc), oracle.linear(x, qw, sc), "extreme codes")
+@pytest.mark.parametrize("M,kind", [(3, "one_hot"), (8, "one_hot"), (13, "one_hot"), (4, "quantized"),
+                                    (11, "quantized")])
+def test_fragment_path_error_bound(M, kind):
+    """The fragment path (M < 16) multiplies the offset codes o = c + 8 and
+    removes 8 * sum(x) per group after the fp32 accumulation, so its error
+    scales with that sum rather than with the output. Every output must lie
+    within half a bf16 step plus 2^-20 * sum_g s_g * (8 |sum_g x| + sum_g |c x|)
+    of the exact result (the tensor cores' fp32 accumulation is good to about
+    2^-21 of the accumulated magnitude). One-hot weights with code 1 and N(0,1)
+    tokens are the adversarial case: the selected value is ~100 times smaller
+    than the removed offset."""
+    N, K = 384, 2048
+    g = synth.rng(60 + M)
+    if kind == "one_hot":
+        codes = np.zeros((N, K), dtype=np.int8)
+        codes[np.arange(N), g.integers(0, K, size=N)] = 1
+        sc = np.full((N, K // 128), np.float16(1.0)).view(np.uint16)
+        qw = oracle.pack_codes(codes)
+    else:
+        qw, sc = oracle.quantize(synth.weights(N, K, seed=61 + M))
+        codes = oracle.unpack_codes(qw, K)
+    x = synth.activations(M, K, seed=62 + M)
+    got = synth.bf16_bits_to_f32(_gpu_linear(x, qw, sc)).astype(np.float64)
+    _, y = oracle.linear(x, qw, sc, want_y=True)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64).reshape(M, K // 128, 128)
+    s = sc.view(np.float16).astype(np.float64)                          # [N, G]
+    c = codes.astype(np.float64).reshape(N, K // 128, 128)
+    offset = 8.0 * np.abs(xf.sum(axis=2))                               # [M, G]
+    cx = np.einsum("mgk,ngk->mng", np.abs(xf), np.abs(c))               # [M, N, G]
+    bound = 2.0 ** -20 * np.einsum("ng,mng->mn", s, offset[:, None, :] + cx)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(got), 1e-300))) - 8)
+    excess = np.abs(got - y) - half_ulp - bound
+    assert excess.max() <= 0, f"{kind} M={M}: worst excess {excess.max():.3e} (bound {bound.max():.3e})"
+
+
+@pytest.mark.parametrize("M", [1, 5, 15])
+def test_token_rows_of_very_different_magnitude(M):
+    # each token row is scaled by its own power of two on the fragment path:
+    # rows from 2^-30 to 2^30 (and a zero row) must each meet the tolerance
+    N, K = 256, 2048
+    j = np.round(np.linspace(-30, 30, M)).astype(np.int32)[:, None]
+    x = synth.bf16_bits_to_f32(synth.activations(M, K, seed=46)) * (2.0 ** j).astype(np.float32)  # exact
+    zero_row = M // 2 if M > 2 else -1
+    if zero_row >= 0:
+        x[zero_row] = 0.0
+    xb = synth.bf16_bits_from_f32(x.astype(np.float32))
+    _, qw, sc = _case(M, N, K, seed=47)
+    got, ref = _gpu_linear(xb, qw, sc), oracle.linear(xb, qw, sc)
+    if zero_row >= 0:
+        assert np.all(got[zero_row] == 0) and np.all(ref[zero_row] == 0)
+    # undo each row's power of two (exact on bf16 values in the normal range) and apply the usual bar
+    unscale = lambda b: synth.bf16_bits_from_f32(synth.bf16_bits_to_f32(b) * (2.0 ** -j).astype(np.float32))
+    for m in range(M):
+        if m != zero_row:
+            assert_linear_close(unscale(got)[m:m + 1], unscale(ref)[m:m + 1], f"row {m} (x scaled by 2^{j[m, 0]})")
 
 
 def test_zero_input_gives_zero():
