@@ -7,13 +7,22 @@ One step = one verify pass of the hot path on Llama-3-70B shapes:
     the weights, 1.32 GB per step, so nothing is served from the 126 MB L2);
   * the stochastic accept step (batch 16, K = 4 drafts, vocab 128256);
   * the greedy tree accept step (batch 16, 64-node tree, vocab 128256).
-`value` is microseconds per step (device time, CUDA events, inputs resident).
-The JSON line also carries the per-call sweep (us, GB/s, fraction of the HBM
-roofline), the full 80-layer + lm_head verify-forward time at M = 1/4/64 and
-its M=64/M=1 ratio, the end-to-end time with host buffers, and the CPU-oracle
-baseline.
+`value` is microseconds per step (device time, CUDA events, inputs resident,
+the step replayed as one CUDA graph).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-stack]
+Besides the contract line the run measures, per call (mean and median of 50
+after 10 warm-up calls; consecutive linear calls stream distinct weight
+copies, together more than 3x the L2; L2 flushed before every accept call): the single 2048 x 2048 linear at
+M = 4; each Llama-3-70B shape including the lm_head at M = 1, 4, 8, 16, 32,
+48, 64 (us, GB/s, TFLOP/s, fraction of the HBM roofline, time relative to
+M = 1); the stochastic accept at K = 4 and 8 and the greedy tree. It times the
+80-layer + lm_head verify forward (one CUDA graph per M) at M = 1, 4, 5, 9, 16,
+32, 48, 64, and the CPU oracle on a bounded sample on one thread and on every
+host core. The contract line carries a summary; `--detail PATH` writes all of
+it as JSON.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--no-stack] [--no-sweep] [--no-cpu-baseline] [--detail PATH]
 """
 from __future__ import annotations
 
@@ -37,17 +46,23 @@ import synth  # noqa: E402
 METRIC = "W4A16 verify-linear µs & % HBM roofline at M=1/4/64, Llama-3-70B shapes"
 SHAPES = [("qkv", 8192, 10240), ("o", 8192, 8192), ("gate_up", 8192, 57344), ("down", 28672, 8192)]
 LM_HEAD = ("lm_head", 8192, 128256)
+CONFIG1 = ("single_2048", 2048, 2048)  # x [4, 2048], W 2048 x 2048
 STEP_MS = (1, 4, 64)
+SWEEP_MS = (1, 4, 8, 16, 32, 48, 64)
+STACK_MS = (1, 4, 5, 9, 16, 32, 48, 64)
 ACC_B, ACC_K, VOCAB = 16, 4, synth.LLAMA3_VOCAB
+ACC_KS = (4, 8)
 TREE_B, TREE_N = 16, 64
 N_LAYERS = 80
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
-# DRAM bytes (read + write) per launch of each kernel, averaged over the step's
-# launches of it, from the ncu capture summarised in profiles/ (the step's
-# launch list with dram__bytes_read.sum / dram__bytes_write.sum); None until a
-# capture of the current kernels exists.
+CALL_REPS, CALL_WARMUP = 50, 10
+L2_BYTES = 126 << 20
+L2_FLUSH_BYTES = 256 << 20
+# DRAM bytes (read + write) per launch of each kernel, from the ncu capture
+# summarised in profiles/ (launches of the same kernel in one bench step,
+# averaged); None where the kernel changed after the capture.
 NCU_DRAM_BYTES_PER_LAUNCH: dict = {
-    "w4a16_skinny_kernel<1> (M<16)": 110635296,
+    "w4a16_skinny_kernel (M<16)": None,
     "w4a16_tc_kernel<64> (M>=16)": 113128128,
     "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": 89212672,
     "accept_argmax_kernel": 525573120,
@@ -65,6 +80,12 @@ def accept_bytes_seq(B, K, V):
 
 def accept_bytes_tree(B, n, V):
     return B * n * V * 4 + 2 * B * n * 4 + 2 * B * 4
+
+
+def launches_per_linear(M):
+    """Kernels one w4a16_linear call launches (the fragment kernel for M <= 8,
+    the tcgen05 kernel from 9 on)."""
+    return 1
 
 
 def peaks():
@@ -145,30 +166,6 @@ def _check(sv, where):
     assert st == 0, f"device status {st} ({sv.status_string(st)}) after {where}"
 
 
-def run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_out, acc_ws, tree_in, tree_out,
-             acc_ws2):
-    """One kind of launch only, eagerly, for profiling (no JSON contract line)."""
-    if args.only == "linear":
-        li = STEP_MS.index(args.m) if args.m in STEP_MS else 0
-        K, N = dict((n, (k, nn)) for n, k, nn in SHAPES)[args.shape]
-        g = torch.Generator(device=stream.device).manual_seed(99)
-        x = torch.randn((args.m, K), generator=g, device=stream.device).to(torch.bfloat16)
-        out = torch.empty((args.m, N), dtype=torch.bfloat16, device=stream.device)
-        ws = torch.zeros(sv.linear_workspace_bytes(args.m, N, K), dtype=torch.uint8, device=stream.device)
-        fn = lambda: sv.linear(x, layers[li][args.shape], out=out, ws=ws)
-    elif args.only == "accept":
-        fn = lambda: sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3],
-                                    accepted_len=acc_out[0], next_token=acc_out[1], ws=acc_ws)
-    else:
-        fn = lambda: sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
-                                    next_token=tree_out[1], ws=acc_ws2)
-    for _ in range(args.warmup + args.steps):
-        fn()
-        torch.cuda.synchronize()
-    _check(sv, "profiling launches")
-    print(json.dumps({"only": args.only, "shape": args.shape, "M": args.m, "launches": args.warmup + args.steps}))
-
-
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -197,6 +194,154 @@ def make_weight(sv, torch, N, K, gen, device):
     return pw
 
 
+def time_per_call(torch, fn, flush=None, reps=CALL_REPS, warmup=CALL_WARMUP):
+    """Device time (us) of one call fn(i) (i = the call's index, to rotate
+    inputs): `warmup` eager calls, then `reps` calls captured in one CUDA graph
+    with timing events around each (and an L2 flush before each, if given);
+    the graph is replayed once to warm up and once timed. Returns (mean,
+    median): event timestamps on this GPU advance in 1.024 us steps, so the
+    median is a multiple of that step while the mean of the reps resolves
+    below it."""
+    for i in range(warmup):
+        if flush:
+            flush()
+        fn(i)
+    torch.cuda.synchronize()
+    evs = [(_event(torch), _event(torch)) for _ in range(reps)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            if flush:
+                flush()
+            evs[i][0].record()
+            fn(i)
+            evs[i][1].record()
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    del g
+    return statistics.fmean(ts), statistics.median(ts)
+
+
+def run_only(args, sv, torch, device, layers, acc_in, acc_out, acc_ws, tree_in, tree_out, acc_ws2):
+    """One kind of launch only, eagerly, for profiling (no JSON contract line)."""
+    if args.only == "linear":
+        K, N = dict((n, (k, nn)) for n, k, nn in SHAPES)[args.shape]
+        g = torch.Generator(device=device).manual_seed(99)
+        x = torch.randn((args.m, K), generator=g, device=device).to(torch.bfloat16)
+        out = torch.empty((args.m, N), dtype=torch.bfloat16, device=device)
+        ws = torch.zeros(sv.linear_workspace_bytes(args.m, N, K), dtype=torch.uint8, device=device)
+        fn = lambda: sv.linear(x, layers[0][args.shape], out=out, ws=ws)
+    elif args.only == "accept":
+        fn = lambda: sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3],
+                                    accepted_len=acc_out[0], next_token=acc_out[1], ws=acc_ws)
+    else:
+        fn = lambda: sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
+                                    next_token=tree_out[1], ws=acc_ws2)
+    for _ in range(args.warmup + args.steps):
+        fn()
+        torch.cuda.synchronize()
+    _check(sv, "profiling launches")
+    print(json.dumps({"only": args.only, "shape": args.shape, "M": args.m, "launches": args.warmup + args.steps}))
+
+
+def run_sweep(sv, torch, device, gen, layers, pk, flush):
+    """Per-call times of every linear configuration (consecutive calls stream
+    distinct copies of the weight, together more than 3x the L2) and of the
+    accept steps (L2 flushed before each call)."""
+    rows = []
+    shapes = [(CONFIG1, (4,))] + [(s, SWEEP_MS) for s in SHAPES] + [(LM_HEAD, SWEEP_MS)]
+    for (name, K, N), ms in shapes:
+        copies = min(160, max(2, -(-3 * L2_BYTES // (N * K // 2)) + 1))
+        wts = [make_weight(sv, torch, N, K, gen, device) for _ in range(copies)]
+        base = None
+        for M in ms:
+            x = torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16)
+            out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+            ws = torch.zeros(sv.linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=device)
+            us, us_med = time_per_call(torch, lambda i: sv.linear(x, wts[i % copies], out=out, ws=ws))
+            b = linear_bytes(M, N, K)
+            base = us if base is None else base
+            rows.append({"shape": name, "M": M, "K": K, "N": N, "us": round(us, 2), "us_median": round(us_med, 2),
+                         "GB_s": round(b / us / 1e3, 1), "TFLOP_s": round(2.0 * M * N * K / us / 1e6, 2),
+                         "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3),
+                         "ideal_us": round(b / pk["hbm_gbs"] / 1e3, 2),
+                         "ratio_to_m1": round(us / base, 3) if ms[0] == 1 else None, "weight_copies": copies})
+        del wts
+        torch.cuda.empty_cache()
+    _check(sv, "the linear sweep")
+    acc = []
+    for K in ACC_KS:
+        p, q, d, u = synth.accept_seq_case(ACC_B, K, VOCAB, seed=17 + K)
+        t = [torch.from_numpy(a).to(device) for a in (p, q, d, u)]
+        a_out = [torch.empty(ACC_B, dtype=torch.int32, device=device) for _ in range(2)]
+        ws = torch.zeros(sv.accept_workspace_bytes(ACC_B, K, VOCAB), dtype=torch.uint8, device=device)
+        us, _ = time_per_call(torch, lambda i: sv.spec_accept(t[0], t[2], q_logits=t[1], uniforms=t[3],
+                                                              accepted_len=a_out[0], next_token=a_out[1], ws=ws), flush)
+        b = accept_bytes_seq(ACC_B, K, VOCAB)
+        acc.append({"mode": "stochastic sequence", "B": ACC_B, "K": K, "V": VOCAB, "us": round(us, 2),
+                    "GB_s": round(b / us / 1e3, 1), "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3)})
+        del t
+    tp, td, tpar = synth.greedy_tree_case(TREE_B, TREE_N, VOCAB, seed=27)
+    t = [torch.from_numpy(a).to(device) for a in (tp, td, tpar)]
+    a_out = [torch.empty(TREE_B, dtype=torch.int32, device=device) for _ in range(2)]
+    ws = torch.zeros(sv.accept_workspace_bytes(TREE_B, TREE_N, VOCAB), dtype=torch.uint8, device=device)
+    us, _ = time_per_call(torch, lambda i: sv.spec_accept(t[0], t[1], tree_parents=t[2], accepted_len=a_out[0],
+                                                          next_token=a_out[1], ws=ws), flush)
+    b = accept_bytes_tree(TREE_B, TREE_N, VOCAB)
+    acc.append({"mode": "greedy tree", "B": TREE_B, "nodes": TREE_N, "V": VOCAB, "us": round(us, 2),
+                "GB_s": round(b / us / 1e3, 1), "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3)})
+    _check(sv, "the accept sweep")
+    return rows, acc
+
+
+def run_stack(sv, torch, device, gen, layers, lm_head, pk, stream):
+    """The 80-layer + lm_head verify forward, one CUDA graph per M (median of 10 replays)."""
+    stack = {}
+    for M in STACK_MS:
+        sx = {K: torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16) for K in (8192, 28672)}
+        souts = {name: torch.empty((M, N), dtype=torch.bfloat16, device=device) for name, K, N in SHAPES + [LM_HEAD]}
+        need = max(sv.linear_workspace_bytes(M, N, K) for _, K, N in SHAPES + [LM_HEAD])
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+
+        def forward():
+            for li in range(N_LAYERS):
+                for name, K, N in SHAPES:
+                    sv.linear(sx[K], layers[li][name], out=souts[name], ws=ws)
+            sv.linear(sx[8192], lm_head, out=souts["lm_head"], ws=ws)
+
+        forward()
+        torch.cuda.synchronize()
+        gm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gm):
+            forward()
+        gm.replay()
+        gm.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            gm.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        del gm
+        us = statistics.median(ts)
+        b = N_LAYERS * sum(linear_bytes(M, N, K) for _, K, N in SHAPES) + linear_bytes(M, LM_HEAD[2], LM_HEAD[1])
+        stack[str(M)] = {"us": round(us, 1), "GB_s": round(b / us / 1e3, 1),
+                         "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3),
+                         "ideal_us": round(b / pk["hbm_gbs"] / 1e3, 1), "tokens_per_s": round(M / (us * 1e-6), 1)}
+        del sx, souts, ws
+    for M in STACK_MS:
+        stack[str(M)]["ratio_to_m1"] = round(stack[str(M)]["us"] / stack["1"]["us"], 3)
+    stack["ratio_m64_m1"] = stack["64"]["ratio_to_m1"]
+    _check(sv, "the stack forward")
+    return stack
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -217,7 +362,9 @@ def run_ours(args):
     layers = []
     for li in range(n_layers):
         layers.append({name: make_weight(sv, torch, N, K, gen, device) for name, K, N in SHAPES})
-    lm_head = make_weight(sv, torch, LM_HEAD[2], LM_HEAD[1], gen, device) if args.stack else None
+    lm_head = make_weight(sv, torch, LM_HEAD[2], LM_HEAD[1], gen, device) if (args.stack or args.sweep) else None
+    if lm_head is not None:
+        layers[0]["lm_head"] = lm_head
     torch.cuda.synchronize()
 
     # ---- step inputs
@@ -242,7 +389,7 @@ def run_ours(args):
     tree_out = [torch.empty(TREE_B, dtype=torch.int32, device=device) for _ in range(2)]
     stream = torch.cuda.current_stream()
     calls = [(M, name, K, N, li) for li, M in enumerate(STEP_MS) for name, K, N in SHAPES]
-    n_launch_per_step = len(calls) + 3 + 1  # linears, stochastic accept (3 kernels), greedy tree (1)
+    n_launch_per_step = sum(launches_per_linear(M) for M, _, _, _, _ in calls) + 3 + 1
 
     def step(evs=None):
         for j, (M, name, K, N, li) in enumerate(calls):
@@ -264,8 +411,7 @@ def run_ours(args):
             evs[len(calls) + 1][1].record()
 
     if args.only:
-        return run_only(args, sv, torch, stream, calls, layers, xs, outs, wss, acc_in, acc_out, acc_ws, tree_in,
-                        tree_out, acc_ws2)
+        return run_only(args, sv, torch, device, layers, acc_in, acc_out, acc_ws, tree_in, tree_out, acc_ws2)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -306,41 +452,22 @@ def run_ours(args):
     clk = clocks.stop()
     total_ms = max_over_ranks(t0.elapsed_time(t1), ws, device)
     _check(sv, "timed graph replays")
-    # per-call device durations: the step with event nodes, one replay at a time
+    # per-call device durations inside the step: the step with event nodes, one replay at a time
     seg = []
-    for s in range(args.steps):
+    for s in range(max(args.steps, 10)):
         graph_ev.replay()
         torch.cuda.synchronize()
         seg.append([evs[j][0].elapsed_time(evs[j][1]) * 1e3 for j in range(nseg)])
-    seg_mean = np.array(seg).mean(axis=0)
+    seg_med = np.mean(np.array(seg), axis=0)  # mean: event timestamps advance in 1.024 us steps
     pk = peaks()
 
-    sweep = []
-    for j, (M, name, K, N, li) in enumerate(calls):
-        b = linear_bytes(M, N, K)
-        us = float(seg_mean[j])
-        gbs = b / (us * 1e-6) / 1e9
-        tflops = 2.0 * M * N * K / (us * 1e-6) / 1e12
-        sweep.append({"shape": name, "M": M, "K": K, "N": N, "us": round(us, 2), "GB_s": round(gbs, 1),
-                      "TFLOP_s": round(tflops, 2), "frac_hbm": round(gbs / pk["hbm_gbs"], 3)})
-    acc_us, tree_us = float(seg_mean[len(calls)]), float(seg_mean[len(calls) + 1])
+    acc_us, tree_us = float(seg_med[len(calls)]), float(seg_med[len(calls) + 1])
     ab, tb = accept_bytes_seq(ACC_B, ACC_K, VOCAB), accept_bytes_tree(TREE_B, TREE_N, VOCAB)
-    accept = {"seq_us": round(acc_us, 2), "seq_GB_s": round(ab / (acc_us * 1e-6) / 1e9, 1),
-              "seq_frac_hbm": round(ab / (acc_us * 1e-6) / 1e9 / pk["hbm_gbs"], 3),
-              "tree_us": round(tree_us, 2), "tree_GB_s": round(tb / (tree_us * 1e-6) / 1e9, 1),
-              "tree_frac_hbm": round(tb / (tree_us * 1e-6) / 1e9 / pk["hbm_gbs"], 3)}
-    per_m = {}
-    for M in STEP_MS:
-        sel = [s for s in sweep if s["M"] == M]
-        us = sum(s["us"] for s in sel)
-        b = sum(linear_bytes(M, s["N"], s["K"]) for s in sel)
-        per_m[str(M)] = {"layer_us": round(us, 2), "GB_s": round(b / (us * 1e-6) / 1e9, 1),
-                         "frac_hbm": round(b / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 3)}
     # per kernel (all launches of the step): time, algorithmic bytes, roofline fraction
     groups = {
-        "w4a16_skinny_kernel<1> (M<16)": [(linear_bytes(M, N, K), float(seg_mean[j]))
-                                          for j, (M, name, K, N, li) in enumerate(calls) if M < 16],
-        "w4a16_tc_kernel<64> (M>=16)": [(linear_bytes(M, N, K), float(seg_mean[j]))
+        "w4a16_skinny_kernel (M<16)": [(linear_bytes(M, N, K), float(seg_med[j]))
+                                       for j, (M, name, K, N, li) in enumerate(calls) if M < 16],
+        "w4a16_tc_kernel<64> (M>=16)": [(linear_bytes(M, N, K), float(seg_med[j]))
                                         for j, (M, name, K, N, li) in enumerate(calls) if M >= 16],
         "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": [(ab, acc_us)],
         "accept_argmax_kernel": [(tb, tree_us)],
@@ -358,55 +485,35 @@ def run_ours(args):
     dom = per_kernel[dominant]
     dom_launch_bytes = dom["bytes"] / dom["launches_per_step"]
     traffic = NCU_DRAM_BYTES_PER_LAUNCH.get(dominant)
+    step_calls = [{"shape": name, "M": M, "us": round(float(seg_med[j]), 2),
+                   "frac_hbm": round(linear_bytes(M, N, K) / float(seg_med[j]) / 1e3 / pk["hbm_gbs"], 3)}
+                  for j, (M, name, K, N, li) in enumerate(calls)]
 
-    # ---- full 80-layer + lm_head verify forward at M = 1 / 4 / 64 (outside the timed step)
-    stack = None
-    if args.stack:
-        stack = {}
-        sx = {M: {K: torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16) for K in (8192, 28672)}
-              for M in STEP_MS}
-        souts = {M: {name: torch.empty((M, N), dtype=torch.bfloat16, device=device)
-                     for name, K, N in SHAPES + [LM_HEAD]} for M in STEP_MS}
+    # ---- per-call sweep and accept (L2 flushed before each call), outside the timed step
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = lambda: flush_buf.zero_()
+    sweep, accept = (run_sweep(sv, torch, device, gen, layers, pk, flush) if args.sweep else ([], []))
+    del flush_buf
 
-        def forward(M):
-            for li in range(N_LAYERS):
-                for name, K, N in SHAPES:
-                    sv.linear(sx[M][K], layers[li][name], out=souts[M][name], ws=wss[M])
-            sv.linear(sx[M][8192], lm_head, out=souts[M]["lm_head"], ws=wss[M])
-
-        stack_bytes = {M: N_LAYERS * sum(linear_bytes(M, N, K) for _, K, N in SHAPES)
-                       + linear_bytes(M, LM_HEAD[2], LM_HEAD[1]) for M in STEP_MS}
-        for M in STEP_MS:
-            forward(M)
-            torch.cuda.synchronize()
-            gm = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gm):
-                forward(M)
-            gm.replay()
-            gm.replay()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            reps = 5
-            e0.record(stream)
-            for _ in range(reps):
-                gm.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            del gm
-            us = e0.elapsed_time(e1) * 1e3 / reps
-            gbs = stack_bytes[M] / (us * 1e-6) / 1e9
-            stack[str(M)] = {"us": round(us, 1), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
-                             "tokens_per_s": round(M / (us * 1e-6), 1)}
-        stack["ratio_m64_m1"] = round(stack["64"]["us"] / stack["1"]["us"], 3)
-        stack["ratio_m4_m1"] = round(stack["4"]["us"] / stack["1"]["us"], 3)
-        stack["weights_GB"] = round(stack_bytes[1] / 1e9, 2)
-        _check(sv, "the stack forward")
+    # ---- the full verify forward (outside the timed step)
+    stack = run_stack(sv, torch, device, gen, layers, lm_head, pk, stream) if args.stack else None
 
     # ---- end to end: host buffers, H2D of the step's inputs and D2H of its results inside the timing
-    e2e = run_e2e(sv, torch, device, stream, calls, layers, wss, (p_np, q_np, d_np, u_np), (tp_np, td_np, tpar_np),
+    e2e = run_e2e(sv, torch, device, calls, layers, wss, (p_np, q_np, d_np, u_np), (tp_np, td_np, tpar_np),
                   acc_ws, acc_ws2, args)
 
     ms_per_step = total_ms / args.steps
+    summary = {"step_calls_us": {f"{c['shape']}/M{c['M']}": c["us"] for c in step_calls}}
+    if sweep:
+        summary["linear_frac_hbm"] = {f"{r['shape']}/M{r['M']}": r["frac_hbm"] for r in sweep
+                                      if r["M"] in (1, 4, 8, 64)}
+        summary["linear_ratio_m64_m1"] = {r["shape"]: r["ratio_to_m1"] for r in sweep if r["M"] == 64}
+        summary["accept"] = {(f"seq K={a['K']}" if "K" in a else "tree"): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
+                             for a in accept}
+    if stack:
+        summary["stack_us"] = {m: v["us"] for m, v in stack.items() if isinstance(v, dict)}
+        summary["stack_frac_hbm"] = {m: v["frac_hbm"] for m, v in stack.items() if isinstance(v, dict)}
+        summary["stack_ratio_m64_m1"] = stack["ratio_m64_m1"]
     line = {
         "metric": METRIC,
         "value": round(ms_per_step * 1e3, 2),
@@ -425,26 +532,28 @@ def run_ours(args):
             "workload": "Llama-3-70B verify linears (QKV/O/gate-up/down) at M=1,4,64 + spec_accept seq "
                         "(B=16,K=4,V=128256) + greedy tree (B=16,64 nodes,V=128256)",
             "weights_int4": "g128, fp16 scales, 8 nibbles/uint32",
-            "l2": "inputs larger than L2: 1.32 GB of distinct weights streamed per step",
+            "l2": "step: inputs larger than L2 (1.32 GB of distinct weights per step); per-call sweep: "
+                  "linear calls rotate weight copies (> 3x L2), accept calls after a 256 MB L2 flush",
             "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
         },
-        "sweep": sweep,
-        "per_m_layer": per_m,
-        "accept": accept,
-        "stack_verify_forward": stack,
-        "per_kernel": per_kernel,
         "roofline": {"bound": "hbm", "kernel": dominant,
                      "achieved": dom["GB_s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": dom["frac_hbm"],
                      "traffic": traffic,
                      "algorithmic_bytes_per_launch": int(dom_launch_bytes),
                      "peak_source": pk["source"] + " (copy bandwidth)"},
+        "per_kernel": per_kernel,
+        "summary": summary,
         "clocks": clk,
         "gpu_launches": n_launch_per_step * args.steps,
         "e2e": e2e,
     }
     if rank == 0 and args.cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample(sample_cols=args.cpu_cols)
+        line["cpu_baseline"] = cpu_baseline(sample_cols=args.cpu_cols)
+    if rank == 0 and args.detail:
+        with open(args.detail, "w") as f:
+            json.dump({"line": line, "step_calls": step_calls, "sweep": sweep, "accept": accept, "stack": stack,
+                       "peaks": pk}, f, indent=1)
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
@@ -452,7 +561,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(sv, torch, device, stream, calls, layers, wss, acc_np, tree_np, acc_ws, acc_ws2, args):
+def run_e2e(sv, torch, device, calls, layers, wss, acc_np, tree_np, acc_ws, acc_ws2, args):
     """The same step through the public API with pinned host inputs and outputs."""
     cpu_gen = torch.Generator().manual_seed(4321)
     h_x = {(M, name): torch.randn((M, K), generator=cpu_gen).to(torch.bfloat16).pin_memory()
@@ -498,15 +607,19 @@ def run_e2e(sv, torch, device, stream, calls, layers, wss, acc_np, tree_np, acc_
 
 # ------------------------------------------------------- CPU oracle baseline
 
-def cpu_baseline_sample(sample_cols=64, seed=0):
+def cpu_baseline_sample(sample_cols=None, seed=0):
     """The oracle (plain C, fp64, OpenMP over output columns) on a bounded
-    sample of one step: `sample_cols` output columns of each of the 12 linear
-    calls (extrapolated to all N columns) plus the full accept and tree steps."""
+    sample of one step with the thread count in effect: `sample_cols` output
+    columns of each of the 12 linear calls, their measured time scaled by
+    N / sample_cols (labelled extrapolated), plus the full accept and tree
+    steps."""
     import oracle
 
     oracle.build()
-    t_lin = 0.0
-    g = synth.rng(seed)
+    threads = oracle.num_threads()
+    if sample_cols is None:
+        sample_cols = max(64, 4 * threads)  # every thread gets output columns
+    t_lin = t_lin_measured = 0.0
     for M in STEP_MS:
         for name, K, N in SHAPES:
             # only the sampled rows of W are generated and quantised (the rest do not enter the sample)
@@ -516,7 +629,9 @@ def cpu_baseline_sample(sample_cols=64, seed=0):
             cols = np.arange(sample_cols, dtype=np.int64)
             t = time.perf_counter()
             oracle.linear_cols(x, qw, sc, cols)
-            t_lin += (time.perf_counter() - t) * (N / sample_cols)
+            dt = time.perf_counter() - t
+            t_lin_measured += dt
+            t_lin += dt * (N / sample_cols)
     p, q, d, u = synth.accept_seq_case(ACC_B, ACC_K, VOCAB, seed=seed + 1)
     t = time.perf_counter()
     oracle.spec_accept_seq(p, q, d, u)
@@ -526,10 +641,27 @@ def cpu_baseline_sample(sample_cols=64, seed=0):
     oracle.greedy_tree(tp, td, tpar)
     t_tree = time.perf_counter() - t
     total_us = (t_lin + t_acc + t_tree) * 1e6
-    return {"value": round(total_us, 1), "unit": "us/step", "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": round(total_us, 1), "unit": "us/step", "cores": threads, "kind": "oracle",
+            "extrapolated": True,
             "sample": f"{sample_cols} output columns of each of the 12 linear calls (time scaled by N/"
                       f"{sample_cols}) + full accept (B=16,K=4) + full greedy tree (B=16,64 nodes)",
+            "sample_measured_us": round((t_lin_measured + t_acc + t_tree) * 1e6, 1),
             "linear_us": round(t_lin * 1e6, 1), "accept_us": round(t_acc * 1e6, 1), "tree_us": round(t_tree * 1e6, 1)}
+
+
+def cpu_baseline(sample_cols=None):
+    """The oracle on every host core (the reported baseline) and on one thread."""
+    import oracle
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    oracle.set_num_threads(1)
+    one = cpu_baseline_sample(sample_cols=sample_cols)
+    oracle.set_num_threads(cores)
+    allc = cpu_baseline_sample(sample_cols=sample_cols)
+    allc["single_thread"] = {k: one[k] for k in ("value", "cores", "sample_measured_us", "linear_us", "accept_us",
+                                                  "tree_us")}
+    return allc
 
 
 def run_reference(args):
@@ -538,10 +670,12 @@ def run_reference(args):
         return
     for _ in range(args.warmup):
         cpu_baseline_sample(sample_cols=args.cpu_cols)
-    vals = []
+    vals, measured = [], []
     t = time.perf_counter()
     for s in range(args.steps):
-        vals.append(cpu_baseline_sample(sample_cols=args.cpu_cols, seed=s)["value"])
+        r = cpu_baseline_sample(sample_cols=args.cpu_cols, seed=s)
+        vals.append(r["value"])
+        measured.append(r["sample_measured_us"])
     wall = time.perf_counter() - t
     v = float(np.mean(vals))
     last = cpu_baseline_sample(sample_cols=args.cpu_cols)
@@ -551,8 +685,10 @@ def run_reference(args):
             "config": {"workload": "Llama-3-70B verify linears (QKV/O/gate-up/down) at M=1,4,64 + spec_accept seq "
                                    "(B=16,K=4,V=128256) + greedy tree (B=16,64 nodes,V=128256)",
                        "parallelism": "CPU oracle, host cores"},
+            "extrapolated": True,
+            "sample_measured_us_per_step": round(float(np.mean(measured)), 1),
             "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": last["cores"], "kind": "oracle",
-                             "sample": last["sample"]},
+                             "sample": last["sample"], "extrapolated": True},
             "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(wall, 1)}
     print(json.dumps(line))
@@ -565,8 +701,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-stack", dest="stack", action="store_false")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-cols", type=int, default=64)
+    ap.add_argument("--cpu-cols", type=int, default=None,
+                    help="output columns of each linear in the CPU oracle sample (default max(64, 4 x threads))")
+    ap.add_argument("--detail", default=None, help="write every measurement as JSON to this path")
     ap.add_argument("--only", choices=["linear", "accept", "tree"], default=None,
                     help="profiling mode: run one kind of launch eagerly, print no contract line")
     ap.add_argument("--shape", default="gate_up", choices=[n for n, _, _ in SHAPES])

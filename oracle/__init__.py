@@ -71,6 +71,8 @@ def lib():
             L.oracle_greedy_chain.argtypes = [_P(np.float32), _P(np.int32), i32, i32, i32, _P(np.int32),
                                               _P(np.int32)]
             L.oracle_num_threads.restype = ctypes.c_int
+            L.oracle_set_num_threads.argtypes = [ctypes.c_int]
+            L.oracle_set_num_threads.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -81,6 +83,11 @@ def _c(a, dt):
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops from now on; returns the count in effect."""
+    return int(lib().oracle_set_num_threads(int(n)))
 
 
 def bf16_round(f: float) -> int:

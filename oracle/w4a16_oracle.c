@@ -345,6 +345,20 @@ void oracle_greedy_chain(const float* p, const int32_t* draft, int B, int K, int
     }
 }
 
+/* Threads the parallel loops use from now on (the timed CPU baseline runs
+ * once on one thread and once on every host core); returns the new count. */
+int oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    extern void omp_set_num_threads(int);
+    extern int omp_get_max_threads(void);
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

@@ -22,14 +22,17 @@ Readings (the pages give no cost model):
 * Draft tokens are accepted independently with probability alpha, so the
   accepted run of a K-token sequence draft is geometric truncated at K, and
   the target always adds one token (the corrected draw or the extra token).
-* The verify time at an M between two measured token counts is interpolated
-  linearly; outside the measured range it is not extrapolated.
+* The verify time is read at measured token counts (bench.py measures the
+  stack at M = 1, 4, 5, 9, 16, 32, 48, 64, i.e. at K + 1 for K = 4 and 8 and at
+  the tree sizes); between two measured counts it is interpolated linearly
+  (used only for counts the bench did not measure), never extrapolated.
 * A tree draft's tokens per verification (tau) depends on the drafter and the
   tree, which no synthetic input fixes, so the model reports the break-even
   tau: what the tree must yield to match a sequence draft.
 
 Usage: python -m speculative_decode_verify_w4a16_gb300.cost_model BENCH.json
-(one JSON line of bench.py with its `stack_verify_forward` figures).
+(one JSON line of bench.py with its stack figures, or the file bench.py
+--detail writes).
 """
 from __future__ import annotations
 
@@ -134,9 +137,16 @@ def table(times: Mapping[int, float], alphas=(0.7, 0.8, 0.9), Ks=(4, 8), draft_p
 
 
 def times_from_bench(line: Mapping) -> dict[int, float]:
-    """{M: microseconds} of the verify stack from one bench.py JSON line."""
-    st = line["stack_verify_forward"]
-    out = {int(k): float(v["us"]) for k, v in st.items() if k.isdigit()}
+    """{M: microseconds} of the verify stack from a bench.py JSON line
+    (summary.stack_us), the --detail file (stack) or an older line
+    (stack_verify_forward)."""
+    if "line" in line and isinstance(line.get("stack"), Mapping):
+        st = {k: v["us"] for k, v in line["stack"].items() if isinstance(v, Mapping)}
+    elif "summary" in line and "stack_us" in line["summary"]:
+        st = line["summary"]["stack_us"]
+    else:
+        st = {k: v["us"] for k, v in line["stack_verify_forward"].items() if isinstance(v, Mapping)}
+    out = {int(k): float(v) for k, v in st.items() if str(k).isdigit()}
     if 1 not in out:
         raise ValueError("the bench line has no M = 1 stack time")
     if any(not math.isfinite(v) or v <= 0 for v in out.values()):
@@ -154,7 +164,11 @@ def main(argv=None) -> int:
     ap.add_argument("--nodes", type=int, default=64)
     args = ap.parse_args(argv)
     with open(args.bench_json) as f:
-        line = json.loads(f.readline())
+        text = f.read()
+    try:
+        line = json.loads(text)
+    except json.JSONDecodeError:
+        line = json.loads(text.splitlines()[0])
     times = times_from_bench(line)
     print(json.dumps({"verify_us": times, "rows": table(times, draft_per_token=args.draft_per_token,
                                                        nodes=args.nodes, tree_draft_cost=args.tree_draft_cost)}))

@@ -134,14 +134,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// Warm L2 with [src, src + bytes) (16-byte aligned, bytes a multiple of 16).
-// L2 is the device's point of coherence, so a prefetch may be issued before
-// the kernel has waited for the grid it depends on: a later read still sees
-// any write that grid makes.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ------------------------------------------------- programmatic dependent launch
 // Kernels are launched with programmatic stream serialisation: they may start
 // while the previous kernel on the stream is still running. Everything that
@@ -175,6 +167,18 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
       "mov.b64 {%0, %1}, rd;\n\t}"
       : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// (d0, d1) = (a0 * b0, a1 * b1): two IEEE fp32 multiplies (round to nearest)
+// in one instruction.
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 

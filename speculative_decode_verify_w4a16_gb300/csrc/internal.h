@@ -54,12 +54,7 @@ cudaError_t launch_quantize(const float* w, int64_t N, int64_t K, uint32_t* qwei
 cudaError_t launch_prepack(const uint32_t* qweight, const uint16_t* scales, int64_t N, int64_t K,
                            uint32_t* qw_packed, uint16_t* sc_packed, cudaStream_t stream);
 
-// ---- token pre-pass of the fragment path (fp16 tokens, group sums, row exponents)
-cudaError_t launch_xprep(const void* x, int M, int64_t K, int MP, void* xh, float* xs, int* xe,
-                         cudaStream_t stream);
-
-// ---- linear (tensor-core fragments via mma.sync; M < 16; items of contiguous units)
-constexpr int kSkTokenStride = 16;  // tokens per group record of the pre-pass (M <= 15)
+// ---- linear (tensor-core fragments via mma.sync; M <= 8; items of contiguous units)
 struct SkinnyPlan {
   int mt8 = 0;          // ceil(M / 8)
   int64_t units = 0;    // (N/128) * (K/128)
@@ -67,8 +62,6 @@ struct SkinnyPlan {
   ItemSched sched = {};
   size_t counter_bytes = 0;
   size_t partial_bytes = 0;
-  size_t xh_off = 0, xs_off = 0, xe_off = 0;  // pre-pass outputs (from the workspace start)
-  size_t total_bytes = 0;
   size_t smem_bytes = 0;
 };
 cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes,
@@ -79,7 +72,7 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
                           cudaStream_t stream);
 
 // ---- linear on tcgen05 / TMEM (M >= kTcMinM)
-constexpr int kTcMinM = 16;
+constexpr int kTcMinM = 9;
 struct TcPlan {
   int nt = 0;           // MMA N: M rounded up to a multiple of 16
   int64_t units = 0;

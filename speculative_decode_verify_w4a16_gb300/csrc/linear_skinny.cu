@@ -1,5 +1,5 @@
-// W4A16 verify linear, tensor-core fragment path (mma.sync m16n8k16 f16),
-// for the sequence-draft token counts (M = 1..15).
+// W4A16 verify linear, tensor-core fragment path (mma.sync m16n8k16 bf16),
+// for the sequence-draft token counts (M = 1..8).
 //
 // out[M][N] = bf16(x[M][K] . W^T) with W = code * scale (int4, group 128).
 // Work split: the (row-tile, group) units of the packed weight stream are cut
@@ -15,19 +15,13 @@
 // together (four independent CTAs per SM let the hardware's oldest-first
 // scheduling starve the youngest, which then finished far behind). The
 // groups' sums of a segment meet in shared memory, group 0 stores the tile.
-//
-// Dequantisation is one AND per pair of codes: the offset-binary code
-// o = c + 8 of a nibble at bits 0-3 (16-19) of a 16-bit half is the fp16
-// subnormal o * 2^-24, and one at bits 4-7 (20-23) is 16 * o * 2^-24, so a
-// packed word gives its four A-fragment registers with one shift and four
-// masks (the packed layout puts rows r and r + 8 of a 16-row MMA tile in the
-// low and high nibble of each byte; the tensor cores take fp16 subnormal
-// operands exactly). The tokens are the fp16 copy x * 2^-e_m made by the
-// pre-pass (xprep.cu). The MMA (swap-AB: weight rows are the MMA's M
-// dimension, tokens its N = 8) accumulates each 128-wide group in fp32; the
-// epilogue removes the offset (2^-24 h * 8 * sum x, h = 1 or 16 by row half,
-// from the pre-pass) and applies the fp16 group scale once, in fp32; the
-// store multiplies by 2^(24 + e_m) / h.
+// A consumer dequantises 16 packed words per unit into
+// exact bf16 codes (offset-binary nibble OR'ed into the mantissa of 128.0,
+// then 136 subtracted: a bit trick in the spirit of Kim et al. 2022, "Who
+// Says Elephants Can't Run", arXiv:2211.10017), multiplies them with the
+// token fragments on the tensor cores (swap-AB: weight rows are the MMA's M
+// dimension, tokens its N = 8), accumulates the group in fp32 and applies
+// the fp16 group scale once in fp32.
 //
 // A tile covered by one item is stored directly; a tile whose K range is
 // split between items is finished by its last contributor, which adds the
@@ -64,10 +58,7 @@ struct SkinnyLayout {
   static constexpr int kW = kGroups * kUnitBytes;       // codes of the stage's units
   static constexpr int kS = kGroups * kUnitScaleBytes;  // their scales
   static constexpr int kX = MT8 * 8 * kXRowStride;      // token rows
-  // the units' offset records: per group, kSkTokenStride fp32 token sums
-  static constexpr int kXsBytes = kGroups * kSkTokenStride * 4;
-  static constexpr int kXs = (kXsBytes + 127) / 128 * 128;
-  static constexpr int kStage = kW + kS + kX + kXs;
+  static constexpr int kStage = kW + kS + kX;
   // group sums of a segment end, double-buffered: [2][group 1..3][slice][2*MT8 float4][32 lanes]
   static constexpr int kRedSlot = 2 * MT8 * 32 * 16;
   static constexpr int kRedOff = kStages * kStage;
@@ -75,16 +66,13 @@ struct SkinnyLayout {
   static constexpr int kBarOff = kMetaOff + kStages * 16;
   // full[stages], empty[stages], red_full[2], red_empty[2]
   static constexpr int kTotal = kBarOff + (2 * kStages + 4) * 8;
-  static_assert(kStage % 128 == 0 && kW % 16 == 0 && (kW + kS) % 16 == 0 && kXRowStride % 128 == 32 &&
-                    (kW + kS + kX) % 16 == 0,
+  static_assert(kStage % 128 == 0 && kW % 16 == 0 && (kW + kS) % 16 == 0 && kXRowStride % 128 == 32,
                 "stage alignment");
   static_assert(kTotal <= 227 * 1024, "shared memory");
 };
 
 struct SkinnyParams {
-  const __half* xh;  // fp16 tokens x * 2^-e_m [M][K] (pre-pass)
-  const float* xs;   // offset records [G][kSkTokenStride] (pre-pass)
-  const int* xe;     // row exponents e_m [kSkTokenStride] (pre-pass)
+  const __nv_bfloat16* x;
   const uint8_t* qw;
   const uint8_t* sc;
   __nv_bfloat16* out;
@@ -98,43 +86,52 @@ struct SkinnyParams {
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One packed word (8 offset-binary nibbles) -> the four fp16x2 A-fragment
-// registers: a[0] (row gid, k 4c..4c+1) and a[2] (row gid, k 4c+2..4c+3) hold
-// o * 2^-24; a[1] and a[3] (row gid + 8, same k) hold 16 * o * 2^-24.
-__device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t w8 = w >> 8;
-  a[0] = w & 0x000F000Fu;
-  a[1] = w & 0x00F000F0u;
-  a[2] = w8 & 0x000F000Fu;
-  a[3] = w8 & 0x00F000F0u;
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));  // (a & b) | c
+  return d;
 }
 
-// acc (rows gid: 2^-24 * sum c x' * s; rows gid + 8: 16 times that) -> bf16
-// outputs x . W^T, i.e. times 2^(24 + e_m) and 2^(20 + e_m).
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 8 offset-binary nibbles -> four bf16x2 registers of exact signed codes:
+// (nibble | 0x4300) is the bf16 value 128 + c, and (128 + c) * 1 - 136 = c - 8.
+__device__ __forceinline__ void dequant8(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t mask = 0x000F000Fu, magic = 0x43004300u;
+  const uint32_t one = 0x3F803F80u, neg136 = 0xC308C308u;
+  a[0] = fma_bf16x2(lop3_and_or(w, mask, magic), one, neg136);
+  a[1] = fma_bf16x2(lop3_and_or(w >> 4, mask, magic), one, neg136);
+  a[2] = fma_bf16x2(lop3_and_or(w >> 8, mask, magic), one, neg136);
+  a[3] = fma_bf16x2(lop3_and_or(w >> 12, mask, magic), one, neg136);
+}
+
 template <int MT8>
 __device__ __forceinline__ void store_tile(const SkinnyParams& p, int64_t t, int warp, int lane,
                                            const float (&acc)[2][MT8][4]) {
   const int gid = lane >> 2, cq = lane & 3;
 #pragma unroll
-  for (int nt = 0; nt < MT8; ++nt) {
-    const int m0 = nt * 8 + 2 * cq;  // < kSkTokenStride: the exponent table is padded
-    const int e0 = __ldcg(&p.xe[m0]), e1 = __ldcg(&p.xe[m0 + 1]);
+  for (int rt = 0; rt < 2; ++rt) {
+    const int64_t n_lo = t * kUnitRows + warp * 32 + rt * 16 + gid;
 #pragma unroll
-    for (int rt = 0; rt < 2; ++rt) {
-      const int64_t n_lo = t * kUnitRows + warp * 32 + rt * 16 + gid;
+    for (int nt = 0; nt < MT8; ++nt) {
+      const int m0 = nt * 8 + 2 * cq;
       if (m0 < p.M) {
-        p.out[(int64_t)m0 * p.N + n_lo] = __float2bfloat16_rn(ldexpf(acc[rt][nt][0], 24 + e0));
-        p.out[(int64_t)m0 * p.N + n_lo + 8] = __float2bfloat16_rn(ldexpf(acc[rt][nt][2], 20 + e0));
+        p.out[(int64_t)m0 * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][0]);
+        p.out[(int64_t)m0 * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][2]);
       }
       if (m0 + 1 < p.M) {
-        p.out[(int64_t)(m0 + 1) * p.N + n_lo] = __float2bfloat16_rn(ldexpf(acc[rt][nt][1], 24 + e1));
-        p.out[(int64_t)(m0 + 1) * p.N + n_lo + 8] = __float2bfloat16_rn(ldexpf(acc[rt][nt][3], 20 + e1));
+        p.out[(int64_t)(m0 + 1) * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][1]);
+        p.out[(int64_t)(m0 + 1) * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][3]);
       }
     }
   }
@@ -236,14 +233,6 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       mbar_init(&red_empty[b], kSkConsumerWarps);
     }
     fence_mbarrier_init();
-  } else if (threadIdx.x == 32 * kSkProducerWarp && (int)blockIdx.x < p.items) {
-    // The packed weights are not written by the kernel this one may overlap:
-    // pull the first units of this CTA's first item into L2.
-    const int64_t u0 = item_begin(p.sched, blockIdx.x);
-    int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
-    if (n > 2 * S * kSkGroups) n = 2 * S * kSkGroups;
-    prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
-    prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
   }
   // token rows M .. 8*MT8-1 of every stage are never copied: zero them once
   {
@@ -262,44 +251,76 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
     // A stage takes up to kSkGroups consecutive units of one tile segment of
     // the item: codes, scales and each token row's K range are contiguous in
     // global memory, so a stage is 2 + M bulk copies.
-    // CTA c takes items c, c + C, ... (C = grid size). The stage copies wait
-    // for the preceding grid (x may come from it; issuing the codes earlier
-    // and the token rows after would queue a stage's token rows behind
-    // several stages of codes, and the L2 prefetch above already moves the
-    // first units' codes during that grid's tail).
+    // CTA c takes items c, c + C, ... (C = grid size). The packed weights are
+    // never written by the kernel this one may overlap, so the first ring
+    // stages' codes and scales go out at once, before the grid dependency
+    // resolves; their token rows (x may come from that kernel) follow after
+    // it, on the same stage barrier. Measured in a CUDA graph of back-to-back
+    // verify linears, this beat both waiting first and an L2 prefetch of the
+    // first units (which delayed the first stage's own copies).
     if (lane != 0) return;
-    grid_dependency_wait();
     const uint64_t pol = policy_evict_first();
     int n_stage = 0;  // stages filled so far
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.items; item += gridDim.x) {
-      const int64_t ub = item_begin(p.sched, item);
-      const int64_t ue = item_begin(p.sched, item + 1);
-      for (int64_t u = ub; u < ue; ++n_stage) {
-        const int64_t t = u / p.G, g0 = u - t * p.G;
-        int64_t n = ue - u;
-        if (n > kSkGroups) n = kSkGroups;
-        if (n > p.G - g0) n = p.G - g0;
-        const int st = n_stage % S;
-        if (n_stage >= S && !mbar_wait(&empty[st], ((uint32_t)(n_stage / S) & 1u) ^ 1u, p.err)) {
-          ok = false;
-          break;
-        }
-        const int flags = (u == ub ? kStItemFirst : 0) | ((u == ub || g0 == 0) ? kStSegFirst : 0) |
-                          ((u + n == ue || g0 + n == p.G) ? kStSegLast : 0) | ((int)n << 8);
-        meta[st] = make_int4(item, (int)t, (int)g0, flags);
-        uint8_t* sb = smem + st * L::kStage;
-        const uint32_t nb = (uint32_t)n;
-        mbar_arrive_expect_tx(&full[st],
-                              nb * (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256 + kSkTokenStride * 4));
-        bulk_g2s_hint(sb, p.qw + u * kUnitBytes, nb * kUnitBytes, &full[st], pol);
-        bulk_g2s(sb + L::kW, p.sc + u * kUnitScaleBytes, nb * kUnitScaleBytes, &full[st]);
-        for (int m = 0; m < p.M; ++m)
-          bulk_g2s(sb + L::kW + L::kS + m * kXRowStride, p.xh + (int64_t)m * p.K + g0 * kGroup, nb * 256u, &full[st]);
-        bulk_g2s(sb + L::kW + L::kS + L::kX, p.xs + g0 * kSkTokenStride, nb * (uint32_t)(kSkTokenStride * 4),
+    int item = blockIdx.x;
+    int64_t ub = 0, ue = 0, u = 0;
+    if (item < p.items) {
+      ub = item_begin(p.sched, item);
+      ue = item_begin(p.sched, item + 1);
+      u = ub;
+    }
+    // one stage: up to kSkGroups units of the current tile segment; returns the units taken
+    auto stage_codes = [&](int st, int64_t& g0_out) -> int64_t {
+      const int64_t t = u / p.G, g0 = u - t * p.G;
+      int64_t n = ue - u;
+      if (n > kSkGroups) n = kSkGroups;
+      if (n > p.G - g0) n = p.G - g0;
+      const int flags = (u == ub ? kStItemFirst : 0) | ((u == ub || g0 == 0) ? kStSegFirst : 0) |
+                        ((u + n == ue || g0 + n == p.G) ? kStSegLast : 0) | ((int)n << 8);
+      meta[st] = make_int4(item, (int)t, (int)g0, flags);
+      uint8_t* sb = smem + st * L::kStage;
+      const uint32_t nb = (uint32_t)n;
+      mbar_arrive_expect_tx(&full[st], nb * (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256));
+      bulk_g2s_hint(sb, p.qw + u * kUnitBytes, nb * kUnitBytes, &full[st], pol);
+      bulk_g2s(sb + L::kW, p.sc + u * kUnitScaleBytes, nb * kUnitScaleBytes, &full[st]);
+      g0_out = g0;
+      return n;
+    };
+    auto stage_tokens = [&](int st, int64_t g0, int64_t n) {
+      uint8_t* sb = smem + st * L::kStage;
+      for (int m = 0; m < p.M; ++m)
+        bulk_g2s(sb + L::kW + L::kS + m * kXRowStride, p.x + (int64_t)m * p.K + g0 * kGroup, (uint32_t)n * 256u,
                  &full[st]);
-        u += n;
+    };
+    int64_t early_g0[S], early_n[S];
+    int n_early = 0;
+    while (n_early < S && item < p.items && u < ue) {
+      early_n[n_early] = stage_codes(n_early, early_g0[n_early]);
+      u += early_n[n_early];
+      ++n_early;
+      ++n_stage;
+    }
+    grid_dependency_wait();
+    for (int i = 0; i < n_early; ++i) stage_tokens(i, early_g0[i], early_n[i]);
+    while (ok && item < p.items) {
+      if (u >= ue) {  // next item of this CTA
+        item += gridDim.x;
+        if (item >= p.items) break;
+        ub = item_begin(p.sched, item);
+        ue = item_begin(p.sched, item + 1);
+        u = ub;
+        continue;
       }
+      const int st = n_stage % S;
+      if (n_stage >= S && !mbar_wait(&empty[st], ((uint32_t)(n_stage / S) & 1u) ^ 1u, p.err)) {
+        ok = false;
+        break;
+      }
+      int64_t g0;
+      const int64_t n = stage_codes(st, g0);
+      stage_tokens(st, g0, n);
+      u += n;
+      ++n_stage;
     }
     if (ok) {  // stop marker for the consumers
       const int st = n_stage % S;
@@ -348,10 +369,6 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
 #pragma unroll
         for (int h = 0; h < 2; ++h) wq[rt][h] = lds128(wb + (rt * 2 + h) * 512);
       const uint2 sc2 = lds64(sb + L::kW + grp * kUnitScaleBytes + (q * 8 + gid) * 8);
-      uint2 xsv[MT8];  // offset sums of this unit's group for tokens m0, m0 + 1 of each token tile
-#pragma unroll
-      for (int nt = 0; nt < MT8; ++nt)
-        xsv[nt] = lds64(sb + L::kW + L::kS + L::kX + grp * (kSkTokenStride * 4) + (nt * 8 + 2 * cq) * 4);
 
       float part[2][MT8][4];
 #pragma unroll
@@ -387,10 +404,6 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
         for (int nt = 0; nt < MT8; ++nt) {
-          // remove the code offset (h * 2^-24 * 8 * sum x'), then scale: acc += s * (part - h * xs)
-          const float xs0 = __uint_as_float(xsv[nt].x), xs1 = __uint_as_float(xsv[nt].y);
-          ffma2(part[rt][nt][0], part[rt][nt][1], -1.0f, -1.0f, xs0, xs1);
-          ffma2(part[rt][nt][2], part[rt][nt][3], -16.0f, -16.0f, xs0, xs1);
           ffma2(acc[rt][nt][0], acc[rt][nt][1], sc[rt][0], sc[rt][0], part[rt][nt][0], part[rt][nt][1]);
           ffma2(acc[rt][nt][2], acc[rt][nt][3], sc[rt][1], sc[rt][1], part[rt][nt][2], part[rt][nt][3]);
         }
@@ -472,7 +485,7 @@ static cudaError_t skinny_occupancy_dispatch(int mt8, int* nb) {
 cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes,
                         SkinnyPlan* plan) {
   static int cached_nb[64][3];  // [device][mt8] blocks per SM (0 = unknown)
-  if (M < 1 || M >= kTcMinM) return cudaErrorInvalidValue;  // M >= 16 runs on the tcgen05 path
+  if (M < 1 || M >= kTcMinM) return cudaErrorInvalidValue;  // M >= 9 runs on the tcgen05 path
   plan->mt8 = (M + 7) / 8;
   plan->units = (N / kUnitRows) * (K / kGroup);
   int nb = 0;
@@ -496,16 +509,11 @@ cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size
   plan->sched = make_item_sched(plan->units, (int)ctas, 1, 1);
   plan->counter_bytes = kCounterRegionBytes;
   plan->partial_bytes = (size_t)plan->sched.R * ctas * per_item;
-  auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
-  plan->xh_off = up256(plan->counter_bytes + plan->partial_bytes);
-  plan->xs_off = plan->xh_off + up256((size_t)M * K * 2);
-  plan->xe_off = plan->xs_off + up256((size_t)(K / kGroup) * kSkTokenStride * 4);
-  plan->total_bytes = plan->xe_off + 256;
   plan->smem_bytes = (size_t)skinny_smem(plan->mt8);
   return cudaSuccess;
 }
 
-size_t skinny_workspace_bytes(const SkinnyPlan& plan) { return plan.total_bytes; }
+size_t skinny_workspace_bytes(const SkinnyPlan& plan) { return plan.counter_bytes + plan.partial_bytes; }
 
 template <int MT8>
 static cudaError_t launch_skinny_t(const SkinnyParams& p, const SkinnyPlan& plan, cudaStream_t stream) {
@@ -517,14 +525,8 @@ static cudaError_t launch_skinny_t(const SkinnyParams& p, const SkinnyPlan& plan
 cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
                           void* out, void* workspace, const SkinnyPlan& plan, const DeviceInfo& dev,
                           cudaStream_t stream) {
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t e = launch_xprep(x, M, K, kSkTokenStride, ws + plan.xh_off, reinterpret_cast<float*>(ws + plan.xs_off),
-                               reinterpret_cast<int*>(ws + plan.xe_off), stream);
-  if (e != cudaSuccess) return e;
   SkinnyParams p;
-  p.xh = reinterpret_cast<const __half*>(ws + plan.xh_off);
-  p.xs = reinterpret_cast<const float*>(ws + plan.xs_off);
-  p.xe = reinterpret_cast<const int*>(ws + plan.xe_off);
+  p.x = static_cast<const __nv_bfloat16*>(x);
   p.qw = static_cast<const uint8_t*>(qw_packed);
   p.sc = static_cast<const uint8_t*>(sc_packed);
   p.out = static_cast<__nv_bfloat16*>(out);

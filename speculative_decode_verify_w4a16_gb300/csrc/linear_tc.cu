@@ -316,15 +316,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   grid_launch_dependents();
-  if (warp == kTcProducerWarp && lane == 0 && (int)blockIdx.x < p.items) {
-    // The packed weights are not written by the kernel this one may overlap:
-    // pull the first units of this CTA's first item into L2.
-    const int64_t u0 = item_begin(p.sched, blockIdx.x);
-    int64_t n = item_begin(p.sched, blockIdx.x + 1) - u0;
-    if (n > 2 * L::kWStages) n = 2 * L::kWStages;
-    prefetch_l2(p.qw + u0 * kUnitBytes, (uint32_t)(n * kUnitBytes));
-    prefetch_l2(p.sc + u0 * kUnitScaleBytes, (uint32_t)(n * kUnitScaleBytes));
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < L::kWStages; ++s) {
       mbar_init(&wfull[s], 1);

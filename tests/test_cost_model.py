@@ -99,4 +99,8 @@ def test_table_and_cli(tmp_path):
     path = tmp_path / "bench.json"
     path.write_text(json.dumps(line) + "\n")
     assert cm.times_from_bench(line) == TIMES
+    # the current line's summary and the --detail file
+    assert cm.times_from_bench({"summary": {"stack_us": {str(m): t for m, t in TIMES.items()}}}) == TIMES
+    assert cm.times_from_bench({"line": {}, "stack": {str(m): {"us": t} for m, t in TIMES.items()}
+                                | {"ratio_m64_m1": 1.625}}) == TIMES
     assert cm.main([str(path)]) == 0
