@@ -88,6 +88,17 @@ __device__ __forceinline__ bool df_gt(DF a, DF b) {
   return d.hi > 0.0f || (d.hi == 0.0f && d.lo > 0.0f);
 }
 
+// exp(a - b) for fp32 a <= b, for the values that decide a draw: the
+// difference is formed exactly (TwoSum: hi + lo, |lo| <= 2^-24 |hi|), and
+// exp(hi + lo) = exp(hi) * (1 + lo) to within lo^2 / 2; exp(hi) is the
+// library's accurate expf (not the fast approximation, whose error grows with
+// |hi|).
+__device__ __forceinline__ float exp_diff(float a, float b) {
+  const DF d = two_sum(a, -b);
+  const float e = expf(d.hi);
+  return __fmaf_rn(e, d.lo, e);
+}
+
 struct RowStat {
   float m;
   float pad;
@@ -378,8 +389,8 @@ __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
       reject = true;
     } else {
       // alpha = min(1, P / Q) = min(1, (e_p * Z_q) / (e_q * Z_p)), fp32 (a few ulp)
-      const float ep = expf(__fsub_rn(sLp[i], sM[i]));
-      const float eq = expf(__fsub_rn(sLq[i], sM[n + 1 + i]));
+      const float ep = exp_diff(sLp[i], sM[i]);
+      const float eq = exp_diff(sLq[i], sM[n + 1 + i]);
       const float num = __fmul_rn(ep, df_val(sZ[n + 1 + i])), den = __fmul_rn(eq, df_val(sZ[i]));
       const float alpha = den > 0.0f ? fminf(1.0f, __fdiv_rn(num, den)) : 1.0f;
       reject = !(u[(int64_t)b * (n + 1) + i] < alpha);
@@ -410,11 +421,11 @@ struct ResidFn {
   const float* prow;  // P_r row logits (or P_{n+1} after full acceptance)
   const float* qrow;  // Q_r row logits, NULL after full acceptance
   float mp, ip, mq, iq;
-  __device__ __forceinline__ float pv_of(float lp) const { return __fmul_rn(__expf(__fsub_rn(lp, mp)), ip); }
+  __device__ __forceinline__ float pv_of(float lp) const { return __fmul_rn(exp_diff(lp, mp), ip); }
   __device__ __forceinline__ float rv_of(float lp, float lq) const {
     const float pv = pv_of(lp);
     if (!qrow) return pv;
-    const float qv = __fmul_rn(__expf(__fsub_rn(lq, mq)), iq);
+    const float qv = __fmul_rn(exp_diff(lq, mq), iq);
     return fmaxf(__fsub_rn(pv, qv), 0.0f);
   }
   __device__ __forceinline__ float pval(int x) const { return pv_of(prow[x]); }
