@@ -41,22 +41,29 @@ def _deps():
     return sorted(glob.glob(os.path.join(CSRC, "*"))) + [os.path.join(os.path.dirname(PKG), "include", "w4a16sv.h")]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
-        return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in _deps())
+# Debug build for the tests that make a kernel's bounded wait run out: a
+# separate library outside the package (the product never loads it) with a
+# 5 ms wait limit and the test hooks compiled in.
+DEBUG_LIB = os.path.join(os.path.dirname(PKG), "_build", "libw4a16sv_debug.so")
+DEBUG_FLAGS = ["-DW4A16_WAIT_LIMIT_NS=5000000ull", "-DW4A16_TEST_HOOKS=1"]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build_debug(force: bool = False) -> str:
+    """Build the debug library (see DEBUG_FLAGS) and return its path."""
+    return build(force=force, extra_flags=DEBUG_FLAGS, out=DEBUG_LIB,
+                 obj_dir=os.path.join(os.path.dirname(PKG), "_build", "w4a16sv_debug"))
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str = LIB, obj_dir: str = BUILD) -> str:
+    stale = not os.path.exists(out) or any(os.path.getmtime(f) > os.path.getmtime(out) for f in _deps())
+    if not force and not stale:
+        return out
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc] + ARCH + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,13 +74,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -13,8 +13,13 @@ namespace w4a16 {
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrInput = 2u;
 
-// Upper bound on any spin wait inside a kernel (ns of %globaltimer).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Upper bound on any spin wait inside a kernel (ns of %globaltimer). A
+// debug build of the library (for the tests that make a wait run out) sets
+// a few milliseconds instead.
+#ifndef W4A16_WAIT_LIMIT_NS
+#define W4A16_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kWaitLimitNs = W4A16_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;

@@ -36,6 +36,18 @@ namespace w4a16 {
 
 constexpr int kSkConsumerWarps = 4;  // warps of a group: one 32-row slice each
 
+#if W4A16_TEST_HOOKS
+// Debug builds only: the producer of CTA 0 leaves out the ring stage with
+// this index (no copies, no arrival), so that the consumers' bounded wait on
+// it runs out and the kernel reports a timeout. -1: off.
+__device__ int g_test_skip_stage = -1;
+__device__ __forceinline__ bool test_skip_stage(int n_stage) {
+  return blockIdx.x == 0 && n_stage == *(volatile int*)&g_test_skip_stage;
+}
+#else
+__device__ __forceinline__ bool test_skip_stage(int) { return false; }
+#endif
+
 
 // Stage metadata written by the producer: {item, tile, first group, flags | n << 8}
 constexpr int kStItemFirst = 1;  // the stage holds the item's first unit
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       u = ub;
     }
     // one stage: up to kSkGroups units of the current tile segment; returns the units taken
-    auto stage_codes = [&](int st, int64_t& g0_out) -> int64_t {
+    auto stage_codes = [&](int st, int64_t& g0_out, bool skip) -> int64_t {
       const int64_t t = u / p.G, g0 = u - t * p.G;
       int64_t n = ue - u;
       if (n > kSkGroups) n = kSkGroups;
@@ -278,12 +290,13 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       const int flags = (u == ub ? kStItemFirst : 0) | ((u == ub || g0 == 0) ? kStSegFirst : 0) |
                         ((u + n == ue || g0 + n == p.G) ? kStSegLast : 0) | ((int)n << 8);
       meta[st] = make_int4(item, (int)t, (int)g0, flags);
+      g0_out = g0;
+      if (skip) return n;
       uint8_t* sb = smem + st * L::kStage;
       const uint32_t nb = (uint32_t)n;
       mbar_arrive_expect_tx(&full[st], nb * (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256));
       bulk_g2s_hint(sb, p.qw + u * kUnitBytes, nb * kUnitBytes, &full[st], pol);
       bulk_g2s(sb + L::kW, p.sc + u * kUnitScaleBytes, nb * kUnitScaleBytes, &full[st]);
-      g0_out = g0;
       return n;
     };
     auto stage_tokens = [&](int st, int64_t g0, int64_t n) {
@@ -295,7 +308,7 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
     int64_t early_g0[S], early_n[S];
     int n_early = 0;
     while (n_early < S && item < p.items && u < ue) {
-      early_n[n_early] = stage_codes(n_early, early_g0[n_early]);
+      early_n[n_early] = stage_codes(n_early, early_g0[n_early], false);
       u += early_n[n_early];
       ++n_early;
       ++n_stage;
@@ -317,8 +330,9 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
         break;
       }
       int64_t g0;
-      const int64_t n = stage_codes(st, g0);
-      stage_tokens(st, g0, n);
+      const bool skip = test_skip_stage(n_stage);
+      const int64_t n = stage_codes(st, g0, skip);
+      if (!skip) stage_tokens(st, g0, n);
       u += n;
       ++n_stage;
     }
@@ -547,3 +561,10 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
 }
 
 }  // namespace w4a16
+
+#if W4A16_TEST_HOOKS
+// Debug builds only (not part of the C ABI header): see g_test_skip_stage.
+extern "C" int w4a16_test_set_skip_stage(int n_stage) {
+  return (int)cudaMemcpyToSymbol(w4a16::g_test_skip_stage, &n_stage, sizeof(int));
+}
+#endif

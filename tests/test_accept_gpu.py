@@ -16,8 +16,13 @@ import synth
 from helpers import dev
 
 pytestmark = pytest.mark.gpu
-NEAR_TIE = 1e-6       # |u_i - alpha_i|
-NEAR_TIE_CDF = 1e-6   # distance of u * S from the drawn token's interval ends, / S
+NEAR_TIE = 1e-6       # |u_i - alpha_i|: the task's bar
+# Distance of u * S from the drawn token's interval ends, / S. The GPU forms
+# each probability with the accurate expf of an exactly formed argument
+# (relative error ~1e-7, random across tokens) and sums in double-float, so
+# interval ends move by ~1e-9 of S on flat 130k-token distributions; no row
+# has differed at margins down to 1e-8 in the cases below.
+NEAR_TIE_CDF = 1e-8
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -62,13 +67,16 @@ def test_config_seq_full_vocab(K):
     assert tie.sum() == 0  # every row of the task's configuration is compared bit for bit
 
 
-def test_seq_flat_large_vocab_many_rows():
+@pytest.mark.parametrize("seed", range(8))
+def test_seq_flat_large_vocab_many_rows(seed):
     # flat target distributions over a large vocabulary put many CDF
-    # boundaries close to u * S: the residual and extra-token draws must still
-    # agree with the fp64 oracle on nearly every row
-    p, q, d, u = synth.accept_seq_case(256, 2, 130000, seed=55, p_std=2.0)
-    _, tie = _compare_seq(p, q, d, u, "B=256 K=2 V=130000 flat")
+    # boundaries close to u * S (mean token mass ~1e-5): the residual and
+    # extra-token draws must still agree with the fp64 oracle on all but a
+    # few per mille of the rows
+    p, q, d, u = synth.accept_seq_case(256, 2, 130000, seed=55 + 10 * seed, p_std=2.0)
+    _, tie = _compare_seq(p, q, d, u, f"B=256 K=2 V=130000 flat seed {seed}")
     print(f"compared {100.0 * (1 - tie.mean()):.2f} % of rows")
+    assert tie.mean() <= 0.01
 
 
 @pytest.mark.parametrize("B,K,V,seed", [(512, 4, 1000, 1), (300, 1, 2, 2), (200, 3, 5, 3), (64, 8, 50000, 4),
@@ -80,9 +88,9 @@ def test_seq_flat_large_vocab_many_rows():
 def test_seq_random_cases(B, K, V, seed):
     p, q, d, u = synth.accept_seq_case(B, K, V, seed=60 + seed, p_std=2.0)
     acc_r, tie = _compare_seq(p, q, d, u, f"B={B} K={K} V={V}")
-    # flat distributions over a large vocabulary put many CDF boundaries within
-    # 1e-6 of u * S; the rest of the rows still compare exactly
-    assert tie.mean() < 0.35
+    # flat distributions over a large vocabulary put CDF boundaries close to
+    # u * S; all but a few rows still compare exactly
+    assert tie.mean() < 0.01
 
 
 def test_seq_all_accepted_when_p_equals_q():
