@@ -52,6 +52,7 @@ SWEEP_MS = (1, 4, 8, 16, 32, 48, 64)
 STACK_MS = (1, 4, 5, 9, 16, 32, 48, 64)
 ACC_B, ACC_K, VOCAB = 16, 4, synth.LLAMA3_VOCAB
 ACC_KS = (4, 8)
+FUSED_KS = (3, 4)  # lm_head + accept chains at M = 64 and 80 (the linear takes M <= 80)
 TREE_B, TREE_N = 16, 64
 N_LAYERS = 80
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -294,7 +295,55 @@ def run_sweep(sv, torch, device, gen, layers, pk, flush):
     acc.append({"mode": "greedy tree", "B": TREE_B, "nodes": TREE_N, "V": VOCAB, "us": round(us, 2),
                 "GB_s": round(b / us / 1e3, 1), "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3)})
     _check(sv, "the accept sweep")
+    for Kd in FUSED_KS:
+        acc.append(run_fused_lm_head_accept(sv, torch, device, gen, pk, flush, Kd))
     return rows, acc
+
+
+def run_fused_lm_head_accept(sv, torch, device, gen, pk, flush, Kd):
+    """The lm_head of the verify pass feeding the stochastic accept (B = 16,
+    K drafts: M = 16 (K + 1) token rows), two ways: the plain linear (bf16 logits) then
+    spec_accept, which recomputes every target row's softmax statistics;
+    and linear_logits (fp32 logits + per-32-logit-slice max / sum-exp from the
+    epilogue) then spec_accept_prestat, whose statistics pass reads the draft
+    rows only. Each chain and each call timed alone (L2 flushed before each,
+    two lm_head weight copies alternating)."""
+    name, K, N = LM_HEAD
+    B = ACC_B
+    M = B * (Kd + 1)
+    wts = [make_weight(sv, torch, N, K, gen, device) for _ in range(2)]
+    x = torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16)
+    p, q, d, u = synth.accept_seq_case(B, Kd, N, seed=37)
+    pt, qt, dt, ut = (torch.from_numpy(a).to(device) for a in (p, q, d, u))
+    out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    logits = torch.empty((M, N), dtype=torch.float32, device=device)
+    stats = torch.empty((M, N // 32, 2), dtype=torch.float32, device=device)
+    lws = torch.zeros(max(sv.linear_workspace_bytes(M, N, K), sv.linear_logits_workspace_bytes(M, N, K)),
+                      dtype=torch.uint8, device=device)
+    aws = torch.zeros(sv.accept_workspace_bytes(B, Kd, N), dtype=torch.uint8, device=device)
+    a_out = [torch.empty(B, dtype=torch.int32, device=device) for _ in range(2)]
+    lg3, st3 = logits.view(B, Kd + 1, N), stats.view(B, Kd + 1, N // 32, 2)
+    plain_lin = lambda i: sv.linear(x, wts[i % 2], out=out, ws=lws)
+    plain_acc = lambda i: sv.spec_accept(pt, dt, q_logits=qt, uniforms=ut, accepted_len=a_out[0],
+                                         next_token=a_out[1], ws=aws)
+    fused_lin = lambda i: sv.linear_logits(x, wts[i % 2], logits=logits, stats=stats, ws=lws)
+    fused_acc = lambda i: sv.spec_accept_prestat(lg3, st3, dt, qt, ut, accepted_len=a_out[0],
+                                                 next_token=a_out[1], ws=aws)
+    t = {}
+    for key, fn in (("linear_bf16", plain_lin), ("spec_accept", plain_acc), ("linear_logits", fused_lin),
+                    ("spec_accept_prestat", fused_acc),
+                    ("chain_plain", lambda i: (plain_lin(i), plain_acc(i))),
+                    ("chain_fused", lambda i: (fused_lin(i), fused_acc(i)))):
+        t[key] = round(time_per_call(torch, fn, flush)[0], 2)
+    _check(sv, "the fused lm_head + accept comparison")
+    del wts
+    torch.cuda.empty_cache()
+    # bytes: the fused lm_head writes fp32 logits and the slice statistics;
+    # the prestat accept skips reading the B (K + 1) target rows in its statistics pass
+    return {"mode": "lm_head + stochastic accept", "B": B, "K": Kd, "V": N, "M": M, "us": t,
+            "saved_us": round(t["chain_plain"] - t["chain_fused"], 2),
+            "linear_logits_frac_hbm": round((linear_bytes(M, N, K) + M * N * 2 + M * (N // 32) * 8)
+                                            / t["linear_logits"] / 1e3 / pk["hbm_gbs"], 3)}
 
 
 def run_stack(sv, torch, device, gen, layers, lm_head, pk, stream):
@@ -509,7 +558,8 @@ def run_ours(args):
                                       if r["M"] in (1, 4, 8, 64)}
         summary["linear_ratio_m64_m1"] = {r["shape"]: r["ratio_to_m1"] for r in sweep if r["M"] == 64}
         summary["accept"] = {(f"seq K={a['K']}" if "K" in a else "tree"): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
-                             for a in accept}
+                             for a in accept if "frac_hbm" in a}
+        summary["lm_head_accept_us"] = {f"K={a['K']}": a["us"] for a in accept if a["mode"].startswith("lm_head")}
     if stack:
         summary["stack_us"] = {m: v["us"] for m, v in stack.items() if isinstance(v, dict)}
         summary["stack_frac_hbm"] = {m: v["frac_hbm"] for m, v in stack.items() if isinstance(v, dict)}

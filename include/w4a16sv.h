@@ -91,7 +91,7 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
  * each 128-wide group is accumulated in fp32 and scaled once in fp32.
  *
  *   x            device, bf16 [M][K] row-major, 16-byte aligned
- *   M            1 .. 64
+ *   M            1 .. 80
  *   K, N         multiples of 128, K >= 1024, N <= 2^20
  *   qweight_packed, scales_packed   from w4a16_prepack (device)
  *   out          device, bf16 [M][N] row-major
@@ -116,6 +116,35 @@ size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K);
 w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_packed,
                           const void* scales_packed, int64_t N, void* out, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * The target's lm_head for the verify pass with its softmax statistics
+ * fused into the epilogue ("Speculative Decoding Meets Quantization": the
+ * verify forward of the 4-bit target ends in the lm_head over every draft
+ * position; the tutorial page, section 3 Step 3: the acceptance test needs
+ * p = softmax of those logits). The accept step needs, per target row, the
+ * maximum and sum of exp(l - max) over the vocabulary and the logits at the
+ * drafted and drawn tokens. The epilogue produces the statistics of each
+ * 32-logit slice while the logits are still in registers, so
+ * spec_accept_prestat does not read the target rows to normalise them.
+ *
+ *   x, M, K, qweight_packed, scales_packed, N   as for w4a16_linear, with
+ *                M in 1 .. 80 (this call always runs on the tcgen05 kernel)
+ *   logits       device, fp32 [M][N] (4-byte aligned; 16-byte aligned lets
+ *                the kernel write whole tiles with TMA stores): x . W^T, the
+ *                fp32 sum unrounded
+ *   row_stats    device, fp32 pairs [M][N / 32] (8-byte aligned): for row m
+ *                and slice s, (max_j l, sum_j exp(l - max)) over the logits
+ *                l = logits[m][32 s + j], j = 0..31; the exponential within a
+ *                few ulp, the sum in fp32 (four partial sums over j mod 4,
+ *                added pairwise)
+ *   workspace    as for w4a16_linear, of w4a16_linear_logits_workspace_bytes
+ * Same launch and error rules as w4a16_linear.
+ */
+size_t w4a16_linear_logits_workspace_bytes(int M, int64_t N, int64_t K);
+w4a16_status w4a16_linear_logits(const void* x, int M, int64_t K, const void* qweight_packed,
+                                 const void* scales_packed, int64_t N, float* logits, float* row_stats,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Speculative accept step (the tutorial page, section 3 Steps 3-4 and
@@ -160,6 +189,22 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
                          const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
                          int32_t* accepted_len, int32_t* next_token, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Stochastic sequence accept with the target rows' statistics supplied
+ * (from w4a16_linear_logits over the B * (n + 1) verify positions): the same
+ * decisions, draw and outputs as spec_accept in stochastic sequence mode, but
+ * the statistics pass reads only the draft rows q_logits.
+ *   p_stats   device, fp32 pairs [B * (n + 1)][V / 32]: row_stats of
+ *             w4a16_linear_logits for the rows of p_logits
+ *   V         a multiple of 32
+ *   other arguments, limits, workspace and errors as for spec_accept
+ *   (q_logits and uniforms required).
+ */
+w4a16_status spec_accept_prestat(const float* p_logits, const float* p_stats, const float* q_logits,
+                                 const int32_t* draft_ids, const float* uniforms, int B, int n, int V,
+                                 int32_t* accepted_len, int32_t* next_token, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * Allocation-free W4A16 linear. The pages have no counterpart to this call:

@@ -42,6 +42,9 @@ SIGNATURES = {
     "w4a16_item_rounds": (ctypes.c_int, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "w4a16_item_begin": (_i64, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "w4a16_item_owner": (_i64, [_i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i64]),
+    "w4a16_linear_logits_workspace_bytes": (_sz, [_i32, _i64, _i64]),
+    "w4a16_linear_logits": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "spec_accept_prestat": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
     "w4a16_linear_noalloc_scratch_bytes": (_sz, []),
     "w4a16_linear_noalloc": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp]),
 }

@@ -141,6 +141,32 @@ def linear_noalloc(x: torch.Tensor, w: PackedWeight, out: Optional[torch.Tensor]
     return out
 
 
+def linear_logits_workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().w4a16_linear_logits_workspace_bytes(M, N, K))
+
+
+def linear_logits(x: torch.Tensor, w: PackedWeight, logits: Optional[torch.Tensor] = None,
+                  stats: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    """The lm_head of the verify pass with fused softmax statistics:
+    returns (logits fp32 [M, N], stats fp32 [M, N/32, 2] = (max, sum exp(l - max))
+    per 32-logit slice)."""
+    _need(x, "x", torch.bfloat16)
+    M, K = x.shape
+    if K != w.K:
+        raise ValueError(f"x has K={K}, weight has K={w.K}")
+    if logits is None:
+        logits = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
+    if stats is None:
+        stats = torch.empty((M, w.N // 32, 2), dtype=torch.float32, device=x.device)
+    _need(logits, "logits", torch.float32, (M, w.N))
+    _need(stats, "stats", torch.float32, (M, w.N // 32, 2))
+    if ws is None:
+        ws = workspace(linear_logits_workspace_bytes(M, w.N, K), x.device, "linear")
+    check(lib().w4a16_linear_logits(_ptr(x), M, K, _ptr(w.qweight), _ptr(w.scales), w.N, _ptr(logits), _ptr(stats),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "w4a16_linear_logits")
+    return logits, stats
+
+
 # ------------------------------------------------------------------ accept
 
 def accept_workspace_bytes(B: int, n: int, V: int) -> int:
@@ -176,6 +202,30 @@ def spec_accept(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: Optio
     check(lib().spec_accept(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), _ptr(tree_parents), _ptr(uniforms),
                             B, n, V, _ptr(accepted_len), _ptr(next_token), _ptr(ws), ws.numel(),
                             _stream(stream)), "spec_accept")
+    return accepted_len, next_token
+
+
+def spec_accept_prestat(p_logits: torch.Tensor, p_stats: torch.Tensor, draft_ids: torch.Tensor,
+                        q_logits: torch.Tensor, uniforms: torch.Tensor, accepted_len: Optional[torch.Tensor] = None,
+                        next_token: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None):
+    """Stochastic sequence accept with the target rows' statistics supplied
+    (p_stats [B, n+1, V/32, 2] from linear_logits). Returns (accepted_len, next_token)."""
+    _need(p_logits, "p_logits", torch.float32)
+    B, n1, V = p_logits.shape
+    n = n1 - 1
+    _need(p_stats, "p_stats", torch.float32, (B, n1, V // 32, 2))
+    _need(draft_ids, "draft_ids", torch.int32, (B, n))
+    _need(q_logits, "q_logits", torch.float32, (B, n, V))
+    _need(uniforms, "uniforms", torch.float32, (B, n + 1))
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=p_logits.device)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=p_logits.device)
+    if ws is None:
+        ws = workspace(accept_workspace_bytes(B, n, V), p_logits.device, "accept")
+    check(lib().spec_accept_prestat(_ptr(p_logits), _ptr(p_stats), _ptr(q_logits), _ptr(draft_ids), _ptr(uniforms),
+                                    B, n, V, _ptr(accepted_len), _ptr(next_token), _ptr(ws), ws.numel(),
+                                    _stream(stream)), "spec_accept_prestat")
     return accepted_len, next_token
 
 

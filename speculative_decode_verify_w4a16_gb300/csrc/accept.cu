@@ -6,7 +6,10 @@
 //     into items of 1024 logits; a warp holds an item in registers (one HBM
 //     pass, the next item's loads in flight meanwhile), takes the exact item
 //     maximum and the sum of exp(l - max) (pairwise fp32 per lane,
-//     double-float across lanes).
+//     double-float across lanes). When the caller supplies the target
+//     rows' statistics per 32-logit slice (spec_accept_prestat, from the
+//     fused lm_head), the pass reads the draft rows only and merges the
+//     supplied slices, 512 to an item, into the same item statistics.
 //  2. accept_decide_kernel, one block per batch row: merges each row's item
 //     statistics (one warp per row), evaluates alpha_i = min(1, P(d_i) /
 //     Q(d_i)) for every draft, finds the first rejection r and records r
@@ -39,6 +42,7 @@ constexpr int kArgPT = 64;                           // logits a thread holds in
 constexpr int kArgChunk = kAccThreads * kArgPT;      // 16384
 constexpr int kStatPT = 32;                          // logits a lane holds per statistics item
 constexpr int kStatItem = 32 * kStatPT;              // 1024 logits: one warp's item
+constexpr int kSliceItem = 32 * kStatPT / 2;         // 512 caller-supplied slice statistics: one warp's item
 constexpr int kStatBlocksPerSm = 2;                  // statistics blocks resident per SM (launch bounds)
 constexpr int kDecThreads = 512;                     // decide kernel: 15 merging warps + 1 loading warp
 constexpr int kMaxStatRows = 2 * 1024 + 1;           // statistics rows of one batch row (n <= 1024)
@@ -86,17 +90,6 @@ __device__ __forceinline__ float df_val(DF a) { return __fadd_rn(a.hi, a.lo); }
 __device__ __forceinline__ bool df_gt(DF a, DF b) {
   const DF d = df_add(a, DF{-b.hi, -b.lo});
   return d.hi > 0.0f || (d.hi == 0.0f && d.lo > 0.0f);
-}
-
-// exp(a - b) for fp32 a <= b, for the values that decide a draw: the
-// difference is formed exactly (TwoSum: hi + lo, |lo| <= 2^-24 |hi|), and
-// exp(hi + lo) = exp(hi) * (1 + lo) to within lo^2 / 2; exp(hi) is the
-// library's accurate expf (not the fast approximation, whose error grows with
-// |hi|).
-__device__ __forceinline__ float exp_diff(float a, float b) {
-  const DF d = two_sum(a, -b);
-  const float e = expf(d.hi);
-  return __fmaf_rn(e, d.lo, e);
 }
 
 struct RowStat {
@@ -173,8 +166,12 @@ __device__ DF block_exclusive_scan(DF v) {
   return df_add(before, df_add(incl, DF{-v.hi, -v.lo}));
 }
 
-// Statistics row rr of a batch row's 2n+1 rows: target rows 0..n, then draft rows.
-__device__ __forceinline__ const float* stat_row_ptr(const float* p, const float* q, int n, int64_t V, int rr) {
+// Statistics row rr of a batch row's 2n+1 rows: target rows 0..n, then draft
+// rows; with q_only (target statistics supplied by the caller) the rows are
+// the draft rows alone, rr = b * n + i.
+__device__ __forceinline__ const float* stat_row_ptr(const float* p, const float* q, int n, int64_t V, int rr,
+                                                     bool q_only) {
+  if (q_only) return q + (int64_t)rr * V;
   const int per = 2 * n + 1;
   const int b = rr / per, i = rr % per;
   if (i <= n) return p + ((int64_t)b * (n + 1) + i) * V;
@@ -288,11 +285,11 @@ __device__ __forceinline__ void item_range(int n, int V, int ch, int it, int& rr
 // row). Each warp keeps the next item's loads in flight while it reduces the
 // current one, so the HBM stream does not stop while the exponentials run.
 template <bool VEC>
-__device__ __forceinline__ void load_item(const float* p, const float* q, int n, int V, int ch, int it,
+__device__ __forceinline__ void load_item(const float* p, const float* q, int n, int V, int ch, int it, bool q_only,
                                           float (&v)[kStatPT]) {
   int rr, x0, x1;
   item_range(n, V, ch, it, rr, x0, x1);
-  const float* row = stat_row_ptr(p, q, n, V, rr);
+  const float* row = stat_row_ptr(p, q, n, V, rr, q_only);
   const int lane = threadIdx.x & 31;
   if (VEC) {
 #pragma unroll
@@ -314,25 +311,84 @@ __device__ __forceinline__ void load_item(const float* p, const float* q, int n,
   }
 }
 
+// Items over the caller-supplied statistics of the target rows (the fused
+// lm_head's (max, sum exp(l - max)) per 32-logit slice, V / 32 per row): an
+// item is kSliceItem consecutive slices of one row, a lane holding
+// kStatPT / 2 (max, sum) pairs; missing slices are (-FLT_MAX, 0).
+__device__ __forceinline__ void load_slice_item(const float2* ps, int V, int chs, int it, float (&v)[kStatPT]) {
+  const int ns = V / 32;
+  const int row = it / chs;
+  const int s0 = (it - row * chs) * kSliceItem;
+  const float2* src = ps + (int64_t)row * ns;
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < kStatPT / 2; ++j) {
+    const int si = s0 + j * 32 + lane;
+    float2 t = make_float2(-FLT_MAX, 0.0f);
+    if (si < ns) t = __ldcs(src + si);
+    v[2 * j] = t.x;
+    v[2 * j + 1] = t.y;
+  }
+}
+
+// Merged statistics of an item of slices: m = max of the slice maxima,
+// sum of s_j exp(m_j - m) (fp32 per lane, pairwise; double-float across
+// lanes), as item_stats does for raw logits.
+__device__ __forceinline__ void slice_item_stats(const float (&v)[kStatPT], RowStat* out) {
+  float m = -FLT_MAX;
+#pragma unroll
+  for (int j = 0; j < kStatPT / 2; ++j) m = fmaxf(m, v[2 * j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float t[kStatPT / 4];
+#pragma unroll
+  for (int j = 0; j < kStatPT / 4; ++j)
+    t[j] = __fmul_rn(v[4 * j + 1], __expf(v[4 * j] - m)) + __fmul_rn(v[4 * j + 3], __expf(v[4 * j + 2] - m));
+#pragma unroll
+  for (int w = kStatPT / 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] += t[j + w];
+  DF s{t[0], 0.0f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s = df_add(s, shfl_xor_df(s, o));
+  if ((threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_kernel(const float* __restrict__ p,
                                                                        const float* __restrict__ q, int n, int V,
-                                                                       int ch, int items,
-                                                                       RowStat* __restrict__ stats) {
+                                                                       int ch, int items, int q_only,
+                                                                       const float2* __restrict__ p_stats, int chs,
+                                                                       int slice_items, RowStat* __restrict__ stats) {
   grid_launch_dependents();
   grid_dependency_wait();
+  // items [0, items): logit chunks; [items, items + slice_items): slices of
+  // the supplied target statistics (q_only mode), written after them
+  const int all = items + slice_items;
+  auto load = [&](int i, float (&v)[kStatPT]) {
+    if (i < items)
+      load_item<VEC>(p, q, n, V, ch, i, q_only, v);
+    else
+      load_slice_item(p_stats, V, chs, i - items, v);
+  };
+  auto reduce = [&](int i, const float (&v)[kStatPT]) {
+    if (i < items)
+      item_stats(v, stats + i);
+    else
+      slice_item_stats(v, stats + i);
+  };
   const int nw = gridDim.x * kAccWarps;
   int it = blockIdx.x * kAccWarps + (threadIdx.x >> 5);
   float va[kStatPT], vb[kStatPT];
-  if (it < items) load_item<VEC>(p, q, n, V, ch, it, va);
-  while (it < items) {  // two items per trip: the buffers swap roles
+  if (it < all) load(it, va);
+  while (it < all) {  // two items per trip: the buffers swap roles
     const int i1 = it + nw;
-    if (i1 < items) load_item<VEC>(p, q, n, V, ch, i1, vb);
-    item_stats(va, stats + it);
-    if (i1 >= items) break;
+    if (i1 < all) load(i1, vb);
+    reduce(it, va);
+    if (i1 >= all) break;
     const int i2 = i1 + nw;
-    if (i2 < items) load_item<VEC>(p, q, n, V, ch, i2, va);
-    item_stats(vb, stats + i1);
+    if (i2 < all) load(i2, va);
+    reduce(i1, vb);
     it = i2;
   }
 }
@@ -342,14 +398,19 @@ __global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_ke
 // the first rejection r and record r with the normalisers of row r.
 __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
-    const float* __restrict__ u, int n, int V, int ch, const RowStat* __restrict__ stats,
+    const float* __restrict__ u, int n, int V, int ch, const RowStat* __restrict__ stats, int prestat, int chs,
     Decision* __restrict__ dec, unsigned* err) {
   grid_launch_dependents();
   grid_dependency_wait();
   constexpr int kMergeWarps = kDecThreads / 32 - 1;
   const int b = blockIdx.x;
   const int per = 2 * n + 1;
-  const RowStat* st = stats + (int64_t)b * per * ch;
+  // row statistics: all 2n + 1 rows from the statistics pass (ch items a
+  // row), or (prestat) the draft rows (ch items a row) followed, after all
+  // batch rows' draft rows, by the target rows merged from the caller's
+  // slices (chs items a row)
+  const RowStat* st = prestat ? stats + (int64_t)b * n * ch : stats + (int64_t)b * per * ch;
+  const RowStat* st_p = stats + (int64_t)gridDim.x * n * ch + (int64_t)b * (n + 1) * chs;
   __shared__ float sM[kMaxStatRows];
   __shared__ DF sZ[kMaxStatRows];
   __shared__ float sLp[kMaxNodes], sLq[kMaxNodes];  // P_i / Q_i logits at d_i (n <= 1024)
@@ -374,7 +435,12 @@ __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
     for (int row = warp; row < per; row += kMergeWarps) {
       float M;
       DF Z;
-      warp_merge_row(st + (int64_t)row * ch, ch, M, Z);
+      if (!prestat)
+        warp_merge_row(st + (int64_t)row * ch, ch, M, Z);
+      else if (row <= n)
+        warp_merge_row(st_p + (int64_t)row * chs, chs, M, Z);
+      else
+        warp_merge_row(st + (int64_t)(row - n - 1) * ch, ch, M, Z);
       if (lane == 0) {
         sM[row] = M;
         sZ[row] = Z;
@@ -389,8 +455,8 @@ __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
       reject = true;
     } else {
       // alpha = min(1, P / Q) = min(1, (e_p * Z_q) / (e_q * Z_p)), fp32 (a few ulp)
-      const float ep = exp_diff(sLp[i], sM[i]);
-      const float eq = exp_diff(sLq[i], sM[n + 1 + i]);
+      const float ep = exp_of_diff(sLp[i], sM[i]);
+      const float eq = exp_of_diff(sLq[i], sM[n + 1 + i]);
       const float num = __fmul_rn(ep, df_val(sZ[n + 1 + i])), den = __fmul_rn(eq, df_val(sZ[i]));
       const float alpha = den > 0.0f ? fminf(1.0f, __fdiv_rn(num, den)) : 1.0f;
       reject = !(u[(int64_t)b * (n + 1) + i] < alpha);
@@ -421,11 +487,11 @@ struct ResidFn {
   const float* prow;  // P_r row logits (or P_{n+1} after full acceptance)
   const float* qrow;  // Q_r row logits, NULL after full acceptance
   float mp, ip, mq, iq;
-  __device__ __forceinline__ float pv_of(float lp) const { return __fmul_rn(exp_diff(lp, mp), ip); }
+  __device__ __forceinline__ float pv_of(float lp) const { return __fmul_rn(exp_of_diff(lp, mp), ip); }
   __device__ __forceinline__ float rv_of(float lp, float lq) const {
     const float pv = pv_of(lp);
     if (!qrow) return pv;
-    const float qv = __fmul_rn(exp_diff(lq, mq), iq);
+    const float qv = __fmul_rn(exp_of_diff(lq, mq), iq);
     return fmaxf(__fsub_rn(pv, qv), 0.0f);
   }
   __device__ __forceinline__ float pval(int x) const { return pv_of(prow[x]); }
@@ -808,7 +874,7 @@ AcceptPlan accept_plan(int B, int n, int V) {
 
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
                               int32_t* acc, int32_t* next, void* ws, const AcceptPlan& pl, int num_sms, unsigned* err,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const float2* p_stats) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   RowStat* stats = reinterpret_cast<RowStat*>(w + pl.stats_off);
   Decision* dec = reinterpret_cast<Decision*>(w + pl.dec_off);
@@ -816,18 +882,24 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   int* cnt2 = reinterpret_cast<int*>(w) + kCounterBank2;
   cudaError_t e;
   // statistics grid: persistent warps, one wave of resident blocks (the
-  // kernel's launch bounds give two per SM)
-  const int items = pl.rows_seq * pl.ch;
-  int g1 = (items + kAccWarps - 1) / kAccWarps;
+  // kernel's launch bounds give two per SM); with the target statistics
+  // supplied, the draft rows only
+  const int q_only = p_stats ? 1 : 0;
+  const int items = (q_only ? B * n : pl.rows_seq) * pl.ch;
+  // supplied target statistics: V / 32 slices a row, kSliceItem an item
+  const int chs = q_only ? (V / 32 + kSliceItem - 1) / kSliceItem : 0;
+  const int slice_items = B * (n + 1) * chs;  // fits: chs <= ch, so the total stays within rows_seq * ch
+  int g1 = (items + slice_items + kAccWarps - 1) / kAccWarps;
   if (g1 > kStatBlocksPerSm * num_sms) g1 = kStatBlocksPerSm * num_sms;
   if (V % 4 == 0)
-    e = launch_pdl(accept_stats_kernel<true>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, stats);
+    e = launch_pdl(accept_stats_kernel<true>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, q_only,
+                   p_stats, chs, slice_items, stats);
   else
-    e = launch_pdl(accept_stats_kernel<false>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items,
-                   stats);
+    e = launch_pdl(accept_stats_kernel<false>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, q_only,
+                   p_stats, chs, slice_items, stats);
   if (e != cudaSuccess) return e;
   e = launch_pdl(accept_decide_kernel, dim3(B), dim3(kDecThreads), 0, stream, p, q, d, u, n, V, pl.ch,
-                 (const RowStat*)stats, dec, err);
+                 (const RowStat*)stats, q_only, chs, dec, err);
   if (e != cudaSuccess) return e;
   // residual grid: as many chunks per batch row as one wave of resident
   // blocks allows, within [ch2_lo, ch2]

@@ -134,7 +134,9 @@ w4a16_status w4a16_prepack(const uint32_t* qweight, const uint16_t* scales, int6
              : W4A16_ERR_CUDA;
 }
 
-static bool linear_shape_ok(int M, int64_t N, int64_t K) { return M >= 1 && M <= 64 && valid_nk(N, K) && K >= 1024; }
+static bool linear_shape_ok(int M, int64_t N, int64_t K) {
+  return M >= 1 && M <= kTcMaxM && valid_nk(N, K) && K >= 1024;
+}
 
 size_t w4a16_linear_workspace_bytes(int M, int64_t N, int64_t K) {
   if (!linear_shape_ok(M, N, K)) return 0;
@@ -149,7 +151,7 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
                           int64_t N, void* out, void* workspace, size_t workspace_bytes, void* stream) {
   if (!x || !qweight_packed || !scales_packed || !out) return W4A16_ERR_INVALID_ARG;
   if (M < 1 || !valid_nk(N, K)) return W4A16_ERR_INVALID_ARG;
-  if (M > 64 || K < 1024) return W4A16_ERR_UNSUPPORTED;
+  if (M > kTcMaxM || K < 1024) return W4A16_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(qweight_packed, 16) || !aligned(scales_packed, 16) || !aligned(out, 4))
     return W4A16_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return W4A16_ERR_WORKSPACE;
@@ -160,6 +162,36 @@ w4a16_status w4a16_linear(const void* x, int M, int64_t K, const void* qweight_p
   if (workspace_bytes < plan.workspace_bytes) return W4A16_ERR_WORKSPACE;
   return launch_linear(x, M, K, qweight_packed, scales_packed, N, out, workspace, plan, dev,
                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+size_t w4a16_linear_logits_workspace_bytes(int M, int64_t N, int64_t K) {
+  if (!linear_shape_ok(M, N, K)) return 0;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return 0;
+  TcPlan plan;
+  if (tc_plan_fused(M, N, K, dev, &plan) != cudaSuccess) return 0;
+  return tc_workspace_bytes(plan);
+}
+
+w4a16_status w4a16_linear_logits(const void* x, int M, int64_t K, const void* qweight_packed,
+                                 const void* scales_packed, int64_t N, float* logits, float* row_stats,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!x || !qweight_packed || !scales_packed || !logits || !row_stats) return W4A16_ERR_INVALID_ARG;
+  if (M < 1 || !valid_nk(N, K)) return W4A16_ERR_INVALID_ARG;
+  if (M > kTcMaxM || K < 1024) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(qweight_packed, 16) || !aligned(scales_packed, 16) || !aligned(logits, 4) ||
+      !aligned(row_stats, 8))
+    return W4A16_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return W4A16_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  TcPlan plan;
+  if (tc_plan_fused(M, N, K, dev, &plan) != cudaSuccess) return W4A16_ERR_CUDA;
+  if (workspace_bytes < tc_workspace_bytes(plan)) return W4A16_ERR_WORKSPACE;
+  return launch_tc_fused(x, M, K, qweight_packed, scales_packed, N, logits, reinterpret_cast<float2*>(row_stats),
+                         workspace, plan, dev, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? W4A16_OK
              : W4A16_ERR_CUDA;
 }
@@ -198,6 +230,27 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
     e = launch_accept_greedy(p_logits, draft_ids, tree_parents, B, n, V, accepted_len, next_token, workspace, plan,
                              dev.err, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+w4a16_status spec_accept_prestat(const float* p_logits, const float* p_stats, const float* q_logits,
+                                 const int32_t* draft_ids, const float* uniforms, int B, int n, int V,
+                                 int32_t* accepted_len, int32_t* next_token, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (!p_logits || !p_stats || !q_logits || !draft_ids || !uniforms || !accepted_len || !next_token)
+    return W4A16_ERR_INVALID_ARG;
+  if (!accept_shape_ok(B, n, V) || V % 32 != 0) return W4A16_ERR_INVALID_ARG;
+  if (!aligned(p_logits, 16) || !aligned(q_logits, 16) || !aligned(p_stats, 8) || !aligned(draft_ids, 4) ||
+      !aligned(uniforms, 4) || !aligned(accepted_len, 4) || !aligned(next_token, 4))
+    return W4A16_ERR_INVALID_ARG;
+  const AcceptPlan plan = accept_plan(B, n, V);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < plan.total) return W4A16_ERR_WORKSPACE;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  return launch_accept_seq(p_logits, q_logits, draft_ids, uniforms, B, n, V, accepted_len, next_token, workspace,
+                           plan, dev.num_sms, dev.err, static_cast<cudaStream_t>(stream),
+                           reinterpret_cast<const float2*>(p_stats)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
 }
 
 w4a16_status w4a16_check_device_status(void* stream) {

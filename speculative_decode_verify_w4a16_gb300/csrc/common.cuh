@@ -187,6 +187,19 @@ __device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, 
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// exp(a - b) for finite fp32 a <= b, for values that decide a draw or an
+// acceptance: the difference is formed exactly as hi + lo (TwoSum, Knuth,
+// TAOCP vol. 2, 4.2.2; |lo| <= 2^-24 |hi|) and exp(hi + lo) = exp(hi) (1 + lo)
+// to within lo^2 / 2; exp(hi) is the library's accurate expf (the fast
+// approximation's error grows with |hi|).
+__device__ __forceinline__ float exp_of_diff(float a, float b) {
+  const float s = __fsub_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float lo = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(-b, bb));
+  const float e = expf(s);
+  return __fmaf_rn(e, lo, e);
+}
+
 // ------------------------------------------------------------ shared loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

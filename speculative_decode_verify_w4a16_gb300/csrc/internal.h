@@ -73,6 +73,7 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
 
 // ---- linear on tcgen05 / TMEM (M >= kTcMinM)
 constexpr int kTcMinM = 9;
+constexpr int kTcMaxM = 80;  // largest token tile (ring depth 2 in tensor memory)
 struct TcPlan {
   int nt = 0;           // MMA N: M rounded up to a multiple of 16
   int64_t units = 0;
@@ -86,6 +87,12 @@ cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t m
 size_t tc_workspace_bytes(const TcPlan& plan);
 cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
                       void* out, void* workspace, const TcPlan& plan, const DeviceInfo& dev, cudaStream_t stream);
+// The fused-statistics variant (any M in 1..kTcMaxM): fp32 outputs [M][N] and
+// (max, sum exp(l - max)) per (token, 32-row slice) [M][N/32].
+cudaError_t tc_plan_fused(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan);
+cudaError_t launch_tc_fused(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                            float* logits, float2* stats, void* workspace, const TcPlan& plan, const DeviceInfo& dev,
+                            cudaStream_t stream);
 
 // ---- linear dispatch (by M)
 struct LinearPlan {
@@ -114,9 +121,11 @@ struct AcceptPlan {
   size_t stats_off = 0, dec_off = 0, csum_off = 0, total = 0;  // counters at offset 0
 };
 AcceptPlan accept_plan(int B, int n, int V);
+// p_stats: NULL, or the target rows' (max, sum exp(l - max)) per 32-logit
+// slice [B * (n + 1)][V / 32] (the statistics pass then reads the draft rows only)
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
                               int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, int num_sms,
-                              unsigned* err, cudaStream_t stream);
+                              unsigned* err, cudaStream_t stream, const float2* p_stats = nullptr);
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
                                  int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
                                  cudaStream_t stream);

@@ -29,6 +29,7 @@
 // A tile split between items is finished by its last contributor, which
 // adds the fp32 partials of all contributors in item order.
 #include <cudaTypedefs.h>
+#include <float.h>
 
 #include <mutex>
 #include <string.h>
@@ -51,7 +52,7 @@ constexpr int kTcThreads = 32 * (kTcXWarp + 1);
 constexpr uint32_t kTcTmemCols = 512;  // the whole tensor memory of the SM
 constexpr int kTcRing = 16;            // scale / metadata hand-off ring (units)
 
-template <int NT>
+template <int NT, bool FUSED = false>
 struct TcLayout {
   // TMEM ring depths: kA dequantised units (64 columns each) at column 0,
   // kD accumulators (NT columns each) after them
@@ -61,17 +62,22 @@ struct TcLayout {
   // each waiter is then at most one phase ahead of the slot's barrier, which
   // a parity wait requires (units are dealt round-robin to the groups).
   //
-  // The A buffers, the accumulators and the token tiles have the same depth
-  // kR, so that slot i % kR of all three is released by the same event, the
-  // completion of unit i's MMAs: one commit per unit to done[i % kR] serves
-  // the dequant group (A), the epilogue (D) and the token-tile warp (x).
-  // Each tcgen05.commit costs the tensor pipe about as much as an MMA.
-  static constexpr int kR = NT <= 16 ? 6 : 4;
-  static constexpr int kA = kR;
-  static constexpr int kD = kR;
+  // One event releases a unit's A buffer and token tile and hands its
+  // accumulator to the epilogue: the completion of the unit's MMAs, one
+  // commit per unit to done[i % kR] (each tcgen05.commit costs the tensor
+  // pipe about as much as an MMA). kR, the depth of the completion barriers
+  // and of the token-tile ring, is a multiple of both TMEM ring depths, so a
+  // waiter on done[] for unit i finds the barrier at most one phase ahead
+  // (unit i + kR needs slots that unit i's consumers release first).
+  // At 80 tokens four accumulators do not fit beside four A buffers; two
+  // accumulators are then taken one unit at a time.
+  static constexpr int kA = NT <= 16 ? 6 : 4;
+  static constexpr int kD = NT <= 16 ? 6 : (NT <= 64 ? 4 : 2);
+  static constexpr int kR = kA > kD ? kA : kD;
+  static_assert(kR % kA == 0 && kR % kD == 0, "completion barriers shared by the TMEM rings");
   static_assert(kA * 64 + kD * NT <= (int)kTcTmemCols, "TMEM budget");
   static_assert(kA % kTcDqGroups == 0 && kD % kTcDqGroups == 0, "ring slots per group");
-  static_assert(kD >= 2, "the epilogue takes units in pairs");
+  static constexpr bool kPairs = kD >= 4;  // the epilogue takes units in pairs
   // a unit's hand-off entry is rewritten kTcRing units later, by the group
   // that then has finished its previous unit (kTcDqGroups back): that one
   // waited for the MMAs kA units before it, which waited for the epilogue
@@ -86,9 +92,10 @@ struct TcLayout {
   static constexpr int kXStages = kR;
   static constexpr int kWStage = kUnitBytes + kUnitScaleBytes;  // codes, then scales
   static constexpr int kXOff = 0;
-  // output staging: one [NT tokens][32 rows] bf16 slice per epilogue warp,
-  // written to global memory by a 2-D TMA store
-  static constexpr int kOutSlice = NT * 32 * 2;
+  // output staging, one slice per epilogue warp: [NT tokens][32 rows] bf16
+  // written to global memory by a 2-D TMA store; in the fused-statistics
+  // variant fp32 in the 128-byte swizzle (1024-byte aligned)
+  static constexpr int kOutSlice = FUSED ? NT * 32 * 4 : NT * 32 * 2;
   static constexpr int kOutOff = kXOff + kXStages * kXStage;
   static constexpr int kWOff = kOutOff + kTcEpWarps * kOutSlice;
   static constexpr int kWStages = (200 * 1024 - kWOff) / kWStage / kTcDqGroups * kTcDqGroups;
@@ -100,12 +107,15 @@ struct TcLayout {
   static constexpr int kTotal = kBarOff + (2 * kWStages + 4 * kR + kTcDqGroups) * 8 + 16 + 1024;  // +1024: alignment
   static_assert(kX % 1024 == 0, "token tile halves must stay 1024-byte aligned");
   static_assert(kOutSlice % 128 == 0, "TMA store source alignment");
+  static_assert(!FUSED || (kOutSlice % 1024 == 0 && kOutOff % 1024 == 0), "128-byte swizzle atoms");
   static_assert(kWStage % 16 == 0, "bulk copy alignment");
   static_assert(kWStages >= 2 * kTcDqGroups, "ring depth");
   static_assert(kWStages % kTcDqGroups == 0 && kXStages % kTcDqGroups == 0, "ring slots per group");
 };
 
 struct TcParams {
+  float* logits;   // fused-statistics variant: fp32 outputs [M][N]
+  float2* stats;   // and (max, sum exp(l - max)) per (token, 32-row slice) [M][N/32]
   const uint8_t* qw;
   int tma_store;  // output tiles through the 2-D TMA store (out 16-byte aligned)
   const uint8_t* sc;
@@ -148,11 +158,89 @@ __device__ __forceinline__ void tc_dequant(uint32_t w, uint32_t* r) {
 // Epilogue slice of a warp: rows 32q + lane, tokens 0 .. NT - 1. With the
 // TMA store the slice goes through the warp's [NT][32] staging area (token
 // rows past M are not written: the tensor map ends at M); otherwise one
-// 2-byte store per token.
-template <int NT>
+// 2-byte store per token. The fused-statistics variant stages fp32 outputs
+// the same way (or stores each token's 32 rows as one 128-byte store) and
+// reads the staged rows back for the maximum and sum of exp(l - max) of the
+// 32 rows per token.
+template <int NT, bool FUSED>
 __device__ __forceinline__ void tc_store(const TcParams& p, const CUtensorMap* omap, uint8_t* stage, int64_t t, int q,
                                          int lane, const float (&acc)[NT]) {
   const int64_t n = t * kUnitRows + 32 * q + lane;
+  if constexpr (FUSED) {
+    // staging [NT tokens][32 rows] fp32: 128-byte token rows in the 128-byte
+    // swizzle of the TMA store (16-byte chunk c of row m sits at chunk
+    // c ^ (m % 8)), so that both the per-token row writes here and the
+    // 16-byte reads of whole token rows below are free of bank conflicts
+    float* sv = reinterpret_cast<float*>(stage);
+    if (p.tma_store && lane == 0) bulk_wait_group_read0();  // the previous store of this area has read it
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < NT; ++m) sv[m * 32 + ((((lane >> 2) ^ m) & 7) << 2) + (lane & 3)] = acc[m];
+    if (p.tma_store) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(omap, (int32_t)(t * kUnitRows + 32 * q), 0, stage);
+        bulk_commit_group();
+      }
+    } else {
+#pragma unroll
+      for (int m = 0; m < NT; ++m)
+        if (m < p.M) p.logits[(int64_t)m * p.N + n] = acc[m];
+      __syncwarp();
+    }
+    // lane j: tokens j, j + 32, ... (all rounds interleaved, four independent
+    // chains each, so that the latencies overlap); ex2.approx-based
+    // exponential, as the accept step's own statistics pass uses for its
+    // normalisers (about 1e-7 of the sum)
+    constexpr int RN = (NT + 31) / 32;
+    const float* row[RN];
+    int sw[RN];
+    float mx[RN][4], z[RN][4];
+#pragma unroll
+    for (int j = 0; j < RN; ++j) {
+      const int m = min(lane + 32 * j, NT - 1);  // rows past NT: any staged row, not stored
+      row[j] = sv + m * 32;
+      sw[j] = m & 7;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) mx[j][c] = -FLT_MAX;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int j = 0; j < RN; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(row[j] + ((c ^ sw[j]) << 2));
+        mx[j][0] = fmaxf(mx[j][0], v.x);
+        mx[j][1] = fmaxf(mx[j][1], v.y);
+        mx[j][2] = fmaxf(mx[j][2], v.z);
+        mx[j][3] = fmaxf(mx[j][3], v.w);
+      }
+#pragma unroll
+    for (int j = 0; j < RN; ++j) {
+      mx[j][0] = fmaxf(fmaxf(mx[j][0], mx[j][1]), fmaxf(mx[j][2], mx[j][3]));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) z[j][c] = 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int j = 0; j < RN; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(row[j] + ((c ^ sw[j]) << 2));
+        z[j][0] += __expf(v.x - mx[j][0]);
+        z[j][1] += __expf(v.y - mx[j][0]);
+        z[j][2] += __expf(v.z - mx[j][0]);
+        z[j][3] += __expf(v.w - mx[j][0]);
+      }
+    const int64_t slice = t * 4 + q;
+#pragma unroll
+    for (int j = 0; j < RN; ++j) {
+      const int m = lane + 32 * j;
+      if (m < p.M)
+        p.stats[(int64_t)m * (p.N / 32) + slice] = make_float2(mx[j][0], (z[j][0] + z[j][1]) + (z[j][2] + z[j][3]));
+    }
+    __syncwarp();  // every lane has read the staging area before it is rewritten
+    return;
+  }
   if (p.tma_store) {
     if (lane == 0) bulk_wait_group_read0();  // the previous store of this area has read it
     __syncwarp();
@@ -183,7 +271,7 @@ __device__ __forceinline__ float4* tc_slot(const TcParams& p, int item, int seg,
   return p.partials + (((int64_t)item * 2 + seg) * kTcEpWarps + epw) * (int64_t)(NT / 4 * 32);
 }
 
-template <int NT>
+template <int NT, bool FUSED>
 __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint8_t* stage, int item, int seg,
                                 int64_t t, int q, int lane, const float (&acc)[NT]) {
   const int epw = q;
@@ -232,7 +320,7 @@ __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint
         }
     }
   }
-  tc_store<NT>(p, omap, stage, t, q, lane, sum);
+  tc_store<NT, FUSED>(p, omap, stage, t, q, lane, sum);
   if (lane == 0) *counter = 0;
 }
 
@@ -257,11 +345,11 @@ __device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&a
   }
 }
 
-template <int NT>
+template <int NT, bool FUSED>
 __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                 const __grid_constant__ CUtensorMap omap,
                                                                 const TcParams p) {
-  using L = TcLayout<NT>;
+  using L = TcLayout<NT, FUSED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -397,7 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_bf16(NT);
       for (uint32_t i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
-        const uint32_t sx = i % L::kXStages, b = i % L::kA, db = i % L::kD;
+        const uint32_t sx = i % L::kXStages, b = i % L::kA, db = i % L::kD, cb = i % L::kR;
         const uint32_t pa = (i / L::kA) & 1u, pd = ((i / L::kD) & 1u) ^ 1u, px = (i / L::kXStages) & 1u;
         // the three barriers tested at once (one latency); waits in order only
         // for those still open (the token tile after the stop check)
@@ -409,8 +497,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
         const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
         if (mk < 0) {  // stop marker
           if (mk == -1) {  // the epilogue's last index: complete its phase without MMAs
-            mbar_arrive(&mma_done[db]);
-            mbar_arrive(&mma_done[db]);
+            mbar_arrive(&mma_done[cb]);
+            mbar_arrive(&mma_done[cb]);
           }
           break;
         }
@@ -423,9 +511,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           const uint64_t bd = bd0 + (uint64_t)(((kk < 4 ? 0 : L::kX) + 32 * (kk & 3)) >> 4);
           umma_bf16_ts(tmem + d_col(db), tmem + a_col(b) + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&done[db]);  // frees A[b] and the token tile, hands D[db] to the epilogue (b == db == sx)
+        umma_commit(&done[cb]);  // frees A[b] and the token tile (cb == sx), hands D[db] to the epilogue
         // release (to the epilogue) of the hand-off entry this thread acquired through a_full
-        mbar_arrive(&done[db]);
+        mbar_arrive(&done[cb]);
         mma_issued = (int)i + 1;
       }
       if (mma_issued > 0) umma_commit(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this thread's MMAs
@@ -435,16 +523,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     const int grp = warp >> 2, q = warp & 3;
     for (uint32_t i = grp;; i += kTcDqGroups) {
       const uint32_t s = i % L::kWStages, b = i % L::kA;
-      const uint32_t pw = (i / L::kWStages) & 1u, pa = (i / L::kA - 1u) & 1u;
-      // A[b] is free once the MMAs of unit i - kA have completed; both
-      // barriers tested at once, waits only for one still open
+      // A[b] is free once the MMAs of unit i - kA have completed
+      const uint32_t ia = i - (uint32_t)L::kA, fb = ia % L::kR;
+      const uint32_t pw = (i / L::kWStages) & 1u, pa = (ia / L::kR) & 1u;
+      // both barriers tested at once, waits only for one still open
       const bool tw = mbar_test(&wfull[s], pw);
-      const bool ta = mbar_test(&a_free[b], pa) | (i < (uint32_t)L::kA);
+      const bool ta = i < (uint32_t)L::kA || mbar_test(&a_free[fb], pa);
       if (!tw && !mbar_wait(&wfull[s], pw, p.err)) break;
       const uint4 mu = lds128(smem_u32(&meta[s]));
       const bool stop = (int)mu.x < 0;
       if (stop) {
-        if (!ta && !mbar_wait(&a_free[b], pa, p.err)) break;
+        if (!ta && !mbar_wait(&a_free[fb], pa, p.err)) break;
         // forward the marker to this group's MMA warp (and through it to the
         // epilogue, which stops at the first one)
         if (q == 0 && lane == 0) meta_ring[i % kTcRing] = make_int4((int)mu.x, 0, 0, 0);
@@ -481,7 +570,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       // completed: release it to the producer
       __syncwarp();
       if (lane == 0) mbar_arrive(&wempty[s]);
-      if (!ta && !mbar_wait(&a_free[b], pa, p.err)) break;
+      if (!ta && !mbar_wait(&a_free[fb], pa, p.err)) break;
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
@@ -510,14 +599,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       return make_int4((int)mu.x, (int)mu.y, (int)mu.z, (int)mu.w);
     };
     // Units are taken two at a time (one barrier round trip for both) unless
-    // the first one ends a tile segment or the second is the stop marker.
+    // the first one ends a tile segment or the second is the stop marker;
+    // one at a time with two accumulators, which a pair would both hold.
     for (uint32_t e = 0;;) {
       const uint32_t db = e % L::kD, db1 = (e + 1) % L::kD;
-      const uint32_t p0 = (e / L::kD) & 1u, p1 = ((e + 1) / L::kD) & 1u;
+      const uint32_t cb = e % L::kR, cb1 = (e + 1) % L::kR;
+      const uint32_t p0 = (e / L::kR) & 1u, p1 = ((e + 1) / L::kR) & 1u;
       // both accumulators tested at once; waits only for one still open
-      const bool t0 = mbar_test(&mma_done[db], p0);
-      const bool t1 = mbar_test(&mma_done[db1], p1);
-      if (!t0 && !mbar_wait(&mma_done[db], p0, p.err)) break;
+      const bool t0 = mbar_test(&mma_done[cb], p0);
+      const bool t1 = L::kPairs && mbar_test(&mma_done[cb1], p1);
+      if (!t0 && !mbar_wait(&mma_done[cb], p0, p.err)) break;
       const int4 me = meta_of(e);
       if (me.x < 0) break;  // stop marker
       if (me.w & kTcUnitFirst) {
@@ -528,8 +619,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       const bool seg_end = me.z == p.G - 1 || (me.w & kTcUnitLast);
       bool pair = false;
       int4 me1 = me;
-      if (!seg_end) {
-        if (!t1 && !mbar_wait(&mma_done[db1], p1, p.err)) break;
+      if (L::kPairs && !seg_end) {
+        if (!t1 && !mbar_wait(&mma_done[cb1], p1, p.err)) break;
         me1 = meta_of(e + 1);
         pair = me1.x >= 0;
       }
@@ -546,15 +637,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       const int4 ml = pair ? me1 : me;  // last unit taken
       if (ml.z == p.G - 1 || (ml.w & kTcUnitLast)) {  // end of this item's segment of tile ml.y
         if (seg_g0 == 0 && ml.z == p.G - 1)
-          tc_store<NT>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, ml.y, q, lane, acc);
+          tc_store<NT, FUSED>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, ml.y, q, lane, acc);
         else
-          tc_finish_split<NT>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, item, ml.y == item_t0 ? 0 : 1, ml.y,
-                              q, lane, acc);
+          tc_finish_split<NT, FUSED>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, item, ml.y == item_t0 ? 0 : 1,
+                                     ml.y, q, lane, acc);
 #pragma unroll
         for (int c = 0; c < NT; ++c) acc[c] = 0.0f;
         seg_g0 = 0;
       }
-      if (!pair && !seg_end) break;  // the second unit was the stop marker
+      if (L::kPairs && !pair && !seg_end) break;  // the second unit was the stop marker
       e += pair ? 2u : 1u;
     }
   }
@@ -592,33 +683,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 static int tc_nt(int M) { return (M + 15) / 16 * 16; }
 
-template <int NT>
-static int tc_smem() {
-  return TcLayout<NT>::kTotal;
-}
-
-static int tc_smem_dispatch(int nt) {
-  switch (nt) {
-    case 16: return tc_smem<16>();
-    case 32: return tc_smem<32>();
-    case 48: return tc_smem<48>();
-    default: return tc_smem<64>();
-  }
-}
-
 // CTAs per SM, from the shared-memory, register and TMEM budgets (the
 // occupancy query under-reports for this kernel, so the limits are applied
-// directly).
-template <int NT>
+// directly); also sets the kernel's shared-memory attributes.
+template <int NT, bool FUSED>
 static cudaError_t tc_prepare(int device, int* nb) {
-  cudaError_t e = cudaFuncSetAttribute(w4a16_tc_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       TcLayout<NT>::kTotal);
+  using L = TcLayout<NT, FUSED>;
+  cudaError_t e =
+      cudaFuncSetAttribute(w4a16_tc_kernel<NT, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(w4a16_tc_kernel<NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(w4a16_tc_kernel<NT, FUSED>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, w4a16_tc_kernel<NT>);
+  e = cudaFuncGetAttributes(&fa, w4a16_tc_kernel<NT, FUSED>);
   if (e != cudaSuccess) return e;
   int smem_sm = 0, smem_reserved = 0, regs_sm = 0;
   if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device)) != cudaSuccess)
@@ -627,7 +705,7 @@ static cudaError_t tc_prepare(int device, int* nb) {
     return e;
   if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device)) != cudaSuccess)
     return e;
-  const int by_smem = smem_sm / (TcLayout<NT>::kTotal + (int)fa.sharedSizeBytes + smem_reserved);
+  const int by_smem = smem_sm / (L::kTotal + (int)fa.sharedSizeBytes + smem_reserved);
   const int regs_cta = ((fa.numRegs * 32 + 255) / 256 * 256) * (kTcThreads / 32);
   const int by_regs = regs_sm / (regs_cta > 0 ? regs_cta : 1);
   const int by_tmem = 512 / (int)kTcTmemCols;  // 1: the kernel takes the whole tensor memory
@@ -637,24 +715,35 @@ static cudaError_t tc_prepare(int device, int* nb) {
   return cudaSuccess;
 }
 
-cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes, TcPlan* plan) {
-  static int cached[64][5];
+template <bool FUSED>
+static cudaError_t tc_prepare_dispatch(int nt, int device, int* nb, int* smem) {
+  switch (nt) {
+    case 16: *smem = TcLayout<16, FUSED>::kTotal; return tc_prepare<16, FUSED>(device, nb);
+    case 32: *smem = TcLayout<32, FUSED>::kTotal; return tc_prepare<32, FUSED>(device, nb);
+    case 48: *smem = TcLayout<48, FUSED>::kTotal; return tc_prepare<48, FUSED>(device, nb);
+    case 64: *smem = TcLayout<64, FUSED>::kTotal; return tc_prepare<64, FUSED>(device, nb);
+    case 80: *smem = TcLayout<80, FUSED>::kTotal; return tc_prepare<80, FUSED>(device, nb);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+static cudaError_t tc_plan_impl(int M, int64_t N, int64_t K, const DeviceInfo& dev, bool fused, TcPlan* plan) {
+  static int cached[64][2][6];  // [device][fused][nt / 16]: CTAs per SM (0 = unknown)
+  static int cached_smem[2][6];
   plan->nt = tc_nt(M);
+  if (plan->nt > kTcMaxM) return cudaErrorInvalidValue;
   plan->units = (N / kUnitRows) * (K / kGroup);
   const int slot = plan->nt / 16;
-  int nb = (dev.device >= 0 && dev.device < 64) ? cached[dev.device][slot] : 0;
+  int nb = (dev.device >= 0 && dev.device < 64) ? cached[dev.device][fused][slot] : 0;
+  int smem = cached_smem[fused][slot];
   if (nb == 0) {
-    cudaError_t e;
-    switch (plan->nt) {
-      case 16: e = tc_prepare<16>(dev.device, &nb); break;
-      case 32: e = tc_prepare<32>(dev.device, &nb); break;
-      case 48: e = tc_prepare<48>(dev.device, &nb); break;
-      default: e = tc_prepare<64>(dev.device, &nb); break;
-    }
+    cudaError_t e = fused ? tc_prepare_dispatch<true>(plan->nt, dev.device, &nb, &smem)
+                          : tc_prepare_dispatch<false>(plan->nt, dev.device, &nb, &smem);
     if (e != cudaSuccess) return e;
     if (nb < 1) nb = 1;
     if (nb > 1) nb = 1;  // one CTA owns the SM's 512 TMEM columns
-    if (dev.device >= 0 && dev.device < 64) cached[dev.device][slot] = nb;
+    if (dev.device >= 0 && dev.device < 64) cached[dev.device][fused][slot] = nb;
+    cached_smem[fused][slot] = smem;
   }
   int64_t ctas = (int64_t)dev.num_sms * nb;
   if (ctas > plan->units) ctas = plan->units;
@@ -663,74 +752,121 @@ cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t m
   // 4*NT*128 bytes of partials written and read again (at M = 64, four units'
   // worth of weight bytes), so this path keeps one round: every CTA one
   // contiguous run of units, at most two split tiles per CTA.
-  (void)max_partial_bytes;
   const size_t per_item = (size_t)2 * plan->nt * kUnitRows * sizeof(float);
   plan->sched = make_item_sched(plan->units, (int)ctas, 1, 1);
   plan->counter_bytes = kCounterRegionBytes;
   plan->partial_bytes = (size_t)plan->sched.R * ctas * per_item;
-  plan->smem_bytes = (size_t)tc_smem_dispatch(plan->nt);
+  plan->smem_bytes = (size_t)smem;
   return cudaSuccess;
+}
+
+cudaError_t tc_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes, TcPlan* plan) {
+  (void)max_partial_bytes;
+  return tc_plan_impl(M, N, K, dev, false, plan);
+}
+
+cudaError_t tc_plan_fused(int M, int64_t N, int64_t K, const DeviceInfo& dev, TcPlan* plan) {
+  return tc_plan_impl(M, N, K, dev, true, plan);
 }
 
 size_t tc_workspace_bytes(const TcPlan& plan) { return plan.counter_bytes + plan.partial_bytes; }
 
-template <int NT>
+template <int NT, bool FUSED>
 static cudaError_t launch_tc_t(const CUtensorMap& map, const CUtensorMap& omap, const TcParams& p, const TcPlan& plan,
                                cudaStream_t stream) {
-  return launch_pdl(w4a16_tc_kernel<NT>, dim3((unsigned)plan.ctas), dim3(kTcThreads), (size_t)TcLayout<NT>::kTotal,
-                    stream, map, omap, p);
+  return launch_pdl(w4a16_tc_kernel<NT, FUSED>, dim3((unsigned)plan.ctas), dim3(kTcThreads),
+                    (size_t)TcLayout<NT, FUSED>::kTotal, stream, map, omap, p);
 }
 
-cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
-                      void* out, void* workspace, const TcPlan& plan, const DeviceInfo& dev, cudaStream_t stream) {
+template <bool FUSED>
+static cudaError_t launch_tc_dispatch(const CUtensorMap& map, const CUtensorMap& omap, const TcParams& p,
+                                      const TcPlan& plan, cudaStream_t stream) {
+  switch (plan.nt) {
+    case 16: return launch_tc_t<16, FUSED>(map, omap, p, plan, stream);
+    case 32: return launch_tc_t<32, FUSED>(map, omap, p, plan, stream);
+    case 48: return launch_tc_t<48, FUSED>(map, omap, p, plan, stream);
+    case 64: return launch_tc_t<64, FUSED>(map, omap, p, plan, stream);
+    case 80: return launch_tc_t<80, FUSED>(map, omap, p, plan, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// Shared part of both launches: the token tensor map and the kernel parameters.
+static cudaError_t tc_setup(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                            void* workspace, const TcPlan& plan, const DeviceInfo& dev, CUtensorMap* map, TcParams* p) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
-  CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   const cuuint32_t box[2] = {64u, (cuuint32_t)plan.nt};
   const cuuint32_t es[2] = {1u, 1u};
-  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
+  if (encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  memset(p, 0, sizeof(*p));
+  p->qw = static_cast<const uint8_t*>(qw_packed);
+  p->sc = static_cast<const uint8_t*>(sc_packed);
+  p->counters = static_cast<int*>(workspace);
+  p->partials = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + plan.counter_bytes);
+  p->err = dev.err;
+  p->K = K;
+  p->N = N;
+  p->G = K / kGroup;
+  p->M = M;
+  p->items = plan.sched.R * plan.sched.C;
+  p->sched = plan.sched;
+  return cudaSuccess;
+}
+
+cudaError_t launch_tc(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                      void* out, void* workspace, const TcPlan& plan, const DeviceInfo& dev, cudaStream_t stream) {
+  CUtensorMap map;
+  TcParams p;
+  cudaError_t e = tc_setup(x, M, K, qw_packed, sc_packed, N, workspace, plan, dev, &map, &p);
+  if (e != cudaSuccess) return e;
   // output tiles: [M][N] bf16, boxes of 32 rows (n) x NT tokens (m); the TMA
   // store wants a 16-byte aligned base, else the kernel stores per element
   CUtensorMap omap;
   memset(&omap, 0, sizeof(omap));
-  int tma_store = 0;
   if ((reinterpret_cast<uintptr_t>(out) & 15) == 0) {
     const cuuint64_t odims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     const cuuint64_t ostrides[1] = {(cuuint64_t)N * 2};
     const cuuint32_t obox[2] = {32u, (cuuint32_t)plan.nt};
-    if (encode(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, odims, ostrides, obox, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-        CUDA_SUCCESS)
-      tma_store = 1;
+    const cuuint32_t es[2] = {1u, 1u};
+    if (tensor_map_encoder()(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out, odims, ostrides, obox, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      p.tma_store = 1;
   }
-  TcParams p;
-  p.tma_store = tma_store;
-  p.qw = static_cast<const uint8_t*>(qw_packed);
-  p.sc = static_cast<const uint8_t*>(sc_packed);
   p.out = static_cast<__nv_bfloat16*>(out);
-  p.counters = static_cast<int*>(workspace);
-  p.partials = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + plan.counter_bytes);
-  p.err = dev.err;
-  p.K = K;
-  p.N = N;
-  p.G = K / kGroup;
-  p.M = M;
-  p.items = plan.sched.R * plan.sched.C;
-  p.sched = plan.sched;
-  cudaError_t e;
-  switch (plan.nt) {
-    case 16: e = launch_tc_t<16>(map, omap, p, plan, stream); break;
-    case 32: e = launch_tc_t<32>(map, omap, p, plan, stream); break;
-    case 48: e = launch_tc_t<48>(map, omap, p, plan, stream); break;
-    case 64: e = launch_tc_t<64>(map, omap, p, plan, stream); break;
-    default: return cudaErrorInvalidValue;
+  return launch_tc_dispatch<false>(map, omap, p, plan, stream);
+}
+
+cudaError_t launch_tc_fused(const void* x, int M, int64_t K, const void* qw_packed, const void* sc_packed, int64_t N,
+                            float* logits, float2* stats, void* workspace, const TcPlan& plan, const DeviceInfo& dev,
+                            cudaStream_t stream) {
+  CUtensorMap map;
+  TcParams p;
+  cudaError_t e = tc_setup(x, M, K, qw_packed, sc_packed, N, workspace, plan, dev, &map, &p);
+  if (e != cudaSuccess) return e;
+  // fp32 output tiles: [M][N], boxes of 32 rows (n, 128 bytes) x NT tokens,
+  // 128-byte swizzle; per element when the base is not 16-byte aligned
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  if ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+    const cuuint64_t odims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    const cuuint64_t ostrides[1] = {(cuuint64_t)N * 4};
+    const cuuint32_t obox[2] = {32u, (cuuint32_t)plan.nt};
+    const cuuint32_t es[2] = {1u, 1u};
+    if (tensor_map_encoder()(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, logits, odims, ostrides, obox, es,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      p.tma_store = 1;
   }
-  return e;
+  p.logits = logits;
+  p.stats = stats;
+  return launch_tc_dispatch<true>(map, omap, p, plan, stream);
 }
 
 }  // namespace w4a16

@@ -51,7 +51,7 @@ extern "C" w4a16_status w4a16_linear_noalloc(const void* x, int M, int64_t K, co
   if (M < 1 || N <= 0 || K <= 0 || N % kUnitRows != 0 || K % kGroup != 0 || N > (int64_t(1) << 20) ||
       K > (int64_t(1) << 24))
     return W4A16_ERR_INVALID_ARG;
-  if (M > 64 || K < 1024) return W4A16_ERR_UNSUPPORTED;
+  if (M > kTcMaxM || K < 1024) return W4A16_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(qweight_packed) |
        reinterpret_cast<uintptr_t>(scales_packed)) % 16 != 0 ||
       reinterpret_cast<uintptr_t>(out) % 4 != 0)

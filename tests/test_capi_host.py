@@ -67,7 +67,7 @@ def test_linear_rejects_bad_arguments_before_any_launch(L):
     assert args(p, 0, 2048, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG
     assert args(p, 4, 2000, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG
     assert args(p, 4, 2048, 2000, ws, 1 << 20) == _lib.ERR_INVALID_ARG
-    assert args(p, 65, 2048, 2048, ws, 1 << 20) == _lib.ERR_UNSUPPORTED
+    assert args(p, 81, 2048, 2048, ws, 1 << 20) == _lib.ERR_UNSUPPORTED
     assert args(p, 4, 512, 2048, ws, 1 << 20) == _lib.ERR_UNSUPPORTED
     assert args(ctypes.c_void_p(0x10008), 4, 2048, 2048, ws, 1 << 20) == _lib.ERR_INVALID_ARG  # misaligned x
     assert args(p, 4, 2048, 2048, None, 1 << 20) == _lib.ERR_WORKSPACE
@@ -88,6 +88,25 @@ def test_accept_rejects_bad_arguments_before_any_launch(L):
              None) == _lib.ERR_INVALID_ARG  # V % 4 == 0 wants 16-byte rows
     assert f(p, None, p, None, None, 1, 4, 100, p, p, None, 1 << 20, None) == _lib.ERR_WORKSPACE
     assert f(p, None, p, None, None, 1, 4, 100, p, p, ws, 16, None) == _lib.ERR_WORKSPACE
+
+
+def test_fused_lm_head_and_prestat_accept_reject_bad_arguments(L):
+    p = ctypes.c_void_p(0x10000)
+    ws = ctypes.c_void_p(0x20000)
+    lg = lambda x, M, K, N, logits, stats, ws_: L.w4a16_linear_logits(x, M, K, p, p, N, logits, stats, ws_, 1 << 20,
+                                                                      None)
+    assert lg(None, 4, 2048, 2048, p, p, ws) == _lib.ERR_INVALID_ARG
+    assert lg(p, 4, 2048, 2048, p, None, ws) == _lib.ERR_INVALID_ARG
+    assert lg(p, 81, 2048, 2048, p, p, ws) == _lib.ERR_UNSUPPORTED
+    assert lg(p, 4, 2048, 2000, p, p, ws) == _lib.ERR_INVALID_ARG
+    assert lg(p, 4, 2048, 2048, p, ctypes.c_void_p(0x10004), ws) == _lib.ERR_INVALID_ARG  # stats 8-byte aligned
+    assert lg(p, 4, 2048, 2048, p, p, None) == _lib.ERR_WORKSPACE
+    assert L.w4a16_linear_logits_workspace_bytes(0, 2048, 2048) == 0
+    f = L.spec_accept_prestat
+    assert f(p, None, p, p, p, 1, 4, 128, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # no target statistics
+    assert f(p, p, None, p, p, 1, 4, 128, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # stochastic only
+    assert f(p, p, p, p, p, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # V % 32 != 0
+    assert f(p, p, p, p, p, 1, 4, 128, p, p, ws, 16, None) == _lib.ERR_WORKSPACE
 
 
 def test_format_calls_reject_bad_arguments(L):

@@ -50,7 +50,7 @@ def test_config_single_linear_m4():
     assert_linear_close(_gpu_linear(x, qw, sc), oracle.linear(x, qw, sc), "config 2048x2048 M=4")
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 24, 32, 33, 48, 63, 64])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 24, 32, 33, 48, 63, 64, 65, 72, 80])
 def test_all_token_counts(M):
     # several tiles along N and K, K range split across CTAs
     x, qw, sc = _case(M, 640, 3072, seed=10 + M)
@@ -198,7 +198,7 @@ def test_llama70b_shapes_sampled(full_weights, name, K, N):
     qw, sc, w = full_weights(name, K, N)
     g = synth.rng(2000 + N)
     cols = np.unique(np.concatenate([np.arange(0, 128), np.arange(N - 128, N), g.integers(0, N, 256)]))
-    for M in (1, 4, 8, 9, 16, 40, 64):  # the fragment path and four token-tile widths of the tcgen05 path
+    for M in (1, 4, 8, 9, 16, 40, 64, 80):  # the fragment path and five token-tile widths of the tcgen05 path
         x = synth.activations(M, K, seed=3000 + M)
         out = bf16_bits(sv.linear(bf16_to_dev(x), w))
         ref = oracle.linear_cols(x, qw, sc, cols)

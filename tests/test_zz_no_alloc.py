@@ -61,4 +61,4 @@ def test_noalloc_matches_workspace_linear_twice(L, M, N, K):
 def test_noalloc_rejects_bad_arguments(L):
     p = ctypes.c_void_p(0x10000)
     assert L.w4a16_linear_noalloc(None, 4, 2048, p, p, 2048, p, None) == 1
-    assert L.w4a16_linear_noalloc(p, 65, 2048, p, p, 2048, p, None) == 2
+    assert L.w4a16_linear_noalloc(p, 81, 2048, p, p, 2048, p, None) == 2
