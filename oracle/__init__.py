@@ -1,4 +1,5 @@
-"""CPU oracle for the W4A16 verify linear and the speculative accept step.
+"""CPU oracle for the W4A16 verify linear, the speculative accept step, and the
+tree-masked verify attention with its KV compaction.
 
 TEST INFRASTRUCTURE ONLY: imported by `tests/`, by `__graft_entry__.smoke()`
 and by the benchmark's CPU-baseline leg, never by the library. It is plain C
@@ -67,7 +68,12 @@ def lib():
                                                  i32, i32, i32, _P(np.int32), _P(np.int32), _P(np.float64),
                                                  _P(np.float64), _P(np.float64)]
             L.oracle_greedy_tree.argtypes = [_P(np.float32), _P(np.int32), _P(np.int32), i32, i32, i32,
-                                             _P(np.int32), _P(np.int32)]
+                                             _P(np.int32), _P(np.int32), _P(np.int32)]
+            L.oracle_tree_attention.argtypes = [_P(np.uint16), _P(np.uint16), _P(np.uint16), _P(np.int32),
+                                                ctypes.c_void_p, i32, i32, i32, i32, i32, i32, ctypes.c_double,
+                                                _P(np.float64)]
+            L.oracle_kv_compact.argtypes = [_P(np.uint16), _P(np.uint16), _P(np.int32), ctypes.c_void_p,
+                                            _P(np.int32), i32, i32, i32, i32, i32, i32, _P(np.int32)]
             L.oracle_greedy_chain.argtypes = [_P(np.float32), _P(np.int32), i32, i32, i32, _P(np.int32),
                                               _P(np.int32)]
             L.oracle_num_threads.restype = ctypes.c_int
@@ -179,18 +185,59 @@ def spec_accept_seq(p, q, d, u):
     return acc, nxt, alpha, margin_alpha, margin_cdf
 
 
-def greedy_tree(p, draft, parents):
-    """Greedy tree verification. p [B,n,V], draft [B,n], parents [B,n] (or [n])."""
+def greedy_tree(p, draft, parents, want_node: bool = False):
+    """Greedy tree verification. p [B,n,V], draft [B,n], parents [B,n] (or [n]).
+    Returns (accepted_len, next_token) and, with want_node, the deepest
+    accepted node's index."""
     p, draft = _c(p, np.float32), _c(draft, np.int32)
     B, n, V = p.shape
+    parents = _parents(parents, B, n)
+    acc = np.empty(B, dtype=np.int32)
+    nxt = np.empty(B, dtype=np.int32)
+    node = np.empty(B, dtype=np.int32)
+    lib().oracle_greedy_tree(p, draft, parents, B, n, V, acc, nxt, node)
+    return (acc, nxt, node) if want_node else (acc, nxt)
+
+
+def _parents(parents, B, n):
     parents = np.asarray(parents, dtype=np.int32)
     if parents.ndim == 1:
         parents = np.broadcast_to(parents, (B, n))
-    parents = _c(parents, np.int32)
-    acc = np.empty(B, dtype=np.int32)
-    nxt = np.empty(B, dtype=np.int32)
-    lib().oracle_greedy_tree(p, draft, parents, B, n, V, acc, nxt)
-    return acc, nxt
+    return _c(parents, np.int32)
+
+
+def tree_attention(q, k_cache, v_cache, lens, parents=None, scale=None):
+    """Tree-masked attention of the verify pass. q bf16 bits [B,n,H,D];
+    caches bf16 bits [B,Hkv,Lcap,D] holding the prefix at 0..lens-1 and the
+    tree nodes at lens..lens+n-1; parents [B,n] / [n] or None (chain).
+    Returns fp64 [B,n,H,D]."""
+    q, k_cache, v_cache = _c(q, np.uint16), _c(k_cache, np.uint16), _c(v_cache, np.uint16)
+    B, n, H, D = q.shape
+    _, Hkv, Lcap, _ = k_cache.shape
+    lens = _c(lens, np.int32)
+    assert k_cache.shape == v_cache.shape == (B, Hkv, Lcap, D) and lens.shape == (B,)
+    assert int(lens.max()) + n <= Lcap and H % Hkv == 0
+    par = None if parents is None else _parents(parents, B, n)
+    out = np.empty((B, n, H, D), dtype=np.float64)
+    lib().oracle_tree_attention(q, k_cache, v_cache, lens, None if par is None else par.ctypes.data, B, n, H, Hkv, D,
+                                Lcap, float(D ** -0.5 if scale is None else scale), out)
+    return out
+
+
+def kv_compact(k_cache, v_cache, lens, parents, accepted_node):
+    """Moves the accepted root path's keys/values to lens..lens+depth (copies;
+    caches bf16 bits [layers,B,Hkv,Lcap,D]). Returns (k, v, new_lens)."""
+    k = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    v = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    nl, B, Hkv, Lcap, D = k.shape
+    node = _c(accepted_node, np.int32)
+    lens = _c(lens, np.int32)
+    n = int(np.asarray(parents).shape[-1]) if parents is not None else int(node.max()) + 1
+    par = None if parents is None else _parents(parents, B, n)
+    new_lens = np.empty(B, dtype=np.int32)
+    lib().oracle_kv_compact(k, v, lens, None if par is None else par.ctypes.data, node, B, n, Hkv, D, Lcap, nl,
+                            new_lens)
+    return k, v, new_lens
 
 
 def greedy_chain(p, draft):

@@ -17,6 +17,10 @@
  *    min(1, p(d_i)/q(d_i)), accept when u < alpha_i, sequential acceptance,
  *    and sampling from the corrected distribution at the first rejection;
  *    greedy decoding gives the target's own output.
+ *  - "Speculative Decoding이란?", section 10.1 (Medusa tree-based attention),
+ *    section 10.4 (ReDrafter dynamic tree attention) and section 8.7 (KV cache
+ *    reuse in serving): the tree-masked attention of the verify pass and the
+ *    compaction of the accepted path's keys and values.
  *  - The 4-bit format (int4 symmetric, group 128 along K, fp16 scale =
  *    max|w|/7, 8 nibbles per uint32) is fixed by the task specification, not
  *    by the pages.
@@ -303,10 +307,11 @@ static int argmax_row(const float* row, int V) {
  * Greedy verification of a token tree. p [B][n][V]: row j is the target's
  * distribution after the path root..j. draft [B][n] (slot 0 unused), parents
  * [B][n] (parent[0] = -1, 0 <= parent[j] < j).
- * accepted_len = depth of the deepest accepted node; next = argmax of its row.
+ * accepted_len = depth of the deepest accepted node; next = argmax of its row;
+ * accepted_node (may be NULL) = that node's index.
  */
 void oracle_greedy_tree(const float* p, const int32_t* draft, const int32_t* parents, int B, int n, int V,
-                        int32_t* accepted_len, int32_t* next_token) {
+                        int32_t* accepted_len, int32_t* next_token, int32_t* accepted_node) {
 #pragma omp parallel for schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         int* acc = (int*)malloc(sizeof(int) * (size_t)n);
@@ -323,6 +328,7 @@ void oracle_greedy_tree(const float* p, const int32_t* draft, const int32_t* par
         }
         accepted_len[b] = depth[best];
         next_token[b] = argmax_row(pb + (int64_t)best * V, V);
+        if (accepted_node) accepted_node[b] = best;
         free(acc);
         free(depth);
     }
@@ -342,6 +348,113 @@ void oracle_greedy_chain(const float* p, const int32_t* draft, int B, int K, int
             }
         accepted_len[b] = r;
         next_token[b] = argmax_row(pb + (int64_t)r * V, V);
+    }
+}
+
+/* ------------------------------------------------ tree-masked attention */
+
+/*
+ * Attention of the verify pass over a token tree (the tutorial page, section
+ * 10.1, Medusa "tree-based attention": the candidate continuations form a
+ * tree and the target checks them in one pass; section 10.4, ReDrafter's
+ * dynamic tree attention; a sequence draft is the chain parent[j] = j - 1).
+ *
+ * Readings (the pages give no formula):
+ *  - every tree node j is one query position; it attends to the whole
+ *    committed prefix (cache positions 0 .. lens[b] - 1) and to the tree
+ *    nodes on its own root path, itself included, whose keys and values the
+ *    verify forward has written at cache positions lens[b] + node index;
+ *  - scaled dot-product attention, scale given (1/sqrt(D) in use), softmax at
+ *    temperature 1 over the allowed keys;
+ *  - grouped heads: query head h reads key/value head h / (H / Hkv).
+ *
+ * q bf16 bits [B][n][H][D]; k_cache, v_cache bf16 bits [B][Hkv][Lcap][D];
+ * lens [B]; parents [B][n] (parent[0] = -1, 0 <= parent[j] < j) or NULL for
+ * the chain; out fp64 [B][n][H][D]. Scores, softmax and the weighted sum in
+ * fp64.
+ */
+void oracle_tree_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* lens,
+                           const int32_t* parents, int B, int n, int H, int Hkv, int D, int Lcap, double scale,
+                           double* out) {
+    const int G = H / Hkv;
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < n; ++j) {
+            const int L = lens[b];
+            const int T = L + n;
+            char* allowed = (char*)calloc((size_t)T, 1);
+            double* s = (double*)malloc(sizeof(double) * (size_t)T);
+            for (int x = 0; x < L; ++x) allowed[x] = 1;
+            for (int i = j; i >= 0; i = parents ? parents[(int64_t)b * n + i] : i - 1) allowed[L + i] = 1;
+            for (int h = 0; h < H; ++h) {
+                const int kvh = h / G;
+                const uint16_t* qr = q + (((int64_t)b * n + j) * H + h) * D;
+                const uint16_t* kb = k_cache + ((int64_t)b * Hkv + kvh) * Lcap * D;
+                const uint16_t* vb = v_cache + ((int64_t)b * Hkv + kvh) * Lcap * D;
+                double m = -INFINITY;
+                for (int x = 0; x < T; ++x) {
+                    if (!allowed[x]) continue;
+                    double dot = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dot += (double)bf16_to_f32(qr[d]) * (double)bf16_to_f32(kb[(int64_t)x * D + d]);
+                    s[x] = dot * scale;
+                    if (s[x] > m) m = s[x];
+                }
+                double* o = out + (((int64_t)b * n + j) * H + h) * D;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                double Z = 0.0;
+                for (int x = 0; x < T; ++x) {
+                    if (!allowed[x]) continue;
+                    const double w = exp(s[x] - m);
+                    Z += w;
+                    for (int d = 0; d < D; ++d) o[d] += w * (double)bf16_to_f32(vb[(int64_t)x * D + d]);
+                }
+                for (int d = 0; d < D; ++d) o[d] /= Z;
+            }
+            free(allowed);
+            free(s);
+        }
+}
+
+/*
+ * KV compaction after verification (the tutorial page, section 8.7: the
+ * serving stack must not waste cache on rejected tokens; ReDrafter's dynamic
+ * tree attention). The tree nodes' keys and values sit at cache positions
+ * lens[b] + node index; after acceptance the nodes on the root path of the
+ * deepest accepted node (root first) move to positions lens[b] + 0, 1, ...,
+ * depth, and the committed length becomes lens[b] + depth + 1. Reading: the
+ * root (node 0, the last committed token, verified with the drafts) is
+ * always kept; positions past the new length keep whatever they held.
+ *
+ * caches bf16 bits [n_layers][B][Hkv][Lcap][D], updated in place; parents
+ * [B][n] or NULL (chain); accepted_node [B]; new_lens [B].
+ */
+void oracle_kv_compact(uint16_t* k_cache, uint16_t* v_cache, const int32_t* lens, const int32_t* parents,
+                       const int32_t* accepted_node, int B, int n, int Hkv, int D, int Lcap, int n_layers,
+                       int32_t* new_lens) {
+    for (int b = 0; b < B; ++b) {
+        int path[1025];
+        int depth = 0;
+        for (int i = accepted_node[b]; i >= 0 && depth < 1025; i = parents ? parents[(int64_t)b * n + i] : i - 1)
+            path[depth++] = i;
+        /* path[depth - 1] is the root: reverse into root-first order */
+        for (int a = 0, z = depth - 1; a < z; ++a, --z) {
+            const int t = path[a];
+            path[a] = path[z];
+            path[z] = t;
+        }
+        const int L = lens[b];
+        new_lens[b] = L + depth;
+        uint16_t* tmp = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)n * D);
+        for (int layer = 0; layer < n_layers; ++layer)
+            for (int h = 0; h < Hkv; ++h)
+                for (int c = 0; c < 2; ++c) {
+                    uint16_t* base = (c ? v_cache : k_cache) + (((int64_t)layer * B + b) * Hkv + h) * Lcap * D;
+                    memcpy(tmp, base + (int64_t)L * D, sizeof(uint16_t) * (size_t)n * D);
+                    for (int d = 0; d < depth; ++d)
+                        memcpy(base + (int64_t)(L + d) * D, tmp + (int64_t)path[d] * D, sizeof(uint16_t) * (size_t)D);
+                }
+        free(tmp);
     }
 }
 

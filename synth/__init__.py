@@ -156,3 +156,29 @@ def greedy_chain_case(B: int, K: int, V: int, seed: int, match_prob: float = 0.8
                 t = int(g.integers(0, V - 1))
                 draft[b, i] = t if t < planted[b, i] else t + 1
     return p, draft
+
+
+def attention_case(B: int, n: int, H: int, Hkv: int, D: int, lens, Lcap: int, seed: int, tree: bool = True,
+                   max_depth: int = 6):
+    """Verify-attention inputs (Llama-3 geometry: H query heads over Hkv
+    key/value heads of width D): q [B,n,H,D] and the key / value caches
+    [B,Hkv,Lcap,D], all N(0,1) as bf16 bit patterns; the committed prefix of
+    row b at cache positions 0..lens[b]-1 and the n tree nodes' own keys and
+    values at lens[b]..lens[b]+n-1. parents [B,n]: a random tree per row
+    (depth < max_depth), or the chain parent[j] = j - 1 when tree is False."""
+    g = rng(seed)
+    lens = np.asarray(lens, dtype=np.int32)
+    assert lens.shape == (B,) and int(lens.max()) + n <= Lcap
+    q = bf16_bits_from_f32(g.standard_normal((B, n, H, D), dtype=np.float32))
+    k = bf16_bits_from_f32(g.standard_normal((B, Hkv, Lcap, D), dtype=np.float32))
+    v = bf16_bits_from_f32(g.standard_normal((B, Hkv, Lcap, D), dtype=np.float32))
+    if tree:
+        parents = np.stack([random_tree_parents(n, max_depth, g) for _ in range(B)])
+    else:
+        parents = np.broadcast_to(np.arange(-1, n - 1, dtype=np.int32), (B, n)).copy()
+    return q, k, v, lens, parents
+
+
+def attention_lens(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
+    """Ragged committed lengths, uniform in [lo, hi)."""
+    return rng(seed).integers(lo, hi, size=B).astype(np.int32)
