@@ -191,6 +191,78 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_accept that also reports the accepted node: accepted_node[B] int32
+ * (device, required) = the deepest accepted tree node in greedy tree mode,
+ * accepted_len in the sequence modes (a chain's node index is its depth).
+ * kv_compact takes it. Everything else as spec_accept.
+ */
+w4a16_status spec_accept_node(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                              const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                              int32_t* accepted_len, int32_t* next_token, int32_t* accepted_node, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Tree-masked attention of the verify pass (the tutorial page, section
+ * 10.1: Medusa's tree-based attention verifies every candidate continuation
+ * of a token tree in one target pass; section 10.4: ReDrafter's dynamic tree
+ * attention; a sequence draft is the chain parent[j] = j - 1).
+ *
+ * Every tree node j is a query position. It attends to the whole committed
+ * prefix of its batch row (cache positions 0 .. lens[b] - 1) and to the tree
+ * nodes on its own root path, itself included, whose keys and values the
+ * verify forward has written at cache positions lens[b] + node index.
+ * out = softmax(scale * q . k over the allowed keys) . v, per query head;
+ * query head h reads key/value head h / (H / Hkv).
+ *
+ *   q             device bf16 [B][n][H][D] (16-byte aligned)
+ *   k_cache, v_cache  device bf16 [B][Hkv][Lcap][D] (16-byte aligned)
+ *   lens          device int32 [B]: committed lengths, 0 <= lens[b] <= max_len
+ *   tree_parents  device int32 [B][n] (parent[0] = -1, 0 <= parent[j] < j),
+ *                 or NULL for a sequence draft (the chain)
+ *   n             tree nodes, 1 .. 64; D = 128 (else W4A16_ERR_UNSUPPORTED)
+ *   max_len       an upper bound of lens[] known to the caller (it sizes the
+ *                 key splits); max_len + n <= Lcap
+ *   scale         softmax scale (1 / sqrt(D) for the model), finite, > 0
+ *   out           device bf16 [B][n][H][D] (16-byte aligned)
+ *   workspace     device scratch of tree_attention_workspace_bytes() bytes
+ *                 (256-byte aligned; may be NULL when that is 0); needs no
+ *                 initialisation
+ * Arithmetic: bf16 inputs, fp32 scores and sums; the softmax weights are
+ * rounded to bf16 for the weighted sum of the values and normalised by the
+ * sum of those rounded weights; out rounded to bf16.
+ * A lens[b] outside [0, max_len] or a bad parent sets W4A16_ERR_DEVICE_INPUT
+ * in the device error word (the length is clamped, the node then attends to
+ * itself and the prefix only). Launch rules as for w4a16_linear.
+ */
+size_t tree_attention_workspace_bytes(int B, int n, int H, int Hkv, int D, int Lcap, int max_len);
+w4a16_status tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
+                            const int32_t* tree_parents, int B, int n, int H, int Hkv, int D, int Lcap, int max_len,
+                            float scale, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * KV compaction after verification (the tutorial page, section 8.7: the
+ * cache must not keep rejected tokens; section 10.4). The keys and values of
+ * the nodes on the root path of accepted_node[b] (root first) move to cache
+ * positions lens[b] + 0, 1, ..., depth, in every layer and head, and
+ * new_lens[b] = lens[b] + depth + 1 (the root, node 0, is always kept).
+ * Positions from new_lens[b] on keep stale values.
+ *
+ *   k_cache, v_cache  device bf16 [n_layers][B][Hkv][Lcap][D], updated in
+ *                 place (16-byte aligned; D a multiple of 8,
+ *                 2 * Hkv * D <= 32768)
+ *   lens          device int32 [B], 0 <= lens[b] <= Lcap - n
+ *   tree_parents  as for tree_attention (NULL: chain)
+ *   accepted_node device int32 [B] in [0, n) (spec_accept_node)
+ *   new_lens      device int32 [B] (may not alias lens)
+ *   n             1 .. 64
+ * Bad input sets W4A16_ERR_DEVICE_INPUT in the device error word (the row
+ * then keeps the root only).
+ */
+w4a16_status kv_compact(void* k_cache, void* v_cache, const int32_t* lens, const int32_t* tree_parents,
+                        const int32_t* accepted_node, int B, int n, int Hkv, int D, int Lcap, int n_layers,
+                        int32_t* new_lens, void* stream);
+
+/* ------------------------------------------------------------------------
  * Stochastic sequence accept with the target rows' statistics supplied
  * (from w4a16_linear_logits over the B * (n + 1) verify positions): the same
  * decisions, draw and outputs as spec_accept in stochastic sequence mode, but

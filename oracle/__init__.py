@@ -71,7 +71,7 @@ def lib():
                                              _P(np.int32), _P(np.int32), _P(np.int32)]
             L.oracle_tree_attention.argtypes = [_P(np.uint16), _P(np.uint16), _P(np.uint16), _P(np.int32),
                                                 ctypes.c_void_p, i32, i32, i32, i32, i32, i32, ctypes.c_double,
-                                                _P(np.float64)]
+                                                _P(np.float64), ctypes.c_void_p]
             L.oracle_kv_compact.argtypes = [_P(np.uint16), _P(np.uint16), _P(np.int32), ctypes.c_void_p,
                                             _P(np.int32), i32, i32, i32, i32, i32, i32, _P(np.int32)]
             L.oracle_greedy_chain.argtypes = [_P(np.float32), _P(np.int32), i32, i32, i32, _P(np.int32),
@@ -206,11 +206,12 @@ def _parents(parents, B, n):
     return _c(parents, np.int32)
 
 
-def tree_attention(q, k_cache, v_cache, lens, parents=None, scale=None):
+def tree_attention(q, k_cache, v_cache, lens, parents=None, scale=None, want_abs: bool = False):
     """Tree-masked attention of the verify pass. q bf16 bits [B,n,H,D];
     caches bf16 bits [B,Hkv,Lcap,D] holding the prefix at 0..lens-1 and the
     tree nodes at lens..lens+n-1; parents [B,n] / [n] or None (chain).
-    Returns fp64 [B,n,H,D]."""
+    Returns fp64 [B,n,H,D] (and, with want_abs, the softmax-weighted sum of
+    |v|, same shape)."""
     q, k_cache, v_cache = _c(q, np.uint16), _c(k_cache, np.uint16), _c(v_cache, np.uint16)
     B, n, H, D = q.shape
     _, Hkv, Lcap, _ = k_cache.shape
@@ -219,9 +220,11 @@ def tree_attention(q, k_cache, v_cache, lens, parents=None, scale=None):
     assert int(lens.max()) + n <= Lcap and H % Hkv == 0
     par = None if parents is None else _parents(parents, B, n)
     out = np.empty((B, n, H, D), dtype=np.float64)
+    absw = np.empty((B, n, H, D), dtype=np.float64) if want_abs else None
     lib().oracle_tree_attention(q, k_cache, v_cache, lens, None if par is None else par.ctypes.data, B, n, H, Hkv, D,
-                                Lcap, float(D ** -0.5 if scale is None else scale), out)
-    return out
+                                Lcap, float(D ** -0.5 if scale is None else scale), out,
+                                None if absw is None else absw.ctypes.data)
+    return (out, absw) if want_abs else out
 
 
 def kv_compact(k_cache, v_cache, lens, parents, accepted_node):

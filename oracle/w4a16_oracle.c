@@ -371,11 +371,13 @@ void oracle_greedy_chain(const float* p, const int32_t* draft, int B, int K, int
  * q bf16 bits [B][n][H][D]; k_cache, v_cache bf16 bits [B][Hkv][Lcap][D];
  * lens [B]; parents [B][n] (parent[0] = -1, 0 <= parent[j] < j) or NULL for
  * the chain; out fp64 [B][n][H][D]. Scores, softmax and the weighted sum in
- * fp64.
+ * fp64. absw (may be NULL) [B][n][H][D]: sum over the allowed keys of
+ * softmax weight * |v|, the scale of the rounding errors a reduced-precision
+ * weighted sum can make.
  */
 void oracle_tree_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache, const int32_t* lens,
                            const int32_t* parents, int B, int n, int H, int Hkv, int D, int Lcap, double scale,
-                           double* out) {
+                           double* out, double* absw) {
     const int G = H / Hkv;
 #pragma omp parallel for collapse(2) schedule(dynamic)
     for (int b = 0; b < B; ++b)
@@ -401,15 +403,24 @@ void oracle_tree_attention(const uint16_t* q, const uint16_t* k_cache, const uin
                     if (s[x] > m) m = s[x];
                 }
                 double* o = out + (((int64_t)b * n + j) * H + h) * D;
+                double* a = absw ? absw + (((int64_t)b * n + j) * H + h) * D : NULL;
                 for (int d = 0; d < D; ++d) o[d] = 0.0;
+                if (a)
+                    for (int d = 0; d < D; ++d) a[d] = 0.0;
                 double Z = 0.0;
                 for (int x = 0; x < T; ++x) {
                     if (!allowed[x]) continue;
                     const double w = exp(s[x] - m);
                     Z += w;
-                    for (int d = 0; d < D; ++d) o[d] += w * (double)bf16_to_f32(vb[(int64_t)x * D + d]);
+                    for (int d = 0; d < D; ++d) {
+                        const double vv = (double)bf16_to_f32(vb[(int64_t)x * D + d]);
+                        o[d] += w * vv;
+                        if (a) a[d] += w * fabs(vv);
+                    }
                 }
                 for (int d = 0; d < D; ++d) o[d] /= Z;
+                if (a)
+                    for (int d = 0; d < D; ++d) a[d] /= Z;
             }
             free(allowed);
             free(s);

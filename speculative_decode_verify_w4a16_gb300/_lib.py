@@ -45,6 +45,11 @@ SIGNATURES = {
     "w4a16_linear_logits_workspace_bytes": (_sz, [_i32, _i64, _i64]),
     "w4a16_linear_logits": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp, _vp, _sz, _vp]),
     "spec_accept_prestat": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "spec_accept_node": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tree_attention_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "tree_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
+                              _vp, _vp, _sz, _vp]),
+    "kv_compact": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "w4a16_linear_noalloc_scratch_bytes": (_sz, []),
     "w4a16_linear_noalloc": (_i32, [_vp, _i32, _i64, _vp, _vp, _i64, _vp, _vp]),
 }

@@ -229,6 +229,91 @@ def spec_accept_prestat(p_logits: torch.Tensor, p_stats: torch.Tensor, draft_ids
     return accepted_len, next_token
 
 
+def spec_accept_node(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: Optional[torch.Tensor] = None,
+                     tree_parents: Optional[torch.Tensor] = None, uniforms: Optional[torch.Tensor] = None,
+                     ws: Optional[torch.Tensor] = None, stream=None):
+    """spec_accept that also returns the accepted node:
+    (accepted_len, next_token, accepted_node), int32 [B] each."""
+    _need(p_logits, "p_logits", torch.float32)
+    B, rows, V = p_logits.shape
+    n = rows if tree_parents is not None else rows - 1
+    _need(draft_ids, "draft_ids", torch.int32, (B, n))
+    if tree_parents is not None:
+        _need(tree_parents, "tree_parents", torch.int32, (B, n))
+    if q_logits is not None:
+        _need(q_logits, "q_logits", torch.float32, (B, n, V))
+    if uniforms is not None:
+        _need(uniforms, "uniforms", torch.float32, (B, n + 1))
+    acc, nxt, node = (torch.empty(B, dtype=torch.int32, device=p_logits.device) for _ in range(3))
+    if ws is None:
+        ws = workspace(accept_workspace_bytes(B, n, V), p_logits.device, "accept")
+    check(lib().spec_accept_node(_ptr(p_logits), _ptr(q_logits), _ptr(draft_ids), _ptr(tree_parents),
+                                 _ptr(uniforms), B, n, V, _ptr(acc), _ptr(nxt), _ptr(node), _ptr(ws), ws.numel(),
+                                 _stream(stream)), "spec_accept_node")
+    return acc, nxt, node
+
+
+# ------------------------------------------------------ verify attention
+
+def tree_attention_workspace_bytes(B: int, n: int, H: int, Hkv: int, D: int, Lcap: int, max_len: int) -> int:
+    return int(lib().tree_attention_workspace_bytes(B, n, H, Hkv, D, Lcap, max_len))
+
+
+def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, lens: torch.Tensor,
+                   tree_parents: Optional[torch.Tensor] = None, max_len: Optional[int] = None,
+                   scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                   ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tree-masked verify attention. q bf16 [B, n, H, D]; caches bf16
+    [B, Hkv, Lcap, D] (prefix at 0..lens-1, the tree nodes at lens..lens+n-1);
+    lens int32 [B]; tree_parents int32 [B, n] or None (chain); max_len: an
+    upper bound of lens (default Lcap - n). Returns bf16 [B, n, H, D]."""
+    _need(q, "q", torch.bfloat16)
+    B, n, H, D = q.shape
+    _need(k_cache, "k_cache", torch.bfloat16)
+    Hkv, Lcap = k_cache.shape[1], k_cache.shape[2]
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Hkv, Lcap, D))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Hkv, Lcap, D))
+    _need(lens, "lens", torch.int32, (B,))
+    if tree_parents is not None:
+        _need(tree_parents, "tree_parents", torch.int32, (B, n))
+    max_len = Lcap - n if max_len is None else int(max_len)
+    scale = D ** -0.5 if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, n, H, D), dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, (B, n, H, D))
+    nbytes = tree_attention_workspace_bytes(B, n, H, Hkv, D, Lcap, max_len)
+    if ws is None and nbytes > 0:
+        ws = workspace(nbytes, q.device, "attention")
+    check(lib().tree_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), _ptr(tree_parents), B, n, H, Hkv,
+                               D, Lcap, max_len, scale, _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(),
+                               _stream(stream)), "tree_attention")
+    return out
+
+
+def kv_compact(k_cache: torch.Tensor, v_cache: torch.Tensor, lens: torch.Tensor, accepted_node: torch.Tensor,
+               tree_parents: Optional[torch.Tensor] = None, n: Optional[int] = None,
+               new_lens: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Moves the accepted root path's keys/values to lens..lens+depth in
+    place. Caches bf16 [layers, B, Hkv, Lcap, D] (or [B, Hkv, Lcap, D]);
+    tree_parents [B, n] or None (chain, then n is required). Returns new_lens."""
+    _need(k_cache, "k_cache", torch.bfloat16)
+    kc, vc = (k_cache, v_cache) if k_cache.dim() == 5 else (k_cache.unsqueeze(0), v_cache.unsqueeze(0))
+    layers, B, Hkv, Lcap, D = kc.shape
+    _need(vc, "v_cache", torch.bfloat16, (layers, B, Hkv, Lcap, D))
+    _need(lens, "lens", torch.int32, (B,))
+    _need(accepted_node, "accepted_node", torch.int32, (B,))
+    if tree_parents is not None:
+        n = tree_parents.shape[1]
+        _need(tree_parents, "tree_parents", torch.int32, (B, n))
+    elif n is None:
+        raise ValueError("n is required for a sequence draft")
+    if new_lens is None:
+        new_lens = torch.empty(B, dtype=torch.int32, device=lens.device)
+    check(lib().kv_compact(_ptr(kc), _ptr(vc), _ptr(lens), _ptr(tree_parents), _ptr(accepted_node), B, int(n), Hkv,
+                           D, Lcap, layers, _ptr(new_lens), _stream(stream)), "kv_compact")
+    return new_lens
+
+
 def check_device_status(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status."""
     return int(lib().w4a16_check_device_status(_stream(stream)))

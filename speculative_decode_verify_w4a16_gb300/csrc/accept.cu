@@ -503,7 +503,7 @@ template <int RS, bool VEC>  // values per thread in a chunk: chunk2 <= RS * kAc
 __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
     int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
-    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out) {
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int b = blockIdx.y;
@@ -700,6 +700,7 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
   if (threadIdx.x == 0) {
     acc_out[b] = r;
     next_out[b] = sh_found;
+    if (node_out) node_out[b] = r;  // a sequence draft's node index is its depth
   }
 }
 
@@ -724,7 +725,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     const float* __restrict__ p, const int32_t* __restrict__ d, const int32_t* __restrict__ parents, int n,
     int rows_per_b, int V, int chunk, ArgPart* __restrict__ parts, int* __restrict__ counters,
-    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, unsigned* err) {
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out, unsigned* err) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int rr = blockIdx.y;  // row index over all batch rows
@@ -822,6 +823,7 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     }
     acc_out[b] = acc;
     next_out[b] = gs.amax[best_node];
+    if (node_out) node_out[b] = best_node;
   }
 }
 
@@ -874,7 +876,7 @@ AcceptPlan accept_plan(int B, int n, int V) {
 
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
                               int32_t* acc, int32_t* next, void* ws, const AcceptPlan& pl, int num_sms, unsigned* err,
-                              cudaStream_t stream, const float2* p_stats) {
+                              cudaStream_t stream, const float2* p_stats, int32_t* node) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   RowStat* stats = reinterpret_cast<RowStat*>(w + pl.stats_off);
   Decision* dec = reinterpret_cast<Decision*>(w + pl.dec_off);
@@ -919,14 +921,14 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   ch2 = (V + chunk2 - 1) / chunk2;
   if (V % 4 == 0)
     return launch_pdl(accept_resid_kernel<kResidPT, true>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
-                      chunk2, (const Decision*)dec, csum, cnt2, acc, next);
+                      chunk2, (const Decision*)dec, csum, cnt2, acc, next, node);
   return launch_pdl(accept_resid_kernel<kResidPT, false>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
-                    chunk2, (const Decision*)dec, csum, cnt2, acc, next);
+                    chunk2, (const Decision*)dec, csum, cnt2, acc, next, node);
 }
 
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
                                  int32_t* acc, int32_t* next, void* ws, const AcceptPlan& pl, unsigned* err,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, int32_t* node) {
   uint8_t* w = static_cast<uint8_t*>(ws);
   ArgPart* parts = reinterpret_cast<ArgPart*>(w + pl.stats_off);
   int* cnt = reinterpret_cast<int*>(w);
@@ -934,9 +936,9 @@ cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t
   const dim3 g(pl.cha, B * rows_per_b);
   if (V % 4 == 0)
     return launch_pdl(accept_argmax_kernel<true>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                      pl.chunka, parts, cnt, acc, next, err);
+                      pl.chunka, parts, cnt, acc, next, node, err);
   return launch_pdl(accept_argmax_kernel<false>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                    pl.chunka, parts, cnt, acc, next, err);
+                    pl.chunka, parts, cnt, acc, next, node, err);
 }
 
 }  // namespace w4a16

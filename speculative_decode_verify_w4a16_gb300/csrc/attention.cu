@@ -1,0 +1,523 @@
+// Tree-masked attention of the verify pass and compaction of the accepted
+// path's keys and values ("Speculative Decoding이란?", section 10.1: Medusa's
+// tree-based attention checks all candidate continuations of a token tree in
+// one target pass; section 10.4: ReDrafter's dynamic tree attention; section
+// 8.7: how a serving stack reuses the KV cache across accepted and rejected
+// tokens).
+//
+// tree_attention_kernel: one CTA per (query-row block, key split, KV head,
+// batch row). The query rows of a KV head are its G = H / Hkv query heads at
+// every tree node, row r = node * G + head-in-group, 16 rows per warp. The
+// keys and values stream through a two-stage shared-memory ring of 64-key
+// blocks (2-D TMA, 128-byte swizzle). Each warp forms S = Q K^T with
+// mma.sync m16n8k16 (bf16 in, fp32 accumulate), masks it (the committed
+// prefix: every key; the tree's own keys: the node's ancestors and itself, a
+// 64-bit mask per node), keeps the running maximum and sum of the online
+// softmax in the log2 domain, and accumulates P V with P rounded to bf16
+// (the sum is taken over the same rounded values). With one split the rows
+// are normalised and stored as bf16; otherwise each split stores fp32
+// (m, l, O) and tree_attention_combine_kernel merges the splits.
+//
+// kv_compact_kernel: per (batch row, layer), the keys and values of the
+// accepted root path move to the positions right after the committed prefix.
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <float.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace w4a16 {
+
+constexpr int kAttD = 128;                     // head width
+constexpr int kAttKeys = 64;                   // keys per block
+constexpr int kAttStages = 2;                  // key/value ring depth
+constexpr int kAttHalf = kAttKeys * 64 * 2;    // one 64-wide half of a key or value block: 8 KiB
+constexpr int kAttStage = 4 * kAttHalf;        // key halves, then value halves: 32 KiB
+constexpr int kAttMaxNodes = 64;
+constexpr int kAttCtasPerSm = 2;
+
+struct AttnParams {
+  const __nv_bfloat16* q;  // [B][n][H][D]
+  const int32_t* lens;     // [B]
+  const int32_t* parents;  // [B][n] or null (chain)
+  __nv_bfloat16* out;      // [B][n][H][D]
+  float* part_o;           // splits > 1: [splits][B][Hkv][rows_pad][D] unnormalised sums
+  float2* part_ml;         // and [splits][B][Hkv][rows_pad] (running max, sum), log2 domain
+  unsigned* err;
+  int B, n, H, Hkv, G, Lcap, max_len;
+  int rows;        // n * G query rows per KV head
+  int rows_pad;    // row_blocks * 16 * warps
+  int row_blocks;
+  int splits, blocks_per_split;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void attn_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+               "{%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 2^x by the hardware approximation (a few ulp; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// two fp32 values rounded to a bf16 pair (low half = first), and the rounded values back
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, float& rhi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  rlo = __low2float(h);
+  rhi = __high2float(h);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int NW>
+struct AttnLayout {
+  static constexpr int kKvOff = 0;
+  static constexpr int kQOff = kAttStages * kAttStage;          // [16 NW rows][128] bf16, 256-byte rows
+  static constexpr int kAncOff = kQOff + 16 * NW * kAttD * 2;  // [kAttMaxNodes] uint64
+  static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;   // full[kAttStages]
+  static constexpr int kTotal = kBarOff + kAttStages * 8 + 1024;  // + alignment of the swizzled stages
+};
+
+template <int NW>
+__global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                                const __grid_constant__ CUtensorMap vmap,
+                                                                                const AttnParams p) {
+  using L_ = AttnLayout<NW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* qs = smem + L_::kQOff;
+  uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L_::kAncOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::kBarOff);
+  __shared__ int s_len;
+
+  const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  grid_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+  }
+  grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
+  if (tid == 0) {
+    int len = p.lens[b];
+    const int hi = min(p.max_len, p.Lcap - p.n);
+    if (len < 0 || len > hi) {
+      report_error(p.err, kErrInput);
+      len = len < 0 ? 0 : hi;
+    }
+    s_len = len;
+    // ancestor-or-self mask of every node (node j is bit j)
+    bool bad = false;
+    for (int j = 0; j < p.n; ++j) {
+      int par = p.parents ? p.parents[(int64_t)b * p.n + j] : j - 1;
+      if (j == 0 ? par != -1 : (par < 0 || par >= j)) {
+        bad = true;
+        par = -1;
+      }
+      anc[j] = (par >= 0 ? anc[par] : 0ull) | (1ull << j);
+    }
+    if (bad) report_error(p.err, kErrInput);
+  }
+  __syncthreads();
+  const int len = s_len;
+  const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
+  const int blk0 = split * p.blocks_per_split;
+  const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
+  const int64_t kv_row0 = ((int64_t)b * p.Hkv + kvh) * p.Lcap;
+
+  // block blk0 + i of this split into stage i % kAttStages (rows past the
+  // head's keys are masked; past the whole cache the copy fills zeros)
+  auto issue = [&](int i) {
+    const int s = i % kAttStages;
+    uint8_t* st = smem + L_::kKvOff + s * kAttStage;
+    const int32_t y = (int32_t)(kv_row0 + (int64_t)(blk0 + i) * kAttKeys);
+    mbar_arrive_expect_tx(&full[s], (uint32_t)kAttStage);
+    tma_load_2d(st, &kmap, 0, y, &full[s]);
+    tma_load_2d(st + kAttHalf, &kmap, 64, y, &full[s]);
+    tma_load_2d(st + 2 * kAttHalf, &vmap, 0, y, &full[s]);
+    tma_load_2d(st + 3 * kAttHalf, &vmap, 64, y, &full[s]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < nb && i < kAttStages; ++i) issue(i);
+
+  // the CTA's query rows into shared memory (16-byte chunk c of row r at
+  // chunk c ^ (r % 8): conflict-free row reads for ldmatrix)
+  const int rows0 = rb * 16 * NW;
+  for (int idx = tid; idx < 16 * NW * 16; idx += 32 * NW) {
+    const int r = idx >> 4, c = idx & 15;
+    const int R = rows0 + r;
+    const int j = R / p.G, g = R - j * p.G;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < p.n)
+      v = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD + c * 8);
+    *reinterpret_cast<uint4*>(qs + r * 256 + ((c ^ (r & 7)) << 4)) = v;
+  }
+  __syncthreads();
+
+  // this lane's two rows (mma fragment rows lane / 4 and lane / 4 + 8)
+  const int ra = rows0 + warp * 16 + (lane >> 2), rb8 = ra + 8;
+  const int ja = ra / p.G, jb = rb8 / p.G;
+  const uint64_t anc_a = ja < p.n ? anc[ja] : 0ull, anc_b = jb < p.n ? anc[jb] : 0ull;
+  const uint32_t q_base = smem_u32(qs) + warp * 16 * 256;
+  float o[16][4];
+#pragma unroll
+  for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.0f;
+  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
+
+  for (int i = 0; i < nb; ++i) {
+    const int s = i % kAttStages;
+    const bool ok = mbar_wait(&full[s], (uint32_t)(i / kAttStages) & 1u, p.err);
+    const uint32_t kst = smem_u32(smem + L_::kKvOff + s * kAttStage), vst = kst + 2 * kAttHalf;
+    // ---- S = Q K^T (16 rows x 64 keys per warp)
+    float sc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t qa[4];
+      {
+        const int r = lane & 15, c = 2 * kk + (lane >> 4);
+        ldsm_x4(q_base + r * 256 + ((c ^ (r & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
+      }
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = 2 * kk + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + (c >> 3) * kAttHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4), b0, b1, b2, b3);
+        attn_mma(sc[2 * np], qa, b0, b1);
+        attn_mma(sc[2 * np + 1], qa, b2, b3);
+      }
+    }
+    // ---- mask, online softmax (log2 domain)
+    const int key0 = (blk0 + i) * kAttKeys;
+    const bool prefix_only = key0 + kAttKeys <= len;
+    float mx_a = m_a, mx_b = m_b;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sc[nt][e] * p.scale_log2;
+        if (!prefix_only) {
+          const int pos = key0 + nt * 8 + ((lane & 3) << 1) + (e & 1);
+          const int ti = pos - len;
+          const uint64_t an = e < 2 ? anc_a : anc_b;
+          if (!(pos < len || (ti < p.n && ((an >> ti) & 1ull)))) v = -INFINITY;
+        }
+        sc[nt][e] = v;
+        if (e < 2)
+          mx_a = fmaxf(mx_a, v);
+        else
+          mx_b = fmaxf(mx_b, v);
+      }
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+    const float ua = mx_a == -INFINITY ? 0.0f : mx_a, ub = mx_b == -INFINITY ? 0.0f : mx_b;
+    const float ca = ex2(m_a - ua), cb = ex2(m_b - ub);  // 0 while the row had no key
+    m_a = mx_a;
+    m_b = mx_b;
+    l_a *= ca;
+    l_b *= cb;
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) {
+      o[dt][0] *= ca;
+      o[dt][1] *= ca;
+      o[dt][2] *= cb;
+      o[dt][3] *= cb;
+    }
+    uint32_t pa[4][4];  // P as the A operand of four 16-key steps
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      float r0, r1, r2, r3;
+      const uint32_t x01 = pack_bf16(ex2(sc[nt][0] - ua), ex2(sc[nt][1] - ua), r0, r1);
+      const uint32_t x23 = pack_bf16(ex2(sc[nt][2] - ub), ex2(sc[nt][3] - ub), r2, r3);
+      l_a += r0 + r1;
+      l_b += r2 + r3;
+      pa[nt >> 1][(nt & 1) * 2] = x01;
+      pa[nt >> 1][(nt & 1) * 2 + 1] = x23;
+    }
+    // ---- O += P V
+#pragma unroll
+    for (int kt = 0; kt < 4; ++kt)
+#pragma unroll
+      for (int dp = 0; dp < 8; ++dp) {
+        const int key = kt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int c = 2 * dp + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(vst + (c >> 3) * kAttHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4), b0, b1, b2, b3);
+        attn_mma(o[2 * dp], pa[kt], b0, b1);
+        attn_mma(o[2 * dp + 1], pa[kt], b2, b3);
+      }
+    // every warp is done with stage s: refill it (a timed-out wait ends the loop in every thread)
+    if (__syncthreads_or(!ok)) break;
+    if (tid == 0 && i + kAttStages < nb) issue(i + kAttStages);
+  }
+
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  const int t2 = (lane & 3) << 1;
+  if (p.splits == 1) {
+    const float ia = l_a > 0.0f ? 1.0f / l_a : 0.0f, ib = l_b > 0.0f ? 1.0f / l_b : 0.0f;
+    if (ja < p.n) {
+      __nv_bfloat16* dst = p.out + (((int64_t)b * p.n + ja) * p.H + kvh * p.G + (ra - ja * p.G)) * kAttD + t2;
+#pragma unroll
+      for (int dt = 0; dt < 16; ++dt)
+        *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][0] * ia, o[dt][1] * ia);
+    }
+    if (jb < p.n) {
+      __nv_bfloat16* dst = p.out + (((int64_t)b * p.n + jb) * p.H + kvh * p.G + (rb8 - jb * p.G)) * kAttD + t2;
+#pragma unroll
+      for (int dt = 0; dt < 16; ++dt)
+        *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][2] * ib, o[dt][3] * ib);
+    }
+  } else {
+    const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
+    float* pa_o = p.part_o + (base + ra) * kAttD + t2;
+    float* pb_o = p.part_o + (base + rb8) * kAttD + t2;
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) {
+      *reinterpret_cast<float2*>(pa_o + dt * 8) = make_float2(o[dt][0], o[dt][1]);
+      *reinterpret_cast<float2*>(pb_o + dt * 8) = make_float2(o[dt][2], o[dt][3]);
+    }
+    if ((lane & 3) == 0) {
+      p.part_ml[base + ra] = make_float2(m_a, l_a);
+      p.part_ml[base + rb8] = make_float2(m_b, l_b);
+    }
+  }
+}
+
+// One warp per query row: merge the splits' (m, l, O) and store the
+// normalised row as bf16 (lane k: columns 4k .. 4k + 3).
+__global__ void __launch_bounds__(256) tree_attention_combine_kernel(const AttnParams p) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int64_t per_b = (int64_t)p.Hkv * p.rows;
+  if (row >= (int64_t)p.B * per_b) return;
+  const int b = (int)(row / per_b);
+  const int kvh = (int)((row - b * per_b) / p.rows);
+  const int R = (int)(row - b * per_b - (int64_t)kvh * p.rows);
+  const int j = R / p.G, g = R - j * p.G;
+  const int64_t stride = (int64_t)p.B * p.Hkv * p.rows_pad;
+  const int64_t r0 = ((int64_t)b * p.Hkv + kvh) * p.rows_pad + R;
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&p.part_ml[r0 + s * stride]).x);
+  float lsum = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int s = 0; s < p.splits; ++s) {
+    const float2 ml = __ldcg(&p.part_ml[r0 + s * stride]);
+    if (!(ml.y > 0.0f)) continue;  // no key of this row in the split
+    const float w = ex2(ml.x - M);
+    lsum += w * ml.y;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (r0 + s * stride) * kAttD) + lane);
+    acc[0] += w * v.x;
+    acc[1] += w * v.y;
+    acc[2] += w * v.z;
+    acc[3] += w * v.w;
+  }
+  const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
+  __nv_bfloat16* dst = p.out + (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD + 4 * lane;
+  *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc[0] * inv, acc[1] * inv);
+  *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc[2] * inv, acc[3] * inv);
+}
+
+// --------------------------------------------------------- KV compaction
+// Grid (B, layers). The accepted root path, root first, is path[0 .. depth);
+// path[d] >= d, so a move only reads positions at or past the ones earlier
+// moves have written: the moves go in chunks of depths, each chunk read
+// whole into registers before any of it is written.
+constexpr int kCompactThreads = 256;
+constexpr int kCompactPerThread = 16;  // 16-byte words a thread holds per chunk
+
+__global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(uint4* kc, uint4* vc, const int32_t* lens,
+                                                                     const int32_t* parents, const int32_t* node,
+                                                                     int B, int n, int Hkv, int row_words, int Lcap,
+                                                                     int32_t* new_lens, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  __shared__ int path[kAttMaxNodes + 1];
+  __shared__ int s_depth, s_len;
+  const int b = blockIdx.x, layer = blockIdx.y, tid = threadIdx.x;
+  if (tid == 0) {
+    int len = lens[b];
+    if (len < 0 || len > Lcap - n) {
+      report_error(err, kErrInput);
+      len = len < 0 ? 0 : Lcap - n;
+    }
+    int j = node[b];
+    bool bad = j < 0 || j >= n;
+    if (bad) j = 0;
+    int depth = 0;
+    int tmp[kAttMaxNodes + 1];
+    while (j >= 0 && depth <= n) {
+      tmp[depth++] = j;
+      const int par = parents ? parents[(int64_t)b * n + j] : j - 1;
+      if (j == 0 ? par != -1 : (par < 0 || par >= j)) {
+        bad = true;
+        break;
+      }
+      j = par;
+    }
+    if (bad) {  // the root alone
+      depth = 1;
+      tmp[0] = 0;
+      report_error(err, kErrInput);
+    }
+    for (int d = 0; d < depth; ++d) path[d] = tmp[depth - 1 - d];
+    s_depth = depth;
+    s_len = len;
+    if (layer == 0) new_lens[b] = len + depth;
+  }
+  __syncthreads();
+  const int depth = s_depth, len = s_len;
+  const int per_depth = 2 * Hkv * row_words;  // keys and values of every head
+  const int chunk = max(1, kCompactThreads * kCompactPerThread / per_depth);
+  const int64_t head_words = (int64_t)Lcap * row_words;
+  const int64_t bh0 = ((int64_t)layer * B + b) * Hkv;
+  for (int d0 = 1; d0 < depth; d0 += chunk) {
+    const int d1 = min(depth, d0 + chunk);
+    const int total = (d1 - d0) * per_depth;
+    uint4 v[kCompactPerThread];
+#pragma unroll
+    for (int k = 0; k < kCompactPerThread; ++k) {
+      const int idx = tid + k * kCompactThreads;
+      if (idx < total) {
+        const int d = d0 + idx / per_depth, rem = idx % per_depth;
+        const int c = rem / (Hkv * row_words), h = (rem / row_words) % Hkv, w = rem % row_words;
+        const uint4* src = (c ? vc : kc) + (bh0 + h) * head_words + (int64_t)(len + path[d]) * row_words + w;
+        v[k] = *src;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kCompactPerThread; ++k) {
+      const int idx = tid + k * kCompactThreads;
+      if (idx < total) {
+        const int d = d0 + idx / per_depth, rem = idx % per_depth;
+        if (path[d] == d) continue;  // already in place
+        const int c = rem / (Hkv * row_words), h = (rem / row_words) % Hkv, w = rem % row_words;
+        uint4* dst = (c ? vc : kc) + (bh0 + h) * head_words + (int64_t)(len + d) * row_words + w;
+        *dst = v[k];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+static int attn_warps(int rows) {
+  const int w = (rows + 15) / 16;
+  return w <= 1 ? 1 : (w <= 2 ? 2 : (w <= 4 ? 4 : 8));
+}
+
+AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
+  AttnPlan pl;
+  const int G = H / Hkv;
+  pl.rows = n * G;
+  pl.warps = attn_warps(pl.rows);
+  pl.row_blocks = (pl.rows + 16 * pl.warps - 1) / (16 * pl.warps);
+  pl.rows_pad = pl.row_blocks * 16 * pl.warps;
+  const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
+  const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
+  const int64_t target = (int64_t)2 * kAttCtasPerSm * (num_sms > 0 ? num_sms : 1);  // about two waves
+  int splits = (int)((target + base - 1) / base);
+  if (splits < 1) splits = 1;
+  if (splits > nbmax) splits = nbmax;
+  pl.blocks_per_split = (nbmax + splits - 1) / splits;
+  pl.splits = (nbmax + pl.blocks_per_split - 1) / pl.blocks_per_split;
+  pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * B * Hkv * pl.rows_pad * (kAttD * 4 + 8) : 0;
+  return pl;
+}
+
+template <int NW>
+static cudaError_t launch_attn_t(const CUtensorMap& km, const CUtensorMap& vm, const AttnParams& p, dim3 grid,
+                                 cudaStream_t stream) {
+  constexpr int smem = AttnLayout<NW>::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(tree_attention_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tree_attention_kernel<NW>, grid, dim3(32 * NW), (size_t)smem, stream, km, vm, p);
+}
+
+cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
+                                  const int32_t* parents, int B, int n, int H, int Hkv, int Lcap, int max_len,
+                                  float scale, void* out, void* workspace, const AttnPlan& pl, unsigned* err,
+                                  cudaStream_t stream) {
+  auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap km, vm;
+  const cuuint64_t dims[2] = {(cuuint64_t)kAttD, (cuuint64_t)B * Hkv * Lcap};
+  const cuuint64_t strides[1] = {(cuuint64_t)kAttD * 2};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)kAttKeys};
+  const cuuint32_t es[2] = {1u, 1u};
+  for (int c = 0; c < 2; ++c)
+    if (encode(c ? &vm : &km, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(c ? v_cache : k_cache), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  AttnParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.lens = lens;
+  p.parents = parents;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
+                                        (size_t)pl.splits * B * Hkv * pl.rows_pad * kAttD * 4);
+  p.err = err;
+  p.B = B;
+  p.n = n;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.Lcap = Lcap;
+  p.max_len = max_len;
+  p.rows = pl.rows;
+  p.rows_pad = pl.rows_pad;
+  p.row_blocks = pl.row_blocks;
+  p.splits = pl.splits;
+  p.blocks_per_split = pl.blocks_per_split;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const dim3 grid((unsigned)(pl.row_blocks * pl.splits), (unsigned)Hkv, (unsigned)B);
+  cudaError_t e;
+  switch (pl.warps) {
+    case 1: e = launch_attn_t<1>(km, vm, p, grid, stream); break;
+    case 2: e = launch_attn_t<2>(km, vm, p, grid, stream); break;
+    case 4: e = launch_attn_t<4>(km, vm, p, grid, stream); break;
+    default: e = launch_attn_t<8>(km, vm, p, grid, stream); break;
+  }
+  if (e != cudaSuccess || pl.splits == 1) return e;
+  const int64_t rows = (int64_t)B * Hkv * pl.rows;
+  return launch_pdl(tree_attention_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p);
+}
+
+cudaError_t launch_kv_compact(void* k_cache, void* v_cache, const int32_t* lens, const int32_t* parents,
+                              const int32_t* node, int B, int n, int Hkv, int D, int Lcap, int layers,
+                              int32_t* new_lens, unsigned* err, cudaStream_t stream) {
+  return launch_pdl(kv_compact_kernel, dim3((unsigned)B, (unsigned)layers), dim3(kCompactThreads), 0, stream,
+                    static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), lens, parents, node, B, n, Hkv,
+                    D / 8, Lcap, new_lens, err);
+}
+
+}  // namespace w4a16

@@ -1,10 +1,14 @@
 // C-ABI layer of libw4a16sv: argument checks, dispatch, device state.
 // Declarations and the contract of every entry point are in w4a16sv.h.
+#include <math.h>
+
 #include <mutex>
 
 #include "../../include/w4a16sv.h"
 #include "common.cuh"
 #include "format.cuh"
+#include <math.h>
+
 #include "internal.h"
 
 namespace w4a16 {
@@ -207,11 +211,12 @@ size_t spec_accept_workspace_bytes(int B, int n, int V) {
   return accept_plan(B, n, V).total;
 }
 
-w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
-                         const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
-                         int32_t* accepted_len, int32_t* next_token, void* workspace, size_t workspace_bytes,
-                         void* stream) {
+static w4a16_status accept_impl(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                                const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                                int32_t* accepted_len, int32_t* next_token, int32_t* accepted_node, void* workspace,
+                                size_t workspace_bytes, void* stream) {
   if (!p_logits || !draft_ids || !accepted_len || !next_token) return W4A16_ERR_INVALID_ARG;
+  if (accepted_node && !aligned(accepted_node, 4)) return W4A16_ERR_INVALID_ARG;
   if (!accept_shape_ok(B, n, V)) return W4A16_ERR_INVALID_ARG;
   if (q_logits && tree_parents) return W4A16_ERR_UNSUPPORTED;
   if (q_logits && !uniforms) return W4A16_ERR_INVALID_ARG;
@@ -225,11 +230,81 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
   cudaError_t e;
   if (q_logits)
     e = launch_accept_seq(p_logits, q_logits, draft_ids, uniforms, B, n, V, accepted_len, next_token, workspace, plan,
-                          dev.num_sms, dev.err, static_cast<cudaStream_t>(stream));
+                          dev.num_sms, dev.err, static_cast<cudaStream_t>(stream), nullptr, accepted_node);
   else
     e = launch_accept_greedy(p_logits, draft_ids, tree_parents, B, n, V, accepted_len, next_token, workspace, plan,
-                             dev.err, static_cast<cudaStream_t>(stream));
+                             dev.err, static_cast<cudaStream_t>(stream), accepted_node);
   return e == cudaSuccess ? W4A16_OK : W4A16_ERR_CUDA;
+}
+
+w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                         const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                         int32_t* accepted_len, int32_t* next_token, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  return accept_impl(p_logits, q_logits, draft_ids, tree_parents, uniforms, B, n, V, accepted_len, next_token,
+                     nullptr, workspace, workspace_bytes, stream);
+}
+
+w4a16_status spec_accept_node(const float* p_logits, const float* q_logits, const int32_t* draft_ids,
+                              const int32_t* tree_parents, const float* uniforms, int B, int n, int V,
+                              int32_t* accepted_len, int32_t* next_token, int32_t* accepted_node, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!accepted_node) return W4A16_ERR_INVALID_ARG;
+  return accept_impl(p_logits, q_logits, draft_ids, tree_parents, uniforms, B, n, V, accepted_len, next_token,
+                     accepted_node, workspace, workspace_bytes, stream);
+}
+
+// ---------------------------------------------------- verify attention
+static bool attn_shape_ok(int B, int n, int H, int Hkv, int Lcap, int max_len) {
+  return B >= 1 && B <= 65535 && n >= 1 && H >= 1 && Hkv >= 1 && Hkv <= 65535 && H % Hkv == 0 && max_len >= 0 &&
+         (int64_t)max_len + n <= Lcap && (int64_t)B * Hkv * Lcap <= INT32_MAX && (int64_t)n * H <= INT32_MAX;
+}
+
+size_t tree_attention_workspace_bytes(int B, int n, int H, int Hkv, int D, int Lcap, int max_len) {
+  if (!attn_shape_ok(B, n, H, Hkv, Lcap, max_len) || D != 128 || n > 64) return 0;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return 0;
+  return attn_plan(B, n, H, Hkv, max_len, dev.num_sms).ws_bytes;
+}
+
+w4a16_status tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
+                            const int32_t* tree_parents, int B, int n, int H, int Hkv, int D, int Lcap, int max_len,
+                            float scale, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !k_cache || !v_cache || !lens || !out) return W4A16_ERR_INVALID_ARG;
+  if (!attn_shape_ok(B, n, H, Hkv, Lcap, max_len) || !(scale > 0.0f) || !(scale < INFINITY))
+    return W4A16_ERR_INVALID_ARG;
+  if (D != 128 || n > 64) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) || !aligned(lens, 4) ||
+      (tree_parents && !aligned(tree_parents, 4)))
+    return W4A16_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  const AttnPlan plan = attn_plan(B, n, H, Hkv, max_len, dev.num_sms);
+  if (plan.ws_bytes > 0 && (!workspace || !aligned(workspace, 256) || workspace_bytes < plan.ws_bytes))
+    return W4A16_ERR_WORKSPACE;
+  return launch_tree_attention(q, k_cache, v_cache, lens, tree_parents, B, n, H, Hkv, Lcap, max_len, scale, out,
+                               workspace, plan, dev.err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
+}
+
+w4a16_status kv_compact(void* k_cache, void* v_cache, const int32_t* lens, const int32_t* tree_parents,
+                        const int32_t* accepted_node, int B, int n, int Hkv, int D, int Lcap, int n_layers,
+                        int32_t* new_lens, void* stream) {
+  if (!k_cache || !v_cache || !lens || !accepted_node || !new_lens) return W4A16_ERR_INVALID_ARG;
+  if (B < 1 || n < 1 || Hkv < 1 || D < 8 || D % 8 != 0 || Lcap < n || n_layers < 1 || n_layers > 65535)
+    return W4A16_ERR_INVALID_ARG;
+  // one tree node's keys and values of every head: at most 4096 16-byte words
+  if (n > 64 || (int64_t)2 * Hkv * (D / 8) > 4096) return W4A16_ERR_UNSUPPORTED;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(lens, 4) || !aligned(accepted_node, 4) ||
+      !aligned(new_lens, 4) || (tree_parents && !aligned(tree_parents, 4)))
+    return W4A16_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
+  return launch_kv_compact(k_cache, v_cache, lens, tree_parents, accepted_node, B, n, Hkv, D, Lcap, n_layers,
+                           new_lens, dev.err, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? W4A16_OK
+             : W4A16_ERR_CUDA;
 }
 
 w4a16_status spec_accept_prestat(const float* p_logits, const float* p_stats, const float* q_logits,

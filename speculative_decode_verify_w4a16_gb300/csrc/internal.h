@@ -107,6 +107,28 @@ cudaError_t launch_linear(const void* x, int M, int64_t K, const void* qw_packed
                           void* out, void* workspace, const LinearPlan& plan, const DeviceInfo& dev,
                           cudaStream_t stream);
 
+// The driver's cuTensorMapEncodeTiled (as void*; null if unavailable).
+void* tensor_map_encode_fn();
+
+// ---- tree-masked verify attention and KV compaction
+struct AttnPlan {
+  int rows = 0;        // query rows per KV head: n * (H / Hkv)
+  int warps = 0;       // warps per CTA (16 rows each): 1, 2, 4 or 8
+  int row_blocks = 0;  // CTAs along the rows
+  int rows_pad = 0;
+  int splits = 0;      // CTAs along the keys
+  int blocks_per_split = 0;
+  size_t ws_bytes = 0;  // split partials (0 with one split)
+};
+AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms);
+cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
+                                  const int32_t* parents, int B, int n, int H, int Hkv, int Lcap, int max_len,
+                                  float scale, void* out, void* workspace, const AttnPlan& plan, unsigned* err,
+                                  cudaStream_t stream);
+cudaError_t launch_kv_compact(void* k_cache, void* v_cache, const int32_t* lens, const int32_t* parents,
+                              const int32_t* node, int B, int n, int Hkv, int D, int Lcap, int layers,
+                              int32_t* new_lens, unsigned* err, cudaStream_t stream);
+
 // ---- accept
 struct AcceptPlan {
   int rows = 0;       // logit rows read by the statistics pass (upper bound over modes)
@@ -122,12 +144,15 @@ struct AcceptPlan {
 };
 AcceptPlan accept_plan(int B, int n, int V);
 // p_stats: NULL, or the target rows' (max, sum exp(l - max)) per 32-logit
-// slice [B * (n + 1)][V / 32] (the statistics pass then reads the draft rows only)
+// slice [B * (n + 1)][V / 32] (the statistics pass then reads the draft rows only).
+// node: NULL, or [B] for the accepted node (the deepest accepted tree node;
+// accepted_len for a sequence draft)
 cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, const float* u, int B, int n, int V,
                               int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, int num_sms,
-                              unsigned* err, cudaStream_t stream, const float2* p_stats = nullptr);
+                              unsigned* err, cudaStream_t stream, const float2* p_stats = nullptr,
+                              int32_t* node = nullptr);
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
                                  int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int32_t* node = nullptr);
 
 }  // namespace w4a16

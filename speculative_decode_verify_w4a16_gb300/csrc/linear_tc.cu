@@ -681,6 +681,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+void* tensor_map_encode_fn() { return reinterpret_cast<void*>(tensor_map_encoder()); }
+
 static int tc_nt(int M) { return (M + 15) / 16 * 16; }
 
 // CTAs per SM, from the shared-memory, register and TMEM budgets (the

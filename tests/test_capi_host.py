@@ -109,6 +109,43 @@ def test_fused_lm_head_and_prestat_accept_reject_bad_arguments(L):
     assert f(p, p, p, p, p, 1, 4, 128, p, p, ws, 16, None) == _lib.ERR_WORKSPACE
 
 
+def test_attention_compaction_and_node_accept_reject_bad_arguments(L):
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)  # 8-byte, not 16-byte aligned
+    ws = ctypes.c_void_p(0x20000)
+    f32 = ctypes.c_float
+
+    def att(q=p, lens=p, B=2, n=5, H=64, Hkv=8, D=128, Lcap=4096, max_len=4000, scale=f32(0.088)):
+        return L.tree_attention(q, p, p, lens, None, B, n, H, Hkv, D, Lcap, max_len, scale, p, ws, 1 << 30, None)
+
+    assert att(q=None) == _lib.ERR_INVALID_ARG
+    assert att(lens=None) == _lib.ERR_INVALID_ARG
+    assert att(D=64) == _lib.ERR_UNSUPPORTED
+    assert att(n=65) == _lib.ERR_UNSUPPORTED
+    assert att(H=60, Hkv=8) == _lib.ERR_INVALID_ARG  # H not a multiple of Hkv
+    assert att(max_len=4092) == _lib.ERR_INVALID_ARG  # max_len + n > Lcap
+    assert att(q=odd) == _lib.ERR_INVALID_ARG
+    assert att(scale=f32(0.0)) == _lib.ERR_INVALID_ARG
+    assert att(scale=f32(float("nan"))) == _lib.ERR_INVALID_ARG
+    assert L.tree_attention_workspace_bytes(2, 5, 64, 8, 64, 4096, 4000) == 0
+    assert L.tree_attention_workspace_bytes(2, 5, 64, 8, 128, 4096, 4095) == 0
+
+    def comp(kc=p, node=p, n=5, Hkv=8, D=128, Lcap=4096, layers=80):
+        return L.kv_compact(kc, p, p, None, node, 2, n, Hkv, D, Lcap, layers, p, None)
+
+    assert comp(kc=None) == _lib.ERR_INVALID_ARG
+    assert comp(node=None) == _lib.ERR_INVALID_ARG
+    assert comp(D=12) == _lib.ERR_INVALID_ARG
+    assert comp(n=65) == _lib.ERR_UNSUPPORTED
+    assert comp(Hkv=1024) == _lib.ERR_UNSUPPORTED  # one node's keys and values exceed a pass
+    assert comp(kc=odd) == _lib.ERR_INVALID_ARG
+    assert comp(Lcap=4) == _lib.ERR_INVALID_ARG
+    a = L.spec_accept_node
+    assert a(p, None, p, None, None, 2, 4, 128, p, p, None, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
+    assert a(p, None, p, None, None, 2, 4, 128, p, p, ctypes.c_void_p(0x10002), ws, 1 << 20, None) == \
+        _lib.ERR_INVALID_ARG
+
+
 def test_format_calls_reject_bad_arguments(L):
     p = ctypes.c_void_p(0x10000)
     assert L.w4a16_quantize(None, 128, 128, p, p, None) == _lib.ERR_INVALID_ARG

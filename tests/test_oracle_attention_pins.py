@@ -160,3 +160,15 @@ def test_greedy_tree_reports_the_deepest_accepted_node():
             ok = all(draft[b, c] == int(np.argmax(p[b, a])) for a, c in zip(pj[:-1], pj[1:]))
             if ok:
                 assert len(pj) - 1 < acc[b] or (len(pj) - 1 == acc[b] and j >= node[b])
+
+
+def test_weighted_abs_values():
+    # with all values >= 0 the weighted |v| is the output itself; with v -> -v it is -out
+    B, n, H, Hkv, D, Lcap = 2, 7, 4, 2, 16, 32
+    q, k, v, lens, parents = synth.attention_case(B, n, H, Hkv, D, [3, 9], Lcap, seed=37)
+    vpos = synth.bf16_bits_from_f32(np.abs(synth.bf16_bits_to_f32(v)))
+    out, a = oracle.tree_attention(q, k, vpos, lens, parents, want_abs=True)
+    assert np.array_equal(out, a)
+    vneg = vpos | np.uint16(0x8000)
+    out2, a2 = oracle.tree_attention(q, k, vneg, lens, parents, want_abs=True)
+    assert np.array_equal(out2, -a) and np.array_equal(a2, a)
