@@ -15,7 +15,11 @@ after 10 warm-up calls; consecutive linear calls stream distinct weight
 copies, together more than 3x the L2; L2 flushed before every accept call): the single 2048 x 2048 linear at
 M = 4; each Llama-3-70B shape including the lm_head at M = 1, 4, 8, 16, 32,
 48, 64 (us, GB/s, TFLOP/s, fraction of the HBM roofline, time relative to
-M = 1); the stochastic accept at K = 4 and 8 and the greedy tree. It times the
+M = 1); the stochastic accept at K = 4 and 8 and the greedy tree; the lm_head
+feeding the accept at M = 64 and 80, plain and with the fused softmax
+statistics; the tree-masked verify attention of one Llama-3-70B layer (16
+sequences, a 5-position chain and a 64-node tree) and the accepted-path KV
+compaction over 80 layers. It times the
 80-layer + lm_head verify forward (one CUDA graph per M) at M = 1, 4, 5, 9, 16,
 32, 48, 64, and the CPU oracle on a bounded sample on one thread and on every
 host core. The contract line carries a summary; `--detail PATH` writes all of
@@ -54,6 +58,7 @@ ACC_B, ACC_K, VOCAB = 16, 4, synth.LLAMA3_VOCAB
 ACC_KS = (4, 8)
 FUSED_KS = (3, 4)  # lm_head + accept chains at M = 64 and 80 (the linear takes M <= 80)
 TREE_B, TREE_N = 16, 64
+ATT_B, ATT_H, ATT_HKV = 16, 64, 8  # Llama-3-70B attention: 64 query heads on 8 key/value heads of 128
 N_LAYERS = 80
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 CALL_REPS, CALL_WARMUP = 50, 10
@@ -297,7 +302,75 @@ def run_sweep(sv, torch, device, gen, layers, pk, flush):
     _check(sv, "the accept sweep")
     for Kd in FUSED_KS:
         acc.append(run_fused_lm_head_accept(sv, torch, device, gen, pk, flush, Kd))
+    acc += run_attention(sv, torch, device, gen, pk, flush)
     return rows, acc
+
+
+def run_attention(sv, torch, device, gen, pk, flush):
+    """Tree-masked verify attention of one Llama-3-70B layer (64 query heads
+    on 8 KV heads of 128; 16 sequences with committed lengths uniform in
+    [1024, 4096)) for a sequence draft (K = 4: 5 query positions, causal) and
+    a 64-node tree; and the accepted-path KV compaction over all 80 layers.
+    L2 flushed before each call (the two caches are 272 MB anyway)."""
+    H, Hkv, D, B = ATT_H, ATT_HKV, 128, ATT_B
+    lens_np = synth.attention_lens(B, 1024, 4096, seed=41)
+    max_len = 4096
+    Lcap = max_len + 64
+    lens = torch.from_numpy(lens_np).to(device)
+    kc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
+    res = []
+    for label, n, tree in (("sequence K=4", 5, False), ("tree 64", 64, True)):
+        q = torch.randn((B, n, H, D), generator=gen, device=device).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        par_np = np.stack([synth.random_tree_parents(n, 6, synth.rng(43 + b)) for b in range(B)]) if tree else \
+            np.broadcast_to(np.arange(-1, n - 1, dtype=np.int32), (B, n)).copy()
+        par = torch.from_numpy(par_np).to(device) if tree else None
+        nbytes = sv.tree_attention_workspace_bytes(B, n, H, Hkv, D, Lcap, max_len)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        us, _ = time_per_call(torch, lambda i: sv.tree_attention(q, kc, vc, lens, par, max_len=max_len, out=out,
+                                                                ws=ws), flush)
+        depth = np.zeros((B, n), dtype=np.int64)
+        for j in range(1, n):
+            depth[:, j] = depth[np.arange(B), par_np[:, j]] + 1
+        keys = int(((lens_np[:, None] + depth + 1) * H).sum())     # allowed (query, key) pairs
+        b = int((lens_np + n).sum()) * Hkv * D * 2 * 2 + 2 * B * n * H * D * 2
+        flops = 4.0 * D * keys
+        res.append({"mode": "tree attention", "draft": label, "B": B, "n": n, "H": H, "Hkv": Hkv,
+                    "lens": "U[1024,4096)", "us": round(us, 2), "GB_s": round(b / us / 1e3, 1),
+                    "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3),
+                    "TFLOP_s": round(flops / us / 1e6, 1),
+                    "frac_tensor": round(flops / us / 1e6 / pk["bf16_tflops"], 3),
+                    "ideal_us": round(max(b / pk["hbm_gbs"] / 1e3, flops / pk["bf16_tflops"] / 1e6), 2),
+                    "splits_workspace_bytes": nbytes})
+    _check(sv, "the verify attention")
+    del kc, vc
+    # accepted-path compaction: 80 layers, 64-node trees, accepted node per row
+    layers, n = N_LAYERS, 64
+    kall = torch.empty((layers, B, Hkv, Lcap, D), dtype=torch.bfloat16, device=device)
+    vall = torch.empty_like(kall)
+    g = synth.rng(47)
+    par_np = np.stack([synth.random_tree_parents(n, 6, g) for _ in range(B)])
+    node_np = g.integers(1, n, size=B).astype(np.int32)
+    par, node = torch.from_numpy(par_np).to(device), torch.from_numpy(node_np).to(device)
+    new_lens = torch.empty(B, dtype=torch.int32, device=device)
+    us, _ = time_per_call(torch, lambda i: sv.kv_compact(kall, vall, lens, node, par, new_lens=new_lens), flush)
+    moved = 0
+    for b in range(B):
+        path, j = [], int(node_np[b])
+        while j >= 0:
+            path.append(j)
+            j = int(par_np[b, j])
+        path.reverse()
+        moved += sum(1 for d, x in enumerate(path) if x != d)
+    b = moved * layers * Hkv * D * 2 * 2 * 2  # keys and values, read and written
+    res.append({"mode": "kv compaction", "B": B, "layers": layers, "n": n, "rows_moved": moved * layers,
+                "us": round(us, 2), "GB_s": round(b / us / 1e3, 1) if b else 0.0,
+                "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3) if b else 0.0})
+    _check(sv, "the KV compaction")
+    del kall, vall
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_fused_lm_head_accept(sv, torch, device, gen, pk, flush, Kd):
@@ -558,8 +631,11 @@ def run_ours(args):
                                       if r["M"] in (1, 4, 8, 64)}
         summary["linear_ratio_m64_m1"] = {r["shape"]: r["ratio_to_m1"] for r in sweep if r["M"] == 64}
         summary["accept"] = {(f"seq K={a['K']}" if "K" in a else "tree"): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
-                             for a in accept if "frac_hbm" in a}
+                             for a in accept if a["mode"] in ("stochastic sequence", "greedy tree")}
         summary["lm_head_accept_us"] = {f"K={a['K']}": a["us"] for a in accept if a["mode"].startswith("lm_head")}
+        summary["attention"] = {a["draft"]: {"us": a["us"], "frac_hbm": a["frac_hbm"], "frac_tensor": a["frac_tensor"]}
+                                for a in accept if a["mode"] == "tree attention"}
+        summary["kv_compaction_us"] = next((a["us"] for a in accept if a["mode"] == "kv compaction"), None)
     if stack:
         summary["stack_us"] = {m: v["us"] for m, v in stack.items() if isinstance(v, dict)}
         summary["stack_frac_hbm"] = {m: v["frac_hbm"] for m, v in stack.items() if isinstance(v, dict)}

@@ -8,8 +8,8 @@
 // tree_attention_kernel: one CTA per (query-row block, key split, KV head,
 // batch row). The query rows of a KV head are its G = H / Hkv query heads at
 // every tree node, row r = node * G + head-in-group, 16 rows per warp. The
-// keys and values stream through a two-stage shared-memory ring of 64-key
-// blocks (2-D TMA, 128-byte swizzle). Each warp forms S = Q K^T with
+// keys and values stream through a shared-memory ring of 64-key blocks
+// (2-D TMA, 128-byte swizzle; two or three stages). Each warp forms S = Q K^T with
 // mma.sync m16n8k16 (bf16 in, fp32 accumulate), masks it (the committed
 // prefix: every key; the tree's own keys: the node's ancestors and itself, a
 // 64-bit mask per node), keeps the running maximum and sum of the online
@@ -33,7 +33,6 @@ namespace w4a16 {
 
 constexpr int kAttD = 128;                     // head width
 constexpr int kAttKeys = 64;                   // keys per block
-constexpr int kAttStages = 2;                  // key/value ring depth
 constexpr int kAttHalf = kAttKeys * 64 * 2;    // one 64-wide half of a key or value block: 8 KiB
 constexpr int kAttStage = 4 * kAttHalf;        // key halves, then value halves: 32 KiB
 constexpr int kAttMaxNodes = 64;
@@ -87,11 +86,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, fl
 
 template <int NW>
 struct AttnLayout {
+  // key/value ring depth: three stages while two CTAs still fit an SM's
+  // 228 KiB (each CTA: this layout, 1 KiB of alignment slack, 1 KiB the
+  // system reserves and a few static bytes)
+  static constexpr int kFixed = 16 * NW * kAttD * 2 + kAttMaxNodes * 8 + 3 * 8 + 1024;
+  static constexpr int kStages = 2 * (3 * kAttStage + kFixed + 1024 + 64) <= 228 * 1024 ? 3 : 2;
   static constexpr int kKvOff = 0;
-  static constexpr int kQOff = kAttStages * kAttStage;          // [16 NW rows][128] bf16, 256-byte rows
+  static constexpr int kQOff = kStages * kAttStage;             // [16 NW rows][128] bf16, 256-byte rows
   static constexpr int kAncOff = kQOff + 16 * NW * kAttD * 2;  // [kAttMaxNodes] uint64
-  static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;   // full[kAttStages]
-  static constexpr int kTotal = kBarOff + kAttStages * 8 + 1024;  // + alignment of the swizzled stages
+  static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;   // full[kStages]
+  static constexpr int kTotal = kBarOff + kStages * 8 + 1024;  // + alignment of the swizzled stages
 };
 
 template <int NW>
@@ -112,7 +116,7 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
 
   grid_launch_dependents();
   if (tid == 0) {
-    for (int s = 0; s < kAttStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < L_::kStages; ++s) mbar_init(&full[s], 1);
     fence_mbarrier_init();
   }
   grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
@@ -143,10 +147,10 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
   const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
   const int64_t kv_row0 = ((int64_t)b * p.Hkv + kvh) * p.Lcap;
 
-  // block blk0 + i of this split into stage i % kAttStages (rows past the
+  // block blk0 + i of this split into stage i % L_::kStages (rows past the
   // head's keys are masked; past the whole cache the copy fills zeros)
   auto issue = [&](int i) {
-    const int s = i % kAttStages;
+    const int s = i % L_::kStages;
     uint8_t* st = smem + L_::kKvOff + s * kAttStage;
     const int32_t y = (int32_t)(kv_row0 + (int64_t)(blk0 + i) * kAttKeys);
     mbar_arrive_expect_tx(&full[s], (uint32_t)kAttStage);
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
     tma_load_2d(st + 3 * kAttHalf, &vmap, 64, y, &full[s]);
   };
   if (tid == 0)
-    for (int i = 0; i < nb && i < kAttStages; ++i) issue(i);
+    for (int i = 0; i < nb && i < L_::kStages; ++i) issue(i);
 
   // the CTA's query rows into shared memory (16-byte chunk c of row r at
   // chunk c ^ (r % 8): conflict-free row reads for ldmatrix)
@@ -182,9 +186,16 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
   for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.0f;
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
 
+  // a warp whose 16 rows are all padding only keeps the ring's rhythm
+  const bool idle = rows0 + warp * 16 >= p.rows;
   for (int i = 0; i < nb; ++i) {
-    const int s = i % kAttStages;
-    const bool ok = mbar_wait(&full[s], (uint32_t)(i / kAttStages) & 1u, p.err);
+    const int s = i % L_::kStages;
+    if (idle) {
+      if (__syncthreads_or(0)) break;
+      if (tid == 0 && i + L_::kStages < nb) issue(i + L_::kStages);
+      continue;
+    }
+    const bool ok = mbar_wait(&full[s], (uint32_t)(i / L_::kStages) & 1u, p.err);
     const uint32_t kst = smem_u32(smem + L_::kKvOff + s * kAttStage), vst = kst + 2 * kAttHalf;
     // ---- S = Q K^T (16 rows x 64 keys per warp)
     float sc[8][4];
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
       }
     // every warp is done with stage s: refill it (a timed-out wait ends the loop in every thread)
     if (__syncthreads_or(!ok)) break;
-    if (tid == 0 && i + kAttStages < nb) issue(i + kAttStages);
+    if (tid == 0 && i + L_::kStages < nb) issue(i + L_::kStages);
   }
 
   l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
@@ -428,6 +439,8 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(uint4* kc, 
 
 // ------------------------------------------------------------------ host
 
+// warps per CTA: 1, 2, 4 or 8 (measured on the 5-position chain with 64
+// heads on 8: four warps with two stages beat three with three stages)
 static int attn_warps(int rows) {
   const int w = (rows + 15) / 16;
   return w <= 1 ? 1 : (w <= 2 ? 2 : (w <= 4 ? 4 : 8));
