@@ -243,6 +243,8 @@ def run_only(args, sv, torch, device, layers, acc_in, acc_out, acc_ws, tree_in, 
     elif args.only == "accept":
         fn = lambda: sv.spec_accept(acc_in[0], acc_in[2], q_logits=acc_in[1], uniforms=acc_in[3],
                                     accepted_len=acc_out[0], next_token=acc_out[1], ws=acc_ws)
+    elif args.only == "attention":  # --m tree nodes: 5 = the K = 4 chain, otherwise a random tree
+        fn = attention_call(sv, torch, device, args.m, args.m != 5)
     else:
         fn = lambda: sv.spec_accept(tree_in[0], tree_in[1], tree_parents=tree_in[2], accepted_len=tree_out[0],
                                     next_token=tree_out[1], ws=acc_ws2)
@@ -306,6 +308,33 @@ def run_sweep(sv, torch, device, gen, layers, pk, flush):
     return rows, acc
 
 
+def attention_inputs(torch, device, gen, n, tree):
+    """One Llama-3-70B layer's verify attention inputs: 16 sequences, committed
+    lengths uniform in [1024, 4096), n query positions (a chain or a random
+    tree of depth < 6)."""
+    H, Hkv, D, B = ATT_H, ATT_HKV, 128, ATT_B
+    lens_np = synth.attention_lens(B, 1024, 4096, seed=41)
+    max_len = 4096
+    Lcap = max_len + 64
+    kc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
+    vc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
+    q = torch.randn((B, n, H, D), generator=gen, device=device).to(torch.bfloat16)
+    par_np = np.stack([synth.random_tree_parents(n, 6, synth.rng(43 + b)) for b in range(B)]) if tree else \
+        np.broadcast_to(np.arange(-1, n - 1, dtype=np.int32), (B, n)).copy()
+    return q, kc, vc, lens_np, par_np, max_len, Lcap
+
+
+def attention_call(sv, torch, device, n, tree):
+    gen = torch.Generator(device=device).manual_seed(98)
+    q, kc, vc, lens_np, par_np, max_len, Lcap = attention_inputs(torch, device, gen, n, tree)
+    lens = torch.from_numpy(lens_np).to(device)
+    par = torch.from_numpy(par_np).to(device) if tree else None
+    out = torch.empty_like(q)
+    nbytes = sv.tree_attention_workspace_bytes(ATT_B, n, ATT_H, ATT_HKV, 128, Lcap, max_len)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return lambda: sv.tree_attention(q, kc, vc, lens, par, max_len=max_len, out=out, ws=ws)
+
+
 def run_attention(sv, torch, device, gen, pk, flush):
     """Tree-masked verify attention of one Llama-3-70B layer (64 query heads
     on 8 KV heads of 128; 16 sequences with committed lengths uniform in
@@ -313,18 +342,11 @@ def run_attention(sv, torch, device, gen, pk, flush):
     a 64-node tree; and the accepted-path KV compaction over all 80 layers.
     L2 flushed before each call (the two caches are 272 MB anyway)."""
     H, Hkv, D, B = ATT_H, ATT_HKV, 128, ATT_B
-    lens_np = synth.attention_lens(B, 1024, 4096, seed=41)
-    max_len = 4096
-    Lcap = max_len + 64
-    lens = torch.from_numpy(lens_np).to(device)
-    kc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
-    vc = torch.randn((B, Hkv, Lcap, D), generator=gen, device=device).to(torch.bfloat16)
     res = []
     for label, n, tree in (("sequence K=4", 5, False), ("tree 64", 64, True)):
-        q = torch.randn((B, n, H, D), generator=gen, device=device).to(torch.bfloat16)
+        q, kc, vc, lens_np, par_np, max_len, Lcap = attention_inputs(torch, device, gen, n, tree)
+        lens = torch.from_numpy(lens_np).to(device)
         out = torch.empty_like(q)
-        par_np = np.stack([synth.random_tree_parents(n, 6, synth.rng(43 + b)) for b in range(B)]) if tree else \
-            np.broadcast_to(np.arange(-1, n - 1, dtype=np.int32), (B, n)).copy()
         par = torch.from_numpy(par_np).to(device) if tree else None
         nbytes = sv.tree_attention_workspace_bytes(B, n, H, Hkv, D, Lcap, max_len)
         ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -343,8 +365,9 @@ def run_attention(sv, torch, device, gen, pk, flush):
                     "frac_tensor": round(flops / us / 1e6 / pk["bf16_tflops"], 3),
                     "ideal_us": round(max(b / pk["hbm_gbs"] / 1e3, flops / pk["bf16_tflops"] / 1e6), 2),
                     "splits_workspace_bytes": nbytes})
+        del q, kc, vc
     _check(sv, "the verify attention")
-    del kc, vc
+    lens = torch.from_numpy(lens_np).to(device)
     # accepted-path compaction: 80 layers, 64-node trees, accepted node per row
     layers, n = N_LAYERS, 64
     kall = torch.empty((layers, B, Hkv, Lcap, D), dtype=torch.bfloat16, device=device)
@@ -832,7 +855,7 @@ def main():
     ap.add_argument("--cpu-cols", type=int, default=None,
                     help="output columns of each linear in the CPU oracle sample (default max(64, 4 x threads))")
     ap.add_argument("--detail", default=None, help="write every measurement as JSON to this path")
-    ap.add_argument("--only", choices=["linear", "accept", "tree"], default=None,
+    ap.add_argument("--only", choices=["linear", "accept", "tree", "attention"], default=None,
                     help="profiling mode: run one kind of launch eagerly, print no contract line")
     ap.add_argument("--shape", default="gate_up", choices=[n for n, _, _ in SHAPES])
     ap.add_argument("--m", type=int, default=4)

@@ -69,6 +69,9 @@ def lib():
                                                  _P(np.float64), _P(np.float64)]
             L.oracle_greedy_tree.argtypes = [_P(np.float32), _P(np.int32), _P(np.int32), i32, i32, i32,
                                              _P(np.int32), _P(np.int32), _P(np.int32)]
+            L.oracle_spec_accept_tree.argtypes = [_P(np.float32), _P(np.float32), _P(np.int32), _P(np.int32),
+                                                  _P(np.float32), i32, i32, i32, _P(np.int32), _P(np.int32),
+                                                  _P(np.int32), _P(np.float64), _P(np.float64)]
             L.oracle_tree_attention.argtypes = [_P(np.uint16), _P(np.uint16), _P(np.uint16), _P(np.int32),
                                                 ctypes.c_void_p, i32, i32, i32, i32, i32, i32, ctypes.c_double,
                                                 _P(np.float64), ctypes.c_void_p]
@@ -197,6 +200,21 @@ def greedy_tree(p, draft, parents, want_node: bool = False):
     node = np.empty(B, dtype=np.int32)
     lib().oracle_greedy_tree(p, draft, parents, B, n, V, acc, nxt, node)
     return (acc, nxt, node) if want_node else (acc, nxt)
+
+
+def spec_accept_tree(p, q, d, parents, u):
+    """Stochastic acceptance of a token tree (multi-step speculative
+    sampling). p, q [B,n,V] logits at every node, d [B,n], parents [B,n] (or
+    [n]), u [B,n] (u[:, j] tests node j, u[:, 0] draws the next token).
+    Returns (accepted_len, next_token, accepted_node, margin_alpha, margin_cdf)."""
+    p, q, d, u = _c(p, np.float32), _c(q, np.float32), _c(d, np.int32), _c(u, np.float32)
+    B, n, V = p.shape
+    assert q.shape == (B, n, V) and d.shape == (B, n) and u.shape == (B, n)
+    par = _parents(parents, B, n)
+    acc, nxt, node = (np.empty(B, dtype=np.int32) for _ in range(3))
+    ma, mc = np.empty(B, dtype=np.float64), np.empty(B, dtype=np.float64)
+    lib().oracle_spec_accept_tree(p, q, d, par, u, B, n, V, acc, nxt, node, ma, mc)
+    return acc, nxt, node, ma, mc
 
 
 def _parents(parents, B, n):

@@ -295,6 +295,75 @@ void oracle_spec_accept_seq(const float* p, const float* q, const int32_t* d, co
     }
 }
 
+/*
+ * Stochastic acceptance of a token tree. The pages give the rule for a
+ * sequence draft only (the tutorial page, section 3 Steps 3-4); for a tree
+ * this follows multi-step speculative sampling as SpecInfer (Miao et al.
+ * 2024, "SpecInfer: Accelerating Large Language Model Serving with Tree-based
+ * Speculative Inference and Verification", section 4.2) defines it, for
+ * children drawn independently from the draft's distribution at their parent:
+ *  - start at the root (node 0) with R = P_0, the target's distribution there;
+ *  - at node u, try u's children in ascending index: child s with token x is
+ *    accepted iff u_s < min(1, R(x) / Q_u(x)) (alpha = 1 when Q_u(x) = 0);
+ *    on acceptance move to s with R = P_s; on rejection
+ *    R <- max(0, R - Q_u) / sum (R is kept when that sums to 0) and try the
+ *    next child;
+ *  - when u has no child left, draw the next token from R with u_0.
+ * p, q [B][n][V]: target and draft logits at every node (row j: after the
+ * path root..j; q row j is the distribution j's children were drawn from);
+ * d [B][n] (slot 0 unused), parents [B][n], u [B][n] (u_j tests node j,
+ * u_0 the final draw). Outputs accepted_len (the final node's depth),
+ * next_token, accepted_node, margin_alpha (smallest |u_s - alpha| over the
+ * tests made) and margin_cdf (see sample_cdf). fp64 throughout.
+ */
+void oracle_spec_accept_tree(const float* p, const float* q, const int32_t* d, const int32_t* parents, const float* u,
+                             int B, int n, int V, int32_t* accepted_len, int32_t* next_token, int32_t* accepted_node,
+                             double* margin_alpha, double* margin_cdf) {
+#pragma omp parallel for schedule(dynamic)
+    for (int b = 0; b < B; ++b) {
+        double* R = (double*)malloc(sizeof(double) * (size_t)V);
+        double* Q = (double*)malloc(sizeof(double) * (size_t)V);
+        const int32_t* par = parents + (int64_t)b * n;
+        const float* ub = u + (int64_t)b * n;
+        int node = 0, depth = 0;
+        double mg = INFINITY;
+        softmax64(p + (int64_t)b * n * V, V, R);
+        softmax64(q + (int64_t)b * n * V, V, Q);
+        for (;;) {
+            int accepted = -1;
+            for (int s = node + 1; s < n; ++s) {
+                if (par[s] != node) continue;
+                const int x = d[(int64_t)b * n + s];
+                const double a = Q[x] > 0.0 ? fmin(1.0, R[x] / Q[x]) : 1.0;
+                const double gap = fabs((double)ub[s] - a);
+                mg = gap < mg ? gap : mg;
+                if ((double)ub[s] < a) {
+                    accepted = s;
+                    break;
+                }
+                double S = 0.0;
+                for (int y = 0; y < V; ++y) S += R[y] - Q[y] > 0.0 ? R[y] - Q[y] : 0.0;
+                if (S > 0.0)
+                    for (int y = 0; y < V; ++y) R[y] = (R[y] - Q[y] > 0.0 ? R[y] - Q[y] : 0.0) / S;
+            }
+            if (accepted < 0) break;
+            node = accepted;
+            ++depth;
+            softmax64(p + ((int64_t)b * n + node) * V, V, R);
+            softmax64(q + ((int64_t)b * n + node) * V, V, Q);
+        }
+        double S = 0.0, cm;
+        for (int y = 0; y < V; ++y) S += R[y];
+        next_token[b] = sample_cdf(R, V, S, (double)ub[0], &cm);
+        accepted_len[b] = depth;
+        accepted_node[b] = node;
+        margin_alpha[b] = mg;
+        margin_cdf[b] = cm;
+        free(R);
+        free(Q);
+    }
+}
+
 /* argmax over raw logits, ties to the smallest index. */
 static int argmax_row(const float* row, int V) {
     int best = 0;
