@@ -301,6 +301,21 @@ def run_sweep(sv, torch, device, gen, layers, pk, flush):
     b = accept_bytes_tree(TREE_B, TREE_N, VOCAB)
     acc.append({"mode": "greedy tree", "B": TREE_B, "nodes": TREE_N, "V": VOCAB, "us": round(us, 2),
                 "GB_s": round(b / us / 1e3, 1), "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3)})
+    # stochastic tree: only the visited nodes' target and draft rows are read
+    sp, sq, sd, spar, su = synth.accept_tree_case(TREE_B, TREE_N, VOCAB, seed=29)
+    t = [torch.from_numpy(a).to(device) for a in (sp, sq, sd, spar, su)]
+    node_out = torch.empty(TREE_B, dtype=torch.int32, device=device)
+    ws = torch.zeros(sv.accept_workspace_bytes(TREE_B, TREE_N, VOCAB), dtype=torch.uint8, device=device)
+    us, _ = time_per_call(torch, lambda i: sv.lib().spec_accept_node(
+        t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), t[3].data_ptr(), t[4].data_ptr(), TREE_B, TREE_N, VOCAB,
+        a_out[0].data_ptr(), a_out[1].data_ptr(), node_out.data_ptr(), ws.data_ptr(), ws.numel(),
+        torch.cuda.current_stream().cuda_stream), flush)
+    depth = a_out[0].cpu().numpy()
+    b = int((depth + 1).sum()) * 2 * VOCAB * 4  # the visited nodes' two rows, once
+    acc.append({"mode": "stochastic tree", "B": TREE_B, "nodes": TREE_N, "V": VOCAB, "us": round(us, 2),
+                "visited_nodes": int((depth + 1).sum()), "GB_s": round(b / us / 1e3, 1),
+                "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3)})
+    del t
     _check(sv, "the accept sweep")
     for Kd in FUSED_KS:
         acc.append(run_fused_lm_head_accept(sv, torch, device, gen, pk, flush, Kd))
@@ -653,8 +668,8 @@ def run_ours(args):
         summary["linear_frac_hbm"] = {f"{r['shape']}/M{r['M']}": r["frac_hbm"] for r in sweep
                                       if r["M"] in (1, 4, 8, 64)}
         summary["linear_ratio_m64_m1"] = {r["shape"]: r["ratio_to_m1"] for r in sweep if r["M"] == 64}
-        summary["accept"] = {(f"seq K={a['K']}" if "K" in a else "tree"): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
-                             for a in accept if a["mode"] in ("stochastic sequence", "greedy tree")}
+        summary["accept"] = {(f"seq K={a['K']}" if "K" in a else a["mode"]): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
+                             for a in accept if a["mode"] in ("stochastic sequence", "greedy tree", "stochastic tree")}
         summary["lm_head_accept_us"] = {f"K={a['K']}": a["us"] for a in accept if a["mode"].startswith("lm_head")}
         summary["attention"] = {a["draft"]: {"us": a["us"], "frac_hbm": a["frac_hbm"], "frac_tensor": a["frac_tensor"]}
                                 for a in accept if a["mode"] == "tree attention"}

@@ -174,7 +174,19 @@ w4a16_status w4a16_linear_logits(const void* x, int M, int64_t K, const void* qw
  *       parent is and draft[j] == argmax(parent's row); accepted_len is the
  *       depth of the deepest accepted node (smallest index on ties) and
  *       next_token the argmax of its row.
- *   q_logits != NULL with tree_parents != NULL -> W4A16_ERR_UNSUPPORTED.
+ *   stochastic tree      q_logits != NULL, tree_parents != NULL
+ *       p_logits, q_logits [B][n][V] (row j: target / draft distribution
+ *       after the path root..j; node j's children were drawn from q row j),
+ *       draft_ids [B][n] (slot 0 = root), tree_parents as above, uniforms
+ *       [B][n] (u_j tests node j, u_0 draws the next token); V <= 131072
+ *       (else W4A16_ERR_UNSUPPORTED). The pages give no rule for a tree:
+ *       multi-step speculative sampling as SpecInfer defines it for children
+ *       drawn independently from the draft: at node u (from the root, with
+ *       R = P_u) the children are tried in ascending index, child s with
+ *       token x is accepted iff u_s < min(1, R(x) / Q_u(x)) (then u = s,
+ *       R = P_s), a rejection replaces R by normalize(max(0, R - Q_u)) (kept
+ *       when that sums to 0); with no child left next_token is drawn from R
+ *       with u_0. accepted_len = the final node's depth.
  * Logits must be finite. Outputs accepted_len[B], next_token[B] int32
  * (device). An id outside [0, V) or a bad parent sets W4A16_ERR_DEVICE_INPUT
  * in the device error word (the row then reports accepted_len = 0).
@@ -192,8 +204,9 @@ w4a16_status spec_accept(const float* p_logits, const float* q_logits, const int
 
 /* ------------------------------------------------------------------------
  * spec_accept that also reports the accepted node: accepted_node[B] int32
- * (device, required) = the deepest accepted tree node in greedy tree mode,
- * accepted_len in the sequence modes (a chain's node index is its depth).
+ * (device, required) = the final node of the accepted root path in the tree
+ * modes (the deepest accepted node in greedy mode), accepted_len in the
+ * sequence modes (a chain's node index is its depth).
  * kv_compact takes it. Everything else as spec_accept.
  */
 w4a16_status spec_accept_node(const float* p_logits, const float* q_logits, const int32_t* draft_ids,

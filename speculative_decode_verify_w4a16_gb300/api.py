@@ -191,8 +191,8 @@ def spec_accept(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: Optio
         _need(draft_ids, "draft_ids", torch.int32, (B, n))
     if q_logits is not None:
         _need(q_logits, "q_logits", torch.float32, (B, n, V))
-    if uniforms is not None:
-        _need(uniforms, "uniforms", torch.float32, (B, n + 1))
+    if uniforms is not None:  # stochastic tree: [B, n] (u_0 draws); sequence: [B, n + 1]
+        _need(uniforms, "uniforms", torch.float32, (B, n) if tree_parents is not None else (B, n + 1))
     if accepted_len is None:
         accepted_len = torch.empty(B, dtype=torch.int32, device=p_logits.device)
     if next_token is None:
@@ -243,7 +243,7 @@ def spec_accept_node(p_logits: torch.Tensor, draft_ids: torch.Tensor, q_logits: 
     if q_logits is not None:
         _need(q_logits, "q_logits", torch.float32, (B, n, V))
     if uniforms is not None:
-        _need(uniforms, "uniforms", torch.float32, (B, n + 1))
+        _need(uniforms, "uniforms", torch.float32, (B, n) if tree_parents is not None else (B, n + 1))
     acc, nxt, node = (torch.empty(B, dtype=torch.int32, device=p_logits.device) for _ in range(3))
     if ws is None:
         ws = workspace(accept_workspace_bytes(B, n, V), p_logits.device, "accept")

@@ -30,11 +30,14 @@
 #include <float.h>
 
 #include <atomic>
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace w4a16 {
+
+namespace cg = cooperative_groups;
 
 constexpr int kAccThreads = 256;
 constexpr int kAccWarps = kAccThreads / 32;
@@ -825,6 +828,287 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     next_out[b] = gs.amax[best_node];
     if (node_out) node_out[b] = best_node;
   }
+}
+
+// ------------------------------------------------- stochastic token tree
+// Multi-step speculative sampling over a token tree (SpecInfer, section 4.2;
+// the pages give the rule for a sequence draft only): at node u the
+// children are tried in ascending index, child s with token x accepted iff
+// u_s < min(1, R(x) / Q_u(x)); a rejection replaces R by the normalised
+// max(0, R - Q_u); with no child left the next token is drawn from R.
+// R after k rejections at u equals max(0, P_u - c_k Q_u) / T_k with
+// c_0 = 0, T_0 = 1, c_{k+1} = c_k + T_k and T_{k+1} the sum of
+// max(0, P_u - c_{k+1} Q_u) (induction on the update), so each rejection
+// costs one vocabulary-wide sum.
+//
+// One cluster of kTreeCtas CTAs per batch row; CTA r holds logits
+// [r kTreeSlice, (r + 1) kTreeSlice) of the visited node's target and draft
+// rows in registers (kTreePT contiguous logits per thread), so every sum
+// over the vocabulary is a register pass; partial results meet through
+// distributed shared memory, each CTA adding the kTreeCtas partials in rank
+// order (every CTA holds the same totals and takes the same decisions).
+constexpr int kTreeCtas = 8;
+constexpr int kTreeThreads = 512;
+constexpr int kTreeWarps = kTreeThreads / 32;
+constexpr int kTreePT = 32;
+constexpr int kTreeSlice = kTreeThreads * kTreePT;  // 16384
+constexpr int kTreeMaxV = kTreeCtas * kTreeSlice;   // 131072
+
+struct TreeShared {
+  int par[kMaxNodes];
+  int draft[kMaxNodes];
+  DF red[2][2];      // this CTA's partials for the cluster (double-buffered): two quantities
+  DF warp_part[kTreeWarps][2];
+  DF total[2];
+  int found, last_pos;
+};
+
+// Sum (kind 0) or max (kind 1, in .hi) of two values over the cluster.
+template <int KIND>
+__device__ void cluster_reduce2(cg::cluster_group& cluster, TreeShared& sh, int& phase, DF a, DF b, DF& ra, DF& rb) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    if (KIND == 0) {
+      a = df_add(a, shfl_xor_df(a, o));
+      b = df_add(b, shfl_xor_df(b, o));
+    } else {
+      a.hi = fmaxf(a.hi, __shfl_xor_sync(0xffffffffu, a.hi, o));
+      b.hi = fmaxf(b.hi, __shfl_xor_sync(0xffffffffu, b.hi, o));
+    }
+  }
+  if (lane == 0) {
+    sh.warp_part[w][0] = a;
+    sh.warp_part[w][1] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    DF x = sh.warp_part[0][0], y = sh.warp_part[0][1];
+    for (int i = 1; i < kTreeWarps; ++i) {
+      if (KIND == 0) {
+        x = df_add(x, sh.warp_part[i][0]);
+        y = df_add(y, sh.warp_part[i][1]);
+      } else {
+        x.hi = fmaxf(x.hi, sh.warp_part[i][0].hi);
+        y.hi = fmaxf(y.hi, sh.warp_part[i][1].hi);
+      }
+    }
+    sh.red[phase][0] = x;
+    sh.red[phase][1] = y;
+  }
+  cluster.sync();
+  if (threadIdx.x == 0) {
+    DF x = KIND == 0 ? DF{0.0f, 0.0f} : DF{-FLT_MAX, 0.0f}, y = x;
+    for (int r = 0; r < kTreeCtas; ++r) {
+      const TreeShared* o = cluster.map_shared_rank(&sh, r);
+      const DF ox = o->red[phase][0], oy = o->red[phase][1];
+      if (KIND == 0) {
+        x = df_add(x, ox);
+        y = df_add(y, oy);
+      } else {
+        x.hi = fmaxf(x.hi, ox.hi);
+        y.hi = fmaxf(y.hi, oy.hi);
+      }
+    }
+    sh.total[0] = x;
+    sh.total[1] = y;
+  }
+  __syncthreads();
+  ra = sh.total[0];
+  rb = sh.total[1];
+  __syncthreads();
+  phase ^= 1;
+}
+
+template <bool VEC>
+__global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads, 1) accept_tree_kernel(
+    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
+    const int32_t* __restrict__ parents, const float* __restrict__ u, int n, int V, int32_t* __restrict__ acc_out,
+    int32_t* __restrict__ next_out, int32_t* __restrict__ node_out, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ TreeShared sh;
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / kTreeCtas;
+  const int x0 = rank * kTreeSlice + (int)threadIdx.x * kTreePT;  // this thread's logits
+  int phase = 0;
+  for (int j = threadIdx.x; j < n; j += kTreeThreads) {
+    int pj = parents[(int64_t)b * n + j];
+    const int dj = d[(int64_t)b * n + j];
+    if (j == 0 ? pj != -1 : (pj < 0 || pj >= j)) {
+      if (rank == 0) report_error(err, kErrInput);
+      pj = -2;  // never anyone's child
+    }
+    if (j > 0 && (dj < 0 || dj >= V)) {
+      if (rank == 0) report_error(err, kErrInput);
+      pj = -2;
+    }
+    sh.par[j] = pj;
+    sh.draft[j] = dj;
+  }
+  __syncthreads();
+  const float* ub = u + (int64_t)b * n;
+  float lp[kTreePT], lq[kTreePT];
+  int node = 0, depth = 0, s = 1;
+  float mp = 0.0f, mq = 0.0f, izp = 0.0f, izq = 0.0f, c = 0.0f, T = 1.0f;
+  bool load = true;
+  for (;;) {
+    if (load) {  // the node's rows into registers, their maxima and normalisers
+      const float* prow = p + ((int64_t)b * n + node) * V;
+      const float* qrow = q + ((int64_t)b * n + node) * V;
+      if (VEC) {
+#pragma unroll
+        for (int k = 0; k < kTreePT; k += 4) {
+          float4 a = make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX), e = a;
+          if (x0 + k < V) {
+            a = ldg_stream_f4(reinterpret_cast<const float4*>(prow + x0 + k));
+            e = ldg_stream_f4(reinterpret_cast<const float4*>(qrow + x0 + k));
+          }
+          lp[k] = a.x, lp[k + 1] = a.y, lp[k + 2] = a.z, lp[k + 3] = a.w;
+          lq[k] = e.x, lq[k + 1] = e.y, lq[k + 2] = e.z, lq[k + 3] = e.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kTreePT; ++k) {
+          lp[k] = x0 + k < V ? ldg_stream_f(prow + x0 + k) : -FLT_MAX;
+          lq[k] = x0 + k < V ? ldg_stream_f(qrow + x0 + k) : -FLT_MAX;
+        }
+      }
+      float a = -FLT_MAX, e = -FLT_MAX;
+#pragma unroll
+      for (int k = 0; k < kTreePT; ++k) {
+        a = fmaxf(a, lp[k]);
+        e = fmaxf(e, lq[k]);
+      }
+      DF M1, M2;
+      cluster_reduce2<1>(cluster, sh, phase, DF{a, 0.0f}, DF{e, 0.0f}, M1, M2);
+      mp = M1.hi;
+      mq = M2.hi;
+      DF zp{0.0f, 0.0f}, zq{0.0f, 0.0f};
+#pragma unroll
+      for (int k = 0; k < kTreePT; ++k)
+        if (x0 + k < V) {
+          zp = df_add_f(zp, exp_of_diff(lp[k], mp));
+          zq = df_add_f(zq, exp_of_diff(lq[k], mq));
+        }
+      DF Zp, Zq;
+      cluster_reduce2<0>(cluster, sh, phase, zp, zq, Zp, Zq);
+      izp = __frcp_rn(df_val(Zp));
+      izq = __frcp_rn(df_val(Zq));
+      c = 0.0f;
+      T = 1.0f;
+      s = node + 1;
+      load = false;
+    }
+    while (s < n && sh.par[s] != node) ++s;  // the node's next child
+    if (s >= n) break;
+    // the child's test (every thread of the cluster computes the same value)
+    const int x = sh.draft[s];
+    const float px = __fmul_rn(exp_of_diff(__ldg(p + ((int64_t)b * n + node) * V + x), mp), izp);
+    const float qx = __fmul_rn(exp_of_diff(__ldg(q + ((int64_t)b * n + node) * V + x), mq), izq);
+    const float rx = fmaxf(__fsub_rn(px, __fmul_rn(c, qx)), 0.0f);
+    const float alpha = qx > 0.0f ? fminf(1.0f, __fdiv_rn(__fdiv_rn(rx, T), qx)) : 1.0f;
+    if (ub[s] < alpha) {
+      node = s;
+      ++depth;
+      load = true;
+      continue;
+    }
+    // rejected: R <- max(0, P - c' Q) / T' with c' = c + T
+    const float c1 = __fadd_rn(c, T);
+    DF t{0.0f, 0.0f};
+#pragma unroll
+    for (int k = 0; k < kTreePT; ++k)
+      if (x0 + k < V) {
+        const float pv = __fmul_rn(exp_of_diff(lp[k], mp), izp);
+        const float qv = __fmul_rn(exp_of_diff(lq[k], mq), izq);
+        t = df_add_f(t, fmaxf(__fsub_rn(pv, __fmul_rn(c1, qv)), 0.0f));
+      }
+    DF T1, unused;
+    cluster_reduce2<0>(cluster, sh, phase, t, DF{0.0f, 0.0f}, T1, unused);
+    const float tv = df_val(T1);
+    if (tv > 0.0f) {  // else the residual keeps its previous value
+      c = c1;
+      T = tv;
+    }
+    ++s;
+  }
+  // ---- the next token: inverse CDF of r(x) = max(0, P - c Q) (P itself when c = 0), ascending x
+  float rv[kTreePT];
+  DF mine{0.0f, 0.0f};
+  int lastp = -1;
+#pragma unroll
+  for (int k = 0; k < kTreePT; ++k) {
+    float v = 0.0f;
+    if (x0 + k < V) {
+      const float pv = __fmul_rn(exp_of_diff(lp[k], mp), izp);
+      v = c == 0.0f ? pv : fmaxf(__fsub_rn(pv, __fmul_rn(c, __fmul_rn(exp_of_diff(lq[k], mq), izq))), 0.0f);
+    }
+    rv[k] = v;
+    if (v > 0.0f) lastp = x0 + k;
+    mine = df_add_f(mine, v);
+  }
+  // this thread's exclusive prefix within the CTA, then the CTAs before it
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  DF incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+    if (lane >= o) incl = df_add(y, incl);
+  }
+  if (lane == 31) sh.warp_part[w][0] = incl;
+  __syncthreads();
+  DF before{0.0f, 0.0f};
+  for (int i = 0; i < w; ++i) before = df_add(before, sh.warp_part[i][0]);
+  DF cta_total{0.0f, 0.0f};
+  for (int i = 0; i < kTreeWarps; ++i) cta_total = df_add(cta_total, sh.warp_part[i][0]);
+  const DF excl_thread = df_add(before, df_add(incl, DF{-mine.hi, -mine.lo}));
+  if (threadIdx.x == 0) {
+    sh.red[phase][0] = cta_total;
+    sh.found = INT_MAX;
+    sh.last_pos = -1;
+  }
+  cluster.sync();
+  DF below{0.0f, 0.0f}, S{0.0f, 0.0f};
+  for (int r = 0; r < kTreeCtas; ++r) {
+    const DF o = cluster.map_shared_rank(&sh, r)->red[phase][0];
+    if (r < rank) below = df_add(below, o);
+    S = df_add(S, o);
+  }
+  const DF tt = df_mul_f(S, ub[0]);
+  DF run = df_add(below, excl_thread);
+  int hit = INT_MAX;
+#pragma unroll
+  for (int k = 0; k < kTreePT; ++k) {
+    run = df_add_f(run, rv[k]);
+    if (hit == INT_MAX && x0 + k < V && df_gt(run, tt)) hit = x0 + k;
+  }
+  if (hit != INT_MAX) atomicMin(&sh.found, hit);
+  if (lastp >= 0) atomicMax(&sh.last_pos, lastp);
+  cluster.sync();  // every CTA's candidates are in
+  if (rank == 0 && threadIdx.x == 0) {
+    int best = INT_MAX, lastv = -1;
+    for (int r = 0; r < kTreeCtas; ++r) {
+      const TreeShared* o = cluster.map_shared_rank(&sh, r);
+      best = min(best, o->found);
+      lastv = max(lastv, o->last_pos);
+    }
+    acc_out[b] = depth;
+    next_out[b] = best != INT_MAX ? best : (lastv >= 0 ? lastv : 0);
+    if (node_out) node_out[b] = node;
+  }
+  cluster.sync();  // no CTA leaves while rank 0 may still read its shared memory
+}
+
+cudaError_t launch_accept_tree(const float* p, const float* q, const int32_t* d, const int32_t* parents,
+                               const float* u, int B, int n, int V, int32_t* acc, int32_t* next, int32_t* node,
+                               unsigned* err, cudaStream_t stream) {
+  if (V % 4 == 0)
+    return launch_pdl(accept_tree_kernel<true>, dim3((unsigned)(B * kTreeCtas)), dim3(kTreeThreads), 0, stream, p, q,
+                      d, parents, u, n, V, acc, next, node, err);
+  return launch_pdl(accept_tree_kernel<false>, dim3((unsigned)(B * kTreeCtas)), dim3(kTreeThreads), 0, stream, p, q,
+                    d, parents, u, n, V, acc, next, node, err);
 }
 
 // ------------------------------------------------------------------ host

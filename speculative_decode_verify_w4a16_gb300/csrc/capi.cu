@@ -218,8 +218,8 @@ static w4a16_status accept_impl(const float* p_logits, const float* q_logits, co
   if (!p_logits || !draft_ids || !accepted_len || !next_token) return W4A16_ERR_INVALID_ARG;
   if (accepted_node && !aligned(accepted_node, 4)) return W4A16_ERR_INVALID_ARG;
   if (!accept_shape_ok(B, n, V)) return W4A16_ERR_INVALID_ARG;
-  if (q_logits && tree_parents) return W4A16_ERR_UNSUPPORTED;
   if (q_logits && !uniforms) return W4A16_ERR_INVALID_ARG;
+  if (q_logits && tree_parents && V > kAcceptTreeMaxV) return W4A16_ERR_UNSUPPORTED;
   if (V % 4 == 0 && (!aligned(p_logits, 16) || (q_logits && !aligned(q_logits, 16)))) return W4A16_ERR_INVALID_ARG;
   if (!aligned(p_logits, 4) || !aligned(draft_ids, 4) || !aligned(accepted_len, 4) || !aligned(next_token, 4))
     return W4A16_ERR_INVALID_ARG;
@@ -228,7 +228,10 @@ static w4a16_status accept_impl(const float* p_logits, const float* q_logits, co
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return W4A16_ERR_CUDA;
   cudaError_t e;
-  if (q_logits)
+  if (q_logits && tree_parents)
+    e = launch_accept_tree(p_logits, q_logits, draft_ids, tree_parents, uniforms, B, n, V, accepted_len, next_token,
+                           accepted_node, dev.err, static_cast<cudaStream_t>(stream));
+  else if (q_logits)
     e = launch_accept_seq(p_logits, q_logits, draft_ids, uniforms, B, n, V, accepted_len, next_token, workspace, plan,
                           dev.num_sms, dev.err, static_cast<cudaStream_t>(stream), nullptr, accepted_node);
   else

@@ -151,6 +151,11 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
                               int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, int num_sms,
                               unsigned* err, cudaStream_t stream, const float2* p_stats = nullptr,
                               int32_t* node = nullptr);
+// stochastic token tree (one 8-CTA cluster per batch row; V <= 131072)
+constexpr int kAcceptTreeMaxV = 131072;
+cudaError_t launch_accept_tree(const float* p, const float* q, const int32_t* d, const int32_t* parents,
+                               const float* u, int B, int n, int V, int32_t* acc, int32_t* next, int32_t* node,
+                               unsigned* err, cudaStream_t stream);
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
                                  int32_t* acc, int32_t* next, void* ws, const AcceptPlan& plan, unsigned* err,
                                  cudaStream_t stream, int32_t* node = nullptr);

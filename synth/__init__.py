@@ -182,3 +182,22 @@ def attention_case(B: int, n: int, H: int, Hkv: int, D: int, lens, Lcap: int, se
 def attention_lens(B: int, lo: int, hi: int, seed: int) -> np.ndarray:
     """Ragged committed lengths, uniform in [lo, hi)."""
     return rng(seed).integers(lo, hi, size=B).astype(np.int32)
+
+
+def accept_tree_case(B: int, n: int, V: int, seed: int, max_depth: int = 6, p_std: float = 3.0,
+                     noise: float = 1.0):
+    """Stochastic tree-verify inputs: target logits ~ N(0, p_std^2) at every
+    node, draft logits = target + N(0, noise^2); a random tree per row (depth
+    < max_depth); every child's token drawn from the draft's distribution at
+    its parent (Gumbel-max); uniforms U[0, 1) [B, n] (u[:, 0] draws the next
+    token, u[:, j] tests node j)."""
+    g = rng(seed)
+    p = (g.standard_normal((B, n, V), dtype=np.float32) * np.float32(p_std)).astype(np.float32)
+    q = (p + g.standard_normal((B, n, V), dtype=np.float32) * np.float32(noise)).astype(np.float32)
+    parents = np.stack([random_tree_parents(n, max_depth, g) for _ in range(B)])
+    d = np.full((B, n), -1, dtype=np.int32)
+    if n > 1:
+        for b in range(B):
+            d[b, 1:] = gumbel_max_sample(q[b, parents[b, 1:]], g)
+    u = g.random((B, n), dtype=np.float32)
+    return p, q, d, parents, u

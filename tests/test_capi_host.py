@@ -79,7 +79,8 @@ def test_accept_rejects_bad_arguments_before_any_launch(L):
     ws = ctypes.c_void_p(0x20000)
     f = L.spec_accept
     assert f(None, None, p, None, None, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
-    assert f(p, p, p, p, p, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_UNSUPPORTED  # stochastic tree
+    assert f(p, p, p, p, p, 1, 4, 131076, p, p, ws, 1 << 30, None) == _lib.ERR_UNSUPPORTED  # stochastic tree, V
+    assert f(p, p, p, p, None, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # stochastic tree, no u
     assert f(p, p, p, None, None, 1, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG  # no uniforms
     assert f(p, None, p, None, None, 0, 4, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
     assert f(p, None, p, None, None, 1, 0, 100, p, p, ws, 1 << 20, None) == _lib.ERR_INVALID_ARG
