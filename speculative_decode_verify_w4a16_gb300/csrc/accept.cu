@@ -863,6 +863,10 @@ struct TreeShared {
   int found, last_pos;
 };
 
+__device__ __forceinline__ DF shfl_df(DF v, int src) {
+  return DF{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
 // Sum (kind 0) or max (kind 1, in .hi) of two values over the cluster.
 template <int KIND>
 __device__ void cluster_reduce2(cg::cluster_group& cluster, TreeShared& sh, int& phase, DF a, DF b, DF& ra, DF& rb) {
@@ -897,21 +901,29 @@ __device__ void cluster_reduce2(cg::cluster_group& cluster, TreeShared& sh, int&
     sh.red[phase][1] = y;
   }
   cluster.sync();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // lane r fetches rank r's partials; lane 0 combines them in rank order
+    DF ox{0.0f, 0.0f}, oy{0.0f, 0.0f};
+    if (lane < kTreeCtas) {
+      const TreeShared* o = cluster.map_shared_rank(&sh, lane);
+      ox = o->red[phase][0];
+      oy = o->red[phase][1];
+    }
     DF x = KIND == 0 ? DF{0.0f, 0.0f} : DF{-FLT_MAX, 0.0f}, y = x;
+#pragma unroll
     for (int r = 0; r < kTreeCtas; ++r) {
-      const TreeShared* o = cluster.map_shared_rank(&sh, r);
-      const DF ox = o->red[phase][0], oy = o->red[phase][1];
+      const DF rx = shfl_df(ox, r), ry = shfl_df(oy, r);
       if (KIND == 0) {
-        x = df_add(x, ox);
-        y = df_add(y, oy);
+        x = df_add(x, rx);
+        y = df_add(y, ry);
       } else {
-        x.hi = fmaxf(x.hi, ox.hi);
-        y.hi = fmaxf(y.hi, oy.hi);
+        x.hi = fmaxf(x.hi, rx.hi);
+        y.hi = fmaxf(y.hi, ry.hi);
       }
     }
-    sh.total[0] = x;
-    sh.total[1] = y;
+    if (lane == 0) {
+      sh.total[0] = x;
+      sh.total[1] = y;
+    }
   }
   __syncthreads();
   ra = sh.total[0];
@@ -985,17 +997,25 @@ __global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads
       cluster_reduce2<1>(cluster, sh, phase, DF{a, 0.0f}, DF{e, 0.0f}, M1, M2);
       mp = M1.hi;
       mq = M2.hi;
+      // the registers now hold exp(l - max), then the probabilities
       DF zp{0.0f, 0.0f}, zq{0.0f, 0.0f};
 #pragma unroll
-      for (int k = 0; k < kTreePT; ++k)
-        if (x0 + k < V) {
-          zp = df_add_f(zp, exp_of_diff(lp[k], mp));
-          zq = df_add_f(zq, exp_of_diff(lq[k], mq));
-        }
+      for (int k = 0; k < kTreePT; ++k) {
+        const bool in = x0 + k < V;
+        lp[k] = in ? exp_of_diff(lp[k], mp) : 0.0f;
+        lq[k] = in ? exp_of_diff(lq[k], mq) : 0.0f;
+        zp = df_add_f(zp, lp[k]);
+        zq = df_add_f(zq, lq[k]);
+      }
       DF Zp, Zq;
       cluster_reduce2<0>(cluster, sh, phase, zp, zq, Zp, Zq);
       izp = __frcp_rn(df_val(Zp));
       izq = __frcp_rn(df_val(Zq));
+#pragma unroll
+      for (int k = 0; k < kTreePT; ++k) {
+        lp[k] = __fmul_rn(lp[k], izp);
+        lq[k] = __fmul_rn(lq[k], izq);
+      }
       c = 0.0f;
       T = 1.0f;
       s = node + 1;
@@ -1019,12 +1039,7 @@ __global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads
     const float c1 = __fadd_rn(c, T);
     DF t{0.0f, 0.0f};
 #pragma unroll
-    for (int k = 0; k < kTreePT; ++k)
-      if (x0 + k < V) {
-        const float pv = __fmul_rn(exp_of_diff(lp[k], mp), izp);
-        const float qv = __fmul_rn(exp_of_diff(lq[k], mq), izq);
-        t = df_add_f(t, fmaxf(__fsub_rn(pv, __fmul_rn(c1, qv)), 0.0f));
-      }
+    for (int k = 0; k < kTreePT; ++k) t = df_add_f(t, fmaxf(__fsub_rn(lp[k], __fmul_rn(c1, lq[k])), 0.0f));
     DF T1, unused;
     cluster_reduce2<0>(cluster, sh, phase, t, DF{0.0f, 0.0f}, T1, unused);
     const float tv = df_val(T1);
@@ -1040,11 +1055,7 @@ __global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads
   int lastp = -1;
 #pragma unroll
   for (int k = 0; k < kTreePT; ++k) {
-    float v = 0.0f;
-    if (x0 + k < V) {
-      const float pv = __fmul_rn(exp_of_diff(lp[k], mp), izp);
-      v = c == 0.0f ? pv : fmaxf(__fsub_rn(pv, __fmul_rn(c, __fmul_rn(exp_of_diff(lq[k], mq), izq))), 0.0f);
-    }
+    const float v = c == 0.0f ? lp[k] : fmaxf(__fsub_rn(lp[k], __fmul_rn(c, lq[k])), 0.0f);
     rv[k] = v;
     if (v > 0.0f) lastp = x0 + k;
     mine = df_add_f(mine, v);
