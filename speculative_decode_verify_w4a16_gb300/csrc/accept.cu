@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     f.iq = 0.0f;
   }
   const int x0 = blockIdx.x * chunk2, x1 = min(V, x0 + chunk2);
+  const uint64_t pol = policy_evict_first();
   // all of this thread's logits are loaded before any is used (one latency)
   float lp[RS], lq[RS];
   auto index_of = [&](int j) {
@@ -535,9 +536,9 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     for (int j = 0; j < RS / 4; ++j) {
       const int xi = x0 + (j * kAccThreads + (int)threadIdx.x) * 4;
       float4 tp = make_float4(0.f, 0.f, 0.f, 0.f), tq = tp;
-      if (xi < x1) {
-        tp = ldg_stream_f4(reinterpret_cast<const float4*>(f.prow + xi));
-        if (f.qrow) tq = ldg_stream_f4(reinterpret_cast<const float4*>(f.qrow + xi));
+      if (xi < x1) {  // the rows' last read: evict-first
+        tp = ldg_hint_f4(reinterpret_cast<const float4*>(f.prow + xi), pol);
+        if (f.qrow) tq = ldg_hint_f4(reinterpret_cast<const float4*>(f.qrow + xi), pol);
       }
       lp[4 * j] = tp.x, lp[4 * j + 1] = tp.y, lp[4 * j + 2] = tp.z, lp[4 * j + 3] = tp.w;
       lq[4 * j] = tq.x, lq[4 * j + 1] = tq.y, lq[4 * j + 2] = tq.z, lq[4 * j + 3] = tq.w;
@@ -554,8 +555,13 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
 #pragma unroll
   for (int j = 0; j < RS; ++j) {
     if (index_of(j) < x1) {
-      sr += f.rv_of(lp[j], lq[j]);
-      if (f.qrow) sp += f.pv_of(lp[j]);
+      const float pv = f.pv_of(lp[j]);
+      if (f.qrow) {
+        sr += fmaxf(__fsub_rn(pv, __fmul_rn(exp_of_diff(lq[j], f.mq), f.iq)), 0.0f);  // as rv_of
+        sp += pv;
+      } else {
+        sr += pv;
+      }
     }
   }
   const DF SR = block_sum(DF{sr, 0.0f});

@@ -490,10 +490,12 @@ static cudaError_t skinny_occupancy(int* blocks_per_sm) {
                                                       L::kTotal);
 }
 
-static int skinny_smem(int mt8) { return mt8 == 1 ? SkinnyLayout<1>::kTotal : SkinnyLayout<2>::kTotal; }
+// token tiles of 8: the fragment path serves M = 1..8 (one tile); the
+// tcgen05 path takes M >= 9
+static int skinny_smem(int) { return SkinnyLayout<1>::kTotal; }
 
 static cudaError_t skinny_occupancy_dispatch(int mt8, int* nb) {
-  return mt8 == 1 ? skinny_occupancy<1>(nb) : skinny_occupancy<2>(nb);
+  return mt8 == 1 ? skinny_occupancy<1>(nb) : cudaErrorInvalidValue;
 }
 
 cudaError_t skinny_plan(int M, int64_t N, int64_t K, const DeviceInfo& dev, size_t max_partial_bytes,
@@ -555,7 +557,6 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
   p.sched = plan.sched;
   switch (plan.mt8) {
     case 1: return launch_skinny_t<1>(p, plan, stream);
-    case 2: return launch_skinny_t<2>(p, plan, stream);
     default: return cudaErrorInvalidValue;
   }
 }
