@@ -938,6 +938,73 @@ __device__ void cluster_reduce2(cg::cluster_group& cluster, TreeShared& sh, int&
   phase ^= 1;
 }
 
+// Inverse-CDF draw over the cluster's vocabulary slices: rv holds this
+// thread's kTreePT values at x0, x0 + 1, ... (zero past V). The smallest x
+// whose ascending running sum exceeds u * S (double-float sums: the thread's
+// own run, the CTA's warps, the CTAs of lower rank); if rounding leaves no
+// such x, the last x with positive mass. Returns the index in rank 0's
+// thread 0; the caller writes its outputs there and synchronises the
+// cluster once more before any CTA exits.
+__device__ int cluster_draw(cg::cluster_group& cluster, TreeShared& sh, int phase, int rank, int x0, int V,
+                            const float (&rv)[kTreePT], float uval) {
+  DF mine{0.0f, 0.0f};
+  int lastp = -1;
+#pragma unroll
+  for (int k = 0; k < kTreePT; ++k) {
+    if (rv[k] > 0.0f) lastp = x0 + k;
+    mine = df_add_f(mine, rv[k]);
+  }
+  // this thread's exclusive prefix within the CTA, then the CTAs before it
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  DF incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const DF y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+    if (lane >= o) incl = df_add(y, incl);
+  }
+  if (lane == 31) sh.warp_part[w][0] = incl;
+  __syncthreads();
+  DF before{0.0f, 0.0f};
+  for (int i = 0; i < w; ++i) before = df_add(before, sh.warp_part[i][0]);
+  DF cta_total{0.0f, 0.0f};
+  for (int i = 0; i < kTreeWarps; ++i) cta_total = df_add(cta_total, sh.warp_part[i][0]);
+  const DF excl_thread = df_add(before, df_add(incl, DF{-mine.hi, -mine.lo}));
+  if (threadIdx.x == 0) {
+    sh.red[phase][0] = cta_total;
+    sh.found = INT_MAX;
+    sh.last_pos = -1;
+  }
+  cluster.sync();
+  DF below{0.0f, 0.0f}, S{0.0f, 0.0f};
+  for (int r = 0; r < kTreeCtas; ++r) {
+    const DF o = cluster.map_shared_rank(&sh, r)->red[phase][0];
+    if (r < rank) below = df_add(below, o);
+    S = df_add(S, o);
+  }
+  const DF tt = df_mul_f(S, uval);
+  DF run = df_add(below, excl_thread);
+  int hit = INT_MAX;
+#pragma unroll
+  for (int k = 0; k < kTreePT; ++k) {
+    run = df_add_f(run, rv[k]);
+    if (hit == INT_MAX && x0 + k < V && df_gt(run, tt)) hit = x0 + k;
+  }
+  if (hit != INT_MAX) atomicMin(&sh.found, hit);
+  if (lastp >= 0) atomicMax(&sh.last_pos, lastp);
+  cluster.sync();  // every CTA's candidates are in
+  int best = 0;
+  if (rank == 0 && threadIdx.x == 0) {
+    int found = INT_MAX, lastv = -1;
+    for (int r = 0; r < kTreeCtas; ++r) {
+      const TreeShared* o = cluster.map_shared_rank(&sh, r);
+      found = min(found, o->found);
+      lastv = max(lastv, o->last_pos);
+    }
+    best = found != INT_MAX ? found : (lastv >= 0 ? lastv : 0);
+  }
+  return best;
+}
+
 template <bool VEC>
 __global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads, 1) accept_tree_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
@@ -1057,62 +1124,12 @@ __global__ void __cluster_dims__(kTreeCtas, 1, 1) __launch_bounds__(kTreeThreads
   }
   // ---- the next token: inverse CDF of r(x) = max(0, P - c Q) (P itself when c = 0), ascending x
   float rv[kTreePT];
-  DF mine{0.0f, 0.0f};
-  int lastp = -1;
 #pragma unroll
-  for (int k = 0; k < kTreePT; ++k) {
-    const float v = c == 0.0f ? lp[k] : fmaxf(__fsub_rn(lp[k], __fmul_rn(c, lq[k])), 0.0f);
-    rv[k] = v;
-    if (v > 0.0f) lastp = x0 + k;
-    mine = df_add_f(mine, v);
-  }
-  // this thread's exclusive prefix within the CTA, then the CTAs before it
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  DF incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const DF y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
-    if (lane >= o) incl = df_add(y, incl);
-  }
-  if (lane == 31) sh.warp_part[w][0] = incl;
-  __syncthreads();
-  DF before{0.0f, 0.0f};
-  for (int i = 0; i < w; ++i) before = df_add(before, sh.warp_part[i][0]);
-  DF cta_total{0.0f, 0.0f};
-  for (int i = 0; i < kTreeWarps; ++i) cta_total = df_add(cta_total, sh.warp_part[i][0]);
-  const DF excl_thread = df_add(before, df_add(incl, DF{-mine.hi, -mine.lo}));
-  if (threadIdx.x == 0) {
-    sh.red[phase][0] = cta_total;
-    sh.found = INT_MAX;
-    sh.last_pos = -1;
-  }
-  cluster.sync();
-  DF below{0.0f, 0.0f}, S{0.0f, 0.0f};
-  for (int r = 0; r < kTreeCtas; ++r) {
-    const DF o = cluster.map_shared_rank(&sh, r)->red[phase][0];
-    if (r < rank) below = df_add(below, o);
-    S = df_add(S, o);
-  }
-  const DF tt = df_mul_f(S, ub[0]);
-  DF run = df_add(below, excl_thread);
-  int hit = INT_MAX;
-#pragma unroll
-  for (int k = 0; k < kTreePT; ++k) {
-    run = df_add_f(run, rv[k]);
-    if (hit == INT_MAX && x0 + k < V && df_gt(run, tt)) hit = x0 + k;
-  }
-  if (hit != INT_MAX) atomicMin(&sh.found, hit);
-  if (lastp >= 0) atomicMax(&sh.last_pos, lastp);
-  cluster.sync();  // every CTA's candidates are in
+  for (int k = 0; k < kTreePT; ++k) rv[k] = c == 0.0f ? lp[k] : fmaxf(__fsub_rn(lp[k], __fmul_rn(c, lq[k])), 0.0f);
+  const int best = cluster_draw(cluster, sh, phase, rank, x0, V, rv, ub[0]);
   if (rank == 0 && threadIdx.x == 0) {
-    int best = INT_MAX, lastv = -1;
-    for (int r = 0; r < kTreeCtas; ++r) {
-      const TreeShared* o = cluster.map_shared_rank(&sh, r);
-      best = min(best, o->found);
-      lastv = max(lastv, o->last_pos);
-    }
     acc_out[b] = depth;
-    next_out[b] = best != INT_MAX ? best : (lastv >= 0 ? lastv : 0);
+    next_out[b] = best;
     if (node_out) node_out[b] = node;
   }
   cluster.sync();  // no CTA leaves while rank 0 may still read its shared memory
