@@ -36,6 +36,8 @@ typedef int w4a16_status;
 #define W4A16_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait ran out (device error word) */
 #define W4A16_ERR_DEVICE_INPUT 5    /* a kernel found an out-of-range id or a bad parent (device error word) */
 #define W4A16_ERR_WORKSPACE 6       /* workspace pointer missing or smaller than required */
+#define W4A16_ERR_BOUNDS 7          /* bounds-checked debug build only: a kernel's computed index left its
+                                       buffer (recorded in the device error word, the access skipped) */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* w4a16_status_string(w4a16_status status);

@@ -5,6 +5,7 @@ Python fallback for any entry point.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -20,6 +21,7 @@ ERR_CUDA = 3
 ERR_DEVICE_TIMEOUT = 4
 ERR_DEVICE_INPUT = 5
 ERR_WORKSPACE = 6
+ERR_BOUNDS = 7
 
 _lock = threading.Lock()
 _lib = None
@@ -61,6 +63,15 @@ class W4A16Error(RuntimeError):
         super().__init__(f"{what}: {status_string(status)} ({status})" if what else status_string(status))
 
 
+def _load(path: str):
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
 def lib():
     """The loaded library (built in-tree by __graft_entry__.build())."""
     global _lib
@@ -69,13 +80,23 @@ def lib():
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(
                     f"{LIB_PATH} is missing: build it with `python -m speculative_decode_verify_w4a16_gb300.build`")
-            L = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(L, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = L
+            _lib = _load(LIB_PATH)
     return _lib
+
+
+@contextlib.contextmanager
+def use_library(path: str):
+    """Route every call of this binding through another build of the same
+    ABI (the debug builds the tests load) while the context is open."""
+    global _lib
+    lib()
+    with _lock:
+        saved, _lib = _lib, _load(path)
+    try:
+        yield _lib
+    finally:
+        with _lock:
+            _lib = saved
 
 
 def status_string(status: int) -> str:

@@ -54,6 +54,20 @@ def build_debug(force: bool = False) -> str:
                  obj_dir=os.path.join(os.path.dirname(PKG), "_build", "w4a16sv_debug"))
 
 
+# Bounds-checked library for the tests: every instrumented global index is
+# checked against its buffer and a miss is recorded in the device error word
+# (W4A16_ERR_BOUNDS) instead of being performed. Outside the package; the
+# product never loads it.
+BOUNDS_LIB = os.path.join(os.path.dirname(PKG), "_build", "libw4a16sv_bounds.so")
+BOUNDS_FLAGS = ["-DW4A16_BOUNDS_CHECK=1"]
+
+
+def build_bounds(force: bool = False) -> str:
+    """Build the bounds-checked library (see BOUNDS_FLAGS) and return its path."""
+    return build(force=force, extra_flags=BOUNDS_FLAGS, out=BOUNDS_LIB,
+                 obj_dir=os.path.join(os.path.dirname(PKG), "_build", "w4a16sv_bounds"))
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None, out: str = LIB, obj_dir: str = BUILD) -> str:
     stale = not os.path.exists(out) or any(os.path.getmtime(f) > os.path.getmtime(out) for f in _deps())
     if not force and not stale:

@@ -257,7 +257,7 @@ __device__ __forceinline__ void load_chunk(const float* row, int x0, int x1, flo
 // double-float across lanes); lane 0 stores them. Padding (-FLT_MAX) adds 0.
 // exp via ex2.approx (__expf): its relative error grows with |l - m|, so it is
 // smallest on the terms that carry the sum; about 1e-7 of the total.
-__device__ __forceinline__ void item_stats(const float (&v)[kStatPT], RowStat* out) {
+__device__ __forceinline__ void item_stats(const float (&v)[kStatPT], RowStat* out, bool store) {
   float m = -FLT_MAX;
 #pragma unroll
   for (int j = 0; j < kStatPT; ++j) m = fmaxf(m, v[j]);
@@ -274,7 +274,7 @@ __device__ __forceinline__ void item_stats(const float (&v)[kStatPT], RowStat* o
   DF s{t[0], 0.0f};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = df_add(s, shfl_xor_df(s, o));
-  if ((threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
+  if (store && (threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
 }
 
 __device__ __forceinline__ void item_range(int n, int V, int ch, int it, int& rr, int& x0, int& x1) {
@@ -337,7 +337,7 @@ __device__ __forceinline__ void load_slice_item(const float2* ps, int V, int chs
 // Merged statistics of an item of slices: m = max of the slice maxima,
 // sum of s_j exp(m_j - m) (fp32 per lane, pairwise; double-float across
 // lanes), as item_stats does for raw logits.
-__device__ __forceinline__ void slice_item_stats(const float (&v)[kStatPT], RowStat* out) {
+__device__ __forceinline__ void slice_item_stats(const float (&v)[kStatPT], RowStat* out, bool store) {
   float m = -FLT_MAX;
 #pragma unroll
   for (int j = 0; j < kStatPT / 2; ++j) m = fmaxf(m, v[2 * j]);
@@ -354,7 +354,7 @@ __device__ __forceinline__ void slice_item_stats(const float (&v)[kStatPT], RowS
   DF s{t[0], 0.0f};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s = df_add(s, shfl_xor_df(s, o));
-  if ((threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
+  if (store && (threadIdx.x & 31) == 0) *out = RowStat{m, 0.0f, s};
 }
 
 template <bool VEC>
@@ -362,7 +362,8 @@ __global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_ke
                                                                        const float* __restrict__ q, int n, int V,
                                                                        int ch, int items, int q_only,
                                                                        const float2* __restrict__ p_stats, int chs,
-                                                                       int slice_items, RowStat* __restrict__ stats) {
+                                                                       int slice_items, RowStat* __restrict__ stats,
+                                                                       int64_t stats_cap, unsigned* err) {
   grid_launch_dependents();
   grid_dependency_wait();
   // items [0, items): logit chunks; [items, items + slice_items): slices of
@@ -375,10 +376,11 @@ __global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_ke
       load_slice_item(p_stats, V, chs, i - items, v);
   };
   auto reduce = [&](int i, const float (&v)[kStatPT]) {
+    const bool ok = in_bounds(err, i, stats_cap);
     if (i < items)
-      item_stats(v, stats + i);
+      item_stats(v, stats + i, ok);
     else
-      slice_item_stats(v, stats + i);
+      slice_item_stats(v, stats + i, ok);
   };
   const int nw = gridDim.x * kAccWarps;
   int it = blockIdx.x * kAccWarps + (threadIdx.x >> 5);
@@ -506,7 +508,8 @@ template <int RS, bool VEC>  // values per thread in a chunk: chunk2 <= RS * kAc
 __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
     const float* __restrict__ p, const float* __restrict__ q, const float* __restrict__ u, int n, int V,
     int chunk2, const Decision* __restrict__ dec, ChunkSum* __restrict__ csum, int* __restrict__ counters,
-    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out) {
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out, int64_t csum_cap,
+    unsigned* err) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int b = blockIdx.y;
@@ -568,9 +571,10 @@ __global__ void __launch_bounds__(kAccThreads, 4) accept_resid_kernel(
   const DF SP = block_sum(DF{sp, 0.0f});
   __shared__ int last;
   if (threadIdx.x == 0) {
-    csum[(int64_t)b * gridDim.x + blockIdx.x] = ChunkSum{SR, SP};
+    const int64_t ci = (int64_t)b * gridDim.x + blockIdx.x;
+    if (in_bounds(err, ci, csum_cap)) csum[ci] = ChunkSum{SR, SP};
     __threadfence();
-    last = atomicAdd(&counters[b], 1) == (int)gridDim.x - 1;
+    last = in_bounds(err, kCounterBank2 + b, kMaxCounters) && atomicAdd(&counters[b], 1) == (int)gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
@@ -734,7 +738,8 @@ template <bool VEC>
 __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
     const float* __restrict__ p, const int32_t* __restrict__ d, const int32_t* __restrict__ parents, int n,
     int rows_per_b, int V, int chunk, ArgPart* __restrict__ parts, int* __restrict__ counters,
-    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out, unsigned* err) {
+    int32_t* __restrict__ acc_out, int32_t* __restrict__ next_out, int32_t* __restrict__ node_out, unsigned* err,
+    int64_t parts_cap) {
   grid_launch_dependents();
   grid_dependency_wait();
   const int rr = blockIdx.y;  // row index over all batch rows
@@ -765,9 +770,10 @@ __global__ void __launch_bounds__(kAccThreads) accept_argmax_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 1; i < kAccWarps; ++i) best = arg_better(best, wbest[i]);
-    parts[(int64_t)rr * gridDim.x + blockIdx.x] = best;
+    const int64_t pi = (int64_t)rr * gridDim.x + blockIdx.x;
+    if (in_bounds(err, pi, parts_cap)) parts[pi] = best;
     __threadfence();
-    last = atomicAdd(&counters[b], 1) == rows_per_b * (int)gridDim.x - 1;
+    last = in_bounds(err, b, kCounterBank2) && atomicAdd(&counters[b], 1) == rows_per_b * (int)gridDim.x - 1;
   }
   __syncthreads();
   if (!last) return;
@@ -858,7 +864,7 @@ constexpr int kTreeThreads = 512;
 constexpr int kTreeWarps = kTreeThreads / 32;
 constexpr int kTreePT = 32;
 constexpr int kTreeSlice = kTreeThreads * kTreePT;  // 16384
-constexpr int kTreeMaxV = kTreeCtas * kTreeSlice;   // 131072
+static_assert(kTreeCtas * kTreeSlice == kAcceptTreeMaxV, "vocabulary limit of the cluster kernels");
 
 struct TreeShared {
   int par[kMaxNodes];
@@ -1200,6 +1206,8 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   Decision* dec = reinterpret_cast<Decision*>(w + pl.dec_off);
   ChunkSum* csum = reinterpret_cast<ChunkSum*>(w + pl.csum_off);
   int* cnt2 = reinterpret_cast<int*>(w) + kCounterBank2;
+  const int64_t stats_cap = (int64_t)((pl.dec_off - pl.stats_off) / sizeof(RowStat));
+  const int64_t csum_cap = (int64_t)((pl.total - pl.csum_off) / sizeof(ChunkSum));
   cudaError_t e;
   // statistics grid: persistent warps, one wave of resident blocks (the
   // kernel's launch bounds give two per SM); with the target statistics
@@ -1213,10 +1221,10 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   if (g1 > kStatBlocksPerSm * num_sms) g1 = kStatBlocksPerSm * num_sms;
   if (V % 4 == 0)
     e = launch_pdl(accept_stats_kernel<true>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, q_only,
-                   p_stats, chs, slice_items, stats);
+                   p_stats, chs, slice_items, stats, stats_cap, err);
   else
     e = launch_pdl(accept_stats_kernel<false>, dim3(g1), dim3(kAccThreads), 0, stream, p, q, n, V, pl.ch, items, q_only,
-                   p_stats, chs, slice_items, stats);
+                   p_stats, chs, slice_items, stats, stats_cap, err);
   if (e != cudaSuccess) return e;
   e = launch_pdl(accept_decide_kernel, dim3(B), dim3(kDecThreads), 0, stream, p, q, d, u, n, V, pl.ch,
                  (const RowStat*)stats, q_only, chs, dec, err);
@@ -1239,9 +1247,9 @@ cudaError_t launch_accept_seq(const float* p, const float* q, const int32_t* d, 
   ch2 = (V + chunk2 - 1) / chunk2;
   if (V % 4 == 0)
     return launch_pdl(accept_resid_kernel<kResidPT, true>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
-                      chunk2, (const Decision*)dec, csum, cnt2, acc, next, node);
+                      chunk2, (const Decision*)dec, csum, cnt2, acc, next, node, csum_cap, err);
   return launch_pdl(accept_resid_kernel<kResidPT, false>, dim3(ch2, B), dim3(kAccThreads), 0, stream, p, q, u, n, V,
-                    chunk2, (const Decision*)dec, csum, cnt2, acc, next, node);
+                    chunk2, (const Decision*)dec, csum, cnt2, acc, next, node, csum_cap, err);
 }
 
 cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t* parents, int B, int n, int V,
@@ -1252,11 +1260,12 @@ cudaError_t launch_accept_greedy(const float* p, const int32_t* d, const int32_t
   int* cnt = reinterpret_cast<int*>(w);
   const int rows_per_b = parents ? n : n + 1;
   const dim3 g(pl.cha, B * rows_per_b);
+  const int64_t parts_cap = (int64_t)((pl.dec_off - pl.stats_off) / sizeof(ArgPart));
   if (V % 4 == 0)
     return launch_pdl(accept_argmax_kernel<true>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                      pl.chunka, parts, cnt, acc, next, node, err);
+                      pl.chunka, parts, cnt, acc, next, node, err, parts_cap);
   return launch_pdl(accept_argmax_kernel<false>, g, dim3(kAccThreads), 0, stream, p, d, parents, n, rows_per_b, V,
-                    pl.chunka, parts, cnt, acc, next, node, err);
+                    pl.chunka, parts, cnt, acc, next, node, err, parts_cap);
 }
 
 }  // namespace w4a16

@@ -170,8 +170,9 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
     const int R = rows0 + r;
     const int j = R / p.G, g = R - j * p.G;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (j < p.n)
-      v = *reinterpret_cast<const uint4*>(p.q + (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD + c * 8);
+    const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD + c * 8;
+    if (j < p.n && in_bounds(p.err, qi + 7, (int64_t)p.B * p.n * p.H * kAttD))
+      v = *reinterpret_cast<const uint4*>(p.q + qi);
     *reinterpret_cast<uint4*>(qs + r * 256 + ((c ^ (r & 7)) << 4)) = v;
   }
   __syncthreads();
@@ -291,28 +292,34 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
   const int t2 = (lane & 3) << 1;
   if (p.splits == 1) {
     const float ia = l_a > 0.0f ? 1.0f / l_a : 0.0f, ib = l_b > 0.0f ? 1.0f / l_b : 0.0f;
-    if (ja < p.n) {
-      __nv_bfloat16* dst = p.out + (((int64_t)b * p.n + ja) * p.H + kvh * p.G + (ra - ja * p.G)) * kAttD + t2;
+    const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
+    const int64_t oa = (((int64_t)b * p.n + ja) * p.H + kvh * p.G + (ra - ja * p.G)) * kAttD;
+    const int64_t ob = (((int64_t)b * p.n + jb) * p.H + kvh * p.G + (rb8 - jb * p.G)) * kAttD;
+    if (ja < p.n && in_bounds(p.err, oa + kAttD - 1, out_cap)) {
+      __nv_bfloat16* dst = p.out + oa + t2;
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt)
         *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][0] * ia, o[dt][1] * ia);
     }
-    if (jb < p.n) {
-      __nv_bfloat16* dst = p.out + (((int64_t)b * p.n + jb) * p.H + kvh * p.G + (rb8 - jb * p.G)) * kAttD + t2;
+    if (jb < p.n && in_bounds(p.err, ob + kAttD - 1, out_cap)) {
+      __nv_bfloat16* dst = p.out + ob + t2;
 #pragma unroll
       for (int dt = 0; dt < 16; ++dt)
         *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][2] * ib, o[dt][3] * ib);
     }
   } else {
     const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
+    const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
     float* pa_o = p.part_o + (base + ra) * kAttD + t2;
     float* pb_o = p.part_o + (base + rb8) * kAttD + t2;
+    const bool ok = in_bounds(p.err, base + ra, rows_cap) && in_bounds(p.err, base + rb8, rows_cap);
 #pragma unroll
     for (int dt = 0; dt < 16; ++dt) {
+      if (!ok) break;
       *reinterpret_cast<float2*>(pa_o + dt * 8) = make_float2(o[dt][0], o[dt][1]);
       *reinterpret_cast<float2*>(pb_o + dt * 8) = make_float2(o[dt][2], o[dt][3]);
     }
-    if ((lane & 3) == 0) {
+    if (ok && (lane & 3) == 0) {
       p.part_ml[base + ra] = make_float2(m_a, l_a);
       p.part_ml[base + rb8] = make_float2(m_b, l_b);
     }
@@ -418,7 +425,7 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(uint4* kc, 
         const int d = d0 + idx / per_depth, rem = idx % per_depth;
         const int c = rem / (Hkv * row_words), h = (rem / row_words) % Hkv, w = rem % row_words;
         const uint4* src = (c ? vc : kc) + (bh0 + h) * head_words + (int64_t)(len + path[d]) * row_words + w;
-        v[k] = *src;
+        if (in_bounds(err, (int64_t)(len + path[d]) * row_words + w, head_words)) v[k] = *src;
       }
     }
     __syncthreads();
@@ -430,7 +437,7 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(uint4* kc, 
         if (path[d] == d) continue;  // already in place
         const int c = rem / (Hkv * row_words), h = (rem / row_words) % Hkv, w = rem % row_words;
         uint4* dst = (c ? vc : kc) + (bh0 + h) * head_words + (int64_t)(len + d) * row_words + w;
-        *dst = v[k];
+        if (in_bounds(err, (int64_t)(len + d) * row_words + w, head_words)) *dst = v[k];
       }
     }
     __syncthreads();

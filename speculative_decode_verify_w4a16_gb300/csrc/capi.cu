@@ -85,6 +85,7 @@ const char* w4a16_status_string(w4a16_status s) {
     case W4A16_ERR_DEVICE_TIMEOUT: return "W4A16_ERR_DEVICE_TIMEOUT";
     case W4A16_ERR_DEVICE_INPUT: return "W4A16_ERR_DEVICE_INPUT";
     case W4A16_ERR_WORKSPACE: return "W4A16_ERR_WORKSPACE";
+    case W4A16_ERR_BOUNDS: return "W4A16_ERR_BOUNDS";
     default: return "W4A16_ERR_UNKNOWN";
   }
 }
@@ -342,6 +343,7 @@ w4a16_status w4a16_check_device_status(void* stream) {
     if (cudaMemcpy(dev.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return W4A16_ERR_CUDA;
   }
   if (word & kErrTimeout) return W4A16_ERR_DEVICE_TIMEOUT;
+  if (word & kErrBounds) return W4A16_ERR_BOUNDS;
   if (word & kErrInput) return W4A16_ERR_DEVICE_INPUT;
   return W4A16_OK;
 }

@@ -12,6 +12,7 @@ namespace w4a16 {
 // Bits of the device error word.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrInput = 2u;
+constexpr unsigned kErrBounds = 4u;  // bounds-checked builds: a computed index left its buffer
 
 // Upper bound on any spin wait inside a kernel (ns of %globaltimer). A
 // debug build of the library (for the tests that make a wait run out) sets
@@ -29,6 +30,28 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 
 __device__ __forceinline__ void report_error(unsigned* err, unsigned bit) {
   if (err) atomicOr(err, bit);
+}
+
+// Bounds-checked builds (-DW4A16_BOUNDS_CHECK=1, a separate debug library)
+// test every instrumented global index against its buffer: one outside
+// [0, limit) sets kErrBounds in the device error word and the access is
+// skipped (no trap). In the product build this is always true and costs
+// nothing.
+#ifndef W4A16_BOUNDS_CHECK
+#define W4A16_BOUNDS_CHECK 0
+#endif
+__device__ __forceinline__ bool in_bounds(unsigned* err, int64_t idx, int64_t limit) {
+#if W4A16_BOUNDS_CHECK
+  if (idx < 0 || idx >= limit) {
+    report_error(err, kErrBounds);
+    return false;
+  }
+#else
+  (void)err;
+  (void)idx;
+  (void)limit;
+#endif
+  return true;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -95,6 +95,7 @@ struct SkinnyParams {
   int M;
   int items;  // R * C
   ItemSched sched;
+  int64_t partial_cap;  // float4 slots in partials (bounds-checked builds)
 };
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -137,11 +138,12 @@ __device__ __forceinline__ void store_tile(const SkinnyParams& p, int64_t t, int
 #pragma unroll
     for (int nt = 0; nt < MT8; ++nt) {
       const int m0 = nt * 8 + 2 * cq;
-      if (m0 < p.M) {
+      const int64_t mn = (int64_t)p.M * p.N;
+      if (m0 < p.M && in_bounds(p.err, (int64_t)m0 * p.N + n_lo + 8, mn)) {
         p.out[(int64_t)m0 * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][0]);
         p.out[(int64_t)m0 * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][2]);
       }
-      if (m0 + 1 < p.M) {
+      if (m0 + 1 < p.M && in_bounds(p.err, (int64_t)(m0 + 1) * p.N + n_lo + 8, mn)) {
         p.out[(int64_t)(m0 + 1) * p.N + n_lo] = __float2bfloat16_rn(acc[rt][nt][1]);
         p.out[(int64_t)(m0 + 1) * p.N + n_lo + 8] = __float2bfloat16_rn(acc[rt][nt][3]);
       }
@@ -163,14 +165,18 @@ template <int MT8>
 __device__ void finish_split_tile(const SkinnyParams& p, int item, int seg, int64_t t, int warp, int lane,
                                   const float (&acc)[2][MT8][4]) {
   float4* slot = partial_slot<MT8>(p, item, seg, warp);
+  const bool slot_ok = in_bounds(p.err, (slot - p.partials) + 2 * MT8 * 32 - 1, p.partial_cap);
 #pragma unroll
   for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
     for (int nt = 0; nt < MT8; ++nt)
-      __stcg(&slot[(rt * MT8 + nt) * 32 + lane],
-             make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]));
+      if (slot_ok)
+        __stcg(&slot[(rt * MT8 + nt) * 32 + lane],
+               make_float4(acc[rt][nt][0], acc[rt][nt][1], acc[rt][nt][2], acc[rt][nt][3]));
   __syncwarp();
-  int* counter = &p.counters[kTileCounterBase + t * kSkConsumerWarps + warp];
+  const int64_t ci = kTileCounterBase + t * kSkConsumerWarps + warp;
+  if (!in_bounds(p.err, ci, kMaxCounters)) return;
+  int* counter = &p.counters[ci];
   int old = 0;
   if (lane == 0) old = atomic_add_acq_rel(counter, 1);
   old = __shfl_sync(0xffffffffu, old, 0);
@@ -196,11 +202,12 @@ __device__ void finish_split_tile(const SkinnyParams& p, int item, int seg, int6
     for (int j = 0; j < RB; ++j) {
       const int cc = c0 + j;
       const float4* sl = partial_slot<MT8>(p, cc, cc == cf ? seg_cf : 0, warp);
+      const bool ok = cc <= cl && in_bounds(p.err, (sl - p.partials) + 2 * MT8 * 32 - 1, p.partial_cap);
 #pragma unroll
       for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
         for (int nt = 0; nt < MT8; ++nt)
-          v[j][rt][nt] = cc <= cl ? __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[j][rt][nt] = ok ? __ldcg(&sl[(rt * MT8 + nt) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int j = 0; j < RB; ++j)
@@ -281,6 +288,11 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       ue = item_begin(p.sched, item + 1);
       u = ub;
     }
+    // the stage's units and token columns lie inside the packed weights and x
+    auto stage_in_bounds = [&](int64_t u0, int64_t g0, int64_t n) {
+      return in_bounds(p.err, u0 + n - 1, (p.N / kUnitRows) * p.G) &&
+             in_bounds(p.err, (int64_t)(p.M - 1) * p.K + (g0 + n) * kGroup - 1, (int64_t)p.M * p.K);
+    };
     // one stage: up to kSkGroups units of the current tile segment; returns the units taken
     auto stage_codes = [&](int st, int64_t& g0_out, bool skip) -> int64_t {
       const int64_t t = u / p.G, g0 = u - t * p.G;
@@ -294,27 +306,33 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       if (skip) return n;
       uint8_t* sb = smem + st * L::kStage;
       const uint32_t nb = (uint32_t)n;
+      if (!stage_in_bounds(u, g0, n)) {  // bounds-checked builds: complete the stage without copies
+        mbar_arrive(&full[st]);
+        return n;
+      }
       mbar_arrive_expect_tx(&full[st], nb * (uint32_t)(kUnitBytes + kUnitScaleBytes + p.M * 256));
       bulk_g2s_hint(sb, p.qw + u * kUnitBytes, nb * kUnitBytes, &full[st], pol);
       bulk_g2s(sb + L::kW, p.sc + u * kUnitScaleBytes, nb * kUnitScaleBytes, &full[st]);
       return n;
     };
-    auto stage_tokens = [&](int st, int64_t g0, int64_t n) {
+    auto stage_tokens = [&](int st, int64_t u0, int64_t g0, int64_t n) {
+      if (!stage_in_bounds(u0, g0, n)) return;  // the stage went without copies
       uint8_t* sb = smem + st * L::kStage;
       for (int m = 0; m < p.M; ++m)
         bulk_g2s(sb + L::kW + L::kS + m * kXRowStride, p.x + (int64_t)m * p.K + g0 * kGroup, (uint32_t)n * 256u,
                  &full[st]);
     };
-    int64_t early_g0[S], early_n[S];
+    int64_t early_g0[S], early_n[S], early_u[S];
     int n_early = 0;
     while (n_early < S && item < p.items && u < ue) {
+      early_u[n_early] = u;
       early_n[n_early] = stage_codes(n_early, early_g0[n_early], false);
       u += early_n[n_early];
       ++n_early;
       ++n_stage;
     }
     grid_dependency_wait();
-    for (int i = 0; i < n_early; ++i) stage_tokens(i, early_g0[i], early_n[i]);
+    for (int i = 0; i < n_early; ++i) stage_tokens(i, early_u[i], early_g0[i], early_n[i]);
     while (ok && item < p.items) {
       if (u >= ue) {  // next item of this CTA
         item += gridDim.x;
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
       int64_t g0;
       const bool skip = test_skip_stage(n_stage);
       const int64_t n = stage_codes(st, g0, skip);
-      if (!skip) stage_tokens(st, g0, n);
+      if (!skip) stage_tokens(st, u, g0, n);
       u += n;
       ++n_stage;
     }
@@ -548,6 +566,7 @@ cudaError_t launch_skinny(const void* x, int M, int64_t K, const void* qw_packed
   p.out = static_cast<__nv_bfloat16*>(out);
   p.counters = static_cast<int*>(workspace);
   p.partials = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + plan.counter_bytes);
+  p.partial_cap = (int64_t)(plan.partial_bytes / sizeof(float4));
   p.err = dev.err;
   p.K = K;
   p.N = N;

@@ -127,6 +127,7 @@ struct TcParams {
   int M;
   int items;  // R * C
   ItemSched sched;
+  int64_t partial_cap;  // float4 slots in partials (bounds-checked builds)
 };
 
 // Stage metadata written by the producer: the unit's item, tile and group.
@@ -186,7 +187,7 @@ __device__ __forceinline__ void tc_store(const TcParams& p, const CUtensorMap* o
     } else {
 #pragma unroll
       for (int m = 0; m < NT; ++m)
-        if (m < p.M) p.logits[(int64_t)m * p.N + n] = acc[m];
+        if (m < p.M && in_bounds(p.err, (int64_t)m * p.N + n, (int64_t)p.M * p.N)) p.logits[(int64_t)m * p.N + n] = acc[m];
       __syncwarp();
     }
     // lane j: tokens j, j + 32, ... (all rounds interleaved, four independent
@@ -235,7 +236,7 @@ __device__ __forceinline__ void tc_store(const TcParams& p, const CUtensorMap* o
 #pragma unroll
     for (int j = 0; j < RN; ++j) {
       const int m = lane + 32 * j;
-      if (m < p.M)
+      if (m < p.M && in_bounds(p.err, (int64_t)m * (p.N / 32) + slice, (int64_t)p.M * (p.N / 32)))
         p.stats[(int64_t)m * (p.N / 32) + slice] = make_float2(mx[j][0], (z[j][0] + z[j][1]) + (z[j][2] + z[j][3]));
     }
     __syncwarp();  // every lane has read the staging area before it is rewritten
@@ -257,7 +258,8 @@ __device__ __forceinline__ void tc_store(const TcParams& p, const CUtensorMap* o
   }
 #pragma unroll
   for (int m = 0; m < NT; ++m)
-    if (m < p.M) p.out[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
+    if (m < p.M && in_bounds(p.err, (int64_t)m * p.N + n, (int64_t)p.M * p.N))
+      p.out[(int64_t)m * p.N + n] = __float2bfloat16_rn(acc[m]);
 }
 
 // Split tiles. Each item that covers part of a tile's K range writes the
@@ -276,11 +278,15 @@ __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint
                                 int64_t t, int q, int lane, const float (&acc)[NT]) {
   const int epw = q;
   float4* slot = tc_slot<NT>(p, item, seg, epw);
+  const bool slot_ok = in_bounds(p.err, (slot - p.partials) + NT / 4 * 32 - 1, p.partial_cap);
 #pragma unroll
   for (int j = 0; j < NT / 4; ++j)
-    __stcg(&slot[j * 32 + lane], make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+    if (slot_ok)
+      __stcg(&slot[j * 32 + lane], make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
   __syncwarp();
-  int* counter = &p.counters[kTileCounterBase + t * kTcEpWarps + epw];
+  const int64_t ci = kTileCounterBase + t * kTcEpWarps + epw;
+  if (!in_bounds(p.err, ci, kMaxCounters)) return;
+  int* counter = &p.counters[ci];
   int old = 0;
   if (lane == 0) old = atomic_add_acq_rel(counter, 1);
   old = __shfl_sync(0xffffffffu, old, 0);
@@ -305,9 +311,10 @@ __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint
       for (int r = 0; r < RB; ++r) {
         const int cc = c0 + r;
         const float4* sl = tc_slot<NT>(p, cc, cc == cf ? seg_cf : 0, epw);
+        const bool ok = cc <= cl && in_bounds(p.err, (sl - p.partials) + NT / 4 * 32 - 1, p.partial_cap);
 #pragma unroll
         for (int j = 0; j < JB; ++j)
-          v[r][j] = cc <= cl ? __ldcg(&sl[(j0 + j) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[r][j] = ok ? __ldcg(&sl[(j0 + j) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int r = 0; r < RB; ++r)
@@ -421,9 +428,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           }
           meta[s] = make_int4(item, (int)t, (int)g, (u == ub ? kTcUnitFirst : 0) | (u == ue - 1 ? kTcUnitLast : 0));
           uint8_t* ws = smem + L::kWOff + s * L::kWStage;
-          mbar_arrive_expect_tx(&wfull[s], (uint32_t)L::kWStage);
-          bulk_g2s_hint(ws, p.qw + u * kUnitBytes, kUnitBytes, &wfull[s], pol);
-          bulk_g2s(ws + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &wfull[s]);
+          if (in_bounds(p.err, u, (p.N / kUnitRows) * p.G)) {
+            mbar_arrive_expect_tx(&wfull[s], (uint32_t)L::kWStage);
+            bulk_g2s_hint(ws, p.qw + u * kUnitBytes, kUnitBytes, &wfull[s], pol);
+            bulk_g2s(ws + kUnitBytes, p.sc + u * kUnitScaleBytes, kUnitScaleBytes, &wfull[s]);
+          } else {
+            mbar_arrive(&wfull[s]);  // bounds-checked builds: the stage without copies
+          }
           if (++g == p.G) {
             g = 0;
             ++t;
@@ -818,6 +829,7 @@ static cudaError_t tc_setup(const void* x, int M, int64_t K, const void* qw_pack
   p->M = M;
   p->items = plan.sched.R * plan.sched.C;
   p->sched = plan.sched;
+  p->partial_cap = (int64_t)(plan.partial_bytes / sizeof(float4));
   return cudaSuccess;
 }
 
