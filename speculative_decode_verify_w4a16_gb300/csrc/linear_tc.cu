@@ -332,23 +332,32 @@ __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint
 }
 
 // acc[j] += sc * D[lane][col + j], j < W (TMEM columns of this warp's slice;
-// W a multiple of 16). The accumulator is read 8 columns per load with two
-// loads in flight: measured against wider loads and against reading two
-// units' accumulators together, this keeps the MMAs that write other
-// accumulators fastest (gate+up M = 64: 900 -> 784 cycles per unit).
+// W a multiple of 16), up to 32 columns per round trip: a round trip of
+// tcgen05.ld + wait::ld costs about 160 cycles however many columns it
+// carries (measured on GB300), and the other warps' TMEM traffic does not
+// slow the MMAs, so the epilogue of a unit takes as few rounds as the
+// registers allow. The accumulator goes back to the MMAs (arrival on
+// `release`) as soon as its last columns are in registers: the ring of
+// accumulators is the loop that paces the kernel (MMA, completion, epilogue,
+// release), and the last multiply-adds need not be inside it.
 template <int W>
-__device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&acc)[W]) {
+__device__ __forceinline__ void tc_epilogue_fma(uint32_t dt, float sc, float (&acc)[W], uint64_t* release, int lane) {
 #pragma unroll
-  for (int c0 = 0; c0 + 16 <= W; c0 += 16) {
-    uint32_t v0[8], v1[8];
-    tmem_ld_32x32b_x8(dt + c0, v0);
-    tmem_ld_32x32b_x8(dt + c0 + 8, v1);
+  for (int c0 = 0; c0 < W; c0 += 32) {
+    const int cw = W - c0 < 32 ? W - c0 : 32;
+    uint32_t v[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 8)
+      if (j < cw) tmem_ld_32x32b_x8(dt + c0 + j, *reinterpret_cast<uint32_t(*)[8]>(&v[j]));
     tmem_wait_ld();
-#pragma unroll
-    for (int c = 0; c < 8; c += 2) {
-      ffma2(acc[c0 + c], acc[c0 + c + 1], sc, sc, __uint_as_float(v0[c]), __uint_as_float(v0[c + 1]));
-      ffma2(acc[c0 + 8 + c], acc[c0 + 8 + c + 1], sc, sc, __uint_as_float(v1[c]), __uint_as_float(v1[c + 1]));
+    if (c0 + 32 >= W) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(release);
     }
+#pragma unroll
+    for (int c = 0; c < 32; c += 2)
+      if (c < cw) ffma2(acc[c0 + c], acc[c0 + c + 1], sc, sc, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
   }
 }
 
@@ -490,45 +499,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
     }
   } else if (warp >= kTcMmaWarp0) {
     // ------------------------------------------------------------- MMA
-    // MMA warp j issues the units of dequant group j (i = j, j + 3, ...).
+    // MMA warp j issues the units of dequant group j (i = j, j + 2, ...).
     // The group waited for the unit's stage before it arrived on a_full, so
     // the token tile is in shared memory once a_full completes.
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(NT);
-      for (uint32_t i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
-        const uint32_t sx = i % L::kXStages, b = i % L::kA, db = i % L::kD, cb = i % L::kR;
-        const uint32_t pa = (i / L::kA) & 1u, pd = ((i / L::kD) & 1u) ^ 1u, px = (i / L::kXStages) & 1u;
+    const uint32_t idesc = umma_idesc_bf16(NT);
+    for (uint32_t i = warp - kTcMmaWarp0;; i += kTcDqGroups) {
+      const uint32_t sx = i % L::kXStages, b = i % L::kA, db = i % L::kD, cb = i % L::kR;
+      const uint32_t pa = (i / L::kA) & 1u, pd = ((i / L::kD) & 1u) ^ 1u, px = (i / L::kXStages) & 1u;
+      int st = 1;  // 1: go on, 0: a wait ran out, 2: stop marker
+      if (lane == 0) {
         // the three barriers tested at once (one latency); waits in order only
         // for those still open (the token tile after the stop check)
         const bool ta = mbar_test(&a_full[b], pa);
         const bool td = mbar_test(&d_free[db], pd) | (i < (uint32_t)L::kD);
         const bool tx = mbar_test(&xfull[sx], px);
-        if (!ta && !mbar_wait(&a_full[b], pa, p.err)) break;
-        if (!td && !mbar_wait(&d_free[db], pd, p.err)) break;
-        const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
-        if (mk < 0) {  // stop marker
-          if (mk == -1) {  // the epilogue's last index: complete its phase without MMAs
-            mbar_arrive(&mma_done[cb]);
-            mbar_arrive(&mma_done[cb]);
+        if ((!ta && !mbar_wait(&a_full[b], pa, p.err)) || (!td && !mbar_wait(&d_free[db], pd, p.err))) {
+          st = 0;
+        } else {
+          const int mk = meta_ring[i % kTcRing].x;  // written by the group before a_full
+          if (mk < 0) {  // stop marker
+            if (mk == -1) {  // the epilogue's last index: complete its phase without MMAs
+              mbar_arrive(&mma_done[cb]);
+              mbar_arrive(&mma_done[cb]);
+            }
+            st = 2;
+          } else if (!tx && !mbar_wait(&xfull[sx], px, p.err)) {
+            st = 0;
           }
-          break;
         }
-        if (!tx && !mbar_wait(&xfull[sx], px, p.err)) break;
-        tc_fence_after();
-        const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + L::kXOff + sx * L::kXStage));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // start-address field (bits 0..13, 16-byte units) of the K step's rows
-          const uint64_t bd = bd0 + (uint64_t)(((kk < 4 ? 0 : L::kX) + 32 * (kk & 3)) >> 4);
-          umma_bf16_ts(tmem + d_col(db), tmem + a_col(b) + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&done[cb]);  // frees A[b] and the token tile (cb == sx), hands D[db] to the epilogue
-        // release (to the epilogue) of the hand-off entry this thread acquired through a_full
-        mbar_arrive(&done[cb]);
-        mma_issued = (int)i + 1;
       }
-      if (mma_issued > 0) umma_commit(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this thread's MMAs
+      st = __shfl_sync(0xffffffffu, st, 0);
+      __syncwarp();
+      if (st != 1) break;
+      tc_fence_after();
+      const uint64_t bd0 = umma_desc_sw128_kmajor(smem_u32(smem + L::kXOff + sx * L::kXStage));
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        // start-address field (bits 0..13, 16-byte units) of the K step's rows
+        const uint64_t bd = bd0 + (uint64_t)(((kk < 4 ? 0 : L::kX) + 32 * (kk & 3)) >> 4);
+        umma_bf16_ts_warp(tmem + d_col(db), tmem + a_col(b) + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(&done[cb]);  // frees A[b] and the token tile (cb == sx), hands D[db] to the epilogue
+      // release (to the epilogue) of the hand-off entry lane 0 acquired through a_full
+      if (lane == 0) mbar_arrive(&done[cb]);
+      mma_issued = (int)i + 1;
     }
+    if (mma_issued > 0) umma_commit_warp(&mma_fin[warp - kTcMmaWarp0]);  // tracks all of this warp's MMAs
   } else if (warp < kTcDqWarps) {
     // ------------------------------------------------------ dequant groups
     const int grp = warp >> 2, q = warp & 3;
@@ -637,14 +653,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
       }
       tc_fence_after();
       const uint32_t dt = tmem + ((uint32_t)(32 * q) << 16);
-      tc_epilogue_fma<NT>(dt + d_col(db), scale_of(e), acc);  // unit e first, then e + 1
-      if (pair) tc_epilogue_fma<NT>(dt + d_col(db1), scale_of(e + 1), acc);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&d_free[db]);
-        if (pair) mbar_arrive(&d_free[db1]);
-      }
+      tc_epilogue_fma<NT>(dt + d_col(db), scale_of(e), acc, &d_free[db], lane);  // unit e first, then e + 1
+      if (pair) tc_epilogue_fma<NT>(dt + d_col(db1), scale_of(e + 1), acc, &d_free[db1], lane);
       const int4 ml = pair ? me1 : me;  // last unit taken
       if (ml.z == p.G - 1 || (ml.w & kTcUnitLast)) {  // end of this item's segment of tile ml.y
         if (seg_g0 == 0 && ml.z == p.G - 1)
