@@ -11,8 +11,10 @@ One step = one verify pass of the hot path on Llama-3-70B shapes:
 the step replayed as one CUDA graph).
 
 Besides the contract line the run measures, per call (mean and median of 50
-after 10 warm-up calls; consecutive linear calls stream distinct weight
-copies, together more than 3x the L2; L2 flushed before every accept call): the single 2048 x 2048 linear at
+after 10 warm-up calls, each call between two timing events; consecutive
+linear calls stream distinct weight copies, together more than 3x the L2; L2
+flushed before every accept call; linear calls also in sequence: 50 calls back
+to back in one graph, per-call time the median of 5 replays): the single 2048 x 2048 linear at
 M = 4; each Llama-3-70B shape including the lm_head at M = 1, 4, 8, 16, 32,
 48, 64 (us, GB/s, TFLOP/s, fraction of the HBM roofline, time relative to
 M = 1); the stochastic accept at K = 4 and 8 and the greedy tree; the lm_head
@@ -231,6 +233,33 @@ def time_per_call(torch, fn, flush=None, reps=CALL_REPS, warmup=CALL_WARMUP):
     return statistics.fmean(ts), statistics.median(ts)
 
 
+def time_in_sequence(torch, fn, reps=CALL_REPS, replays=5, warmup=CALL_WARMUP):
+    """Device time (us) per call of `reps` calls fn(0..reps-1) issued back to
+    back (one CUDA graph, no event between the calls, so each kernel's launch
+    and weight prefetch overlap the previous kernel's tail as in a verify
+    forward): median over `replays` timed replays of the graph, after
+    `warmup` eager calls and one untimed replay."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    a, b = _event(torch), _event(torch)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        a.record()
+        for i in range(reps):
+            fn(i)
+        b.record()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(replays):
+        g.replay()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3 / reps)
+    del g
+    return statistics.median(ts)
+
+
 def run_only(args, sv, torch, device, layers, acc_in, acc_out, acc_ws, tree_in, tree_out, acc_ws2):
     """One kind of launch only, eagerly, for profiling (no JSON contract line)."""
     if args.only == "linear":
@@ -264,19 +293,25 @@ def run_sweep(sv, torch, device, gen, layers, pk, flush):
     for (name, K, N), ms in shapes:
         copies = min(160, max(2, -(-3 * L2_BYTES // (N * K // 2)) + 1))
         wts = [make_weight(sv, torch, N, K, gen, device) for _ in range(copies)]
-        base = None
+        base = base_seq = None
         for M in ms:
             x = torch.randn((M, K), generator=gen, device=device).to(torch.bfloat16)
             out = torch.empty((M, N), dtype=torch.bfloat16, device=device)
             ws = torch.zeros(sv.linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=device)
-            us, us_med = time_per_call(torch, lambda i: sv.linear(x, wts[i % copies], out=out, ws=ws))
+            call = lambda i: sv.linear(x, wts[i % copies], out=out, ws=ws)
+            us, us_med = time_per_call(torch, call)
+            us_seq = time_in_sequence(torch, call)
             b = linear_bytes(M, N, K)
             base = us if base is None else base
+            base_seq = us_seq if base_seq is None else base_seq
             rows.append({"shape": name, "M": M, "K": K, "N": N, "us": round(us, 2), "us_median": round(us_med, 2),
                          "GB_s": round(b / us / 1e3, 1), "TFLOP_s": round(2.0 * M * N * K / us / 1e6, 2),
                          "frac_hbm": round(b / us / 1e3 / pk["hbm_gbs"], 3),
+                         "us_seq": round(us_seq, 2), "frac_hbm_seq": round(b / us_seq / 1e3 / pk["hbm_gbs"], 3),
                          "ideal_us": round(b / pk["hbm_gbs"] / 1e3, 2),
-                         "ratio_to_m1": round(us / base, 3) if ms[0] == 1 else None, "weight_copies": copies})
+                         "ratio_to_m1": round(us / base, 3) if ms[0] == 1 else None,
+                         "ratio_to_m1_seq": round(us_seq / base_seq, 3) if ms[0] == 1 else None,
+                         "weight_copies": copies})
         del wts
         torch.cuda.empty_cache()
     _check(sv, "the linear sweep")
@@ -667,6 +702,8 @@ def run_ours(args):
     if sweep:
         summary["linear_frac_hbm"] = {f"{r['shape']}/M{r['M']}": r["frac_hbm"] for r in sweep
                                       if r["M"] in (1, 4, 8, 64)}
+        summary["linear_frac_hbm_seq"] = {f"{r['shape']}/M{r['M']}": r["frac_hbm_seq"] for r in sweep
+                                          if r["M"] in (1, 4, 8, 64)}
         summary["linear_ratio_m64_m1"] = {r["shape"]: r["ratio_to_m1"] for r in sweep if r["M"] == 64}
         summary["accept"] = {(f"seq K={a['K']}" if "K" in a else a["mode"]): {"us": a["us"], "frac_hbm": a["frac_hbm"]}
                              for a in accept if a["mode"] in ("stochastic sequence", "greedy tree", "stochastic tree")}

@@ -8,7 +8,7 @@
 // stages filled by 1-D bulk copies (TMA engine), so every weight byte is read
 // from HBM exactly once.
 //
-// One CTA per SM: 4 or 5 consumer groups of 4 warps (a warp owns one 32-row
+// One CTA per SM: 6 consumer groups of 4 warps (a warp owns one 32-row
 // slice of the 128-row unit) and one producer warp. A ring stage holds one
 // unit per group, consecutive units of one tile segment, and group j takes
 // unit j, so all the consumer warps of the SM move through the weight stream
@@ -56,10 +56,11 @@ constexpr int kStSegLast = 4;    // the stage ends it
 
 template <int MT8>
 struct SkinnyLayout {
-  // consumer groups (units per stage) and ring depth: five groups of four
-  // warps when the token tile is one MMA wide (more warps hide more latency),
-  // four when it is two wide (shared memory)
-  static constexpr int kGroups = MT8 == 1 ? 5 : 4;
+  // consumer groups (units per stage) and ring depth: six groups of four
+  // warps when the token tile is one MMA wide (25 warps x 80 registers fill
+  // the register file; more warps hide more latency), four when it is two
+  // wide (shared memory)
+  static constexpr int kGroups = MT8 == 1 ? 6 : 4;
   static constexpr int kStages = 3;
   static constexpr int kConsumers = kGroups * kSkConsumerWarps;  // warps 0 .. kConsumers - 1
   static constexpr int kProducerWarp = kConsumers;               // the last warp
@@ -71,10 +72,13 @@ struct SkinnyLayout {
   static constexpr int kS = kGroups * kUnitScaleBytes;  // their scales
   static constexpr int kX = MT8 * 8 * kXRowStride;      // token rows
   static constexpr int kStage = kW + kS + kX;
-  // group sums of a segment end, double-buffered: [2][group 1..3][slice][2*MT8 float4][32 lanes]
+  // group sums of a segment end: [kRedBufs][group 1..kGroups-1][slice][2*MT8 float4][32 lanes]
+  // (one buffer: segment ends are many stages apart, so the groups never
+  // wait for group 0 to have read the previous segment's sums)
+  static constexpr int kRedBufs = 1;
   static constexpr int kRedSlot = 2 * MT8 * 32 * 16;
   static constexpr int kRedOff = kStages * kStage;
-  static constexpr int kMetaOff = kRedOff + 2 * (kGroups - 1) * kSkConsumerWarps * kRedSlot;
+  static constexpr int kMetaOff = kRedOff + kRedBufs * (kGroups - 1) * kSkConsumerWarps * kRedSlot;
   static constexpr int kBarOff = kMetaOff + kStages * 16;
   // full[stages], empty[stages], red_full[2], red_empty[2]
   static constexpr int kTotal = kBarOff + (2 * kStages + 4) * 8;
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
   int4* meta = reinterpret_cast<int4*>(smem + L::kMetaOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + S;
-  uint64_t* red_full = empty + S;   // [2]: groups 1..3 have written their sums
+  uint64_t* red_full = empty + S;   // [kRedBufs used]: groups 1.. have written their sums
   uint64_t* red_empty = red_full + 2;  // [2]: group 0 has read them
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -445,10 +449,10 @@ __global__ void __launch_bounds__(SkinnyLayout<MT8>::kThreads, 1) w4a16_skinny_k
     }
 
     if (flags & kStSegLast) {  // end of this item's segment of tile mt.y: add the groups' sums
-      const int rb = n_seg & 1;
-      const uint32_t par = (uint32_t)(n_seg >> 1) & 1u;
+      const int rb = n_seg % L::kRedBufs;
+      const uint32_t par = (uint32_t)(n_seg / L::kRedBufs) & 1u;
       if (grp > 0) {
-        if (n_seg >= 2 && !mbar_wait(&red_empty[rb], par ^ 1u, p.err)) return;
+        if (n_seg >= L::kRedBufs && !mbar_wait(&red_empty[rb], par ^ 1u, p.err)) return;
         float4* slot = reinterpret_cast<float4*>(
             smem + L::kRedOff + ((rb * (kSkGroups - 1) + grp - 1) * kSkConsumerWarps + q) * L::kRedSlot);
 #pragma unroll
