@@ -398,28 +398,30 @@ __global__ void __launch_bounds__(kAccThreads, kStatBlocksPerSm) accept_stats_ke
   }
 }
 
-// One block per batch row: merge each statistics row's chunks (one warp per
-// row), evaluate alpha_i = min(1, P_i(d_i) / Q_i(d_i)) for every draft, find
-// the first rejection r and record r with the normalisers of row r.
-__global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
-    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
-    const float* __restrict__ u, int n, int V, int ch, const RowStat* __restrict__ stats, int prestat, int chs,
-    Decision* __restrict__ dec, unsigned* err) {
-  grid_launch_dependents();
-  grid_dependency_wait();
+// Decision of batch row b by one 512-thread block (kDecThreads): merge each
+// statistics row's chunks (one warp per row, 15 merging warps; the last warp
+// fetches the drafts' own logits meanwhile), evaluate alpha_i = min(1,
+// P_i(d_i) / Q_i(d_i)) for every draft, find the first rejection r and return
+// r with the normalisers of row r (the same value in every thread).
+struct DecideShared {
+  float sM[kMaxStatRows];
+  DF sZ[kMaxStatRows];
+  float sLp[kMaxNodes], sLq[kMaxNodes];  // P_i / Q_i logits at d_i (n <= 1024)
+  int first_reject;
+};
+
+__device__ Decision decide_batch_row(const float* __restrict__ p, const float* __restrict__ q,
+                                     const int32_t* __restrict__ d, const float* __restrict__ u, int n, int V, int ch,
+                                     const RowStat* __restrict__ stats, int prestat, int chs, int B, int b,
+                                     DecideShared& ds, unsigned* err) {
   constexpr int kMergeWarps = kDecThreads / 32 - 1;
-  const int b = blockIdx.x;
   const int per = 2 * n + 1;
   // row statistics: all 2n + 1 rows from the statistics pass (ch items a
   // row), or (prestat) the draft rows (ch items a row) followed, after all
   // batch rows' draft rows, by the target rows merged from the caller's
   // slices (chs items a row)
   const RowStat* st = prestat ? stats + (int64_t)b * n * ch : stats + (int64_t)b * per * ch;
-  const RowStat* st_p = stats + (int64_t)gridDim.x * n * ch + (int64_t)b * (n + 1) * chs;
-  __shared__ float sM[kMaxStatRows];
-  __shared__ DF sZ[kMaxStatRows];
-  __shared__ float sLp[kMaxNodes], sLq[kMaxNodes];  // P_i / Q_i logits at d_i (n <= 1024)
-  __shared__ int first_reject;
+  const RowStat* st_p = stats + (int64_t)B * n * ch + (int64_t)b * (n + 1) * chs;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kMergeWarps) {
     // the drafts' own logits, fetched while the other warps merge
@@ -433,8 +435,8 @@ __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
         lp = p[((int64_t)b * (n + 1) + i) * V + di];
         lq = q[((int64_t)b * n + i) * V + di];
       }
-      sLp[i] = lp;
-      sLq[i] = lq;
+      ds.sLp[i] = lp;
+      ds.sLq[i] = lq;
     }
   } else {
     for (int row = warp; row < per; row += kMergeWarps) {
@@ -447,43 +449,54 @@ __global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
       else
         warp_merge_row(st + (int64_t)(row - n - 1) * ch, ch, M, Z);
       if (lane == 0) {
-        sM[row] = M;
-        sZ[row] = Z;
+        ds.sM[row] = M;
+        ds.sZ[row] = Z;
       }
     }
   }
-  if (threadIdx.x == 0) first_reject = n;
+  if (threadIdx.x == 0) ds.first_reject = n;
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += kDecThreads) {
     bool reject;
-    if (sLp[i] == -FLT_MAX) {
+    if (ds.sLp[i] == -FLT_MAX) {
       reject = true;
     } else {
       // alpha = min(1, P / Q) = min(1, (e_p * Z_q) / (e_q * Z_p)), fp32 (a few ulp)
-      const float ep = exp_of_diff(sLp[i], sM[i]);
-      const float eq = exp_of_diff(sLq[i], sM[n + 1 + i]);
-      const float num = __fmul_rn(ep, df_val(sZ[n + 1 + i])), den = __fmul_rn(eq, df_val(sZ[i]));
+      const float ep = exp_of_diff(ds.sLp[i], ds.sM[i]);
+      const float eq = exp_of_diff(ds.sLq[i], ds.sM[n + 1 + i]);
+      const float num = __fmul_rn(ep, df_val(ds.sZ[n + 1 + i])), den = __fmul_rn(eq, df_val(ds.sZ[i]));
       const float alpha = den > 0.0f ? fminf(1.0f, __fdiv_rn(num, den)) : 1.0f;
       reject = !(u[(int64_t)b * (n + 1) + i] < alpha);
     }
-    if (reject) atomicMin(&first_reject, i);
+    if (reject) atomicMin(&ds.first_reject, i);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    Decision D;
-    D.r = first_reject;
-    D.pad[0] = D.pad[1] = D.pad[2] = 0;
-    D.mp = sM[D.r];
-    D.izp = __frcp_rn(df_val(sZ[D.r]));
-    if (D.r < n) {
-      D.mq = sM[n + 1 + D.r];
-      D.izq = __frcp_rn(df_val(sZ[n + 1 + D.r]));
-    } else {
-      D.mq = 0.0f;
-      D.izq = 0.0f;
-    }
-    dec[b] = D;
+  Decision D;
+  D.r = ds.first_reject;
+  D.pad[0] = D.pad[1] = D.pad[2] = 0;
+  D.mp = ds.sM[D.r];
+  D.izp = __frcp_rn(df_val(ds.sZ[D.r]));
+  if (D.r < n) {
+    D.mq = ds.sM[n + 1 + D.r];
+    D.izq = __frcp_rn(df_val(ds.sZ[n + 1 + D.r]));
+  } else {
+    D.mq = 0.0f;
+    D.izq = 0.0f;
   }
+  return D;
+}
+
+// One block per batch row: the decision, for the residual pass.
+__global__ void __launch_bounds__(kDecThreads) accept_decide_kernel(
+    const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ d,
+    const float* __restrict__ u, int n, int V, int ch, const RowStat* __restrict__ stats, int prestat, int chs,
+    Decision* __restrict__ dec, unsigned* err) {
+  grid_launch_dependents();
+  grid_dependency_wait();
+  __shared__ DecideShared ds;
+  const Decision D = decide_batch_row(p, q, d, u, n, V, ch, stats, prestat, chs, (int)gridDim.x, (int)blockIdx.x, ds,
+                                      err);
+  if (threadIdx.x == 0) dec[blockIdx.x] = D;
 }
 
 // --------------------------------------------- pass 2: residual and draw
@@ -953,6 +966,7 @@ __device__ void cluster_reduce2(cg::cluster_group& cluster, TreeShared& sh, int&
 // cluster once more before any CTA exits.
 __device__ int cluster_draw(cg::cluster_group& cluster, TreeShared& sh, int phase, int rank, int x0, int V,
                             const float (&rv)[kTreePT], float uval) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   DF mine{0.0f, 0.0f};
   int lastp = -1;
 #pragma unroll
@@ -961,7 +975,6 @@ __device__ int cluster_draw(cg::cluster_group& cluster, TreeShared& sh, int phas
     mine = df_add_f(mine, rv[k]);
   }
   // this thread's exclusive prefix within the CTA, then the CTAs before it
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   DF incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -981,12 +994,22 @@ __device__ int cluster_draw(cg::cluster_group& cluster, TreeShared& sh, int phas
     sh.last_pos = -1;
   }
   cluster.sync();
-  DF below{0.0f, 0.0f}, S{0.0f, 0.0f};
-  for (int r = 0; r < kTreeCtas; ++r) {
-    const DF o = cluster.map_shared_rank(&sh, r)->red[phase][0];
-    if (r < rank) below = df_add(below, o);
-    S = df_add(S, o);
+  if (threadIdx.x < 32) {  // lane r fetches rank r's total; the sums in rank order go to every thread
+    const DF o = lane < kTreeCtas ? cluster.map_shared_rank(&sh, lane)->red[phase][0] : DF{0.0f, 0.0f};
+    DF bl{0.0f, 0.0f}, tot{0.0f, 0.0f};
+#pragma unroll
+    for (int r = 0; r < kTreeCtas; ++r) {
+      const DF x = shfl_df(o, r);
+      if (r < rank) bl = df_add(bl, x);
+      tot = df_add(tot, x);
+    }
+    if (lane == 0) {
+      sh.total[0] = tot;
+      sh.total[1] = bl;
+    }
   }
+  __syncthreads();
+  const DF S = sh.total[0], below = sh.total[1];
   const DF tt = df_mul_f(S, uval);
   DF run = df_add(below, excl_thread);
   int hit = INT_MAX;
@@ -995,8 +1018,13 @@ __device__ int cluster_draw(cg::cluster_group& cluster, TreeShared& sh, int phas
     run = df_add_f(run, rv[k]);
     if (hit == INT_MAX && x0 + k < V && df_gt(run, tt)) hit = x0 + k;
   }
-  if (hit != INT_MAX) atomicMin(&sh.found, hit);
-  if (lastp >= 0) atomicMax(&sh.last_pos, lastp);
+  // one shared-memory atomic per warp (512 threads on one address serialise)
+  hit = __reduce_min_sync(0xffffffffu, hit);
+  lastp = __reduce_max_sync(0xffffffffu, lastp);
+  if (lane == 0) {
+    if (hit != INT_MAX) atomicMin(&sh.found, hit);
+    if (lastp >= 0) atomicMax(&sh.last_pos, lastp);
+  }
   cluster.sync();  // every CTA's candidates are in
   int best = 0;
   if (rank == 0 && threadIdx.x == 0) {
