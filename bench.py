@@ -70,9 +70,9 @@ L2_FLUSH_BYTES = 256 << 20
 # summarised in profiles/ (launches of the same kernel in one bench step,
 # averaged); None where the kernel changed after the capture.
 NCU_DRAM_BYTES_PER_LAUNCH: dict = {
-    "w4a16_skinny_kernel (M<16)": 110579040,
-    "w4a16_tc_kernel<64> (M>=16)": 112997696,
-    "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": 89321216,
+    "w4a16_skinny_kernel (M<16)": 110580608,
+    "w4a16_tc_kernel<64> (M>=16)": 113033408,
+    "accept_stats_kernel + accept_decide_kernel + accept_resid_kernel": None,
     "accept_argmax_kernel": 525484544,
 }
 
