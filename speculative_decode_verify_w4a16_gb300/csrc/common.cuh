@@ -184,6 +184,15 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
   return old;
 }
 
+// Device-scope acquire load: reading the value the last of a series of
+// atom.acq_rel adds wrote makes every adder's earlier writes visible to this
+// thread's later reads.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // --------------------------------------------------------- packed fp32 math
 // (d0, d1) = (a0 * b0 + d0, a1 * b1 + d1): two IEEE fp32 fused multiply-adds
 // (round to nearest each, the same results as two fmaf) in one instruction.

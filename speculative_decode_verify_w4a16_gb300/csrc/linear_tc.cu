@@ -275,8 +275,54 @@ __device__ __forceinline__ float4* tc_slot(const TcParams& p, int item, int seg,
 
 template <int NT, bool FUSED>
 __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint8_t* stage, int item, int seg,
-                                int64_t t, int q, int lane, const float (&acc)[NT]) {
+                                int64_t t, int q, int lane, float (&acc)[NT], bool ends_item) {
   const int epw = q;
+  constexpr int JB = NT / 4 < 8 ? NT / 4 : 8;  // float4 of a slot per pass (register budget)
+  {
+    // Fast path: every other contributor has already counted in, so this one
+    // is the last. It publishes nothing and adds the others' slots to its own
+    // sums in registers. The sum must still run in item order, c_f + c_f+1 +
+    // ...: with this contributor first or second that is the same as adding
+    // the others, in order, to its own sums (a single fp32 addition is
+    // commutative), which saves the slot stores, the releasing atomic and the
+    // reload of its own slot. Only a segment that ends its item inside the
+    // tile is tested (the item after it began the tile's rest at its start,
+    // so this contributor is almost always the last).
+    const int64_t ci = kTileCounterBase + t * kTcEpWarps + epw;
+    const int64_t t_begin = t * p.G;
+    const int cf = item_owner(p.sched, t_begin);
+    const int cl = item_owner(p.sched, t_begin + p.G - 1);
+    if (ends_item && item - cf <= 1 && in_bounds(p.err, ci, kMaxCounters)) {
+      int seen = 0;
+      if (lane == 0) seen = ld_acquire_gpu(&p.counters[ci]);
+      seen = __shfl_sync(0xffffffffu, seen, 0);
+      __syncwarp();
+      if (seen == cl - cf) {
+        const int seg_cf = item_begin(p.sched, cf) >= t_begin ? 0 : 1;
+        for (int cc = cf; cc <= cl; ++cc) {
+          if (cc == item) continue;
+          const float4* sl = tc_slot<NT>(p, cc, cc == cf ? seg_cf : 0, epw);
+          const bool ok = in_bounds(p.err, (sl - p.partials) + NT / 4 * 32 - 1, p.partial_cap);
+#pragma unroll
+          for (int j0 = 0; j0 < NT / 4; j0 += JB) {
+            float4 v[JB];
+#pragma unroll
+            for (int j = 0; j < JB; ++j) v[j] = ok ? __ldcg(&sl[(j0 + j) * 32 + lane]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < JB; ++j) {
+              acc[4 * (j0 + j)] += v[j].x;
+              acc[4 * (j0 + j) + 1] += v[j].y;
+              acc[4 * (j0 + j) + 2] += v[j].z;
+              acc[4 * (j0 + j) + 3] += v[j].w;
+            }
+          }
+        }
+        tc_store<NT, FUSED>(p, omap, stage, t, q, lane, acc);
+        if (lane == 0) p.counters[ci] = 0;
+        return;
+      }
+    }
+  }
   float4* slot = tc_slot<NT>(p, item, seg, epw);
   const bool slot_ok = in_bounds(p.err, (slot - p.partials) + NT / 4 * 32 - 1, p.partial_cap);
 #pragma unroll
@@ -302,7 +348,6 @@ __device__ void tc_finish_split(const TcParams& p, const CUtensorMap* omap, uint
 #pragma unroll
   for (int j = 0; j < NT; ++j) sum[j] = 0.0f;
   constexpr int RB = NT <= 16 ? 4 : (NT <= 32 ? 2 : 1);  // contributors loaded together
-  constexpr int JB = NT / 4 < 8 ? NT / 4 : 8;             // float4 of a slot per pass (register budget)
   for (int c0 = cf; c0 <= cl; c0 += RB) {
 #pragma unroll
     for (int j0 = 0; j0 < NT / 4; j0 += JB) {
@@ -661,7 +706,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w4a16_tc_kernel(const __grid_co
           tc_store<NT, FUSED>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, ml.y, q, lane, acc);
         else
           tc_finish_split<NT, FUSED>(p, &omap, smem + L::kOutOff + q * L::kOutSlice, item, ml.y == item_t0 ? 0 : 1,
-                                     ml.y, q, lane, acc);
+                                     ml.y, q, lane, acc, ml.z != p.G - 1);
 #pragma unroll
         for (int c = 0; c < NT; ++c) acc[c] = 0.0f;
         seg_g0 = 0;
