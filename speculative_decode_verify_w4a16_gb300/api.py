@@ -26,6 +26,9 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on, and keeps its state for, the current device
+        raise ValueError(f"{name} is on {t.device}, the current device is cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():

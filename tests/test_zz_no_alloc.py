@@ -44,12 +44,22 @@ def test_noalloc_matches_workspace_linear_twice(L, M, N, K):
                           ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(stream)) == 0
     ref = bf16_bits(ref_out)
     outs = []
-    for _ in range(2):
+    for i in range(2):
         out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev())
+        torch.cuda.synchronize()
+        free0, _ = torch.cuda.mem_get_info()
+        alloc0 = torch.cuda.memory_allocated()
         assert L.w4a16_linear_noalloc(ctypes.c_void_p(x.data_ptr()), M, K, ctypes.c_void_p(w.qweight.data_ptr()),
                                       ctypes.c_void_p(w.scales.data_ptr()), N, ctypes.c_void_p(out.data_ptr()),
                                       ctypes.c_void_p(stream)) == 0
         torch.cuda.synchronize()
+        free1, _ = torch.cuda.mem_get_info()
+        # the call allocates nothing: no tensor, and (after the first call,
+        # which may load the library's kernels) no device memory, whose
+        # allocations come in pages of 2 MB or more
+        assert torch.cuda.memory_allocated() == alloc0
+        if i > 0:
+            assert free0 - free1 < (2 << 20), (free0, free1)
         outs.append(bf16_bits(out))
     assert L.w4a16_check_device_status(ctypes.c_void_p(stream)) == 0
     for o in outs:
