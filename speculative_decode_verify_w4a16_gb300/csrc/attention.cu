@@ -76,6 +76,11 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// two fp32 values rounded to a bf16 pair (low half = first)
+__device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 // two fp32 values rounded to a bf16 pair (low half = first), and the rounded values back
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, float& rhi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -326,6 +331,419 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
   }
 }
 
+// ------------------------------------------------ tcgen05 tree attention
+// For KV heads with at least 128 query rows (n * G >= 128): one CTA per
+// (block of 128 query rows, key split, KV head, batch row), 8 warps:
+//   warp 0     2-D TMA of the 64-key blocks of K and V into a 3-stage ring
+//   warp 1     the MMAs (whole warp runs the loop, the elect.sync lane
+//              issues): S = Q K^T (M = 128 query rows, N = 64 keys, K = 128,
+//              A and B from shared memory) into one of two TMEM buffers, and
+//              O += P V (M = 128, N = 128 head columns, K = 64 keys, P from
+//              TMEM, V^T from shared memory) into the TMEM accumulator
+//   warps 2-3  transpose each V block into V^T (head column rows of 64 keys,
+//              128-byte swizzle: the K-major B operand of P V)
+//   warps 4-11 two warps per TMEM lane quadrant (warp % 4), one query row per
+//              thread, the first warp of a pair taking keys 0-31 of every
+//              block and head columns 0-63, the second the rest: the row's
+//              scores from TMEM, the mask (committed prefix: every key; tree
+//              keys: the node's ancestors and itself), the block maximum
+//              (the pair's halves met in shared memory), the online softmax
+//              in the log2 domain and P (rounded to bf16, the row sum taken
+//              over the rounded values) back into TMEM; at the end the
+//              normalised row (or a split's unnormalised partial)
+// The running maximum is raised only when a block's maximum exceeds it by
+// more than 8 (a factor 256: P stays well inside bf16 and fp32), so the
+// accumulator in TMEM is rescaled rarely; the result O / l does not depend on
+// which maximum the weights were taken against.
+constexpr int kTaRows = 128;
+constexpr int kTaStages = 3;
+constexpr int kTaThreads = 384;
+constexpr float kTaLazy = 8.0f;  // log2 of the largest weight before the maximum is raised
+
+struct TaLayout {
+  static constexpr int kQHalf = kTaRows * 128;        // 128 rows x 64 head columns (bf16)
+  static constexpr int kKHalf = kAttKeys * 128;       // 64 keys x 64 head columns
+  static constexpr int kVT = kAttD * 128;             // 128 head columns x 64 keys
+  static constexpr int kStage = 4 * kKHalf + kVT;     // K halves, V halves, V^T
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = 2 * kQHalf;
+  static constexpr int kAncOff = kStageOff + kTaStages * kStage;
+  static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;
+  // kv_full[S], kv_free[S], vt_full[S], s_full[2], s_free[2], p_full[2], pv_done[2], q_ready, mma_fin,
+  // the softmax pairs' exchanges: max[4 quadrants][2 blocks], sum[4 quadrants]
+  static constexpr int kNumBars = 3 * kTaStages + 10 + 12;
+  // the softmax pairs' block maxima [2 blocks][2 halves][128 rows] and row sums [2 halves][128 rows]
+  static constexpr int kXOff = kBarOff + kNumBars * 8 + 16;
+  static constexpr int kTotal = kXOff + (4 * kTaRows + 2 * kTaRows) * 4 + 1024;  // + alignment
+  static_assert(kStage % 1024 == 0 && kQHalf % 1024 == 0 && kKHalf % 1024 == 0, "swizzle atoms");
+};
+constexpr uint32_t kTaSCol = 0;     // S buffers: columns 0 and 64
+constexpr uint32_t kTaPCol = 128;   // P buffers (bf16 pairs): columns 128 and 160
+constexpr uint32_t kTaOCol = 256;   // O accumulator: columns 256 .. 383
+
+// lane 0 waits (bounded), every lane gets the outcome. The hand-offs of
+// this kernel are short and on its critical path, so the first tests do not
+// ask the hardware to suspend the thread (a suspended waiter wakes up late:
+// 382 -> 287 us for 16 sequences x 64-node trees, measured).
+__device__ __forceinline__ bool ta_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    int k = 0;
+    while (k < 64 && !mbar_try_wait(bar, parity)) ++k;
+    if (k == 64) ok = mbar_wait(bar, parity, err) ? 1 : 0;
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+__global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                                          const __grid_constant__ CUtensorMap vmap,
+                                                                          const AttnParams p) {
+  using L = TaLayout;
+  constexpr int S = kTaStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L::kAncOff);
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* kv_free = kv_full + S;   // the block's P V is complete: K, V and V^T of the stage are free
+  uint64_t* vt_full = kv_free + S;
+  uint64_t* s_full = vt_full + S;    // [2]
+  uint64_t* s_free = s_full + 2;     // [2]
+  uint64_t* p_full = s_free + 2;     // [2]
+  uint64_t* pv_done = p_full + 2;    // [2]
+  uint64_t* q_ready = pv_done + 2;
+  uint64_t* mma_fin = q_ready + 1;
+  uint64_t* pair_max = mma_fin + 1;  // [4][2]: both warps of a quadrant have written a block's maxima
+  uint64_t* pair_sum = pair_max + 8; // [4]: and their row sums
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(pair_sum + 4);
+  __shared__ int s_len;
+
+  const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  grid_launch_dependents();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_free[s], 1);
+      mbar_init(&vt_full[s], 2);  // the two transposing warps
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&s_full[j], 1);
+      mbar_init(&s_free[j], 8);  // the eight softmax warps
+      mbar_init(&p_full[j], 8);
+      mbar_init(&pv_done[j], 1);
+    }
+    mbar_init(q_ready, 8);
+    mbar_init(mma_fin, 1);
+    for (int k = 0; k < 12; ++k) mbar_init(&pair_max[k], 2);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_s, 512);
+    tmem_relinquish();
+  }
+  grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
+  if (threadIdx.x == 0) {
+    int len = p.lens[b];
+    const int hi = min(p.max_len, p.Lcap - p.n);
+    if (len < 0 || len > hi) {
+      report_error(p.err, kErrInput);
+      len = len < 0 ? 0 : hi;
+    }
+    s_len = len;
+    bool bad = false;
+    for (int j = 0; j < p.n; ++j) {  // ancestor-or-self mask of every node (node j is bit j)
+      int par = p.parents ? p.parents[(int64_t)b * p.n + j] : j - 1;
+      if (j == 0 ? par != -1 : (par < 0 || par >= j)) {
+        bad = true;
+        par = -1;
+      }
+      anc[j] = (par >= 0 ? anc[par] : 0ull) | (1ull << j);
+    }
+    if (bad) report_error(p.err, kErrInput);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_s;
+  const int len = s_len;
+  const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
+  const int blk0 = split * p.blocks_per_split;
+  const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
+  const int64_t kv_row0 = ((int64_t)b * p.Hkv + kvh) * p.Lcap;
+  int mma_issued = 0;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int i = 0;
+      for (; i < nb; ++i) {
+        const int s = i % S;
+        if (i >= S && !mbar_wait(&kv_free[s], (uint32_t)(i / S - 1) & 1u, p.err)) break;
+        uint8_t* st = smem + L::kStageOff + s * L::kStage;
+        const int32_t y = (int32_t)(kv_row0 + (int64_t)(blk0 + i) * kAttKeys);
+        mbar_arrive_expect_tx(&kv_full[s], (uint32_t)(4 * L::kKHalf));
+        tma_load_2d(st, &kmap, 0, y, &kv_full[s]);
+        tma_load_2d(st + L::kKHalf, &kmap, 64, y, &kv_full[s]);
+        tma_load_2d(st + 2 * L::kKHalf, &vmap, 0, y, &kv_full[s]);
+        tma_load_2d(st + 3 * L::kKHalf, &vmap, 64, y, &kv_full[s]);
+      }
+      if (i < nb)  // a wait ran out: let the copies in flight land before the CTA exits
+        for (int k = i > S ? i - S : 0; k < i; ++k) mbar_wait(&kv_full[k % S], (uint32_t)(k / S) & 1u, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA
+    const uint32_t idesc_s = umma_idesc_bf16((uint32_t)kAttKeys), idesc_o = umma_idesc_bf16((uint32_t)kAttD);
+    bool ok = ta_wait(q_ready, 0u, p.err);
+    tc_fence_after();
+    const uint32_t q0 = smem_u32(smem + L::kQOff);
+    // S(i) = Q K(i)^T into S buffer i % 2
+    auto issue_s = [&](int i) {
+      const int s = i % S, sb = i & 1;
+      if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
+      if (i >= 2 && !ta_wait(&s_free[sb], (uint32_t)(i / 2 - 1) & 1u, p.err)) return false;
+      tc_fence_after();
+      const uint32_t k0 = smem_u32(smem + L::kStageOff + s * L::kStage);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t off = (uint32_t)((kk >> 2) * L::kQHalf + 32 * (kk & 3));
+        const uint32_t koff = (uint32_t)((kk >> 2) * L::kKHalf + 32 * (kk & 3));
+        umma_bf16_ss_warp(tmem + kTaSCol + 64u * (uint32_t)sb, umma_desc_sw128_kmajor(q0 + off),
+                          umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_warp(&s_full[sb]);
+      mma_issued = 1;
+      return true;
+    };
+    if (ok && nb > 0) ok = issue_s(0);
+    for (int i = 0; ok && i < nb; ++i) {
+      if (i + 1 < nb && !issue_s(i + 1)) break;
+      const int s = i % S, pb = i & 1;
+      if (!ta_wait(&p_full[pb], (uint32_t)(i / 2) & 1u, p.err)) break;
+      if (!ta_wait(&vt_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
+      tc_fence_after();
+      const uint32_t vt = smem_u32(smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16_ts_warp(tmem + kTaOCol, tmem + kTaPCol + 32u * (uint32_t)pb + 8u * (uint32_t)kk,
+                          umma_desc_sw128_kmajor(vt + 32u * (uint32_t)kk), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(&pv_done[pb]);
+      umma_commit_warp(&kv_free[s]);
+    }
+    if (mma_issued) umma_commit_warp(mma_fin);  // tracks all of this warp's MMAs
+  } else if (warp < 4) {
+    // ---------------------------------------------------- V transpose
+    // V^T row d, 16-byte chunk c (keys 8c .. 8c + 7) at chunk c ^ (d % 8);
+    // thread t builds rows t and t + 64, every chunk
+    const int t = threadIdx.x - 64;
+    for (int i = 0; i < nb; ++i) {
+      const int s = i % S;
+      if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
+      const uint8_t* vs = smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf;
+      uint8_t* vt = smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int d = t + 64 * h;  // head column = V half h, column t
+        const uint8_t* vcol = vs + h * L::kKHalf + (t & 7) * 2;
+        const int ch = t >> 3;     // the column's 16-byte chunk in a V row
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k0 = 8 * c + 2 * e;
+            const uint16_t lo = *reinterpret_cast<const uint16_t*>(vcol + k0 * 128 + ((ch ^ (k0 & 7)) << 4));
+            const uint16_t hi = *reinterpret_cast<const uint16_t*>(vcol + (k0 + 1) * 128 + ((ch ^ ((k0 + 1) & 7)) << 4));
+            w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          *reinterpret_cast<uint4*>(vt + d * 128 + ((c ^ (d & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();  // generic writes, read by the MMAs
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&vt_full[s]);
+    }
+  } else {
+    // --------------------------------------------------------- softmax
+    const int qd = warp & 3;              // TMEM lane quadrant
+    const int half = (warp - 4) >> 2;     // keys 32 half .. + 31 of a block, head columns 64 half .. + 63
+    const int rl = qd * 32 + lane;
+    const int R = rb * kTaRows + rl;
+    const bool valid = R < p.rows;
+    const int j = valid ? R / p.G : 0, g = R - j * p.G;
+    float* xm = reinterpret_cast<float*>(smem + L::kXOff);  // [2 blocks][2 halves][128]
+    float* xl = xm + 4 * kTaRows;                            // [2 halves][128]
+    // the quadrant's two warps meet on mbarriers (bounded waits), not on a
+    // named barrier, so that a wait that runs out in one of them cannot hold
+    // the other forever
+    // this row's half of Q, 128-byte swizzle, K-major (head columns 64 half ..)
+    {
+      const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
+      const bool qok = valid && in_bounds(p.err, qi + kAttD - 1, (int64_t)p.B * p.n * p.H * kAttD);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v =
+            qok ? *reinterpret_cast<const uint4*>(p.q + qi + 64 * half + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + L::kQOff + half * L::kQHalf + rl * 128 + ((c ^ (rl & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    }
+    const uint64_t an = valid ? anc[j] : 0ull;
+    const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
+    float m_used = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int i = 0; i < nb; ++i) {
+      const int sb = i & 1;
+      if (!ta_wait(&s_full[sb], (uint32_t)(i / 2) & 1u, p.err)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[32];
+      tmem_ld_32x32b_x32(trow + kTaSCol + 64u * (uint32_t)sb + 32u * (uint32_t)half, sv);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      // mask and scale (log2 domain); the block's maximum over both halves.
+      // A block of the committed prefix alone needs no mask.
+      const int key0 = (blk0 + i) * kAttKeys + 32 * half;
+      float mx = -INFINITY;
+      if (key0 + 32 <= len && valid) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float v = __uint_as_float(sv[c]) * p.scale_log2;
+          sv[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int pos = key0 + c, ti = pos - len;
+          const bool vis = valid && (pos < len || (ti < p.n && ((an >> ti) & 1ull)));
+          const float v = vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
+          sv[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
+      }
+      xm[(sb * 2 + half) * kTaRows + rl] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pair_max[qd * 2 + sb]);
+      if (!ta_wait(&pair_max[qd * 2 + sb], (uint32_t)(i / 2) & 1u, p.err)) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xm[(sb * 2 + (half ^ 1)) * kTaRows + rl]);
+      // raise the running maximum only by more than kTaLazy (both halves take
+      // the same decision); rescale l and this half's O columns then
+      float cf = 1.0f;
+      if (mx > m_used + kTaLazy) {
+        cf = m_used == -INFINITY ? 0.0f : ex2(m_used - mx);
+        m_used = mx;
+        l *= cf;
+      }
+      if (__any_sync(0xffffffffu, cf < 1.0f && i > 0)) {
+        // O holds the sums of blocks 0 .. i - 1: wait for the last of them
+        if (!ta_wait(&pv_done[(i - 1) & 1], (uint32_t)((i - 1) / 2) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * cf);
+          tmem_st_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+        }
+        tmem_wait_st();
+      }
+      // P = 2^(s - m), rounded to bf16; l over the rounded values
+      const float u = m_used == -INFINITY ? 0.0f : m_used;
+      uint32_t pr[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float r0, r1;
+        pr[c] = pack_bf16(ex2(__uint_as_float(sv[2 * c]) - u), ex2(__uint_as_float(sv[2 * c + 1]) - u), r0, r1);
+        l += r0 + r1;
+      }
+      // the P buffer was read by block i - 2's P V
+      if (i >= 2 && !ta_wait(&pv_done[sb], (uint32_t)((i - 2) / 2) & 1u, p.err)) {
+        ok = false;
+        break;
+      }
+      tmem_st_32x32b_x16(trow + kTaPCol + 32u * (uint32_t)sb + 16u * (uint32_t)half, pr);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+    }
+    // the row sum over both halves
+    xl[half * kTaRows + rl] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pair_sum[qd]);
+    if (ok && !ta_wait(&pair_sum[qd], 0u, p.err)) ok = false;
+    const float lt = xl[rl] + xl[kTaRows + rl];
+    // ---- the row: O / l (one split) or the split's (m, l, O); a split
+    // without keys for this sequence leaves (m, l) = (-inf, 0)
+    const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
+    const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
+    if (ok && nb == 0 && valid && p.splits > 1 && half == 0 && in_bounds(p.err, base + R, rows_cap))
+      p.part_ml[base + R] = make_float2(-INFINITY, 0.0f);
+    if (ok && nb > 0 && ta_wait(&pv_done[(nb - 1) & 1], (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
+      tc_fence_after();
+      const float il = lt > 0.0f ? 1.0f / lt : 0.0f;
+      const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
+      const int64_t oi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
+      const bool st_ok = valid && (p.splits == 1 ? in_bounds(p.err, oi + kAttD - 1, out_cap)
+                                                 : in_bounds(p.err, base + R, rows_cap));
+#pragma unroll 1
+      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+        tmem_wait_ld();
+        if (!st_ok) continue;
+        if (p.splits == 1) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            w.x = pack_bf16_rn(__uint_as_float(ov[c]) * il, __uint_as_float(ov[c + 1]) * il);
+            w.y = pack_bf16_rn(__uint_as_float(ov[c + 2]) * il, __uint_as_float(ov[c + 3]) * il);
+            w.z = pack_bf16_rn(__uint_as_float(ov[c + 4]) * il, __uint_as_float(ov[c + 5]) * il);
+            w.w = pack_bf16_rn(__uint_as_float(ov[c + 6]) * il, __uint_as_float(ov[c + 7]) * il);
+            *reinterpret_cast<uint4*>(p.out + oi + c0 + c) = w;
+          }
+        } else {
+          float* dst = p.part_o + (base + R) * kAttD + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4)
+            *reinterpret_cast<float4*>(dst + c) = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
+                                                              __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
+        }
+      }
+      if (st_ok && p.splits > 1 && half == 0) p.part_ml[base + R] = make_float2(m_used, lt);
+    }
+  }
+
+  // ---------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1 && lane == 0 && mma_issued) mbar_wait(mma_fin, 0u, p.err);  // no MMA in flight when TMEM is freed
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // One warp per query row: merge the splits' (m, l, O) and store the
 // normalised row as bf16 (lane k: columns 4k .. 4k + 3).
 __global__ void __launch_bounds__(256) tree_attention_combine_kernel(const AttnParams p) {
@@ -457,12 +875,16 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   AttnPlan pl;
   const int G = H / Hkv;
   pl.rows = n * G;
-  pl.warps = attn_warps(pl.rows);
-  pl.row_blocks = (pl.rows + 16 * pl.warps - 1) / (16 * pl.warps);
-  pl.rows_pad = pl.row_blocks * 16 * pl.warps;
+  // a KV head with 128 query rows or more fills the tcgen05 kernel's M = 128
+  pl.tc = pl.rows >= kTaRows ? 1 : 0;
+  pl.warps = pl.tc ? 0 : attn_warps(pl.rows);
+  const int per_cta = pl.tc ? kTaRows : 16 * pl.warps;
+  pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
+  pl.rows_pad = pl.row_blocks * per_cta;
   const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
   const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
-  const int64_t target = (int64_t)2 * kAttCtasPerSm * (num_sms > 0 ? num_sms : 1);  // about two waves
+  const int per_sm = pl.tc ? 1 : kAttCtasPerSm;
+  const int64_t target = (int64_t)2 * per_sm * (num_sms > 0 ? num_sms : 1);  // about two waves
   int splits = (int)((target + base - 1) / base);
   if (splits < 1) splits = 1;
   if (splits > nbmax) splits = nbmax;
@@ -521,7 +943,11 @@ cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   const dim3 grid((unsigned)(pl.row_blocks * pl.splits), (unsigned)Hkv, (unsigned)B);
   cudaError_t e;
-  switch (pl.warps) {
+  if (pl.tc) {
+    e = cudaFuncSetAttribute(tree_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TaLayout::kTotal);
+    if (e == cudaSuccess)
+      e = launch_pdl(tree_attention_tc_kernel, grid, dim3(kTaThreads), (size_t)TaLayout::kTotal, stream, km, vm, p);
+  } else switch (pl.warps) {
     case 1: e = launch_attn_t<1>(km, vm, p, grid, stream); break;
     case 2: e = launch_attn_t<2>(km, vm, p, grid, stream); break;
     case 4: e = launch_attn_t<4>(km, vm, p, grid, stream); break;
