@@ -64,6 +64,13 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+// four 8x8 bf16 tiles stored transposed: lanes 8m .. 8m + 7 give the row
+// addresses of tile m, register m holds tile m in the ldmatrix fragment layout
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
 __device__ __forceinline__ void attn_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                "{%0, %1, %2, %3};"
@@ -518,9 +525,11 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       mma_issued = 1;
       return true;
     };
+    // S runs two blocks ahead of P V (its two buffers): S(i + 2) goes out
+    // right after P V(i), while the softmax works on block i + 1
     if (ok && nb > 0) ok = issue_s(0);
+    if (ok && nb > 1) ok = issue_s(1);
     for (int i = 0; ok && i < nb; ++i) {
-      if (i + 1 < nb && !issue_s(i + 1)) break;
       const int s = i % S, pb = i & 1;
       if (!ta_wait(&p_full[pb], (uint32_t)(i / 2) & 1u, p.err)) break;
       if (!ta_wait(&vt_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
@@ -532,35 +541,31 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
                           umma_desc_sw128_kmajor(vt + 32u * (uint32_t)kk), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(&pv_done[pb]);
       umma_commit_warp(&kv_free[s]);
+      if (i + 2 < nb && !issue_s(i + 2)) break;
     }
     if (mma_issued) umma_commit_warp(mma_fin);  // tracks all of this warp's MMAs
   } else if (warp < 4) {
     // ---------------------------------------------------- V transpose
-    // V^T row d, 16-byte chunk c (keys 8c .. 8c + 7) at chunk c ^ (d % 8);
-    // thread t builds rows t and t + 64, every chunk
-    const int t = threadIdx.x - 64;
+    // V^T row d, 16-byte chunk c (keys 8c .. 8c + 7) at chunk c ^ (d % 8).
+    // 8x8 tiles: ldmatrix reads four tiles of V (keys 8kt .., head columns
+    // 8dt ..), stmatrix.trans writes them as rows of V^T; the two warps take
+    // 16 groups of four tiles each (kt = 4 kq .. 4 kq + 3, one dt)
+    const int tw = warp - 2;
     for (int i = 0; i < nb; ++i) {
       const int s = i % S;
       if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
-      const uint8_t* vs = smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf;
-      uint8_t* vt = smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int d = t + 64 * h;  // head column = V half h, column t
-        const uint8_t* vcol = vs + h * L::kKHalf + (t & 7) * 2;
-        const int ch = t >> 3;     // the column's 16-byte chunk in a V row
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k0 = 8 * c + 2 * e;
-            const uint16_t lo = *reinterpret_cast<const uint16_t*>(vcol + k0 * 128 + ((ch ^ (k0 & 7)) << 4));
-            const uint16_t hi = *reinterpret_cast<const uint16_t*>(vcol + (k0 + 1) * 128 + ((ch ^ ((k0 + 1) & 7)) << 4));
-            w[e] = (uint32_t)lo | ((uint32_t)hi << 16);
-          }
-          *reinterpret_cast<uint4*>(vt + d * 128 + ((c ^ (d & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+      const uint32_t vs = smem_u32(smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf);
+      const uint32_t vt = smem_u32(smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf);
+#pragma unroll 4
+      for (int gidx = tw; gidx < 32; gidx += 2) {
+        const int dt = gidx >> 1, kq = gidx & 1;  // head-column tile 0..15, key quarter 0..1
+        const int kt = 4 * kq + (lane >> 3);       // this lane's tile (key tile) in the group
+        const int r = lane & 7;
+        const int key = 8 * kt + r, hd = dt >> 3, ch = dt & 7;
+        uint32_t r0, r1, r2, r3;
+        ldsm_x4(vs + hd * L::kKHalf + key * 128 + ((ch ^ (key & 7)) << 4), r0, r1, r2, r3);
+        const int d = 8 * dt + r;
+        stsm_x4_trans(vt + d * 128 + ((kt ^ (d & 7)) << 4), r0, r1, r2, r3);
       }
       fence_proxy_async_smem();  // generic writes, read by the MMAs
       __syncwarp();
