@@ -64,13 +64,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint3
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// four 8x8 bf16 tiles stored transposed: lanes 8m .. 8m + 7 give the row
-// addresses of tile m, register m holds tile m in the ldmatrix fragment layout
-__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
-               "r"(r2), "r"(r3)
-               : "memory");
-}
 __device__ __forceinline__ void attn_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
                "{%0, %1, %2, %3};"
@@ -82,6 +75,32 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// two fp32 lanes in one 64-bit register (low half = first), for the paired
+// fp32 instructions of sm_100 and later
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// the largest of three fp32 values
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 // two fp32 values rounded to a bf16 pair (low half = first)
 __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
@@ -340,53 +359,59 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
 
 // ------------------------------------------------ tcgen05 tree attention
 // For KV heads with at least 128 query rows (n * G >= 128): one CTA per
-// (block of 128 query rows, key split, KV head, batch row), 8 warps:
-//   warp 0     2-D TMA of the 64-key blocks of K and V into a 3-stage ring
-//   warp 1     the MMAs (whole warp runs the loop, the elect.sync lane
-//              issues): S = Q K^T (M = 128 query rows, N = 64 keys, K = 128,
-//              A and B from shared memory) into one of two TMEM buffers, and
-//              O += P V (M = 128, N = 128 head columns, K = 64 keys, P from
-//              TMEM, V^T from shared memory) into the TMEM accumulator
-//   warps 2-3  transpose each V block into V^T (head column rows of 64 keys,
-//              128-byte swizzle: the K-major B operand of P V)
-//   warps 4-11 two warps per TMEM lane quadrant (warp % 4), one query row per
-//              thread, the first warp of a pair taking keys 0-31 of every
-//              block and head columns 0-63, the second the rest: the row's
-//              scores from TMEM, the mask (committed prefix: every key; tree
-//              keys: the node's ancestors and itself), the block maximum
-//              (the pair's halves met in shared memory), the online softmax
-//              in the log2 domain and P (rounded to bf16, the row sum taken
-//              over the rounded values) back into TMEM; at the end the
-//              normalised row (or a split's unnormalised partial)
+// (block of 256 query rows, key split, KV head, batch row), two tiles of 128
+// rows that share every key block, 12 warps:
+//   warp 0        2-D TMA of the 64-key blocks of K and V into a 4-stage ring
+//   warps 1, 2    the MMAs of tile 0 and tile 1 (whole warp in the loop, the
+//                 elect.sync lane issuing): S = Q K^T (M = 128 query rows,
+//                 N = 64 keys, K = 128; A and B from shared memory) into the
+//                 tile's TMEM score buffer, and O += P V (M = 128, N = 128
+//                 head columns, K = 64 keys; P from TMEM, V from shared
+//                 memory as it was loaded: key rows of head columns, the
+//                 MN-major B operand) into the tile's TMEM accumulator. Each
+//                 tile has two TMEM score buffers: S for block i + 2 goes out
+//                 once the P V of block i, whose P sits in the same buffer,
+//                 is complete, so the scores of the next block are ready
+//                 when the softmax reaches it; the two tiles' MMAs
+//                 interleave on the tensor pipe.
+//   warp 3        idle
+//   warps 4-11    one query row per thread, tile (warp - 4) / 4, TMEM lane
+//                 quadrant warp % 4: the row's scores from TMEM, the mask
+//                 (committed prefix: every key; tree keys: the node's
+//                 ancestors and itself; skipped on blocks of the prefix), the
+//                 online softmax in the log2 domain and P (rounded to bf16,
+//                 the row sum taken over the rounded values) back into TMEM,
+//                 over the first half of the scores just read;
+//                 at the end the normalised row (or a split's partial)
+// While one tile's softmax runs, the tensor pipe works on the other tile.
 // The running maximum is raised only when a block's maximum exceeds it by
 // more than 8 (a factor 256: P stays well inside bf16 and fp32), so the
 // accumulator in TMEM is rescaled rarely; the result O / l does not depend on
 // which maximum the weights were taken against.
-constexpr int kTaRows = 128;
-constexpr int kTaStages = 3;
+constexpr int kTaRows = 128;   // query rows per tile (UMMA M)
+constexpr int kTaTiles = 2;
+constexpr int kTaStages = 4;
 constexpr int kTaThreads = 384;
 constexpr float kTaLazy = 8.0f;  // log2 of the largest weight before the maximum is raised
 
 struct TaLayout {
   static constexpr int kQHalf = kTaRows * 128;        // 128 rows x 64 head columns (bf16)
   static constexpr int kKHalf = kAttKeys * 128;       // 64 keys x 64 head columns
-  static constexpr int kVT = kAttD * 128;             // 128 head columns x 64 keys
-  static constexpr int kStage = 4 * kKHalf + kVT;     // K halves, V halves, V^T
-  static constexpr int kQOff = 0;
-  static constexpr int kStageOff = 2 * kQHalf;
+  static constexpr int kStage = 4 * kKHalf;          // K halves, V halves
+  static constexpr int kQOff = 0;                     // tile t: two halves at 2 t kQHalf
+  static constexpr int kStageOff = kTaTiles * 2 * kQHalf;
   static constexpr int kAncOff = kStageOff + kTaStages * kStage;
   static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;
-  // kv_full[S], kv_free[S], vt_full[S], s_full[2], s_free[2], p_full[2], pv_done[2], q_ready, mma_fin,
-  // the softmax pairs' exchanges: max[4 quadrants][2 blocks], sum[4 quadrants]
-  static constexpr int kNumBars = 3 * kTaStages + 10 + 12;
-  // the softmax pairs' block maxima [2 blocks][2 halves][128 rows] and row sums [2 halves][128 rows]
-  static constexpr int kXOff = kBarOff + kNumBars * 8 + 16;
-  static constexpr int kTotal = kXOff + (4 * kTaRows + 2 * kTaRows) * 4 + 1024;  // + alignment
+  // kv_full[S], kv_free[S]; per tile s_full[2], p_full[2], pv_done[2], mma_fin; q_ready
+  static constexpr int kNumBars = 2 * kTaStages + kTaTiles * 7 + 1;
+  static constexpr int kTotal = kBarOff + kNumBars * 8 + 16 + 1024;  // + TMEM base, alignment
   static_assert(kStage % 1024 == 0 && kQHalf % 1024 == 0 && kKHalf % 1024 == 0, "swizzle atoms");
+  static_assert(kTotal <= 227 * 1024, "shared memory");
 };
-constexpr uint32_t kTaSCol = 0;     // S buffers: columns 0 and 64
-constexpr uint32_t kTaPCol = 128;   // P buffers (bf16 pairs): columns 128 and 160
-constexpr uint32_t kTaOCol = 256;   // O accumulator: columns 256 .. 383
+// TMEM columns of tile t: score buffer sb at 128 t + 64 sb .. + 63 (P of the
+// block, bf16 pairs, over its first 32 columns); O 256 + 128 t .. + 127
+__device__ __forceinline__ uint32_t ta_s_col(int t, int sb) { return 128u * (uint32_t)t + 64u * (uint32_t)sb; }
+__device__ __forceinline__ uint32_t ta_o_col(int t) { return 256u + 128u * (uint32_t)t; }
 
 // lane 0 waits (bounded), every lane gets the outcome. The hand-offs of
 // this kernel are short and on its critical path, so the first tests do not
@@ -404,6 +429,31 @@ __device__ __forceinline__ bool ta_wait(uint64_t* bar, uint32_t parity, unsigned
   return ok != 0;
 }
 
+// The same without ever suspending: lane 0 polls the phase (the time limit
+// read every 256 polls). For the MMA warps, whose waits last about a softmax
+// pass and whose wake-up is on the critical path.
+__device__ __forceinline__ bool ta_spin(uint64_t* bar, uint32_t parity, unsigned* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    unsigned long long t0 = 0;
+    for (unsigned k = 1; !mbar_test(bar, parity); ++k) {
+      if ((k & 255u) == 0) {
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kWaitLimitNs) {
+          report_error(err, kErrTimeout);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                                                           const __grid_constant__ CUtensorMap vmap,
                                                                           const AttnParams p) {
@@ -413,39 +463,37 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L::kAncOff);
   uint64_t* kv_full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* kv_free = kv_full + S;   // the block's P V is complete: K, V and V^T of the stage are free
-  uint64_t* vt_full = kv_free + S;
-  uint64_t* s_full = vt_full + S;    // [2]
-  uint64_t* s_free = s_full + 2;     // [2]
-  uint64_t* p_full = s_free + 2;     // [2]
-  uint64_t* pv_done = p_full + 2;    // [2]
-  uint64_t* q_ready = pv_done + 2;
-  uint64_t* mma_fin = q_ready + 1;
-  uint64_t* pair_max = mma_fin + 1;  // [4][2]: both warps of a quadrant have written a block's maxima
-  uint64_t* pair_sum = pair_max + 8; // [4]: and their row sums
-  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(pair_sum + 4);
-  __shared__ int s_len;
+  uint64_t* kv_free = kv_full + S;  // both tiles' P V of the block are complete: K and V are free
+  uint64_t* tb = kv_free + S;       // per tile: s_full[2], p_full[2], pv_done[2], mma_fin
+  auto s_full = [&](int t, int sb) { return tb + 7 * t + sb; };
+  auto p_full = [&](int t, int pb) { return tb + 7 * t + 2 + pb; };
+  auto pv_done = [&](int t, int pb) { return tb + 7 * t + 4 + pb; };
+  auto mma_fin = [&](int t) { return tb + 7 * t + 6; };
+  uint64_t* q_ready = tb + 7 * kTaTiles;
+  uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(q_ready + 1);
+  __shared__ int s_len, s_b;
 
   const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // tiles holding query rows (the last row block of a head may need one)
+  const int ntiles = min(kTaTiles, (p.rows - rb * kTaTiles * kTaRows + kTaRows - 1) / kTaRows);
 
   grid_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_free[s], 1);
-      mbar_init(&vt_full[s], 2);  // the two transposing warps
+      mbar_init(&kv_free[s], (uint32_t)ntiles);  // each tile's last P V commit
     }
-    for (int j = 0; j < 2; ++j) {
-      mbar_init(&s_full[j], 1);
-      mbar_init(&s_free[j], 8);  // the eight softmax warps
-      mbar_init(&p_full[j], 8);
-      mbar_init(&pv_done[j], 1);
+    for (int t = 0; t < kTaTiles; ++t) {
+      for (int pb = 0; pb < 2; ++pb) {
+        mbar_init(s_full(t, pb), 1);
+        mbar_init(p_full(t, pb), 4);  // the tile's four softmax warps
+        mbar_init(pv_done(t, pb), 1);
+      }
+      mbar_init(mma_fin(t), 1);
     }
-    mbar_init(q_ready, 8);
-    mbar_init(mma_fin, 1);
-    for (int k = 0; k < 12; ++k) mbar_init(&pair_max[k], 2);
+    mbar_init(q_ready, 4 * kTaTiles);
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -453,7 +501,28 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     tmem_relinquish();
   }
   grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
+  if (warp == 0) {
+    // longest sequences first: the z-th row of CTAs takes the sequence of
+    // rank z in decreasing length (ties by index), so that the shortest
+    // fill the tail of the launch (up to 64 sequences; above, in order)
+    int b = p.B <= 64 ? -1 : (int)blockIdx.z;
+    if (p.B <= 64) {
+      for (int c = lane; c < p.B; c += 32) {
+        const int lc = p.lens[c];
+        int rank = 0;
+        for (int c2 = 0; c2 < p.B; ++c2) {
+          const int l2 = p.lens[c2];
+          rank += (l2 > lc || (l2 == lc && c2 < c)) ? 1 : 0;
+        }
+        if (rank == (int)blockIdx.z) b = c;
+      }
+      b = __reduce_max_sync(0xffffffffu, b);
+      if (b < 0) b = (int)blockIdx.z;
+    }
+    if (lane == 0) s_b = b;
+  }
   if (threadIdx.x == 0) {
+    const int b = s_b;
     int len = p.lens[b];
     const int hi = min(p.max_len, p.Lcap - p.n);
     if (len < 0 || len > hi) {
@@ -476,7 +545,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
-  const int len = s_len;
+  const int len = s_len, b = s_b;
   const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
   const int blk0 = split * p.blocks_per_split;
   const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
@@ -501,98 +570,71 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       if (i < nb)  // a wait ran out: let the copies in flight land before the CTA exits
         for (int k = i > S ? i - S : 0; k < i; ++k) mbar_wait(&kv_full[k % S], (uint32_t)(k / S) & 1u, p.err);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------- MMA
-    const uint32_t idesc_s = umma_idesc_bf16((uint32_t)kAttKeys), idesc_o = umma_idesc_bf16((uint32_t)kAttD);
-    bool ok = ta_wait(q_ready, 0u, p.err);
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------ MMA, tile t
+    const int t = warp - 1;
+    const uint32_t idesc_s = umma_idesc_bf16((uint32_t)kAttKeys), idesc_o = umma_idesc_bf16_bmn((uint32_t)kAttD);
+    bool ok = ta_spin(q_ready, 0u, p.err);
     tc_fence_after();
-    const uint32_t q0 = smem_u32(smem + L::kQOff);
-    // S(i) = Q K(i)^T into S buffer i % 2
+    const uint32_t q0 = smem_u32(smem + L::kQOff + t * 2 * L::kQHalf);
+    // S(i) = Q K(i)^T into score buffer i % 2, once P V (i - 2) (its P in the
+    // same buffer) is complete
     auto issue_s = [&](int i) {
       const int s = i % S, sb = i & 1;
-      if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
-      if (i >= 2 && !ta_wait(&s_free[sb], (uint32_t)(i / 2 - 1) & 1u, p.err)) return false;
+      if (!ta_spin(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
+      if (i >= 2 && !ta_spin(pv_done(t, sb), (uint32_t)((i - 2) / 2) & 1u, p.err)) return false;
       tc_fence_after();
       const uint32_t k0 = smem_u32(smem + L::kStageOff + s * L::kStage);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (uint32_t)((kk >> 2) * L::kQHalf + 32 * (kk & 3));
         const uint32_t koff = (uint32_t)((kk >> 2) * L::kKHalf + 32 * (kk & 3));
-        umma_bf16_ss_warp(tmem + kTaSCol + 64u * (uint32_t)sb, umma_desc_sw128_kmajor(q0 + off),
-                          umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
+        umma_bf16_ss_warp(tmem + ta_s_col(t, sb), umma_desc_sw128_kmajor(q0 + off), umma_desc_sw128_kmajor(k0 + koff),
+                          idesc_s, kk > 0 ? 1u : 0u);
       }
-      umma_commit_warp(&s_full[sb]);
+      umma_commit_warp(s_full(t, sb));
       mma_issued = 1;
       return true;
     };
-    // S runs two blocks ahead of P V (its two buffers): S(i + 2) goes out
-    // right after P V(i), while the softmax works on block i + 1
+    if (t >= ntiles) ok = false;  // no rows in this tile
     if (ok && nb > 0) ok = issue_s(0);
     if (ok && nb > 1) ok = issue_s(1);
     for (int i = 0; ok && i < nb; ++i) {
       const int s = i % S, pb = i & 1;
-      if (!ta_wait(&p_full[pb], (uint32_t)(i / 2) & 1u, p.err)) break;
-      if (!ta_wait(&vt_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
+      if (!ta_spin(p_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) break;
       tc_fence_after();
-      const uint32_t vt = smem_u32(smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf);
+      // V half h: keys 0 .. 63 x head columns 64 h .. 64 h + 63, 128-byte rows;
+      // 16 keys (two 8-row atoms) per MMA, the second head-column half kKHalf on
+      const uint32_t v0 = smem_u32(smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_ts_warp(tmem + kTaOCol, tmem + kTaPCol + 32u * (uint32_t)pb + 8u * (uint32_t)kk,
-                          umma_desc_sw128_kmajor(vt + 32u * (uint32_t)kk), idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_warp(&pv_done[pb]);
+        umma_bf16_ts_warp(tmem + ta_o_col(t), tmem + ta_s_col(t, pb) + 8u * (uint32_t)kk,
+                          umma_desc_sw128_mnmajor(v0 + 2048u * (uint32_t)kk, (uint32_t)L::kKHalf, 1024u), idesc_o,
+                          (i > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_warp(pv_done(t, pb));
       umma_commit_warp(&kv_free[s]);
       if (i + 2 < nb && !issue_s(i + 2)) break;
     }
-    if (mma_issued) umma_commit_warp(mma_fin);  // tracks all of this warp's MMAs
-  } else if (warp < 4) {
-    // ---------------------------------------------------- V transpose
-    // V^T row d, 16-byte chunk c (keys 8c .. 8c + 7) at chunk c ^ (d % 8).
-    // 8x8 tiles: ldmatrix reads four tiles of V (keys 8kt .., head columns
-    // 8dt ..), stmatrix.trans writes them as rows of V^T; the two warps take
-    // 16 groups of four tiles each (kt = 4 kq .. 4 kq + 3, one dt)
-    const int tw = warp - 2;
-    for (int i = 0; i < nb; ++i) {
-      const int s = i % S;
-      if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) break;
-      const uint32_t vs = smem_u32(smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf);
-      const uint32_t vt = smem_u32(smem + L::kStageOff + s * L::kStage + 4 * L::kKHalf);
-#pragma unroll 4
-      for (int gidx = tw; gidx < 32; gidx += 2) {
-        const int dt = gidx >> 1, kq = gidx & 1;  // head-column tile 0..15, key quarter 0..1
-        const int kt = 4 * kq + (lane >> 3);       // this lane's tile (key tile) in the group
-        const int r = lane & 7;
-        const int key = 8 * kt + r, hd = dt >> 3, ch = dt & 7;
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4(vs + hd * L::kKHalf + key * 128 + ((ch ^ (key & 7)) << 4), r0, r1, r2, r3);
-        const int d = 8 * dt + r;
-        stsm_x4_trans(vt + d * 128 + ((kt ^ (d & 7)) << 4), r0, r1, r2, r3);
-      }
-      fence_proxy_async_smem();  // generic writes, read by the MMAs
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&vt_full[s]);
-    }
+    if (mma_issued) umma_commit_warp(mma_fin(t));  // tracks all of this warp's MMAs
+  } else if (warp == 3) {
+    // idle
   } else {
     // --------------------------------------------------------- softmax
-    const int qd = warp & 3;              // TMEM lane quadrant
-    const int half = (warp - 4) >> 2;     // keys 32 half .. + 31 of a block, head columns 64 half .. + 63
+    const int t = (warp - 4) >> 2;  // tile
+    const int qd = warp & 3;        // TMEM lane quadrant
     const int rl = qd * 32 + lane;
-    const int R = rb * kTaRows + rl;
+    const int R = rb * kTaTiles * kTaRows + t * kTaRows + rl;
     const bool valid = R < p.rows;
     const int j = valid ? R / p.G : 0, g = R - j * p.G;
-    float* xm = reinterpret_cast<float*>(smem + L::kXOff);  // [2 blocks][2 halves][128]
-    float* xl = xm + 4 * kTaRows;                            // [2 halves][128]
-    // the quadrant's two warps meet on mbarriers (bounded waits), not on a
-    // named barrier, so that a wait that runs out in one of them cannot hold
-    // the other forever
-    // this row's half of Q, 128-byte swizzle, K-major (head columns 64 half ..)
+    // this row of Q, 128-byte swizzle, K-major (two 64-column halves)
     {
       const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool qok = valid && in_bounds(p.err, qi + kAttD - 1, (int64_t)p.B * p.n * p.H * kAttD);
+      uint8_t* qt = smem + L::kQOff + t * 2 * L::kQHalf;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 v =
-            qok ? *reinterpret_cast<const uint4*>(p.q + qi + 64 * half + c * 8) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + L::kQOff + half * L::kQHalf + rl * 128 + ((c ^ (rl & 7)) << 4)) = v;
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = qok ? *reinterpret_cast<const uint4*>(p.q + qi + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::kQHalf + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = v;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -600,52 +642,43 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     }
     const uint64_t an = valid ? anc[j] : 0ull;
     const uint32_t trow = tmem + ((uint32_t)(32 * qd) << 16);
+    const int nbt = t < ntiles ? nb : 0;
     float m_used = -INFINITY, l = 0.0f;
     bool ok = true;
-    for (int i = 0; i < nb; ++i) {
-      const int sb = i & 1;
-      if (!ta_wait(&s_full[sb], (uint32_t)(i / 2) & 1u, p.err)) {
+    for (int i = 0; i < nbt; ++i) {
+      const int pb = i & 1;
+      if (!ta_wait(s_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld_32x32b_x32(trow + kTaSCol + 64u * (uint32_t)sb + 32u * (uint32_t)half, sv);
+      uint32_t sv[2][32];
+      tmem_ld_32x32b_x32(trow + ta_s_col(t, pb), sv[0]);
+      tmem_ld_32x32b_x32(trow + ta_s_col(t, pb) + 32u, sv[1]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      // mask and scale (log2 domain); the block's maximum over both halves.
-      // A block of the committed prefix alone needs no mask.
-      const int key0 = (blk0 + i) * kAttKeys + 32 * half;
-      float mx = -INFINITY;
-      if (key0 + 32 <= len && valid) {
+      // the mask (keys the row does not see: -inf), then the block's maximum
+      // on the raw scores (the positive scale commutes with it), in the log2
+      // domain. A block of the committed prefix alone needs no mask (every
+      // key is seen by every row).
+      const int key0 = (blk0 + i) * kAttKeys;
+      if (!(key0 + kAttKeys <= len && valid)) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float v = __uint_as_float(sv[c]) * p.scale_log2;
-          sv[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      } else {
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int pos = key0 + c, ti = pos - len;
-          const bool vis = valid && (pos < len || (ti < p.n && ((an >> ti) & 1ull)));
-          const float v = vis ? __uint_as_float(sv[c]) * p.scale_log2 : -INFINITY;
-          sv[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
+          for (int c = 0; c < 32; ++c) {
+            const int pos = key0 + 32 * h + c, ti = pos - len;
+            const bool vis = valid && (pos < len || (ti < p.n && ((an >> ti) & 1ull)));
+            if (!vis) sv[h][c] = __float_as_uint(-INFINITY);
+          }
       }
-      xm[(sb * 2 + half) * kTaRows + rl] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pair_max[qd * 2 + sb]);
-      if (!ta_wait(&pair_max[qd * 2 + sb], (uint32_t)(i / 2) & 1u, p.err)) {
-        ok = false;
-        break;
-      }
-      mx = fmaxf(mx, xm[(sb * 2 + (half ^ 1)) * kTaRows + rl]);
-      // raise the running maximum only by more than kTaLazy (both halves take
-      // the same decision); rescale l and this half's O columns then
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          m4[c & 3] = max3f(m4[c & 3], __uint_as_float(sv[h][2 * c]), __uint_as_float(sv[h][2 * c + 1]));
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
+      // raise the running maximum only by more than kTaLazy; rescale l and O then
       float cf = 1.0f;
       if (mx > m_used + kTaLazy) {
         cf = m_used == -INFINITY ? 0.0f : ex2(m_used - mx);
@@ -654,65 +687,71 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       }
       if (__any_sync(0xffffffffu, cf < 1.0f && i > 0)) {
         // O holds the sums of blocks 0 .. i - 1: wait for the last of them
-        if (!ta_wait(&pv_done[(i - 1) & 1], (uint32_t)((i - 1) / 2) & 1u, p.err)) {
+        if (!ta_wait(pv_done(t, (i - 1) & 1), (uint32_t)((i - 1) / 2) & 1u, p.err)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+        for (int c0 = 0; c0 < kAttD; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+          tmem_ld_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * cf);
-          tmem_st_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+          tmem_st_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
         }
         tmem_wait_st();
       }
-      // P = 2^(s - m), rounded to bf16; l over the rounded values
+      // P = 2^(s scale - m), rounded to bf16; l over the rounded values. The
+      // exponents' arguments and the sums go two lanes per instruction.
       const float u = m_used == -INFINITY ? 0.0f : m_used;
-      uint32_t pr[16];
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nu2 = f2_pack(-u, -u);
+      uint64_t la = f2_pack(0.0f, 0.0f), lb = la;
+      uint32_t pr[32];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float r0, r1;
-        pr[c] = pack_bf16(ex2(__uint_as_float(sv[2 * c]) - u), ex2(__uint_as_float(sv[2 * c + 1]) - u), r0, r1);
-        l += r0 + r1;
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[h][2 * c]), __uint_as_float(sv[h][2 * c + 1])), sc2, nu2), x0, x1);
+          const uint32_t w = pack_bf16_rn(ex2(x0), ex2(x1));
+          pr[16 * h + c] = w;
+          const uint64_t r2 = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+          if (c & 1)
+            lb = f2_add(lb, r2);
+          else
+            la = f2_add(la, r2);
+        }
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(la, a0, a1);
+        f2_unpack(lb, b0, b1);
+        l += (a0 + a1) + (b0 + b1);
       }
-      // the P buffer was read by block i - 2's P V
-      if (i >= 2 && !ta_wait(&pv_done[sb], (uint32_t)((i - 2) / 2) & 1u, p.err)) {
-        ok = false;
-        break;
-      }
-      tmem_st_32x32b_x16(trow + kTaPCol + 32u * (uint32_t)sb + 16u * (uint32_t)half, pr);
+      tmem_st_32x32b_x32(trow + ta_s_col(t, pb), pr);  // over the scores just read
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
+      if (lane == 0) mbar_arrive(p_full(t, pb));
     }
-    // the row sum over both halves
-    xl[half * kTaRows + rl] = l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&pair_sum[qd]);
-    if (ok && !ta_wait(&pair_sum[qd], 0u, p.err)) ok = false;
-    const float lt = xl[rl] + xl[kTaRows + rl];
     // ---- the row: O / l (one split) or the split's (m, l, O); a split
     // without keys for this sequence leaves (m, l) = (-inf, 0)
     const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
     const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
-    if (ok && nb == 0 && valid && p.splits > 1 && half == 0 && in_bounds(p.err, base + R, rows_cap))
+    if (ok && nb == 0 && valid && p.splits > 1 && in_bounds(p.err, base + R, rows_cap))
       p.part_ml[base + R] = make_float2(-INFINITY, 0.0f);
-    if (ok && nb > 0 && ta_wait(&pv_done[(nb - 1) & 1], (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
+    if (ok && nbt > 0 && ta_wait(pv_done(t, (nb - 1) & 1), (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
       tc_fence_after();
-      const float il = lt > 0.0f ? 1.0f / lt : 0.0f;
+      const float il = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
       const int64_t oi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool st_ok = valid && (p.splits == 1 ? in_bounds(p.err, oi + kAttD - 1, out_cap)
                                                  : in_bounds(p.err, base + R, rows_cap));
 #pragma unroll 1
-      for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+      for (int c0 = 0; c0 < kAttD; c0 += 32) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(trow + kTaOCol + (uint32_t)c0, ov);
+        tmem_ld_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
         tmem_wait_ld();
         if (!st_ok) continue;
         if (p.splits == 1) {
@@ -733,14 +772,15 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
                                                               __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
         }
       }
-      if (st_ok && p.splits > 1 && half == 0) p.part_ml[base + R] = make_float2(m_used, lt);
+      if (st_ok && p.splits > 1) p.part_ml[base + R] = make_float2(m_used, l);
     }
   }
 
   // ---------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 1 && lane == 0 && mma_issued) mbar_wait(mma_fin, 0u, p.err);  // no MMA in flight when TMEM is freed
+  if ((warp == 1 || warp == 2) && lane == 0 && mma_issued)
+    mbar_wait(mma_fin(warp - 1), 0u, p.err);  // no MMA in flight when TMEM is freed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -883,13 +923,16 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   // a KV head with 128 query rows or more fills the tcgen05 kernel's M = 128
   pl.tc = pl.rows >= kTaRows ? 1 : 0;
   pl.warps = pl.tc ? 0 : attn_warps(pl.rows);
-  const int per_cta = pl.tc ? kTaRows : 16 * pl.warps;
+  const int per_cta = pl.tc ? kTaTiles * kTaRows : 16 * pl.warps;
   pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
   pl.rows_pad = pl.row_blocks * per_cta;
   const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
   const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
+  // about two waves of the CUDA-core kernel; one of the tcgen05 kernel (a
+  // CTA holds 256 query rows and every block of its split: more splits only
+  // add the combine)
   const int per_sm = pl.tc ? 1 : kAttCtasPerSm;
-  const int64_t target = (int64_t)2 * per_sm * (num_sms > 0 ? num_sms : 1);  // about two waves
+  const int64_t target = (int64_t)(pl.tc ? 1 : 2) * per_sm * (num_sms > 0 ? num_sms : 1);
   int splits = (int)((target + base - 1) / base);
   if (splits < 1) splits = 1;
   if (splits > nbmax) splits = nbmax;

@@ -113,6 +113,25 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_kmajor(uint32_t addr) {
   return d;
 }
 
+// The same with the B operand stored MN-major (N contiguous in shared
+// memory): bit 16 of the instruction descriptor.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16_bmn(uint32_t n) { return umma_idesc_bf16(n) | (1u << 16); }
+
+// Shared-memory matrix descriptor: MN-major operand with the 128-byte
+// swizzle. A row of 128 bytes holds 64 consecutive N (or M) elements of one
+// K index, 8 consecutive K rows form a 1024-byte swizzle atom; the atoms of
+// the next 64 N elements are `lbo` bytes on, the next 8 K rows `sbo` bytes
+// on. `addr` (1024-aligned) is advanced by 2 * sbo per 16-element K step.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mnmajor(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;     // leading byte offset: next 64 N elements
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;     // stride byte offset: next 8 K rows
+  d |= (uint64_t)1u << 46;                          // descriptor version (sm_100)
+  d |= (uint64_t)2u << 61;                          // layout: 128-byte swizzle
+  return d;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]; one thread issues.
 __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {

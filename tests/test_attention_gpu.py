@@ -56,6 +56,7 @@ CASES = [  # B, n, H, Hkv, lens, tree
     (1, 1, 8, 8, [5], False),                 # one query, one head per KV head
     (2, 17, 12, 4, [129, 7], True),           # three query heads per KV head
     (2, 33, 8, 1, [511, 64], True),           # all heads on one KV head
+    (2, 24, 64, 8, [300, 77], True),          # 192 query rows: the second 128-row tile half full
 ]
 
 
