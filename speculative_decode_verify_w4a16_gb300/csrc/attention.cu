@@ -119,15 +119,37 @@ template <int NW>
 struct AttnLayout {
   // key/value ring depth: three stages while two CTAs still fit an SM's
   // 228 KiB (each CTA: this layout, 1 KiB of alignment slack, 1 KiB the
-  // system reserves and a few static bytes)
+  // system reserves and the static bytes: the parents and a few words)
   static constexpr int kFixed = 16 * NW * kAttD * 2 + kAttMaxNodes * 8 + 3 * 8 + 1024;
-  static constexpr int kStages = 2 * (3 * kAttStage + kFixed + 1024 + 64) <= 228 * 1024 ? 3 : 2;
+  static constexpr int kStages = 2 * (3 * kAttStage + kFixed + 1024 + kAttMaxNodes * 4 + 64) <= 228 * 1024 ? 3 : 2;
   static constexpr int kKvOff = 0;
   static constexpr int kQOff = kStages * kAttStage;             // [16 NW rows][128] bf16, 256-byte rows
   static constexpr int kAncOff = kQOff + 16 * NW * kAttD * 2;  // [kAttMaxNodes] uint64
   static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;   // full[kStages]
   static constexpr int kTotal = kBarOff + kStages * 8 + 1024;  // + alignment of the swizzled stages
 };
+
+// Ancestor-or-self mask of every node of sequence b (node j is bit j) into
+// anc. All threads of the CTA take part: the parents are loaded and checked
+// at once (a parent precedes its node, the root's is -1; a bad one is
+// reported and taken as -1) into par, then each node's chain is walked. The
+// caller synchronises before reading the masks.
+__device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* par) {
+  for (int j = threadIdx.x; j < p.n; j += blockDim.x) {
+    int q = p.parents ? p.parents[(int64_t)b * p.n + j] : j - 1;
+    if (j == 0 ? q != -1 : (q < 0 || q >= j)) {
+      report_error(p.err, kErrInput);
+      q = -1;
+    }
+    par[j] = q;
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < p.n; j += blockDim.x) {
+    uint64_t a = 1ull << j;
+    for (int k = par[j]; k >= 0; k = par[k]) a |= 1ull << k;
+    anc[j] = a;
+  }
+}
 
 template <int NW>
 __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(const __grid_constant__ CUtensorMap kmap,
@@ -140,6 +162,7 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
   uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L_::kAncOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::kBarOff);
   __shared__ int s_len;
+  __shared__ int s_par[kAttMaxNodes];
 
   const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -159,18 +182,8 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
       len = len < 0 ? 0 : hi;
     }
     s_len = len;
-    // ancestor-or-self mask of every node (node j is bit j)
-    bool bad = false;
-    for (int j = 0; j < p.n; ++j) {
-      int par = p.parents ? p.parents[(int64_t)b * p.n + j] : j - 1;
-      if (j == 0 ? par != -1 : (par < 0 || par >= j)) {
-        bad = true;
-        par = -1;
-      }
-      anc[j] = (par >= 0 ? anc[par] : 0ull) | (1ull << j);
-    }
-    if (bad) report_error(p.err, kErrInput);
   }
+  attn_ancestors(p, b, anc, s_par);
   __syncthreads();
   const int len = s_len;
   const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
@@ -472,6 +485,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   uint64_t* q_ready = tb + 7 * kTaTiles;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(q_ready + 1);
   __shared__ int s_len, s_b;
+  __shared__ int s_par[kAttMaxNodes];
 
   const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
   const int kvh = blockIdx.y;
@@ -521,8 +535,9 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     }
     if (lane == 0) s_b = b;
   }
+  __syncthreads();
+  const int b = s_b;
   if (threadIdx.x == 0) {
-    const int b = s_b;
     int len = p.lens[b];
     const int hi = min(p.max_len, p.Lcap - p.n);
     if (len < 0 || len > hi) {
@@ -530,22 +545,13 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       len = len < 0 ? 0 : hi;
     }
     s_len = len;
-    bool bad = false;
-    for (int j = 0; j < p.n; ++j) {  // ancestor-or-self mask of every node (node j is bit j)
-      int par = p.parents ? p.parents[(int64_t)b * p.n + j] : j - 1;
-      if (j == 0 ? par != -1 : (par < 0 || par >= j)) {
-        bad = true;
-        par = -1;
-      }
-      anc[j] = (par >= 0 ? anc[par] : 0ull) | (1ull << j);
-    }
-    if (bad) report_error(p.err, kErrInput);
   }
+  attn_ancestors(p, b, anc, s_par);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
-  const int len = s_len, b = s_b;
+  const int len = s_len;
   const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
   const int blk0 = split * p.blocks_per_split;
   const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
