@@ -371,11 +371,14 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
 }
 
 // ------------------------------------------------ tcgen05 tree attention
-// For KV heads with at least 128 query rows (n * G >= 128): one CTA per
-// (block of 256 query rows, key split, KV head, batch row), two tiles of 128
-// rows that share every key block, 12 warps:
-//   warp 0        2-D TMA of the 64-key blocks of K and V into a 4-stage ring
-//   warps 1, 2    the MMAs of tile 0 and tile 1 (whole warp in the loop, the
+// One CTA per SM and per (block of TILES x 128 query rows, key split, KV
+// head, batch row); the TILES tiles of 128 rows share every key block.
+// TILES = 2 (more than 128 query rows per KV head: tree drafts): 12 warps, a
+// 4-stage ring, all 512 TMEM columns. TILES = 1 (up to 128 rows: sequence
+// drafts and small trees, where streaming the keys and values is the cost):
+// 6 warps, a 5-stage ring, 256 TMEM columns.
+//   warp 0        2-D TMA of the 64-key blocks of K and V into the ring
+//   warps 1 ..    the MMAs of tile 0 (and tile 1) (whole warp in the loop, the
 //                 elect.sync lane issuing): S = Q K^T (M = 128 query rows,
 //                 N = 64 keys, K = 128; A and B from shared memory) into the
 //                 tile's TMEM score buffer, and O += P V (M = 128, N = 128
@@ -387,9 +390,10 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
 //                 is complete, so the scores of the next block are ready
 //                 when the softmax reaches it; the two tiles' MMAs
 //                 interleave on the tensor pipe.
-//   warp 3        idle
-//   warps 4-11    one query row per thread, tile (warp - 4) / 4, TMEM lane
-//                 quadrant warp % 4: the row's scores from TMEM, the mask
+//   warp 3        idle (TILES = 2)
+//   4 per tile    the softmax warps from warp 4 (TILES = 2) or 2 (TILES = 1):
+//                 one query row per thread, TMEM lane quadrant warp % 4:
+//                 the row's scores from TMEM, the mask
 //                 (committed prefix: every key; tree keys: the node's
 //                 ancestors and itself; skipped on blocks of the prefix), the
 //                 online softmax in the log2 domain and P (rounded to bf16,
@@ -402,29 +406,39 @@ __global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(
 // accumulator in TMEM is rescaled rarely; the result O / l does not depend on
 // which maximum the weights were taken against.
 constexpr int kTaRows = 128;   // query rows per tile (UMMA M)
-constexpr int kTaTiles = 2;
-constexpr int kTaStages = 4;
-constexpr int kTaThreads = 384;
 constexpr float kTaLazy = 8.0f;  // log2 of the largest weight before the maximum is raised
 
+template <int TILES>
+struct TaConfig {
+  static constexpr int kStages = TILES == 2 ? 4 : 5;
+  static constexpr int kSoftWarp0 = TILES == 2 ? 4 : 2;  // first softmax warp
+  static constexpr int kThreads = 32 * (kSoftWarp0 + 4 * TILES);
+  static constexpr uint32_t kTmemCols = 256u * TILES;
+};
+
+template <int TILES>
 struct TaLayout {
+  static constexpr int S = TaConfig<TILES>::kStages;
   static constexpr int kQHalf = kTaRows * 128;        // 128 rows x 64 head columns (bf16)
   static constexpr int kKHalf = kAttKeys * 128;       // 64 keys x 64 head columns
   static constexpr int kStage = 4 * kKHalf;          // K halves, V halves
   static constexpr int kQOff = 0;                     // tile t: two halves at 2 t kQHalf
-  static constexpr int kStageOff = kTaTiles * 2 * kQHalf;
-  static constexpr int kAncOff = kStageOff + kTaStages * kStage;
+  static constexpr int kStageOff = TILES * 2 * kQHalf;
+  static constexpr int kAncOff = kStageOff + S * kStage;
   static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;
   // kv_full[S], kv_free[S]; per tile s_full[2], p_full[2], pv_done[2], mma_fin; q_ready
-  static constexpr int kNumBars = 2 * kTaStages + kTaTiles * 7 + 1;
+  static constexpr int kNumBars = 2 * S + TILES * 7 + 1;
   static constexpr int kTotal = kBarOff + kNumBars * 8 + 16 + 1024;  // + TMEM base, alignment
   static_assert(kStage % 1024 == 0 && kQHalf % 1024 == 0 && kKHalf % 1024 == 0, "swizzle atoms");
-  static_assert(kTotal <= 227 * 1024, "shared memory");
+  static_assert(kTotal + 512 <= 227 * 1024, "shared memory (with the static words and parents)");
 };
 // TMEM columns of tile t: score buffer sb at 128 t + 64 sb .. + 63 (P of the
-// block, bf16 pairs, over its first 32 columns); O 256 + 128 t .. + 127
+// block, bf16 pairs, over its first 32 columns); O 128 TILES + 128 t .. + 127
 __device__ __forceinline__ uint32_t ta_s_col(int t, int sb) { return 128u * (uint32_t)t + 64u * (uint32_t)sb; }
-__device__ __forceinline__ uint32_t ta_o_col(int t) { return 256u + 128u * (uint32_t)t; }
+template <int TILES>
+__device__ __forceinline__ uint32_t ta_o_col(int t) {
+  return 128u * (uint32_t)TILES + 128u * (uint32_t)t;
+}
 
 // lane 0 waits (bounded), every lane gets the outcome. The hand-offs of
 // this kernel are short and on its critical path, so the first tests do not
@@ -442,36 +456,13 @@ __device__ __forceinline__ bool ta_wait(uint64_t* bar, uint32_t parity, unsigned
   return ok != 0;
 }
 
-// The same without ever suspending: lane 0 polls the phase (the time limit
-// read every 256 polls). For the MMA warps, whose waits last about a softmax
-// pass and whose wake-up is on the critical path.
-__device__ __forceinline__ bool ta_spin(uint64_t* bar, uint32_t parity, unsigned* err) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) {
-    unsigned long long t0 = 0;
-    for (unsigned k = 1; !mbar_test(bar, parity); ++k) {
-      if ((k & 255u) == 0) {
-        const unsigned long long now = globaltimer_ns();
-        if (t0 == 0) {
-          t0 = now;
-        } else if (now - t0 > kWaitLimitNs) {
-          report_error(err, kErrTimeout);
-          ok = 0;
-          break;
-        }
-      }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-
-__global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                          const __grid_constant__ CUtensorMap vmap,
-                                                                          const AttnParams p) {
-  using L = TaLayout;
-  constexpr int S = kTaStages;
+template <int TILES>
+__global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
+    tree_attention_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const AttnParams p) {
+  using L = TaLayout<TILES>;
+  using C = TaConfig<TILES>;
+  constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L::kAncOff);
@@ -482,7 +473,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   auto p_full = [&](int t, int pb) { return tb + 7 * t + 2 + pb; };
   auto pv_done = [&](int t, int pb) { return tb + 7 * t + 4 + pb; };
   auto mma_fin = [&](int t) { return tb + 7 * t + 6; };
-  uint64_t* q_ready = tb + 7 * kTaTiles;
+  uint64_t* q_ready = tb + 7 * TILES;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(q_ready + 1);
   __shared__ int s_len, s_b;
   __shared__ int s_par[kAttMaxNodes];
@@ -491,7 +482,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // tiles holding query rows (the last row block of a head may need one)
-  const int ntiles = min(kTaTiles, (p.rows - rb * kTaTiles * kTaRows + kTaRows - 1) / kTaRows);
+  const int ntiles = min(TILES, (p.rows - rb * TILES * kTaRows + kTaRows - 1) / kTaRows);
 
   grid_launch_dependents();
   if (threadIdx.x == 0) {
@@ -499,7 +490,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_free[s], (uint32_t)ntiles);  // each tile's last P V commit
     }
-    for (int t = 0; t < kTaTiles; ++t) {
+    for (int t = 0; t < TILES; ++t) {
       for (int pb = 0; pb < 2; ++pb) {
         mbar_init(s_full(t, pb), 1);
         mbar_init(p_full(t, pb), 4);  // the tile's four softmax warps
@@ -507,11 +498,11 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       }
       mbar_init(mma_fin(t), 1);
     }
-    mbar_init(q_ready, 4 * kTaTiles);
+    mbar_init(q_ready, 4 * TILES);
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_base_s, 512);
+    tmem_alloc(tmem_base_s, C::kTmemCols);
     tmem_relinquish();
   }
   grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
@@ -576,19 +567,19 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       if (i < nb)  // a wait ran out: let the copies in flight land before the CTA exits
         for (int k = i > S ? i - S : 0; k < i; ++k) mbar_wait(&kv_full[k % S], (uint32_t)(k / S) & 1u, p.err);
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp >= 1 && warp <= TILES) {
     // ------------------------------------------------------ MMA, tile t
     const int t = warp - 1;
     const uint32_t idesc_s = umma_idesc_bf16((uint32_t)kAttKeys), idesc_o = umma_idesc_bf16_bmn((uint32_t)kAttD);
-    bool ok = ta_spin(q_ready, 0u, p.err);
+    bool ok = ta_wait(q_ready, 0u, p.err);
     tc_fence_after();
     const uint32_t q0 = smem_u32(smem + L::kQOff + t * 2 * L::kQHalf);
     // S(i) = Q K(i)^T into score buffer i % 2, once P V (i - 2) (its P in the
     // same buffer) is complete
     auto issue_s = [&](int i) {
       const int s = i % S, sb = i & 1;
-      if (!ta_spin(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
-      if (i >= 2 && !ta_spin(pv_done(t, sb), (uint32_t)((i - 2) / 2) & 1u, p.err)) return false;
+      if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
+      if (i >= 2 && !ta_wait(pv_done(t, sb), (uint32_t)((i - 2) / 2) & 1u, p.err)) return false;
       tc_fence_after();
       const uint32_t k0 = smem_u32(smem + L::kStageOff + s * L::kStage);
 #pragma unroll
@@ -607,14 +598,14 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     if (ok && nb > 1) ok = issue_s(1);
     for (int i = 0; ok && i < nb; ++i) {
       const int s = i % S, pb = i & 1;
-      if (!ta_spin(p_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) break;
+      if (!ta_wait(p_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) break;
       tc_fence_after();
       // V half h: keys 0 .. 63 x head columns 64 h .. 64 h + 63, 128-byte rows;
       // 16 keys (two 8-row atoms) per MMA, the second head-column half kKHalf on
       const uint32_t v0 = smem_u32(smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_ts_warp(tmem + ta_o_col(t), tmem + ta_s_col(t, pb) + 8u * (uint32_t)kk,
+        umma_bf16_ts_warp(tmem + ta_o_col<TILES>(t), tmem + ta_s_col(t, pb) + 8u * (uint32_t)kk,
                           umma_desc_sw128_mnmajor(v0 + 2048u * (uint32_t)kk, (uint32_t)L::kKHalf, 1024u), idesc_o,
                           (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(pv_done(t, pb));
@@ -622,14 +613,14 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       if (i + 2 < nb && !issue_s(i + 2)) break;
     }
     if (mma_issued) umma_commit_warp(mma_fin(t));  // tracks all of this warp's MMAs
-  } else if (warp == 3) {
+  } else if (warp < C::kSoftWarp0) {
     // idle
   } else {
     // --------------------------------------------------------- softmax
-    const int t = (warp - 4) >> 2;  // tile
+    const int t = (warp - C::kSoftWarp0) >> 2;  // tile
     const int qd = warp & 3;        // TMEM lane quadrant
     const int rl = qd * 32 + lane;
-    const int R = rb * kTaTiles * kTaRows + t * kTaRows + rl;
+    const int R = rb * TILES * kTaRows + t * kTaRows + rl;
     const bool valid = R < p.rows;
     const int j = valid ? R / p.G : 0, g = R - j * p.G;
     // this row of Q, 128-byte swizzle, K-major (two 64-column halves)
@@ -637,11 +628,15 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool qok = valid && in_bounds(p.err, qi + kAttD - 1, (int64_t)p.B * p.n * p.H * kAttD);
       uint8_t* qt = smem + L::kQOff + t * 2 * L::kQHalf;
+      // all 16 loads in flight before the first store (a store between two
+      // loads would make each load wait for the one before it)
+      uint4 v[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = qok ? *reinterpret_cast<const uint4*>(p.q + qi + c * 8) : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::kQHalf + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = v;
-      }
+      for (int c = 0; c < 16; ++c)
+        v[c] = qok ? *reinterpret_cast<const uint4*>(p.q + qi + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::kQHalf + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = v[c];
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
@@ -651,11 +646,20 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     const int nbt = t < ntiles ? nb : 0;
     float m_used = -INFINITY, l = 0.0f;
     bool ok = true;
+    // a warp without query rows (padding of the last tile) only keeps the
+    // hand-offs' counts: its Q rows are zero, so are its scores, and the P
+    // it leaves in TMEM (those scores' bits) is zero as well
+    const bool any_row = __any_sync(0xffffffffu, valid);
     for (int i = 0; i < nbt; ++i) {
       const int pb = i & 1;
       if (!ta_wait(s_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) {
         ok = false;
         break;
+      }
+      if (!any_row) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(t, pb));
+        continue;
       }
       tc_fence_after();
       uint32_t sv[2][32];
@@ -665,17 +669,24 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
       // the mask (keys the row does not see: -inf), then the block's maximum
       // on the raw scores (the positive scale commutes with it), in the log2
       // domain. A block of the committed prefix alone needs no mask (every
-      // key is seen by every row).
+      // key is seen by every row); nor does a padding row (never stored).
       const int key0 = (blk0 + i) * kAttKeys;
-      if (!(key0 + kAttKeys <= len && valid)) {
+      if (key0 + kAttKeys > len) {
+        // the block's visible keys as a word (bit k: key key0 + k): the
+        // committed prefix below d, then node t of the tree at bit d + t for
+        // each of the row's ancestors and itself
+        const int d = len - key0;  // < 64 here
+        uint64_t vis = d > 0 ? (1ull << d) - 1ull : 0ull;
+        if (d >= 0)
+          vis |= an << d;
+        else if (d > -64)
+          vis |= an >> (-d);
+        const uint32_t vw[2] = {(uint32_t)vis, (uint32_t)(vis >> 32)};
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int pos = key0 + 32 * h + c, ti = pos - len;
-            const bool vis = valid && (pos < len || (ti < p.n && ((an >> ti) & 1ull)));
-            if (!vis) sv[h][c] = __float_as_uint(-INFINITY);
-          }
+          for (int c = 0; c < 32; ++c)
+            if (!((vw[h] >> c) & 1u)) sv[h][c] = __float_as_uint(-INFINITY);
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -701,11 +712,11 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
 #pragma unroll 1
         for (int c0 = 0; c0 < kAttD; c0 += 32) {
           uint32_t ov[32];
-          tmem_ld_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
+          tmem_ld_32x32b_x32(trow + ta_o_col<TILES>(t) + (uint32_t)c0, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * cf);
-          tmem_st_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
+          tmem_st_32x32b_x32(trow + ta_o_col<TILES>(t) + (uint32_t)c0, ov);
         }
         tmem_wait_st();
       }
@@ -747,7 +758,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
     const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
     if (ok && nb == 0 && valid && p.splits > 1 && in_bounds(p.err, base + R, rows_cap))
       p.part_ml[base + R] = make_float2(-INFINITY, 0.0f);
-    if (ok && nbt > 0 && ta_wait(pv_done(t, (nb - 1) & 1), (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
+    if (ok && nbt > 0 && any_row && ta_wait(pv_done(t, (nb - 1) & 1), (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
       tc_fence_after();
       const float il = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
@@ -757,7 +768,7 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
 #pragma unroll 1
       for (int c0 = 0; c0 < kAttD; c0 += 32) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(trow + ta_o_col(t) + (uint32_t)c0, ov);
+        tmem_ld_32x32b_x32(trow + ta_o_col<TILES>(t) + (uint32_t)c0, ov);
         tmem_wait_ld();
         if (!st_ok) continue;
         if (p.splits == 1) {
@@ -785,13 +796,13 @@ __global__ void __launch_bounds__(kTaThreads, 1) tree_attention_tc_kernel(const 
   // ---------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if ((warp == 1 || warp == 2) && lane == 0 && mma_issued)
+  if (warp >= 1 && warp <= TILES && lane == 0 && mma_issued)
     mbar_wait(mma_fin(warp - 1), 0u, p.err);  // no MMA in flight when TMEM is freed
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
@@ -926,20 +937,21 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   AttnPlan pl;
   const int G = H / Hkv;
   pl.rows = n * G;
-  // a KV head with 128 query rows or more fills the tcgen05 kernel's M = 128
-  pl.tc = pl.rows >= kTaRows ? 1 : 0;
+  // the tcgen05 kernel: two 128-row tiles per CTA above 128 query rows per
+  // KV head, one up to 128
+  pl.tc = pl.rows > kTaRows ? 2 : 1;
   pl.warps = pl.tc ? 0 : attn_warps(pl.rows);
-  const int per_cta = pl.tc ? kTaTiles * kTaRows : 16 * pl.warps;
+  const int per_cta = pl.tc ? pl.tc * kTaRows : 16 * pl.warps;
   pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
   pl.rows_pad = pl.row_blocks * per_cta;
   const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
   const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
-  // about two waves of the CUDA-core kernel; one of the tcgen05 kernel (a
-  // CTA holds 256 query rows and every block of its split: more splits only
-  // add the combine)
+  // about two waves of the CUDA-core kernel; at most one of the tcgen05
+  // kernel (one CTA per SM holds its rows and every block of its split: more
+  // splits only add the combine and more CTA starts)
   const int per_sm = pl.tc ? 1 : kAttCtasPerSm;
   const int64_t target = (int64_t)(pl.tc ? 1 : 2) * per_sm * (num_sms > 0 ? num_sms : 1);
-  int splits = (int)((target + base - 1) / base);
+  int splits = pl.tc ? (int)(target / base) : (int)((target + base - 1) / base);
   if (splits < 1) splits = 1;
   if (splits > nbmax) splits = nbmax;
   pl.blocks_per_split = (nbmax + splits - 1) / splits;
@@ -955,6 +967,17 @@ static cudaError_t launch_attn_t(const CUtensorMap& km, const CUtensorMap& vm, c
   cudaError_t e = cudaFuncSetAttribute(tree_attention_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(tree_attention_kernel<NW>, grid, dim3(32 * NW), (size_t)smem, stream, km, vm, p);
+}
+
+template <int TILES>
+static cudaError_t launch_attn_tc_t(const CUtensorMap& km, const CUtensorMap& vm, const AttnParams& p, dim3 grid,
+                                    cudaStream_t stream) {
+  constexpr int smem = TaLayout<TILES>::kTotal;
+  cudaError_t e =
+      cudaFuncSetAttribute(tree_attention_tc_kernel<TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(tree_attention_tc_kernel<TILES>, grid, dim3(TaConfig<TILES>::kThreads), (size_t)smem, stream,
+                    km, vm, p);
 }
 
 cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
@@ -997,10 +1020,10 @@ cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   const dim3 grid((unsigned)(pl.row_blocks * pl.splits), (unsigned)Hkv, (unsigned)B);
   cudaError_t e;
-  if (pl.tc) {
-    e = cudaFuncSetAttribute(tree_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, TaLayout::kTotal);
-    if (e == cudaSuccess)
-      e = launch_pdl(tree_attention_tc_kernel, grid, dim3(kTaThreads), (size_t)TaLayout::kTotal, stream, km, vm, p);
+  if (pl.tc == 2) {
+    e = launch_attn_tc_t<2>(km, vm, p, grid, stream);
+  } else if (pl.tc == 1) {
+    e = launch_attn_tc_t<1>(km, vm, p, grid, stream);
   } else switch (pl.warps) {
     case 1: e = launch_attn_t<1>(km, vm, p, grid, stream); break;
     case 2: e = launch_attn_t<2>(km, vm, p, grid, stream); break;
