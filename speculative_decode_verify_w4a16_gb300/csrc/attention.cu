@@ -5,18 +5,17 @@
 // 8.7: how a serving stack reuses the KV cache across accepted and rejected
 // tokens).
 //
-// tree_attention_kernel: one CTA per (query-row block, key split, KV head,
-// batch row). The query rows of a KV head are its G = H / Hkv query heads at
-// every tree node, row r = node * G + head-in-group, 16 rows per warp. The
-// keys and values stream through a shared-memory ring of 64-key blocks
-// (2-D TMA, 128-byte swizzle; two or three stages). Each warp forms S = Q K^T with
-// mma.sync m16n8k16 (bf16 in, fp32 accumulate), masks it (the committed
-// prefix: every key; the tree's own keys: the node's ancestors and itself, a
-// 64-bit mask per node), keeps the running maximum and sum of the online
-// softmax in the log2 domain, and accumulates P V with P rounded to bf16
-// (the sum is taken over the same rounded values). With one split the rows
-// are normalised and stored as bf16; otherwise each split stores fp32
-// (m, l, O) and tree_attention_combine_kernel merges the splits.
+// tree_attention_tc_kernel: the query rows of a KV head are its G = H / Hkv
+// query heads at every tree node, row r = node * G + head-in-group, in tiles
+// of 128 (the tcgen05 MMA's M). S = Q K^T and O += P V run on the tensor
+// cores with S, P and O in tensor memory; the keys and values stream through
+// a shared-memory ring of 64-key blocks (2-D TMA, 128-byte swizzle). Each row
+// is masked (the committed prefix: every key; the tree's own keys: the node's
+// ancestors and itself, a 64-bit mask per node), keeps the running maximum
+// and sum of the online softmax in the log2 domain, and accumulates P V with
+// P rounded to bf16 (the sum is taken over the same rounded values). With one
+// split the rows are normalised and stored as bf16; otherwise each split
+// stores fp32 (m, l, O) and tree_attention_combine_kernel merges the splits.
 //
 // kv_compact_kernel: per (batch row, layer), the keys and values of the
 // accepted root path move to the positions right after the committed prefix.
@@ -33,10 +32,7 @@ namespace w4a16 {
 
 constexpr int kAttD = 128;                     // head width
 constexpr int kAttKeys = 64;                   // keys per block
-constexpr int kAttHalf = kAttKeys * 64 * 2;    // one 64-wide half of a key or value block: 8 KiB
-constexpr int kAttStage = 4 * kAttHalf;        // key halves, then value halves: 32 KiB
 constexpr int kAttMaxNodes = 64;
-constexpr int kAttCtasPerSm = 2;
 
 struct AttnParams {
   const __nv_bfloat16* q;  // [B][n][H][D]
@@ -48,28 +44,12 @@ struct AttnParams {
   unsigned* err;
   int B, n, H, Hkv, G, Lcap, max_len;
   int rows;        // n * G query rows per KV head
-  int rows_pad;    // row_blocks * 16 * warps
+  int rows_pad;    // row_blocks * 128 * tiles
   int row_blocks;
   int splits, blocks_per_split;
   float scale_log2;  // softmax scale * log2(e)
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void attn_mma(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-               "{%0, %1, %2, %3};"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // 2^x by the hardware approximation (a few ulp; 2^-inf = 0)
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -107,27 +87,7 @@ __device__ __forceinline__ uint32_t pack_bf16_rn(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-// two fp32 values rounded to a bf16 pair (low half = first), and the rounded values back
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& rlo, float& rhi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  rlo = __low2float(h);
-  rhi = __high2float(h);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
 
-template <int NW>
-struct AttnLayout {
-  // key/value ring depth: three stages while two CTAs still fit an SM's
-  // 228 KiB (each CTA: this layout, 1 KiB of alignment slack, 1 KiB the
-  // system reserves and the static bytes: the parents and a few words)
-  static constexpr int kFixed = 16 * NW * kAttD * 2 + kAttMaxNodes * 8 + 3 * 8 + 1024;
-  static constexpr int kStages = 2 * (3 * kAttStage + kFixed + 1024 + kAttMaxNodes * 4 + 64) <= 228 * 1024 ? 3 : 2;
-  static constexpr int kKvOff = 0;
-  static constexpr int kQOff = kStages * kAttStage;             // [16 NW rows][128] bf16, 256-byte rows
-  static constexpr int kAncOff = kQOff + 16 * NW * kAttD * 2;  // [kAttMaxNodes] uint64
-  static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;   // full[kStages]
-  static constexpr int kTotal = kBarOff + kStages * 8 + 1024;  // + alignment of the swizzled stages
-};
 
 // Ancestor-or-self mask of every node of sequence b (node j is bit j) into
 // anc. All threads of the CTA take part: the parents are loaded and checked
@@ -148,225 +108,6 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
     uint64_t a = 1ull << j;
     for (int k = par[j]; k >= 0; k = par[k]) a |= 1ull << k;
     anc[j] = a;
-  }
-}
-
-template <int NW>
-__global__ void __launch_bounds__(32 * NW, kAttCtasPerSm) tree_attention_kernel(const __grid_constant__ CUtensorMap kmap,
-                                                                                const __grid_constant__ CUtensorMap vmap,
-                                                                                const AttnParams p) {
-  using L_ = AttnLayout<NW>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* qs = smem + L_::kQOff;
-  uint64_t* anc = reinterpret_cast<uint64_t*>(smem + L_::kAncOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L_::kBarOff);
-  __shared__ int s_len;
-  __shared__ int s_par[kAttMaxNodes];
-
-  const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-  grid_launch_dependents();
-  if (tid == 0) {
-    for (int s = 0; s < L_::kStages; ++s) mbar_init(&full[s], 1);
-    fence_mbarrier_init();
-  }
-  grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
-  if (tid == 0) {
-    int len = p.lens[b];
-    const int hi = min(p.max_len, p.Lcap - p.n);
-    if (len < 0 || len > hi) {
-      report_error(p.err, kErrInput);
-      len = len < 0 ? 0 : hi;
-    }
-    s_len = len;
-  }
-  attn_ancestors(p, b, anc, s_par);
-  __syncthreads();
-  const int len = s_len;
-  const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
-  const int blk0 = split * p.blocks_per_split;
-  const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
-  const int64_t kv_row0 = ((int64_t)b * p.Hkv + kvh) * p.Lcap;
-
-  // block blk0 + i of this split into stage i % L_::kStages (rows past the
-  // head's keys are masked; past the whole cache the copy fills zeros)
-  auto issue = [&](int i) {
-    const int s = i % L_::kStages;
-    uint8_t* st = smem + L_::kKvOff + s * kAttStage;
-    const int32_t y = (int32_t)(kv_row0 + (int64_t)(blk0 + i) * kAttKeys);
-    mbar_arrive_expect_tx(&full[s], (uint32_t)kAttStage);
-    tma_load_2d(st, &kmap, 0, y, &full[s]);
-    tma_load_2d(st + kAttHalf, &kmap, 64, y, &full[s]);
-    tma_load_2d(st + 2 * kAttHalf, &vmap, 0, y, &full[s]);
-    tma_load_2d(st + 3 * kAttHalf, &vmap, 64, y, &full[s]);
-  };
-  if (tid == 0)
-    for (int i = 0; i < nb && i < L_::kStages; ++i) issue(i);
-
-  // the CTA's query rows into shared memory (16-byte chunk c of row r at
-  // chunk c ^ (r % 8): conflict-free row reads for ldmatrix)
-  const int rows0 = rb * 16 * NW;
-  for (int idx = tid; idx < 16 * NW * 16; idx += 32 * NW) {
-    const int r = idx >> 4, c = idx & 15;
-    const int R = rows0 + r;
-    const int j = R / p.G, g = R - j * p.G;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD + c * 8;
-    if (j < p.n && in_bounds(p.err, qi + 7, (int64_t)p.B * p.n * p.H * kAttD))
-      v = *reinterpret_cast<const uint4*>(p.q + qi);
-    *reinterpret_cast<uint4*>(qs + r * 256 + ((c ^ (r & 7)) << 4)) = v;
-  }
-  __syncthreads();
-
-  // this lane's two rows (mma fragment rows lane / 4 and lane / 4 + 8)
-  const int ra = rows0 + warp * 16 + (lane >> 2), rb8 = ra + 8;
-  const int ja = ra / p.G, jb = rb8 / p.G;
-  const uint64_t anc_a = ja < p.n ? anc[ja] : 0ull, anc_b = jb < p.n ? anc[jb] : 0ull;
-  const uint32_t q_base = smem_u32(qs) + warp * 16 * 256;
-  float o[16][4];
-#pragma unroll
-  for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.0f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.0f, l_b = 0.0f;
-
-  // a warp whose 16 rows are all padding only keeps the ring's rhythm
-  const bool idle = rows0 + warp * 16 >= p.rows;
-  for (int i = 0; i < nb; ++i) {
-    const int s = i % L_::kStages;
-    if (idle) {
-      if (__syncthreads_or(0)) break;
-      if (tid == 0 && i + L_::kStages < nb) issue(i + L_::kStages);
-      continue;
-    }
-    const bool ok = mbar_wait(&full[s], (uint32_t)(i / L_::kStages) & 1u, p.err);
-    const uint32_t kst = smem_u32(smem + L_::kKvOff + s * kAttStage), vst = kst + 2 * kAttHalf;
-    // ---- S = Q K^T (16 rows x 64 keys per warp)
-    float sc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.0f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t qa[4];
-      {
-        const int r = lane & 15, c = 2 * kk + (lane >> 4);
-        ldsm_x4(q_base + r * 256 + ((c ^ (r & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
-      }
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int c = 2 * kk + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kst + (c >> 3) * kAttHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4), b0, b1, b2, b3);
-        attn_mma(sc[2 * np], qa, b0, b1);
-        attn_mma(sc[2 * np + 1], qa, b2, b3);
-      }
-    }
-    // ---- mask, online softmax (log2 domain)
-    const int key0 = (blk0 + i) * kAttKeys;
-    const bool prefix_only = key0 + kAttKeys <= len;
-    float mx_a = m_a, mx_b = m_b;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sc[nt][e] * p.scale_log2;
-        if (!prefix_only) {
-          const int pos = key0 + nt * 8 + ((lane & 3) << 1) + (e & 1);
-          const int ti = pos - len;
-          const uint64_t an = e < 2 ? anc_a : anc_b;
-          if (!(pos < len || (ti < p.n && ((an >> ti) & 1ull)))) v = -INFINITY;
-        }
-        sc[nt][e] = v;
-        if (e < 2)
-          mx_a = fmaxf(mx_a, v);
-        else
-          mx_b = fmaxf(mx_b, v);
-      }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-    const float ua = mx_a == -INFINITY ? 0.0f : mx_a, ub = mx_b == -INFINITY ? 0.0f : mx_b;
-    const float ca = ex2(m_a - ua), cb = ex2(m_b - ub);  // 0 while the row had no key
-    m_a = mx_a;
-    m_b = mx_b;
-    l_a *= ca;
-    l_b *= cb;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      o[dt][0] *= ca;
-      o[dt][1] *= ca;
-      o[dt][2] *= cb;
-      o[dt][3] *= cb;
-    }
-    uint32_t pa[4][4];  // P as the A operand of four 16-key steps
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      float r0, r1, r2, r3;
-      const uint32_t x01 = pack_bf16(ex2(sc[nt][0] - ua), ex2(sc[nt][1] - ua), r0, r1);
-      const uint32_t x23 = pack_bf16(ex2(sc[nt][2] - ub), ex2(sc[nt][3] - ub), r2, r3);
-      l_a += r0 + r1;
-      l_b += r2 + r3;
-      pa[nt >> 1][(nt & 1) * 2] = x01;
-      pa[nt >> 1][(nt & 1) * 2 + 1] = x23;
-    }
-    // ---- O += P V
-#pragma unroll
-    for (int kt = 0; kt < 4; ++kt)
-#pragma unroll
-      for (int dp = 0; dp < 8; ++dp) {
-        const int key = kt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int c = 2 * dp + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vst + (c >> 3) * kAttHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4), b0, b1, b2, b3);
-        attn_mma(o[2 * dp], pa[kt], b0, b1);
-        attn_mma(o[2 * dp + 1], pa[kt], b2, b3);
-      }
-    // every warp is done with stage s: refill it (a timed-out wait ends the loop in every thread)
-    if (__syncthreads_or(!ok)) break;
-    if (tid == 0 && i + L_::kStages < nb) issue(i + L_::kStages);
-  }
-
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-  const int t2 = (lane & 3) << 1;
-  if (p.splits == 1) {
-    const float ia = l_a > 0.0f ? 1.0f / l_a : 0.0f, ib = l_b > 0.0f ? 1.0f / l_b : 0.0f;
-    const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
-    const int64_t oa = (((int64_t)b * p.n + ja) * p.H + kvh * p.G + (ra - ja * p.G)) * kAttD;
-    const int64_t ob = (((int64_t)b * p.n + jb) * p.H + kvh * p.G + (rb8 - jb * p.G)) * kAttD;
-    if (ja < p.n && in_bounds(p.err, oa + kAttD - 1, out_cap)) {
-      __nv_bfloat16* dst = p.out + oa + t2;
-#pragma unroll
-      for (int dt = 0; dt < 16; ++dt)
-        *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][0] * ia, o[dt][1] * ia);
-    }
-    if (jb < p.n && in_bounds(p.err, ob + kAttD - 1, out_cap)) {
-      __nv_bfloat16* dst = p.out + ob + t2;
-#pragma unroll
-      for (int dt = 0; dt < 16; ++dt)
-        *reinterpret_cast<__nv_bfloat162*>(dst + dt * 8) = __floats2bfloat162_rn(o[dt][2] * ib, o[dt][3] * ib);
-    }
-  } else {
-    const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
-    const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
-    float* pa_o = p.part_o + (base + ra) * kAttD + t2;
-    float* pb_o = p.part_o + (base + rb8) * kAttD + t2;
-    const bool ok = in_bounds(p.err, base + ra, rows_cap) && in_bounds(p.err, base + rb8, rows_cap);
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-      if (!ok) break;
-      *reinterpret_cast<float2*>(pa_o + dt * 8) = make_float2(o[dt][0], o[dt][1]);
-      *reinterpret_cast<float2*>(pb_o + dt * 8) = make_float2(o[dt][2], o[dt][3]);
-    }
-    if (ok && (lane & 3) == 0) {
-      p.part_ml[base + ra] = make_float2(m_a, l_a);
-      p.part_ml[base + rb8] = make_float2(m_b, l_b);
-    }
   }
 }
 
@@ -928,10 +669,6 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(uint4* kc, 
 
 // warps per CTA: 1, 2, 4 or 8 (measured on the 5-position chain with 64
 // heads on 8: four warps with two stages beat three with three stages)
-static int attn_warps(int rows) {
-  const int w = (rows + 15) / 16;
-  return w <= 1 ? 1 : (w <= 2 ? 2 : (w <= 4 ? 4 : 8));
-}
 
 AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   AttnPlan pl;
@@ -939,19 +676,15 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   pl.rows = n * G;
   // the tcgen05 kernel: two 128-row tiles per CTA above 128 query rows per
   // KV head, one up to 128
-  pl.tc = pl.rows > kTaRows ? 2 : 1;
-  pl.warps = pl.tc ? 0 : attn_warps(pl.rows);
-  const int per_cta = pl.tc ? pl.tc * kTaRows : 16 * pl.warps;
+  pl.tiles = pl.rows > kTaRows ? 2 : 1;
+  const int per_cta = pl.tiles * kTaRows;
   pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
   pl.rows_pad = pl.row_blocks * per_cta;
   const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
   const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
-  // about two waves of the CUDA-core kernel; at most one of the tcgen05
-  // kernel (one CTA per SM holds its rows and every block of its split: more
-  // splits only add the combine and more CTA starts)
-  const int per_sm = pl.tc ? 1 : kAttCtasPerSm;
-  const int64_t target = (int64_t)(pl.tc ? 1 : 2) * per_sm * (num_sms > 0 ? num_sms : 1);
-  int splits = pl.tc ? (int)(target / base) : (int)((target + base - 1) / base);
+  // at most one wave of CTAs (one CTA per SM holds its rows and every block
+  // of its split: more splits only add the combine and more CTA starts)
+  int splits = (int)((num_sms > 0 ? num_sms : 1) / base);
   if (splits < 1) splits = 1;
   if (splits > nbmax) splits = nbmax;
   pl.blocks_per_split = (nbmax + splits - 1) / splits;
@@ -960,14 +693,6 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   return pl;
 }
 
-template <int NW>
-static cudaError_t launch_attn_t(const CUtensorMap& km, const CUtensorMap& vm, const AttnParams& p, dim3 grid,
-                                 cudaStream_t stream) {
-  constexpr int smem = AttnLayout<NW>::kTotal;
-  cudaError_t e = cudaFuncSetAttribute(tree_attention_kernel<NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(tree_attention_kernel<NW>, grid, dim3(32 * NW), (size_t)smem, stream, km, vm, p);
-}
 
 template <int TILES>
 static cudaError_t launch_attn_tc_t(const CUtensorMap& km, const CUtensorMap& vm, const AttnParams& p, dim3 grid,
@@ -1020,16 +745,10 @@ cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   const dim3 grid((unsigned)(pl.row_blocks * pl.splits), (unsigned)Hkv, (unsigned)B);
   cudaError_t e;
-  if (pl.tc == 2) {
+  if (pl.tiles == 2)
     e = launch_attn_tc_t<2>(km, vm, p, grid, stream);
-  } else if (pl.tc == 1) {
+  else
     e = launch_attn_tc_t<1>(km, vm, p, grid, stream);
-  } else switch (pl.warps) {
-    case 1: e = launch_attn_t<1>(km, vm, p, grid, stream); break;
-    case 2: e = launch_attn_t<2>(km, vm, p, grid, stream); break;
-    case 4: e = launch_attn_t<4>(km, vm, p, grid, stream); break;
-    default: e = launch_attn_t<8>(km, vm, p, grid, stream); break;
-  }
   if (e != cudaSuccess || pl.splits == 1) return e;
   const int64_t rows = (int64_t)B * Hkv * pl.rows;
   return launch_pdl(tree_attention_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p);

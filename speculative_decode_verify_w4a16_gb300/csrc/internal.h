@@ -113,8 +113,7 @@ void* tensor_map_encode_fn();
 // ---- tree-masked verify attention and KV compaction
 struct AttnPlan {
   int rows = 0;        // query rows per KV head: n * (H / Hkv)
-  int tc = 0;          // tcgen05 kernel tiles of 128 query rows per CTA (1 or 2); 0: the mma.sync kernel
-  int warps = 0;       // mma.sync kernel: warps per CTA (16 rows each): 1 to 4, or 8
+  int tiles = 0;       // 128-row tiles per CTA: 2 above 128 query rows per KV head, else 1
   int row_blocks = 0;  // CTAs along the rows
   int rows_pad = 0;
   int splits = 0;      // CTAs along the keys

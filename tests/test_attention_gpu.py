@@ -71,10 +71,10 @@ def test_tree_attention_matches_oracle(B, n, H, Hkv, lens, tree):
 
 def test_one_split_and_many_splits_agree_with_the_oracle():
     # max_len = 0 leaves one key block (one split: rows normalised in the
-    # kernel); a long prefix on a small grid takes many splits and the combine
-    # the first and the last two go to the tcgen05 kernel (128 query rows or
-    # more per KV head), the last one with splits holding no key of its
-    # first sequence
+    # kernel); a long prefix on a small grid takes many splits and the
+    # combine. The first case takes two 128-row tiles per CTA (320 query rows
+    # per KV head), the others one (40 and 128 rows); the last one has splits
+    # holding no key of its first sequence
     cases = [(16, 40, 64, 8, [0] * 16, 0), (1, 5, 16, 2, [3000], 3000), (1, 16, 64, 8, [3000], 3000),
              (2, 16, 64, 8, [100, 3000], 3000)]
     seen = set()
