@@ -14,8 +14,9 @@
 // ancestors and itself, a 64-bit mask per node), keeps the running maximum
 // and sum of the online softmax in the log2 domain, and accumulates P V with
 // P rounded to bf16 (the sum is taken over the same rounded values). With one
-// split the rows are normalised and stored as bf16; otherwise each split
-// stores fp32 (m, l, O) and tree_attention_combine_kernel merges the splits.
+// piece per sequence the rows are normalised and stored as bf16; a sequence
+// cut into several pieces (CTAs) leaves fp32 (m, l, O) per piece and
+// tree_attention_combine_kernel merges them.
 //
 // kv_compact_kernel: per (batch row, layer), the keys and values of the
 // accepted root path move to the positions right after the committed prefix.
@@ -39,14 +40,17 @@ struct AttnParams {
   const int32_t* lens;     // [B]
   const int32_t* parents;  // [B][n] or null (chain)
   __nv_bfloat16* out;      // [B][n][H][D]
-  float* part_o;           // splits > 1: [splits][B][Hkv][rows_pad][D] unnormalised sums
-  float2* part_ml;         // and [splits][B][Hkv][rows_pad] (running max, sum), log2 domain
+  float* part_o;           // cut: [ctas][unit_rows][D] unnormalised sums, one slot per piece
+  float2* part_ml;         // and [ctas][unit_rows] (running max, sum), log2 domain
   unsigned* err;
   int B, n, H, Hkv, G, Lcap, max_len;
   int rows;        // n * G query rows per KV head
-  int rows_pad;    // row_blocks * 128 * tiles
-  int row_blocks;
-  int splits, blocks_per_split;
+  int unit_rows;   // query rows per CTA: 128 * tiles
+  int row_blocks;  // CTAs along the rows of a KV head
+  int ctas;        // CTAs the pieces are cut for (one wave)
+  int pieces_max;  // grid size: max(ctas, B * Hkv * row_blocks)
+  int cut;         // 1: sequences may be cut into several pieces (partials and the combine)
+  int2* seq_pieces;  // cut: per sequence (first piece, pieces)
   float scale_log2;  // softmax scale * log2(e)
 };
 
@@ -112,8 +116,10 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 }
 
 // ------------------------------------------------ tcgen05 tree attention
-// One CTA per SM and per (block of TILES x 128 query rows, key split, KV
-// head, batch row); the TILES tiles of 128 rows share every key block.
+// One CTA per SM and per piece: a block of TILES x 128 query rows of a KV
+// head of a sequence against a run of its key blocks (all of them, or a piece
+// of a sequence cut to fill one wave of CTAs); the TILES tiles of 128 rows
+// share every key block.
 // TILES = 2 (more than 128 query rows per KV head: tree drafts): 12 warps, a
 // 4-stage ring, all 512 TMEM columns. TILES = 1 (up to 128 rows: sequence
 // drafts and small trees, where streaming the keys and values is the cost):
@@ -140,7 +146,7 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 //                 online softmax in the log2 domain and P (rounded to bf16,
 //                 the row sum taken over the rounded values) back into TMEM,
 //                 over the first half of the scores just read;
-//                 at the end the normalised row (or a split's partial)
+//                 at the end the normalised row (or a piece's partial)
 // While one tile's softmax runs, the tensor pipe works on the other tile.
 // The running maximum is raised only when a block's maximum exceeds it by
 // more than 8 (a factor 256: P stays well inside bf16 and fp32), so the
@@ -197,6 +203,95 @@ __device__ __forceinline__ bool ta_wait(uint64_t* bar, uint32_t parity, unsigned
   return ok != 0;
 }
 
+// The work of one CTA: the query rows of row block rb of KV head kvh of
+// sequence b, against key blocks blk0 .. blk0 + nb - 1 of that sequence, one
+// of the np pieces the sequence was cut into (np = 1: the rows are finished
+// here; otherwise the CTA leaves a partial in its slot). b < 0: no work.
+struct TaWork {
+  int b, kvh, rb, blk0, nb, np, len;
+};
+
+// Warp-collective (one warp): the piece of CTA x. With up to 64 sequences
+// every (sequence, KV head, row block) unit is cut into np pieces of about
+// the same number of key blocks, np = ceil(nblk / Q) for a sequence of nblk
+// blocks, Q the smallest length for which all pieces fit p.ctas CTAs (one
+// wave; when the units alone fill them, np = 1); pieces are numbered in
+// decreasing blocks per piece (ties by sequence), a sequence's pieces unit by
+// unit and piece by piece, so that the longest start first. Above 64
+// sequences: one piece per unit, in order.
+__device__ TaWork ta_assign(const AttnParams& p, int x, int lane) {
+  const int units = p.Hkv * p.row_blocks;
+  const int hi = min(p.max_len, p.Lcap - p.n);
+  TaWork w{-1, 0, 0, 0, 0, 1, 0};
+  if (p.B > 64) {
+    const int b = x / units;
+    if (b < p.B) {
+      const int u = x - b * units;
+      int len = p.lens[b];
+      if (len < 0 || len > hi) {
+        if (lane == 0) report_error(p.err, kErrInput);
+        len = len < 0 ? 0 : hi;
+      }
+      w = TaWork{b, u / p.row_blocks, u % p.row_blocks, 0, (len + p.n + kAttKeys - 1) / kAttKeys, 1, len};
+    }
+    return w;
+  }
+  int len[2], nbk[2], np[2], ps[2], off[2] = {0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    int l = c < p.B ? p.lens[c] : 0;
+    l = l < 0 ? 0 : (l > hi ? hi : l);
+    len[h] = l;
+    nbk[h] = c < p.B ? (l + p.n + kAttKeys - 1) / kAttKeys : 0;
+  }
+  int q = 1, qhi = __reduce_max_sync(0xffffffffu, max(nbk[0], nbk[1]));
+  while (q < qhi) {  // the smallest piece length whose pieces fit the CTAs
+    const int mid = (q + qhi) >> 1;
+    const int cnt = __reduce_add_sync(0xffffffffu, (nbk[0] + mid - 1) / mid + (nbk[1] + mid - 1) / mid);
+    if ((int64_t)cnt * units <= p.ctas)
+      qhi = mid;
+    else
+      q = mid + 1;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    np[h] = (nbk[h] + q - 1) / q;
+    ps[h] = np[h] > 0 ? (nbk[h] + np[h] - 1) / np[h] : 0;
+  }
+  for (int c2 = 0; c2 < p.B; ++c2) {  // pieces numbered before each sequence's first
+    const int ps2 = __shfl_sync(0xffffffffu, c2 < 32 ? ps[0] : ps[1], c2 & 31);
+    const int np2 = __shfl_sync(0xffffffffu, c2 < 32 ? np[0] : np[1], c2 & 31);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = lane + 32 * h;
+      if (c < p.B && (ps2 > ps[h] || (ps2 == ps[h] && c2 < c))) off[h] += np2 * units;
+    }
+  }
+  int found = -1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = lane + 32 * h;
+    if (c < p.B && x >= off[h] && x < off[h] + np[h] * units) {
+      const int li = x - off[h], u = li / np[h], k = li - u * np[h];
+      const int blk0 = k * ps[h];
+      w = TaWork{c, u / p.row_blocks, u % p.row_blocks, blk0, min(nbk[h], blk0 + ps[h]) - blk0, np[h], len[h]};
+      found = h;
+      if (li == 0) {  // the sequence's first piece reports a bad length and records its pieces
+        const int raw = p.lens[c];
+        if (raw < 0 || raw > hi) report_error(p.err, kErrInput);
+        if (p.cut) p.seq_pieces[c] = make_int2(off[h], np[h]);
+      }
+    }
+  }
+  const int src = __ffs(__ballot_sync(0xffffffffu, found >= 0)) - 1;
+  if (src < 0) return TaWork{-1, 0, 0, 0, 0, 1, 0};
+  return TaWork{__shfl_sync(0xffffffffu, w.b, src),   __shfl_sync(0xffffffffu, w.kvh, src),
+                __shfl_sync(0xffffffffu, w.rb, src),  __shfl_sync(0xffffffffu, w.blk0, src),
+                __shfl_sync(0xffffffffu, w.nb, src),  __shfl_sync(0xffffffffu, w.np, src),
+                __shfl_sync(0xffffffffu, w.len, src)};
+}
+
 template <int TILES>
 __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     tree_attention_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -216,16 +311,22 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
   auto mma_fin = [&](int t) { return tb + 7 * t + 6; };
   uint64_t* q_ready = tb + 7 * TILES;
   uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(q_ready + 1);
-  __shared__ int s_len, s_b;
+  __shared__ TaWork s_w;
   __shared__ int s_par[kAttMaxNodes];
-
-  const int rb = blockIdx.x % p.row_blocks, split = blockIdx.x / p.row_blocks;
-  const int kvh = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // tiles holding query rows (the last row block of a head may need one)
-  const int ntiles = min(TILES, (p.rows - rb * TILES * kTaRows + kTaRows - 1) / kTaRows);
 
   grid_launch_dependents();
+  grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
+  if (warp == 0) {
+    const TaWork w = ta_assign(p, (int)blockIdx.x, lane);
+    if (lane == 0) s_w = w;
+  }
+  __syncthreads();
+  const TaWork w = s_w;
+  if (w.b < 0) return;  // the whole CTA: no piece left for it
+  const int b = w.b, kvh = w.kvh, rb = w.rb, len = w.len, blk0 = w.blk0, nb = w.nb;
+  // tiles holding query rows (the last row block of a head may need one)
+  const int ntiles = min(TILES, (p.rows - rb * TILES * kTaRows + kTaRows - 1) / kTaRows);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&kv_full[s], 1);
@@ -246,47 +347,11 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     tmem_alloc(tmem_base_s, C::kTmemCols);
     tmem_relinquish();
   }
-  grid_dependency_wait();  // q, the caches and lens may come from the preceding kernels
-  if (warp == 0) {
-    // longest sequences first: the z-th row of CTAs takes the sequence of
-    // rank z in decreasing length (ties by index), so that the shortest
-    // fill the tail of the launch (up to 64 sequences; above, in order)
-    int b = p.B <= 64 ? -1 : (int)blockIdx.z;
-    if (p.B <= 64) {
-      for (int c = lane; c < p.B; c += 32) {
-        const int lc = p.lens[c];
-        int rank = 0;
-        for (int c2 = 0; c2 < p.B; ++c2) {
-          const int l2 = p.lens[c2];
-          rank += (l2 > lc || (l2 == lc && c2 < c)) ? 1 : 0;
-        }
-        if (rank == (int)blockIdx.z) b = c;
-      }
-      b = __reduce_max_sync(0xffffffffu, b);
-      if (b < 0) b = (int)blockIdx.z;
-    }
-    if (lane == 0) s_b = b;
-  }
-  __syncthreads();
-  const int b = s_b;
-  if (threadIdx.x == 0) {
-    int len = p.lens[b];
-    const int hi = min(p.max_len, p.Lcap - p.n);
-    if (len < 0 || len > hi) {
-      report_error(p.err, kErrInput);
-      len = len < 0 ? 0 : hi;
-    }
-    s_len = len;
-  }
   attn_ancestors(p, b, anc, s_par);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_base_s;
-  const int len = s_len;
-  const int nblk = (len + p.n + kAttKeys - 1) / kAttKeys;
-  const int blk0 = split * p.blocks_per_split;
-  const int nb = max(0, min(nblk, blk0 + p.blocks_per_split) - blk0);
   const int64_t kv_row0 = ((int64_t)b * p.Hkv + kvh) * p.Lcap;
   int mma_issued = 0;
 
@@ -493,26 +558,27 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(t, pb));
     }
-    // ---- the row: O / l (one split) or the split's (m, l, O); a split
-    // without keys for this sequence leaves (m, l) = (-inf, 0)
-    const int64_t base = (((int64_t)split * p.B + b) * p.Hkv + kvh) * p.rows_pad;
-    const int64_t rows_cap = (int64_t)p.splits * p.B * p.Hkv * p.rows_pad;
-    if (ok && nb == 0 && valid && p.splits > 1 && in_bounds(p.err, base + R, rows_cap))
-      p.part_ml[base + R] = make_float2(-INFINITY, 0.0f);
+    // ---- the row: O / l (the sequence in one piece) or the piece's
+    // (m, l, O) in the CTA's slot; a piece without keys leaves (-inf, 0)
+    const int64_t base = (int64_t)blockIdx.x * p.unit_rows;
+    const int64_t rows_cap = (int64_t)p.ctas * p.unit_rows;
+    const int Ru = R - rb * p.unit_rows;  // the row within the CTA's rows
+    if (ok && nb == 0 && valid && w.np > 1 && in_bounds(p.err, base + Ru, rows_cap))
+      p.part_ml[base + Ru] = make_float2(-INFINITY, 0.0f);
     if (ok && nbt > 0 && any_row && ta_wait(pv_done(t, (nb - 1) & 1), (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
       tc_fence_after();
       const float il = l > 0.0f ? 1.0f / l : 0.0f;
       const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
       const int64_t oi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
-      const bool st_ok = valid && (p.splits == 1 ? in_bounds(p.err, oi + kAttD - 1, out_cap)
-                                                 : in_bounds(p.err, base + R, rows_cap));
+      const bool st_ok = valid && (w.np == 1 ? in_bounds(p.err, oi + kAttD - 1, out_cap)
+                                             : in_bounds(p.err, base + Ru, rows_cap));
 #pragma unroll 1
       for (int c0 = 0; c0 < kAttD; c0 += 32) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(trow + ta_o_col<TILES>(t) + (uint32_t)c0, ov);
         tmem_wait_ld();
         if (!st_ok) continue;
-        if (p.splits == 1) {
+        if (w.np == 1) {
 #pragma unroll
           for (int c = 0; c < 32; c += 8) {
             uint4 w;
@@ -523,14 +589,14 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
             *reinterpret_cast<uint4*>(p.out + oi + c0 + c) = w;
           }
         } else {
-          float* dst = p.part_o + (base + R) * kAttD + c0;
+          float* dst = p.part_o + (base + Ru) * kAttD + c0;
 #pragma unroll
           for (int c = 0; c < 32; c += 4)
             *reinterpret_cast<float4*>(dst + c) = make_float4(__uint_as_float(ov[c]), __uint_as_float(ov[c + 1]),
                                                               __uint_as_float(ov[c + 2]), __uint_as_float(ov[c + 3]));
         }
       }
-      if (st_ok && p.splits > 1) p.part_ml[base + R] = make_float2(m_used, l);
+      if (st_ok && w.np > 1) p.part_ml[base + Ru] = make_float2(m_used, l);
     }
   }
 
@@ -549,6 +615,9 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
 
 // One warp per query row: merge the splits' (m, l, O) and store the
 // normalised row as bf16 (lane k: columns 4k .. 4k + 3).
+// One warp per query row of a sequence that was cut into pieces: the
+// pieces' (m, l, O), in the slots the sequence's first piece recorded, merged
+// and normalised (a sequence in one piece was finished by its CTA).
 __global__ void __launch_bounds__(256) tree_attention_combine_kernel(const AttnParams p) {
   grid_launch_dependents();
   grid_dependency_wait();
@@ -560,17 +629,24 @@ __global__ void __launch_bounds__(256) tree_attention_combine_kernel(const AttnP
   const int kvh = (int)((row - b * per_b) / p.rows);
   const int R = (int)(row - b * per_b - (int64_t)kvh * p.rows);
   const int j = R / p.G, g = R - j * p.G;
-  const int64_t stride = (int64_t)p.B * p.Hkv * p.rows_pad;
-  const int64_t r0 = ((int64_t)b * p.Hkv + kvh) * p.rows_pad + R;
+  const int2 sp = __ldcg(&p.seq_pieces[b]);  // (first piece, pieces)
+  if (sp.y <= 1) return;
+  const int rbi = R / p.unit_rows, Ru = R - rbi * p.unit_rows;
+  const int64_t x0 = (int64_t)sp.x + ((int64_t)kvh * p.row_blocks + rbi) * sp.y;
+  if (x0 < 0 || x0 + sp.y > p.ctas) {
+    if (lane == 0) report_error(p.err, kErrBounds);
+    return;
+  }
   float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(&p.part_ml[r0 + s * stride]).x);
+  for (int s = 0; s < sp.y; ++s) M = fmaxf(M, __ldcg(&p.part_ml[(x0 + s) * p.unit_rows + Ru]).x);
   float lsum = 0.0f, acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-  for (int s = 0; s < p.splits; ++s) {
-    const float2 ml = __ldcg(&p.part_ml[r0 + s * stride]);
-    if (!(ml.y > 0.0f)) continue;  // no key of this row in the split
+  for (int s = 0; s < sp.y; ++s) {
+    const int64_t slot_row = (x0 + s) * p.unit_rows + Ru;
+    const float2 ml = __ldcg(&p.part_ml[slot_row]);
+    if (!(ml.y > 0.0f)) continue;  // no key of this row in the piece
     const float w = ex2(ml.x - M);
     lsum += w * ml.y;
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + (r0 + s * stride) * kAttD) + lane);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + slot_row * kAttD) + lane);
     acc[0] += w * v.x;
     acc[1] += w * v.y;
     acc[2] += w * v.z;
@@ -679,17 +755,13 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   pl.tiles = pl.rows > kTaRows ? 2 : 1;
   const int per_cta = pl.tiles * kTaRows;
   pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
-  pl.rows_pad = pl.row_blocks * per_cta;
-  const int nbmax = (max_len + n + kAttKeys - 1) / kAttKeys;
-  const int64_t base = (int64_t)B * Hkv * pl.row_blocks;
-  // at most one wave of CTAs (one CTA per SM holds its rows and every block
-  // of its split: more splits only add the combine and more CTA starts)
-  int splits = (int)((num_sms > 0 ? num_sms : 1) / base);
-  if (splits < 1) splits = 1;
-  if (splits > nbmax) splits = nbmax;
-  pl.blocks_per_split = (nbmax + splits - 1) / splits;
-  pl.splits = (nbmax + pl.blocks_per_split - 1) / pl.blocks_per_split;
-  pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * B * Hkv * pl.rows_pad * (kAttD * 4 + 8) : 0;
+  // one wave of CTAs: up to 64 sequences are cut into pieces on the device
+  // (from the committed lengths) when their units leave CTAs free
+  const int64_t units = (int64_t)B * Hkv * pl.row_blocks;
+  pl.ctas = num_sms > 0 ? num_sms : 1;
+  pl.cut = B <= 64 && units < pl.ctas ? 1 : 0;
+  pl.pieces_max = (int)(units > pl.ctas ? units : pl.ctas);
+  pl.ws_bytes = pl.cut ? (size_t)pl.ctas * per_cta * (kAttD * 4 + 8) + (size_t)B * 8 : 0;
   return pl;
 }
 
@@ -727,8 +799,9 @@ cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void
   p.parents = parents;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
-                                        (size_t)pl.splits * B * Hkv * pl.rows_pad * kAttD * 4);
+  const size_t slot_rows = (size_t)pl.ctas * pl.tiles * kTaRows;
+  p.part_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) + slot_rows * kAttD * 4);
+  p.seq_pieces = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + slot_rows * (kAttD * 4 + 8));
   p.err = err;
   p.B = B;
   p.n = n;
@@ -738,18 +811,19 @@ cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void
   p.Lcap = Lcap;
   p.max_len = max_len;
   p.rows = pl.rows;
-  p.rows_pad = pl.rows_pad;
+  p.unit_rows = pl.tiles * kTaRows;
   p.row_blocks = pl.row_blocks;
-  p.splits = pl.splits;
-  p.blocks_per_split = pl.blocks_per_split;
+  p.ctas = pl.ctas;
+  p.pieces_max = pl.pieces_max;
+  p.cut = pl.cut;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const dim3 grid((unsigned)(pl.row_blocks * pl.splits), (unsigned)Hkv, (unsigned)B);
+  const dim3 grid((unsigned)pl.pieces_max);
   cudaError_t e;
   if (pl.tiles == 2)
     e = launch_attn_tc_t<2>(km, vm, p, grid, stream);
   else
     e = launch_attn_tc_t<1>(km, vm, p, grid, stream);
-  if (e != cudaSuccess || pl.splits == 1) return e;
+  if (e != cudaSuccess || !pl.cut) return e;
   const int64_t rows = (int64_t)B * Hkv * pl.rows;
   return launch_pdl(tree_attention_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, stream, p);
 }

@@ -114,11 +114,11 @@ void* tensor_map_encode_fn();
 struct AttnPlan {
   int rows = 0;        // query rows per KV head: n * (H / Hkv)
   int tiles = 0;       // 128-row tiles per CTA: 2 above 128 query rows per KV head, else 1
-  int row_blocks = 0;  // CTAs along the rows
-  int rows_pad = 0;
-  int splits = 0;      // CTAs along the keys
-  int blocks_per_split = 0;
-  size_t ws_bytes = 0;  // split partials (0 with one split)
+  int row_blocks = 0;  // row blocks (CTAs along the rows) per KV head
+  int ctas = 0;        // CTAs of one wave: the pieces are cut for them
+  int pieces_max = 0;  // grid: max(ctas, B * Hkv * row_blocks)
+  int cut = 0;         // 1: sequences may be cut into pieces (up to 64 sequences, units < ctas)
+  size_t ws_bytes = 0;  // cut: a partial slot per CTA + per sequence (first piece, pieces); else 0
 };
 AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms);
 cudaError_t launch_tree_attention(const void* q, const void* k_cache, const void* v_cache, const int32_t* lens,
