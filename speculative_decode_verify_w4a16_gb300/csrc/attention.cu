@@ -613,11 +613,10 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
   }
 }
 
-// One warp per query row: merge the splits' (m, l, O) and store the
-// normalised row as bf16 (lane k: columns 4k .. 4k + 3).
 // One warp per query row of a sequence that was cut into pieces: the
 // pieces' (m, l, O), in the slots the sequence's first piece recorded, merged
-// and normalised (a sequence in one piece was finished by its CTA).
+// and stored as bf16 (lane k: columns 4k .. 4k + 3); a sequence in one piece
+// was finished by its CTA.
 __global__ void __launch_bounds__(256) tree_attention_combine_kernel(const AttnParams p) {
   grid_launch_dependents();
   grid_dependency_wait();
