@@ -245,7 +245,8 @@ __device__ TaWork ta_assign(const AttnParams& p, int x, int lane) {
     len[h] = l;
     nbk[h] = c < p.B ? (l + p.n + kAttKeys - 1) / kAttKeys : 0;
   }
-  int q = 1, qhi = __reduce_max_sync(0xffffffffu, max(nbk[0], nbk[1]));
+  int qhi = __reduce_max_sync(0xffffffffu, max(nbk[0], nbk[1]));
+  int q = p.cut ? 1 : qhi;  // not cut: one piece per unit
   while (q < qhi) {  // the smallest piece length whose pieces fit the CTAs
     const int mid = (q + qhi) >> 1;
     const int cnt = __reduce_add_sync(0xffffffffu, (nbk[0] + mid - 1) / mid + (nbk[1] + mid - 1) / mid);
@@ -563,7 +564,7 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     const int64_t base = (int64_t)blockIdx.x * p.unit_rows;
     const int64_t rows_cap = (int64_t)p.ctas * p.unit_rows;
     const int Ru = R - rb * p.unit_rows;  // the row within the CTA's rows
-    if (ok && nb == 0 && valid && w.np > 1 && in_bounds(p.err, base + Ru, rows_cap))
+    if (ok && nb == 0 && valid && w.np > 1 && p.cut && in_bounds(p.err, base + Ru, rows_cap))
       p.part_ml[base + Ru] = make_float2(-INFINITY, 0.0f);
     if (ok && nbt > 0 && any_row && ta_wait(pv_done(t, (nb - 1) & 1), (uint32_t)((nb - 1) / 2) & 1u, p.err)) {
       tc_fence_after();
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
       const int64_t out_cap = (int64_t)p.B * p.n * p.H * kAttD;
       const int64_t oi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool st_ok = valid && (w.np == 1 ? in_bounds(p.err, oi + kAttD - 1, out_cap)
-                                             : in_bounds(p.err, base + Ru, rows_cap));
+                                             : p.cut && in_bounds(p.err, base + Ru, rows_cap));
 #pragma unroll 1
       for (int c0 = 0; c0 < kAttD; c0 += 32) {
         uint32_t ov[32];
@@ -755,10 +756,13 @@ AttnPlan attn_plan(int B, int n, int H, int Hkv, int max_len, int num_sms) {
   const int per_cta = pl.tiles * kTaRows;
   pl.row_blocks = (pl.rows + per_cta - 1) / per_cta;
   // one wave of CTAs: up to 64 sequences are cut into pieces on the device
-  // (from the committed lengths) when their units leave CTAs free
+  // (from the committed lengths) when their units leave at least half the
+  // CTAs free (with fewer free, only the longest few would be cut and the
+  // combine costs more than it saves: K = 4 sequence draft at B = 16, 128
+  // units on 152 SMs, 63.3 us uncut against 67.8 us cut)
   const int64_t units = (int64_t)B * Hkv * pl.row_blocks;
   pl.ctas = num_sms > 0 ? num_sms : 1;
-  pl.cut = B <= 64 && units < pl.ctas ? 1 : 0;
+  pl.cut = B <= 64 && 2 * units <= pl.ctas ? 1 : 0;
   pl.pieces_max = (int)(units > pl.ctas ? units : pl.ctas);
   pl.ws_bytes = pl.cut ? (size_t)pl.ctas * per_cta * (kAttD * 4 + 8) + (size_t)B * 8 : 0;
   return pl;
