@@ -57,6 +57,8 @@ CASES = [  # B, n, H, Hkv, lens, tree
     (2, 17, 12, 4, [129, 7], True),           # three query heads per KV head
     (2, 33, 8, 1, [511, 64], True),           # all heads on one KV head
     (2, 24, 64, 8, [300, 77], True),          # 192 query rows: the second 128-row tile half full
+    # 70 sequences: above 64 the units are taken in order, one CTA each
+    (70, 3, 16, 2, [(37 * i) % 260 for i in range(70)], True),
 ]
 
 
