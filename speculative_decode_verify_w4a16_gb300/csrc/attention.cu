@@ -160,7 +160,10 @@ struct TaConfig {
   static constexpr int kStages = TILES == 2 ? 4 : 5;
   static constexpr int kSoftWarp0 = TILES == 2 ? 4 : 2;  // first softmax warp
   static constexpr int kThreads = 32 * (kSoftWarp0 + 4 * TILES);
-  static constexpr uint32_t kTmemCols = 256u * TILES;
+  // TILES = 1: scores 128, O 128, Q 64 columns (Q in TMEM: S = Q K^T reads
+  // its A operand there instead of shared memory); TILES = 2: all 512
+  static constexpr uint32_t kTmemCols = 512u;
+  static constexpr bool kQInTmem = TILES == 1;
 };
 
 template <int TILES>
@@ -180,7 +183,9 @@ struct TaLayout {
   static_assert(kTotal + 512 <= 227 * 1024, "shared memory (with the static words and parents)");
 };
 // TMEM columns of tile t: score buffer sb at 128 t + 64 sb .. + 63 (P of the
-// block, bf16 pairs, over its first 32 columns); O 128 TILES + 128 t .. + 127
+// block, bf16 pairs, over its first 32 columns); O 128 TILES + 128 t .. + 127;
+// with one tile, its Q (bf16 pairs) at 256 .. 319
+constexpr uint32_t kTaQCol = 256u;
 __device__ __forceinline__ uint32_t ta_s_col(int t, int sb) { return 128u * (uint32_t)t + 64u * (uint32_t)sb; }
 template <int TILES>
 __device__ __forceinline__ uint32_t ta_o_col(int t) {
@@ -393,8 +398,12 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (uint32_t)((kk >> 2) * L::kQHalf + 32 * (kk & 3));
         const uint32_t koff = (uint32_t)((kk >> 2) * L::kKHalf + 32 * (kk & 3));
-        umma_bf16_ss_warp(tmem + ta_s_col(t, sb), umma_desc_sw128_kmajor(q0 + off), umma_desc_sw128_kmajor(k0 + koff),
-                          idesc_s, kk > 0 ? 1u : 0u);
+        if constexpr (C::kQInTmem)
+          umma_bf16_ts_warp(tmem + ta_s_col(t, sb), tmem + kTaQCol + 8u * (uint32_t)kk,
+                            umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
+        else
+          umma_bf16_ss_warp(tmem + ta_s_col(t, sb), umma_desc_sw128_kmajor(q0 + off),
+                            umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
       }
       umma_commit_warp(s_full(t, sb));
       mma_issued = 1;
@@ -430,21 +439,40 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     const int R = rb * TILES * kTaRows + t * kTaRows + rl;
     const bool valid = R < p.rows;
     const int j = valid ? R / p.G : 0, g = R - j * p.G;
-    // this row of Q, 128-byte swizzle, K-major (two 64-column halves)
+    // this row of Q: into TMEM (one tile: the row's lane, 64 columns of bf16
+    // pairs) or shared memory (128-byte swizzle, K-major, two 64-column halves)
     {
       const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool qok = valid && in_bounds(p.err, qi + kAttD - 1, (int64_t)p.B * p.n * p.H * kAttD);
-      uint8_t* qt = smem + L::kQOff + t * 2 * L::kQHalf;
       // all 16 loads in flight before the first store (a store between two
       // loads would make each load wait for the one before it)
       uint4 v[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c)
         v[c] = qok ? *reinterpret_cast<const uint4*>(p.q + qi + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (C::kQInTmem) {
+        const uint32_t qrow = tmem + ((uint32_t)(32 * qd) << 16) + kTaQCol;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(qt + (c >> 3) * L::kQHalf + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = v[c];
-      fence_proxy_async_smem();
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            w[4 * c] = v[8 * h + c].x;
+            w[4 * c + 1] = v[8 * h + c].y;
+            w[4 * c + 2] = v[8 * h + c].z;
+            w[4 * c + 3] = v[8 * h + c].w;
+          }
+          tmem_st_32x32b_x32(qrow + 32u * (uint32_t)h, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      } else {
+        uint8_t* qt = smem + L::kQOff + t * 2 * L::kQHalf;
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(qt + (c >> 3) * L::kQHalf + rl * 128 + (((c & 7) ^ (rl & 7)) << 4)) = v[c];
+        fence_proxy_async_smem();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(q_ready);
     }
