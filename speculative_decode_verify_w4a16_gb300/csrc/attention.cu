@@ -123,7 +123,8 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 // TILES = 2 (more than 128 query rows per KV head: tree drafts): 12 warps, a
 // 4-stage ring, all 512 TMEM columns. TILES = 1 (up to 128 rows: sequence
 // drafts and small trees, where streaming the keys and values is the cost):
-// 6 warps, a 5-stage ring, 256 TMEM columns.
+// 6 warps, a 6-stage ring, Q in TMEM beside the scores and O (S = Q K^T then
+// takes its A operand from TMEM).
 //   warp 0        2-D TMA of the 64-key blocks of K and V into the ring
 //   warps 1 ..    the MMAs of tile 0 (and tile 1) (whole warp in the loop, the
 //                 elect.sync lane issuing): S = Q K^T (M = 128 query rows,
@@ -157,7 +158,7 @@ constexpr float kTaLazy = 8.0f;  // log2 of the largest weight before the maximu
 
 template <int TILES>
 struct TaConfig {
-  static constexpr int kStages = TILES == 2 ? 4 : 5;
+  static constexpr int kStages = TILES == 2 ? 4 : 6;
   static constexpr int kSoftWarp0 = TILES == 2 ? 4 : 2;  // first softmax warp
   static constexpr int kThreads = 32 * (kSoftWarp0 + 4 * TILES);
   // TILES = 1: scores 128, O 128, Q 64 columns (Q in TMEM: S = Q K^T reads
@@ -173,7 +174,7 @@ struct TaLayout {
   static constexpr int kKHalf = kAttKeys * 128;       // 64 keys x 64 head columns
   static constexpr int kStage = 4 * kKHalf;          // K halves, V halves
   static constexpr int kQOff = 0;                     // tile t: two halves at 2 t kQHalf
-  static constexpr int kStageOff = TILES * 2 * kQHalf;
+  static constexpr int kStageOff = TaConfig<TILES>::kQInTmem ? 0 : TILES * 2 * kQHalf;
   static constexpr int kAncOff = kStageOff + S * kStage;
   static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;
   // kv_full[S], kv_free[S]; per tile s_full[2], p_full[2], pv_done[2], mma_fin; q_ready
