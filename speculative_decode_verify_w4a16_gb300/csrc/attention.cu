@@ -161,19 +161,24 @@ struct TaConfig {
   static constexpr int kStages = TILES == 2 ? 4 : 6;
   static constexpr int kSoftWarp0 = TILES == 2 ? 4 : 2;  // first softmax warp
   static constexpr int kThreads = 32 * (kSoftWarp0 + 4 * TILES);
-  // TILES = 1: scores 128, O 128, Q 64 columns (Q in TMEM: S = Q K^T reads
-  // its A operand there instead of shared memory); TILES = 2: all 512
+  // two score buffers per tile (S(i + 2) waits for P V (i), whose P sits in
+  // its buffer). One tile: Q in TMEM too (S = Q K^T then reads its A operand
+  // there, 33 instead of ~50 cycles an MMA, and the ring takes Q's shared
+  // memory); two tiles fill the TMEM with scores and O, Q stays in shared
+  // memory (a single score buffer with Q in TMEM measured 158 against 111 us:
+  // S(i + 1) then waits for P V (i))
   static constexpr uint32_t kTmemCols = 512u;
+  static constexpr int kSBufs = 2;
   static constexpr bool kQInTmem = TILES == 1;
 };
 
 template <int TILES>
 struct TaLayout {
   static constexpr int S = TaConfig<TILES>::kStages;
-  static constexpr int kQHalf = kTaRows * 128;        // 128 rows x 64 head columns (bf16)
   static constexpr int kKHalf = kAttKeys * 128;       // 64 keys x 64 head columns
   static constexpr int kStage = 4 * kKHalf;          // K halves, V halves
-  static constexpr int kQOff = 0;                     // tile t: two halves at 2 t kQHalf
+  static constexpr int kQHalf = kTaRows * 128;  // 128 rows x 64 head columns (bf16)
+  static constexpr int kQOff = 0;               // Q in shared memory: tile t's halves at 2 t kQHalf
   static constexpr int kStageOff = TaConfig<TILES>::kQInTmem ? 0 : TILES * 2 * kQHalf;
   static constexpr int kAncOff = kStageOff + S * kStage;
   static constexpr int kBarOff = kAncOff + kAttMaxNodes * 8;
@@ -183,11 +188,14 @@ struct TaLayout {
   static_assert(kStage % 1024 == 0 && kQHalf % 1024 == 0 && kKHalf % 1024 == 0, "swizzle atoms");
   static_assert(kTotal + 512 <= 227 * 1024, "shared memory (with the static words and parents)");
 };
-// TMEM columns of tile t: score buffer sb at 128 t + 64 sb .. + 63 (P of the
-// block, bf16 pairs, over its first 32 columns); O 128 TILES + 128 t .. + 127;
-// with one tile, its Q (bf16 pairs) at 256 .. 319
+// TMEM columns of tile t: score buffer sb at 128 t + 64 sb .. + 63 (the
+// block's P, bf16 pairs, over its first 32 columns); O 128 TILES + 128 t ..
+// + 127; one tile's Q (bf16 pairs) at 256 .. 319
+template <int TILES>
+__device__ __forceinline__ uint32_t ta_s_col(int t, int sb) {
+  return 128u * (uint32_t)t + 64u * (uint32_t)sb;
+}
 constexpr uint32_t kTaQCol = 256u;
-__device__ __forceinline__ uint32_t ta_s_col(int t, int sb) { return 128u * (uint32_t)t + 64u * (uint32_t)sb; }
 template <int TILES>
 __device__ __forceinline__ uint32_t ta_o_col(int t) {
   return 128u * (uint32_t)TILES + 128u * (uint32_t)t;
@@ -386,33 +394,34 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     const uint32_t idesc_s = umma_idesc_bf16((uint32_t)kAttKeys), idesc_o = umma_idesc_bf16_bmn((uint32_t)kAttD);
     bool ok = ta_wait(q_ready, 0u, p.err);
     tc_fence_after();
-    const uint32_t q0 = smem_u32(smem + L::kQOff + t * 2 * L::kQHalf);
-    // S(i) = Q K(i)^T into score buffer i % 2, once P V (i - 2) (its P in the
-    // same buffer) is complete
+    constexpr int lag = C::kSBufs;
+    // S(i) = Q K(i)^T into the tile's score buffer i % kSBufs, once P V
+    // (i - kSBufs) (its P in the same buffer) is complete
     auto issue_s = [&](int i) {
       const int s = i % S, sb = i & 1;
       if (!ta_wait(&kv_full[s], (uint32_t)(i / S) & 1u, p.err)) return false;
-      if (i >= 2 && !ta_wait(pv_done(t, sb), (uint32_t)((i - 2) / 2) & 1u, p.err)) return false;
+      if (i >= lag && !ta_wait(pv_done(t, (i - lag) & 1), (uint32_t)((i - lag) / 2) & 1u, p.err)) return false;
       tc_fence_after();
       const uint32_t k0 = smem_u32(smem + L::kStageOff + s * L::kStage);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (uint32_t)((kk >> 2) * L::kQHalf + 32 * (kk & 3));
         const uint32_t koff = (uint32_t)((kk >> 2) * L::kKHalf + 32 * (kk & 3));
-        if constexpr (C::kQInTmem)
-          umma_bf16_ts_warp(tmem + ta_s_col(t, sb), tmem + kTaQCol + 8u * (uint32_t)kk,
+        if constexpr (C::kQInTmem) {
+          umma_bf16_ts_warp(tmem + ta_s_col<TILES>(t, sb), tmem + kTaQCol + 8u * (uint32_t)kk,
                             umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
-        else
-          umma_bf16_ss_warp(tmem + ta_s_col(t, sb), umma_desc_sw128_kmajor(q0 + off),
+        } else {
+          const uint32_t q0 = smem_u32(smem + L::kQOff + t * 2 * L::kQHalf);
+          umma_bf16_ss_warp(tmem + ta_s_col<TILES>(t, sb),
+                            umma_desc_sw128_kmajor(q0 + (uint32_t)((kk >> 2) * L::kQHalf + 32 * (kk & 3))),
                             umma_desc_sw128_kmajor(k0 + koff), idesc_s, kk > 0 ? 1u : 0u);
+        }
       }
       umma_commit_warp(s_full(t, sb));
       mma_issued = 1;
       return true;
     };
     if (t >= ntiles) ok = false;  // no rows in this tile
-    if (ok && nb > 0) ok = issue_s(0);
-    if (ok && nb > 1) ok = issue_s(1);
+    for (int i = 0; ok && i < lag && i < nb; ++i) ok = issue_s(i);
     for (int i = 0; ok && i < nb; ++i) {
       const int s = i % S, pb = i & 1;
       if (!ta_wait(p_full(t, pb), (uint32_t)(i / 2) & 1u, p.err)) break;
@@ -422,12 +431,12 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
       const uint32_t v0 = smem_u32(smem + L::kStageOff + s * L::kStage + 2 * L::kKHalf);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        umma_bf16_ts_warp(tmem + ta_o_col<TILES>(t), tmem + ta_s_col(t, pb) + 8u * (uint32_t)kk,
+        umma_bf16_ts_warp(tmem + ta_o_col<TILES>(t), tmem + ta_s_col<TILES>(t, pb) + 8u * (uint32_t)kk,
                           umma_desc_sw128_mnmajor(v0 + 2048u * (uint32_t)kk, (uint32_t)L::kKHalf, 1024u), idesc_o,
                           (i > 0 || kk > 0) ? 1u : 0u);
       umma_commit_warp(pv_done(t, pb));
       umma_commit_warp(&kv_free[s]);
-      if (i + 2 < nb && !issue_s(i + 2)) break;
+      if (i + lag < nb && !issue_s(i + lag)) break;
     }
     if (mma_issued) umma_commit_warp(mma_fin(t));  // tracks all of this warp's MMAs
   } else if (warp < C::kSoftWarp0) {
@@ -440,8 +449,9 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
     const int R = rb * TILES * kTaRows + t * kTaRows + rl;
     const bool valid = R < p.rows;
     const int j = valid ? R / p.G : 0, g = R - j * p.G;
-    // this row of Q: into TMEM (one tile: the row's lane, 64 columns of bf16
-    // pairs) or shared memory (128-byte swizzle, K-major, two 64-column halves)
+    // this row of Q: into TMEM with one tile (the row's lane, 64 columns of
+    // bf16 pairs), else into shared memory (128-byte swizzle, K-major, two
+    // 64-column halves)
     {
       const int64_t qi = (((int64_t)b * p.n + j) * p.H + kvh * p.G + g) * kAttD;
       const bool qok = valid && in_bounds(p.err, qi + kAttD - 1, (int64_t)p.B * p.n * p.H * kAttD);
@@ -499,8 +509,8 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
       }
       tc_fence_after();
       uint32_t sv[2][32];
-      tmem_ld_32x32b_x32(trow + ta_s_col(t, pb), sv[0]);
-      tmem_ld_32x32b_x32(trow + ta_s_col(t, pb) + 32u, sv[1]);
+      tmem_ld_32x32b_x32(trow + ta_s_col<TILES>(t, pb), sv[0]);
+      tmem_ld_32x32b_x32(trow + ta_s_col<TILES>(t, pb) + 32u, sv[1]);
       tmem_wait_ld();
       // the mask (keys the row does not see: -inf), then the block's maximum
       // on the raw scores (the positive scale commutes with it), in the log2
@@ -582,7 +592,7 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
         f2_unpack(lb, b0, b1);
         l += (a0 + a1) + (b0 + b1);
       }
-      tmem_st_32x32b_x32(trow + ta_s_col(t, pb), pr);  // over the scores just read
+      tmem_st_32x32b_x32(trow + ta_s_col<TILES>(t, pb), pr);  // over the scores just read
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
