@@ -156,12 +156,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // ------------------------------------------------- programmatic dependent launch
 // Kernels are launched with programmatic stream serialisation: they may start
 // while the previous kernel on the stream is still running. Everything that
@@ -204,18 +198,6 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
       "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
       "mov.b64 {%0, %1}, rd;\n\t}"
       : "+f"(d0), "+f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
-
-// (d0, d1) = (a0 * b0, a1 * b1): two IEEE fp32 multiplies (round to nearest)
-// in one instruction.
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %5};\n\t"
-      "mul.rn.f32x2 rd, ra, rb;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
@@ -262,11 +244,6 @@ __device__ __forceinline__ float4 ldg_hint_f4(const float4* p, uint64_t pol) {
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p), "l"(pol));
-  return v;
-}
-__device__ __forceinline__ float ldg_hint_f(const float* p, uint64_t pol) {
-  float v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
   return v;
 }
 
