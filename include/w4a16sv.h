@@ -235,12 +235,14 @@ w4a16_status spec_accept_node(const float* p_logits, const float* q_logits, cons
  *   tree_parents  device int32 [B][n] (parent[0] = -1, 0 <= parent[j] < j),
  *                 or NULL for a sequence draft (the chain)
  *   n             tree nodes, 1 .. 64; D = 128 (else W4A16_ERR_UNSUPPORTED)
- *   max_len       an upper bound of lens[] known to the caller (it sizes the
- *                 key splits); max_len + n <= Lcap
+ *   max_len       an upper bound of lens[] known to the caller (a larger
+ *                 lens[b] is reported and clamped); max_len + n <= Lcap
  *   scale         softmax scale (1 / sqrt(D) for the model), finite, > 0
  *   out           device bf16 [B][n][H][D] (16-byte aligned)
  *   workspace     device scratch of tree_attention_workspace_bytes() bytes
- *                 (256-byte aligned; may be NULL when that is 0); needs no
+ *                 (256-byte aligned; may be NULL when that is 0: nonzero only
+ *                 for up to 64 sequences whose units leave at least half the
+ *                 SMs free, which the kernel may cut into pieces); needs no
  *                 initialisation
  * Arithmetic: bf16 inputs, fp32 scores and sums; the softmax weights are
  * rounded to bf16 for the weighted sum of the values and normalised by the
