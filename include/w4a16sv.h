@@ -246,7 +246,7 @@ w4a16_status spec_accept_node(const float* p_logits, const float* q_logits, cons
  *                 initialisation
  * Arithmetic: bf16 inputs, fp32 scores and sums; the softmax weights are
  * rounded to bf16 for the weighted sum of the values and normalised by the
- * sum of those rounded weights; out rounded to bf16.
+ * sum of the fp32 weights; out rounded to bf16.
  * A lens[b] outside [0, max_len] or a bad parent sets W4A16_ERR_DEVICE_INPUT
  * in the device error word (the length is clamped, the node then attends to
  * itself and the prefix only). Launch rules as for w4a16_linear.

@@ -12,8 +12,8 @@
 // a shared-memory ring of 64-key blocks (2-D TMA, 128-byte swizzle). Each row
 // is masked (the committed prefix: every key; the tree's own keys: the node's
 // ancestors and itself, a 64-bit mask per node), keeps the running maximum
-// and sum of the online softmax in the log2 domain, and accumulates P V with
-// P rounded to bf16 (the sum is taken over the same rounded values). With one
+// and sum of the online softmax in the log2 domain (the sum over the fp32
+// weights), and accumulates P V with P rounded to bf16. With one
 // piece per sequence the rows are normalised and stored as bf16; a sequence
 // cut into several pieces (CTAs) leaves fp32 (m, l, O) per piece and
 // tree_attention_combine_kernel merges them.
@@ -144,8 +144,8 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 //                 the row's scores from TMEM, the mask
 //                 (committed prefix: every key; tree keys: the node's
 //                 ancestors and itself; skipped on blocks of the prefix), the
-//                 online softmax in the log2 domain and P (rounded to bf16,
-//                 the row sum taken over the rounded values) back into TMEM,
+//                 online softmax in the log2 domain (the row sum over the
+//                 fp32 weights) and P (rounded to bf16) back into TMEM,
 //                 over the first half of the scores just read;
 //                 at the end the normalised row (or a piece's partial)
 // While one tile's softmax runs, the tensor pipe works on the other tile.
@@ -566,8 +566,8 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s scale - m), rounded to bf16; l over the rounded values. The
-      // exponents' arguments and the sums go two lanes per instruction.
+      // P = 2^(s scale - m), rounded to bf16 for P V; l over the fp32 values.
+      // The exponents' arguments and the sums go two lanes per instruction.
       const float u = m_used == -INFINITY ? 0.0f : m_used;
       const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nu2 = f2_pack(-u, -u);
       uint64_t la = f2_pack(0.0f, 0.0f), lb = la;
@@ -578,9 +578,9 @@ __global__ void __launch_bounds__(TaConfig<TILES>::kThreads, 1)
         for (int c = 0; c < 16; ++c) {
           float x0, x1;
           f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[h][2 * c]), __uint_as_float(sv[h][2 * c + 1])), sc2, nu2), x0, x1);
-          const uint32_t w = pack_bf16_rn(ex2(x0), ex2(x1));
-          pr[16 * h + c] = w;
-          const uint64_t r2 = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          pr[16 * h + c] = pack_bf16_rn(e0, e1);
+          const uint64_t r2 = f2_pack(e0, e1);
           if (c & 1)
             lb = f2_add(lb, r2);
           else

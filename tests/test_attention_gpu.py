@@ -4,13 +4,13 @@ section 10.1 Medusa tree-based attention, section 10.4 ReDrafter dynamic tree
 attention, section 8.7 KV cache reuse), through the C ABI.
 
 Attention tolerance, from the arithmetic: the kernel rounds each softmax weight
-p_k to bf16 (an 8-bit significand: relative error delta <= 2^-8, plus the
-fp32 score and exponential errors, about 1e-6) and normalises by the sum of
-the rounded weights, so each normalised weight is within a factor
-(1 +- delta)/(1 -+ delta) of the exact one and the weighted sum moves by at
-most about 2^-7 * A, where A = sum_k w_k |v_k| (the oracle reports it);
-storing the result in bf16 adds 2^-8 |out|. The bound used:
-1.05 * 2^-7 * A + 2^-8 * |out| + 1e-6."""
+p_k to bf16 for the weighted sum of the values (an 8-bit significand: relative
+error delta <= 2^-8, plus the fp32 score and exponential errors, about 1e-6)
+and normalises by the sum of the fp32 weights, so each normalised weight is
+within a factor (1 +- delta) of the exact one and the weighted sum moves by at
+most about 2^-8 * A, where A = sum_k w_k |v_k| (the oracle reports it);
+storing the result in bf16 adds 2^-8 |out|. The bound used keeps a factor of
+two beyond that: 1.05 * 2^-7 * A + 2^-8 * |out| + 1e-6."""
 import numpy as np
 import pytest
 import torch
