@@ -128,8 +128,9 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 //   warp 0        2-D TMA of the 64-key blocks of K and V into the ring
 //   warps 1 ..    the MMAs of tile 0 (and tile 1) (whole warp in the loop, the
 //                 elect.sync lane issuing): S = Q K^T (M = 128 query rows,
-//                 N = 64 keys, K = 128; A and B from shared memory) into the
-//                 tile's TMEM score buffer, and O += P V (M = 128, N = 128
+//                 N = 64 keys, K = 128; A = Q from shared memory with two
+//                 tiles, from TMEM with one; B = K from shared memory) into
+//                 the tile's TMEM score buffer, and O += P V (M = 128, N = 128
 //                 head columns, K = 64 keys; P from TMEM, V from shared
 //                 memory as it was loaded: key rows of head columns, the
 //                 MN-major B operand) into the tile's TMEM accumulator. Each
@@ -141,9 +142,10 @@ __device__ void attn_ancestors(const AttnParams& p, int b, uint64_t* anc, int* p
 //   warp 3        idle (TILES = 2)
 //   4 per tile    the softmax warps from warp 4 (TILES = 2) or 2 (TILES = 1):
 //                 one query row per thread, TMEM lane quadrant warp % 4:
-//                 the row's scores from TMEM, the mask
-//                 (committed prefix: every key; tree keys: the node's
-//                 ancestors and itself; skipped on blocks of the prefix), the
+//                 the row's scores from TMEM, the mask as one 64-bit word
+//                 per block (committed prefix: every key; tree keys: the
+//                 node's ancestors and itself; skipped on blocks of the
+//                 prefix), the
 //                 online softmax in the log2 domain (the row sum over the
 //                 fp32 weights) and P (rounded to bf16) back into TMEM,
 //                 over the first half of the scores just read;
